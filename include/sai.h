@@ -1,0 +1,116 @@
+/*
+ * sai.h -- C ABI of libsai, the GB300 (sm_103a) sparse-attention indexer
+ * top-k library.
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ * - All array pointers are DEVICE pointers on the calling thread's current
+ *   CUDA device, owned by the caller. The library allocates nothing; where
+ *   scratch memory helps, the caller passes a workspace sized by the matching
+ *   *_workspace query (same arguments, same device).
+ * - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
+ *   legacy default stream). No entry point synchronizes, except
+ *   sai_device_status.
+ * - Host-visible argument errors are reported before anything is launched.
+ *   Row metadata that lives on the device (seq_lens, row_starts,
+ *   row_to_batch, page/block ids) is checked by the kernels: an out-of-range
+ *   row is treated as empty (all -1 outputs) and a bit is set in the
+ *   library's device status word, read with sai_device_status. No kernel
+ *   ever reads outside the extents the caller declares.
+ * - Row-local index order of the k outputs: higher score first, equal scores
+ *   to the lower row-local index (-0.0 == +0.0; +-inf are ordinary values;
+ *   NaN scores are not admissible). Positions [min(seq_len, k), k) are -1.
+ * - No C++ exception crosses this boundary.
+ */
+#ifndef SAI_H_
+#define SAI_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so users need no CUDA headers. */
+typedef struct CUstream_st* sai_stream_t;
+
+typedef enum {
+  SAI_OK = 0,
+  SAI_ERR_NULL = -1,        /* a required pointer is NULL */
+  SAI_ERR_SHAPE = -2,       /* a size or count is out of range */
+  SAI_ERR_UNSUPPORTED = -3, /* valid but not implemented (e.g. k != 512) */
+  SAI_ERR_WORKSPACE = -4,   /* workspace too small or misaligned */
+  SAI_ERR_CUDA = -5,        /* a CUDA runtime call or launch failed */
+  SAI_ERR_DEVICE_CHECK = -6,/* a kernel flagged bad device-side metadata */
+  SAI_ERR_ALIGN = -7        /* a pointer lacks the alignment its type needs */
+} sai_status;
+
+/* Fixed top-k of this library (the "512" of topk_transform_512_v2). */
+#define SAI_TOPK 512
+
+/* Human-readable name of a status code (static storage). */
+const char* sai_status_string(int status);
+
+/*
+ * Read (and optionally clear) the device status word of the current device
+ * after synchronizing `stream`. *out_bits receives the OR of the bits set by
+ * kernels since the last clear: 1 = bad row metadata, 2 = an internal
+ * pipeline wait gave up, 4 = a block id out of range. Returns
+ * SAI_ERR_DEVICE_CHECK if any bit was set, else SAI_OK.
+ */
+int sai_device_status(int* out_bits, int clear, sai_stream_t stream);
+
+/*
+ * Workspace bytes that sai_topk_transform wants for these sizes on the
+ * current device (0 when the one-unit-per-row path is used). Long rows on
+ * few rows are split over several CTAs whose partial top-k lists go here.
+ */
+size_t sai_topk_transform_workspace(int64_t rows, int64_t score_stride, int32_t k);
+
+/*
+ * sai_topk_transform -- per-row window top-k and page-table transform.
+ *
+ * Follows sglang PR #37889 "[AMD] Enable GLM DSA prefill top-k to the v2
+ * kernel" (Modifications: the two optional (rows,) int32 indirections of
+ * topk_transform_512_v2) and ROCm/ATOM PR #1282 "merge build sparse block
+ * into topk" (the physical addressing is produced by the top-k kernel).
+ *
+ * For each row i in [0, rows):
+ *   n      = seq_lens[i]
+ *   start  = row_starts ? row_starts[i] : 0
+ *   window = scores[i*score_stride + start + t], t in [0, n)
+ *   b      = row_to_batch ? row_to_batch[i] : i
+ *   idx[j] = row-local position of the j-th best score (j < min(n, k))
+ *   slot[j]= page_tables[b*pt_stride + idx[j]/page_size]*page_size
+ *            + idx[j]%page_size
+ *
+ * scores       fp32 [rows, score_stride], 4-byte aligned; any stride and any
+ *              row start work (the 16-byte-aligned interior of each window
+ *              is streamed with bulk TMA copies, the ragged ends with scalar
+ *              loads).
+ * row_starts   int32 [rows] or NULL. The caller guarantees
+ *              start + n <= score_stride (checked on device).
+ * seq_lens     int32 [rows], >= 0.
+ * page_tables  int32 [pt_rows, pt_stride]; required when out_slots != NULL.
+ *              Without row_to_batch, pt_rows >= rows is checked here; with
+ *              it, 0 <= row_to_batch[i] < pt_rows is checked on device.
+ * page_size    >= 1 (1 = one slot per token, the "wide" table).
+ * k            must be 512 (SAI_ERR_UNSUPPORTED otherwise).
+ * out_slots    int32 [rows, 512] or NULL; out_indices int32 [rows, 512] or
+ *              NULL (row-local positions); at least one must be given.
+ * workspace    device memory of workspace_bytes (16-byte aligned) or NULL.
+ *              If it is smaller than sai_topk_transform_workspace asks for,
+ *              every row is processed by a single CTA (correct, slower for
+ *              few long rows).
+ */
+int sai_topk_transform(const float* scores, int64_t rows, int64_t score_stride, const int32_t* row_starts,
+                       const int32_t* seq_lens, const int32_t* page_tables, int64_t pt_rows, int64_t pt_stride,
+                       const int32_t* row_to_batch, int32_t page_size, int32_t k, int32_t* out_slots,
+                       int32_t* out_indices, void* workspace, size_t workspace_bytes, sai_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAI_H_ */

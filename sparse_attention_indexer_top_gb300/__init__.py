@@ -1,0 +1,95 @@
+"""GB300-native sparse-attention indexer top-k (Python binding of libsai).
+
+Every computation runs in the CUDA kernels of ``libsai.so``; this module only
+checks tensor placement/dtypes, passes raw device pointers and the current
+CUDA stream through the C ABI (include/sai.h), and uses torch to allocate
+outputs and workspaces. There is no CPU fallback: without the built library
+every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from ._lib import SaiError, check, load, status_string  # noqa: F401
+
+TOPK = 512
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need(t: Optional[torch.Tensor], name: str, dtype, dev, ndim=None):
+    if t is None:
+        return
+    if not t.is_cuda or t.device != dev:
+        raise ValueError(f"{name} must be on {dev}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+
+
+def device_status(clear: bool = True, stream=None) -> int:
+    """Synchronize ``stream`` and return the device status bits (0 = clean)."""
+    bits = ctypes.c_int(0)
+    load().sai_device_status(ctypes.byref(bits), int(clear), _stream(stream))
+    return bits.value
+
+
+def topk_transform_workspace(rows: int, score_stride: int, k: int = TOPK) -> int:
+    return int(load().sai_topk_transform_workspace(int(rows), int(score_stride), int(k)))
+
+
+def topk_transform(scores: torch.Tensor, seq_lens: torch.Tensor, page_tables: Optional[torch.Tensor] = None, *,
+                   page_size: int = 1, k: int = TOPK, row_starts: Optional[torch.Tensor] = None,
+                   row_to_batch: Optional[torch.Tensor] = None, out_slots: Optional[torch.Tensor] = None,
+                   out_indices: Optional[torch.Tensor] = None, want_indices: bool = False,
+                   workspace: Optional[torch.Tensor] = None, stream=None):
+    """Top-k of each row's score window mapped through its page-table row.
+
+    ``scores`` is fp32 ``[rows, stride]`` with unit column stride (any row
+    stride); ``seq_lens``, ``row_starts``, ``row_to_batch`` are int32
+    ``[rows]``; ``page_tables`` int32 ``[pt_rows, pt_stride]`` with unit
+    column stride. Returns ``out_slots`` (int32 ``[rows, k]``), or
+    ``(out_slots, out_indices)`` when indices are requested.
+    """
+    dev = scores.device
+    _need(scores, "scores", torch.float32, dev, 2)
+    _need(seq_lens, "seq_lens", torch.int32, dev, 1)
+    _need(page_tables, "page_tables", torch.int32, dev, 2)
+    _need(row_starts, "row_starts", torch.int32, dev, 1)
+    _need(row_to_batch, "row_to_batch", torch.int32, dev, 1)
+    if scores.stride(1) != 1 or (page_tables is not None and page_tables.stride(1) != 1):
+        raise ValueError("scores and page_tables need unit column stride")
+    rows = scores.shape[0]
+    for name, t in (("seq_lens", seq_lens), ("row_starts", row_starts), ("row_to_batch", row_to_batch)):
+        if t is not None and (t.shape[0] != rows or not t.is_contiguous()):
+            raise ValueError(f"{name} must be contiguous [{rows}]")
+    if out_slots is None and page_tables is not None:
+        out_slots = torch.empty((rows, k), dtype=torch.int32, device=dev)
+    if out_indices is None and (want_indices or page_tables is None):
+        out_indices = torch.empty((rows, k), dtype=torch.int32, device=dev)
+    stride = scores.stride(0) if rows > 1 else max(scores.shape[1], 1)
+    ws_bytes = topk_transform_workspace(rows, stride, k) if rows else 0
+    if workspace is None and ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    pt_rows, pt_stride = (page_tables.shape[0], page_tables.stride(0)) if page_tables is not None else (0, 0)
+    st = load().sai_topk_transform(
+        _ptr(scores), rows, stride, _ptr(row_starts), _ptr(seq_lens), _ptr(page_tables), pt_rows, pt_stride,
+        _ptr(row_to_batch), int(page_size), int(k), _ptr(out_slots), _ptr(out_indices), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream))
+    check(st, "sai_topk_transform")
+    if out_slots is None:
+        return out_indices
+    return (out_slots, out_indices) if (want_indices or out_indices is not None) else out_slots

@@ -1,0 +1,140 @@
+// C-ABI layer of libsai: argument validation, workspace planning, device
+// status word, launch on the caller's stream. See include/sai.h.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/sai.h"
+#include "sai_internal.h"
+
+namespace {
+
+__device__ int g_device_status;
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices];
+int g_num_sms[kMaxDevices];
+std::mutex g_mu;
+
+// Per-device set-up, done once with that device current.
+bool device_setup(int* dev_out, int** status, int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return false;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return false;
+    g_num_sms[dev] = n;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  *dev_out = dev;
+  *status = g_status_ptr[dev];
+  *sms = g_num_sms[dev];
+  return true;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* sai_status_string(int status) {
+  switch (status) {
+    case SAI_OK: return "ok";
+    case SAI_ERR_NULL: return "a required pointer is NULL";
+    case SAI_ERR_SHAPE: return "a size or count is out of range";
+    case SAI_ERR_UNSUPPORTED: return "unsupported configuration";
+    case SAI_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case SAI_ERR_CUDA: return "CUDA runtime or launch failure";
+    case SAI_ERR_DEVICE_CHECK: return "a kernel flagged bad device-side metadata";
+    case SAI_ERR_ALIGN: return "misaligned pointer";
+    default: return "unknown status";
+  }
+}
+
+int sai_device_status(int* out_bits, int clear, sai_stream_t stream) {
+  if (!out_bits) return SAI_ERR_NULL;
+  int dev, sms;
+  int* st;
+  if (!device_setup(&dev, &st, &sms)) return SAI_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int bits = 0;
+  if (cudaMemcpyAsync(&bits, st, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return SAI_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SAI_ERR_CUDA;
+  if (clear && bits) {
+    if (cudaMemsetAsync(st, 0, sizeof(int), s) != cudaSuccess) return SAI_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SAI_ERR_CUDA;
+  }
+  *out_bits = bits;
+  return bits ? SAI_ERR_DEVICE_CHECK : SAI_OK;
+}
+
+size_t sai_topk_transform_workspace(int64_t rows, int64_t score_stride, int32_t k) {
+  if (rows <= 0 || score_stride <= 0 || k != SAI_TOPK) return 0;
+  int dev, sms;
+  int* st;
+  if (!device_setup(&dev, &st, &sms)) return 0;
+  return sai::topk_plan(rows, score_stride, sms).workspace_bytes;
+}
+
+int sai_topk_transform(const float* scores, int64_t rows, int64_t score_stride, const int32_t* row_starts,
+                       const int32_t* seq_lens, const int32_t* page_tables, int64_t pt_rows, int64_t pt_stride,
+                       const int32_t* row_to_batch, int32_t page_size, int32_t k, int32_t* out_slots,
+                       int32_t* out_indices, void* workspace, size_t workspace_bytes, sai_stream_t stream) {
+  if (k <= 0 || rows < 0) return SAI_ERR_SHAPE;
+  if (k != SAI_TOPK) return SAI_ERR_UNSUPPORTED;
+  if (rows > INT_MAX / 16) return SAI_ERR_SHAPE;
+  if (!out_slots && !out_indices) return SAI_ERR_NULL;
+  if (rows == 0) return SAI_OK;
+  if (!scores || !seq_lens) return SAI_ERR_NULL;
+  if (score_stride < 1) return SAI_ERR_SHAPE;
+  if (out_slots && !page_tables) return SAI_ERR_NULL;
+  if (page_tables) {
+    if (page_size < 1 || pt_rows < 1 || pt_stride < 1) return SAI_ERR_SHAPE;
+    if (!row_to_batch && pt_rows < rows) return SAI_ERR_SHAPE;
+  }
+  if (!aligned(scores, 4) || !aligned(seq_lens, 4) || (row_starts && !aligned(row_starts, 4)) ||
+      (page_tables && !aligned(page_tables, 4)) || (row_to_batch && !aligned(row_to_batch, 4)) ||
+      (out_slots && !aligned(out_slots, 4)) || (out_indices && !aligned(out_indices, 4)))
+    return SAI_ERR_ALIGN;
+  int dev, sms;
+  int* st;
+  if (!device_setup(&dev, &st, &sms)) return SAI_ERR_CUDA;
+
+  sai::TopkPlan plan = sai::topk_plan(rows, score_stride, sms);
+  if (plan.chunks > 1 && (!workspace || workspace_bytes < plan.workspace_bytes || !aligned(workspace, 16)))
+    plan = sai::TopkPlan{1, 0, 0};
+
+  sai::TopkLaunch p{};
+  p.scores = scores;
+  p.stride = score_stride;
+  p.rows = static_cast<int>(rows);
+  p.row_starts = row_starts;
+  p.seq_lens = seq_lens;
+  p.page_tables = page_tables;
+  p.pt_rows = page_tables ? pt_rows : 0;
+  p.pt_stride = page_tables ? pt_stride : 0;
+  p.row_to_batch = row_to_batch;
+  p.page_size = page_tables ? page_size : 1;
+  p.out_slots = out_slots;
+  p.out_idx = out_indices;
+  p.chunks = plan.chunks;
+  p.chunk_len = plan.chunk_len;
+  if (plan.chunks > 1) {
+    const size_t units = static_cast<size_t>(rows) * plan.chunks;
+    char* w = static_cast<char*>(workspace);
+    p.part_key = reinterpret_cast<uint32_t*>(w);
+    p.part_idx = reinterpret_cast<int32_t*>(w + units * SAI_TOPK * 4);
+    p.part_cnt = reinterpret_cast<int*>(w + units * SAI_TOPK * 8);
+  }
+  p.status = st;
+  cudaError_t e = sai::launch_topk_transform(p, sms, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SAI_OK : SAI_ERR_CUDA;
+}
+
+}  // extern "C"

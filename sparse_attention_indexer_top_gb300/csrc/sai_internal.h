@@ -1,0 +1,67 @@
+// Internal launch interface between the C-ABI layer (sai_api.cu) and the
+// kernel translation units. Not part of the public header.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace sai {
+
+// Device status bits (OR-ed into the library's device status word).
+enum DevStatusBits : int {
+  kDevBadRowMeta = 1,      // a row's seq_len / row_start / row_to_batch was out of range
+  kDevWaitTimeout = 2,     // a pipeline wait gave up (the affected rows are undefined)
+  kDevBadPage = 4,         // a block-table entry was out of range (fused path)
+};
+
+struct TopkLaunch {
+  const float* scores;
+  long long stride;
+  int rows;
+  const int* row_starts;
+  const int* seq_lens;
+  const int* page_tables;
+  long long pt_rows, pt_stride;
+  const int* row_to_batch;
+  int page_size;
+  int* out_slots;
+  int* out_idx;
+  int chunks;      // work units per row (1 = one unit per row)
+  int chunk_len;   // window elements per unit when chunks > 1
+  uint32_t* part_key;  // [rows*chunks, 512] when chunks > 1
+  int32_t* part_idx;
+  int* part_cnt;       // [rows*chunks]
+  int* status;
+};
+
+// How a topk_transform call is split; shared by the workspace query and the
+// launcher so both always agree.
+struct TopkPlan {
+  int chunks;
+  int chunk_len;
+  size_t workspace_bytes;
+};
+
+TopkPlan topk_plan(long long rows, long long max_window, int num_sms);
+cudaError_t launch_topk_transform(const TopkLaunch& p, int num_sms, cudaStream_t stream);
+
+// Final merge of per-unit candidate lists (also used by the fused path).
+struct MergeLaunch {
+  int rows;
+  int units_per_row;
+  const uint32_t* part_key;
+  const int32_t* part_idx;
+  const int* part_cnt;
+  const int* seq_lens;         // for the padding count (may be null: use candidates)
+  const int* page_tables;
+  long long pt_rows, pt_stride;
+  const int* row_to_batch;
+  int page_size;
+  int* out_slots;
+  int* out_idx;
+  float* out_scores;           // optional: scores of the selected (fused path)
+  int* status;
+};
+cudaError_t launch_merge(const MergeLaunch& p, cudaStream_t stream);
+
+}  // namespace sai

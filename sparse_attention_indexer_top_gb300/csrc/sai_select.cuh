@@ -1,0 +1,279 @@
+// Shared-memory top-k building blocks used by every selection kernel:
+//   * order_key: fp32 -> uint32 key whose unsigned order is the score order;
+//   * append: warp-aggregated append of (key, index) candidates;
+//   * select_topk: exact top-K of a candidate list by (key desc, index asc)
+//     with range-based radix passes over 8-bit digits in shared memory;
+//   * bitonic_desc512: sort 512 (key, index) pairs, one per thread.
+//
+// The ordering rule (higher score first, equal scores to the lower row-local
+// index) is the deterministic order the library exposes; the pages of
+// sglang PR #37889 "[AMD] Enable GLM DSA prefill top-k to the v2 kernel"
+// define the window and page-table addressing (Modifications) but not the
+// order among the k outputs.
+#pragma once
+#include <cstdint>
+
+#include "sai_ptx.cuh"
+
+namespace sai {
+
+constexpr int kTopK = 512;
+
+// -0.0 is folded into +0.0 first (the two compare equal as scores).
+__device__ __forceinline__ uint32_t order_key(float x) {
+  uint32_t u = __float_as_uint(__fadd_rn(x, 0.0f));
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+struct SelectScratch {
+  uint32_t hist[256];
+  uint32_t wmin[32], wmax[32], wcnt[32];
+  uint32_t vmin, vmax, nact;
+  uint32_t bin, need_after, bin_count;
+  int out_cnt;
+  uint32_t tau;
+};
+
+// Result of a threshold search over a set of uint32 values: the selected
+// values are those whose offset (v - base) >> lo is > prefix, plus, among
+// the ones equal to prefix, either all of them (all_eq) or `need` of them.
+struct Threshold {
+  uint32_t base, prefix, need;
+  int lo;
+  bool all_eq;
+};
+
+__device__ __forceinline__ uint32_t shr64(uint32_t o, int lo) {
+  return static_cast<uint32_t>(static_cast<uint64_t>(o) >> lo);
+}
+
+// Find the threshold bin of the `need` largest values among the active
+// entries j in [0, n) (active/value given by `get(j, v)`). All NT threads of
+// the group call it; `bar` is the group's named barrier id. `need` must not
+// exceed the number of active entries.
+template <int NT, typename Get>
+__device__ Threshold radix_threshold(int n, uint32_t need, SelectScratch& sc, int tid, int bar, Get get) {
+  constexpr int NW = NT / 32;
+  const int lane = tid & 31, warp = tid >> 5;
+  uint32_t lmin = 0xFFFFFFFFu, lmax = 0u, lcnt = 0u;
+  for (int j = tid; j < n; j += NT) {
+    uint32_t v;
+    if (get(j, v)) {
+      lmin = min(lmin, v);
+      lmax = max(lmax, v);
+      ++lcnt;
+    }
+  }
+  lmin = __reduce_min_sync(0xFFFFFFFFu, lmin);
+  lmax = __reduce_max_sync(0xFFFFFFFFu, lmax);
+  lcnt = __reduce_add_sync(0xFFFFFFFFu, lcnt);
+  if (lane == 0) {
+    sc.wmin[warp] = lmin;
+    sc.wmax[warp] = lmax;
+    sc.wcnt[warp] = lcnt;
+  }
+  named_bar(bar, NT);
+  if (warp == 0) {
+    uint32_t a = lane < NW ? sc.wmin[lane] : 0xFFFFFFFFu;
+    uint32_t b = lane < NW ? sc.wmax[lane] : 0u;
+    uint32_t c = lane < NW ? sc.wcnt[lane] : 0u;
+    a = __reduce_min_sync(0xFFFFFFFFu, a);
+    b = __reduce_max_sync(0xFFFFFFFFu, b);
+    c = __reduce_add_sync(0xFFFFFFFFu, c);
+    if (lane == 0) {
+      sc.vmin = a;
+      sc.vmax = b;
+      sc.nact = c;
+    }
+  }
+  named_bar(bar, NT);
+  Threshold t;
+  t.base = sc.vmin;
+  const uint32_t span = sc.vmax - sc.vmin;
+  t.lo = span ? 32 - __clz(span) : 0;
+  t.prefix = 0;
+  t.need = need;
+  t.all_eq = (sc.nact == need);
+  while (t.lo > 0 && !t.all_eq) {
+    const int dlo = t.lo > 8 ? t.lo - 8 : 0;
+    const int dbits = t.lo - dlo;
+    const uint32_t dmask = (1u << dbits) - 1u;
+    for (int i = tid; i < 256; i += NT) sc.hist[i] = 0;
+    named_bar(bar, NT);
+    for (int j = tid; j < n; j += NT) {
+      uint32_t v;
+      if (get(j, v)) {
+        const uint32_t o = v - t.base;
+        if (shr64(o, t.lo) == t.prefix) atomicAdd(&sc.hist[(o >> dlo) & dmask], 1u);
+      }
+    }
+    named_bar(bar, NT);
+    if (warp == 0) {
+      // Lane l owns bins [8l, 8l+8); scan from the top bin down.
+      uint32_t h[8];
+      uint32_t tot = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        h[i] = sc.hist[lane * 8 + i];
+        tot += h[i];
+      }
+      // inclusive suffix sum over lanes (lane 31 holds the highest bins)
+      uint32_t suf = tot;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        uint32_t o = __shfl_down_sync(0xFFFFFFFFu, suf, d);
+        if (lane + d < 32) suf += o;
+      }
+      uint32_t above = suf - tot;  // count in bins of higher lanes
+      const uint32_t nd = t.need;
+      if (above < nd && nd <= suf) {
+#pragma unroll
+        for (int i = 7; i >= 0; --i) {
+          if (above < nd && nd <= above + h[i]) {
+            sc.bin = lane * 8 + i;
+            sc.need_after = nd - above;
+            sc.bin_count = h[i];
+          }
+          above += h[i];
+        }
+      }
+    }
+    named_bar(bar, NT);
+    t.prefix = (t.prefix << dbits) | sc.bin;
+    t.need = sc.need_after;
+    t.all_eq = (sc.bin_count == t.need);
+    t.lo = dlo;
+  }
+  return t;
+}
+
+__device__ __forceinline__ int thr_cmp(const Threshold& t, uint32_t v) {
+  const uint32_t hi = shr64(v - t.base, t.lo);
+  return hi > t.prefix ? 1 : (hi == t.prefix ? 0 : -1);
+}
+
+// Keep the top K of ckey/cidx[0, n) by (key desc, index asc); the survivors
+// are moved to [0, K) (in no particular order) through `aux_key/aux_idx`
+// (K entries). Returns a valid strict filter threshold: every entry not
+// kept, and every later entry (larger index) with key <= the returned
+// value, is outside the top K. Requires n > K.
+template <int NT>
+__device__ uint32_t select_topk(uint32_t* ckey, int32_t* cidx, int n, int K, uint32_t* aux_key,
+                                int32_t* aux_idx, SelectScratch& sc, int tid, int bar) {
+  const Threshold t = radix_threshold<NT>(n, (uint32_t)K, sc, tid, bar, [&](int j, uint32_t& v) {
+    v = ckey[j];
+    return true;
+  });
+  Threshold ti{};
+  bool ties = !t.all_eq;
+  if (ties) {
+    // All tied entries carry the same key; take the t.need lowest indices.
+    ti = radix_threshold<NT>(n, t.need, sc, tid, bar, [&](int j, uint32_t& v) {
+      v = 0x7FFFFFFFu - static_cast<uint32_t>(cidx[j]);
+      return thr_cmp(t, ckey[j]) == 0;
+    });
+  }
+  if (tid == 0) sc.out_cnt = 0;
+  named_bar(bar, NT);
+  const int lane = tid & 31;
+  for (int j0 = 0; j0 < n; j0 += NT) {
+    const int j = j0 + tid;
+    bool sel = false;
+    uint32_t key = 0;
+    int32_t idx = 0;
+    if (j < n) {
+      key = ckey[j];
+      idx = cidx[j];
+      const int c = thr_cmp(t, key);
+      sel = c > 0 || (c == 0 && (!ties || thr_cmp(ti, 0x7FFFFFFFu - static_cast<uint32_t>(idx)) >= 0));
+    }
+    const uint32_t m = __ballot_sync(0xFFFFFFFFu, sel);
+    if (m) {
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&sc.out_cnt, __popc(m));
+      base = __shfl_sync(0xFFFFFFFFu, base, 0);
+      if (sel) {
+        const int pos = base + __popc(m & ((1u << lane) - 1u));
+        if (pos < K) {  // exactly K are selected; the guard only bounds the buffer
+          aux_key[pos] = key;
+          aux_idx[pos] = idx;
+        }
+      }
+    }
+  }
+  named_bar(bar, NT);
+  for (int j = tid; j < K; j += NT) {
+    ckey[j] = aux_key[j];
+    cidx[j] = aux_idx[j];
+  }
+  // lowest key of the threshold bin: <= the K-th key
+  const uint32_t tau = t.base + static_cast<uint32_t>(static_cast<uint64_t>(t.prefix) << t.lo);
+  named_bar(bar, NT);
+  return tau;
+}
+
+// Append the entries of keys/idxs whose bit is set in `mask` at positions
+// base + (running count in *counter); one shared atomic per warp.
+template <int M>
+__device__ __forceinline__ void append_masked(uint32_t* ckey, int32_t* cidx, int base, int* counter,
+                                              const uint32_t (&keys)[M], const int32_t (&idxs)[M], uint32_t mask,
+                                              int lane) {
+  const int m = __popc(mask);
+  if (!__any_sync(0xFFFFFFFFu, m > 0)) return;
+  int incl = m;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += o;
+  }
+  int start = 0;
+  if (lane == 31) start = atomicAdd(counter, incl);
+  int pos = __shfl_sync(0xFFFFFFFFu, start, 31) + base + incl - m;
+#pragma unroll
+  for (int i = 0; i < M; ++i) {
+    if (mask & (1u << i)) {
+      ckey[pos] = keys[i];
+      cidx[pos] = idxs[i];
+      ++pos;
+    }
+  }
+}
+
+// Composite sort key: key in the high word, bit-inverted index in the low
+// word, so a larger composite means higher score, then lower index. Padding
+// entries use 0, which sorts after every real entry.
+__device__ __forceinline__ unsigned long long composite(uint32_t key, int32_t idx) {
+  return (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(idx));
+}
+
+// Sort 512 composites into descending order, one per thread (tid < 512),
+// using warp shuffles for strides < 32 and `buf` (512 entries) otherwise.
+__device__ __forceinline__ unsigned long long bitonic_desc512(unsigned long long v, unsigned long long* buf, int tid,
+                                                              int bar) {
+#pragma unroll 1
+  for (int size = 2; size <= 512; size <<= 1) {
+    const bool asc = (tid & size) != 0;
+#pragma unroll 1
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      unsigned long long p;
+      if (stride >= 32) {
+        buf[tid] = v;
+        named_bar(bar, 512);
+        p = buf[tid ^ stride];
+        named_bar(bar, 512);
+      } else {
+        p = __shfl_xor_sync(0xFFFFFFFFu, v, stride);
+      }
+      const bool lower = (tid & stride) == 0;
+      const bool keep_max = (lower != asc);
+      v = keep_max ? (v > p ? v : p) : (v < p ? v : p);
+    }
+  }
+  return v;
+}
+
+}  // namespace sai

@@ -1,0 +1,77 @@
+"""The C-ABI library loads, exports every symbol include/sai.h declares, and
+rejects bad host arguments before touching the GPU (CPU only)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_attention_indexer_top_gb300 import build, _lib
+
+    build.build()
+    return _lib.load()
+
+
+def _declared():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", h)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names += re.findall(r"\b(sai_\w+)\s*\(", txt)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(lib):
+    from sparse_attention_indexer_top_gb300._lib import SIGNATURES
+
+    names = _declared()
+    assert names, "no declarations found"
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in SIGNATURES, f"{n} has no ctypes signature"
+
+
+def test_status_strings(lib):
+    from sparse_attention_indexer_top_gb300._lib import status_string
+
+    assert status_string(0) == "ok"
+    assert "NULL" in status_string(-1)
+    assert status_string(12345) == "unknown status"
+
+
+def _call(lib, **kw):
+    a = dict(scores=1 << 20, rows=4, stride=4096, row_starts=None, seq_lens=1 << 21, pt=1 << 22, pt_rows=4,
+             pt_stride=4096, r2b=None, ps=1, k=512, out_slots=1 << 23, out_idx=None, ws=None, ws_bytes=0)
+    a.update(kw)
+    v = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.sai_topk_transform(v(a["scores"]), a["rows"], a["stride"], v(a["row_starts"]), v(a["seq_lens"]),
+                                  v(a["pt"]), a["pt_rows"], a["pt_stride"], v(a["r2b"]), a["ps"], a["k"],
+                                  v(a["out_slots"]), v(a["out_idx"]), v(a["ws"]), a["ws_bytes"], None)
+
+
+def test_host_validation(lib):
+    # every case below is rejected before any CUDA call
+    assert _call(lib, k=0) == -2
+    assert _call(lib, k=256) == -3
+    assert _call(lib, rows=-1) == -2
+    assert _call(lib, out_slots=None, out_idx=None) == -1
+    assert _call(lib, scores=None) == -1
+    assert _call(lib, seq_lens=None) == -1
+    assert _call(lib, pt=None) == -1  # slots requested without a page table
+    assert _call(lib, ps=0) == -2
+    assert _call(lib, pt_rows=3) == -2  # fewer page-table rows than rows, no row_to_batch
+    assert _call(lib, stride=0) == -2
+    assert _call(lib, scores=(1 << 20) + 2) == -7  # fp32 pointer not 4-byte aligned
+    assert _call(lib, rows=0) == 0  # nothing to do
+
+
+def test_workspace_query_without_args(lib):
+    assert lib.sai_topk_transform_workspace(0, 100, 512) == 0
+    assert lib.sai_topk_transform_workspace(10, 100, 256) == 0

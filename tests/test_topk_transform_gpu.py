@@ -1,0 +1,159 @@
+"""GPU parity of sai_topk_transform against the CPU oracle (bit-exact).
+
+Indices and slots are integer outputs selected from given fp32 scores, so
+they must equal the oracle's exactly, element by element.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle.topk import topk_transform as oracle_topk
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+def _t(a):
+    return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def _run(inp, force_single=False, scores_t=None):
+    import sparse_attention_indexer_top_gb300 as sai
+
+    ws = torch.empty(16, dtype=torch.uint8, device=DEV) if force_single else None
+    s = _t(inp.scores) if scores_t is None else scores_t
+    slots, idx = sai.topk_transform(s, _t(inp.seq_lens), _t(inp.page_tables), page_size=inp.page_size,
+                                    row_starts=_t(inp.row_starts), row_to_batch=_t(inp.row_to_batch),
+                                    want_indices=True, workspace=ws)
+    torch.cuda.synchronize()
+    assert sai.device_status() == 0
+    return slots.cpu().numpy(), idx.cpu().numpy()
+
+
+def _oracle(inp, rows=None):
+    return oracle_topk(inp.scores, inp.seq_lens, inp.page_tables, inp.page_size, 512, inp.row_starts,
+                       inp.row_to_batch, rows=rows)
+
+
+def _assert_equal(got, ref, what=""):
+    gs, gi = got
+    rs, ri = ref
+    bad = np.flatnonzero((gi != ri).any(axis=1) | (gs != rs).any(axis=1))
+    assert bad.size == 0, f"{what}: {bad.size} rows differ, first {bad[:5]}"
+
+
+def test_tiny_decode():
+    inp = W.tiny_decode()
+    _assert_equal(_run(inp), _oracle(inp), "tiny decode")
+
+
+@pytest.mark.parametrize("single", [False, True])
+def test_decode_bf16_ties(single):
+    inp = W.decode_topk()
+    _assert_equal(_run(inp, force_single=single), _oracle(inp), f"decode single={single}")
+
+
+@pytest.mark.parametrize("kind", ["normal", "bf16", "int", "const", "signed_zero", "inf", "ascending", "descending"])
+@pytest.mark.parametrize("single", [False, True])
+def test_value_kinds(kind, single):
+    lens = [0, 1, 3, 7, 9, 100, 511, 512, 513, 2047, 2048, 2049, 6000, 9001, 20000, 33333]
+    inp = W.make_topk_inputs(31, lens, 33340, 128, (len(lens), 261), kind=kind, fill=np.inf)
+    _assert_equal(_run(inp, force_single=single), _oracle(inp), kind)
+
+
+@pytest.mark.parametrize("stride_pad", [0, 1, 2, 3])
+def test_packed_extend_ragged(stride_pad):
+    # stride not a multiple of 4 and odd row starts: scalar heads/tails
+    inp = W.packed_extend(seed=12, reqs=3, new_tokens=97, kv_len=12345, fill=np.inf, stride_pad=stride_pad)
+    _assert_equal(_run(inp), _oracle(inp), f"packed pad={stride_pad}")
+    _assert_equal(_run(inp, force_single=True), _oracle(inp), f"packed single pad={stride_pad}")
+
+
+def test_unaligned_base_pointer():
+    inp = W.packed_extend(seed=13, reqs=2, new_tokens=50, kv_len=7001, fill=np.inf)
+    big = np.full((inp.rows, inp.scores.shape[1] + 1), np.inf, np.float32)
+    big[:, 1:] = inp.scores
+    view = _t(big)[:, 1:]  # base pointer 4 bytes past a 16-byte boundary
+    _assert_equal(_run(inp, scores_t=view), _oracle(inp), "unaligned base")
+
+
+def test_many_rows_single_unit_path():
+    inp = W.packed_extend(seed=14, reqs=2, new_tokens=400, kv_len=3000, fill=np.inf)
+    _assert_equal(_run(inp), _oracle(inp), "many rows")
+
+
+def test_packed_equals_decode_layout():
+    inp = W.packed_extend(seed=15, reqs=2, new_tokens=64, kv_len=9000, fill=np.inf)
+    got_packed = _run(inp)
+    dec = np.zeros((inp.rows, 9000), np.float32)
+    pt = np.zeros((inp.rows, 9000), np.int32)
+    for i in range(inp.rows):
+        s0, n = int(inp.row_starts[i]), int(inp.seq_lens[i])
+        dec[i, :n] = inp.scores[i, s0:s0 + n]
+        pt[i] = inp.page_tables[inp.row_to_batch[i]]
+    dinp = W.TopkInputs(dec, inp.seq_lens, pt, 1)
+    got_dec = _run(dinp)
+    _assert_equal(got_packed, got_dec, "packed vs decode layout")
+
+
+def test_indices_only_without_page_table():
+    import sparse_attention_indexer_top_gb300 as sai
+
+    inp = W.tiny_decode(seed=9)
+    idx = sai.topk_transform(_t(inp.scores), _t(inp.seq_lens))
+    torch.cuda.synchronize()
+    assert np.array_equal(idx.cpu().numpy(), _oracle(inp)[1])
+
+
+def test_bad_row_metadata_is_flagged_and_emptied():
+    import sparse_attention_indexer_top_gb300 as sai
+
+    inp = W.make_topk_inputs(5, [100, 600, 700], 1000, 1, (3, 1000), row_starts=[0, 500, 0])
+    # row 1: start 500 + 600 > stride 1000 -> rejected on the device
+    slots, idx = sai.topk_transform(_t(inp.scores), _t(inp.seq_lens), _t(inp.page_tables),
+                                    row_starts=_t(inp.row_starts), want_indices=True)
+    bits = sai.device_status(clear=True)
+    assert bits & 1
+    ref = _oracle(inp, rows=[0, 2])
+    assert np.array_equal(idx.cpu().numpy()[[0, 2]], ref[1])
+    assert (idx.cpu().numpy()[1] == -1).all() and (slots.cpu().numpy()[1] == -1).all()
+    assert sai.device_status() == 0
+
+
+def test_packed_extend_full_size_sampled():
+    """The packed-extend prefill workload at full size ([16384, 140000]
+    scores, two requests on a 70000-token KV, +inf outside the windows), in
+    the launch configuration the benchmark times; sampled rows are checked
+    against the oracle, every row against the output invariants."""
+    import sparse_attention_indexer_top_gb300 as sai
+
+    row_starts, seq_lens, r2b, width = W.packed_extend_meta()
+    rows = seq_lens.size
+    scores = torch.empty((rows, width), dtype=torch.float32, device=DEV)
+    chunk = 1024
+    host = torch.empty((chunk, width), dtype=torch.float32).pin_memory()
+    hn = host.numpy()
+    for r0 in range(0, rows, chunk):
+        W.fill_rows(hn, r0, 3, row_starts, seq_lens, fill=np.inf)
+        scores[r0:r0 + chunk].copy_(host)
+    pt = W.page_table_perm(3, (2, 70000))
+    slots, idx = sai.topk_transform(scores, _t(seq_lens), _t(pt), row_starts=_t(row_starts),
+                                    row_to_batch=_t(r2b), want_indices=True)
+    torch.cuda.synchronize()
+    assert sai.device_status() == 0
+    gi = idx.cpu().numpy()
+    gs = slots.cpu().numpy()
+    # every row: 512 distinct in-window indices, slots = transform of them
+    assert (gi >= 0).all() and (gi < seq_lens[:, None]).all()
+    srt = np.sort(gi, axis=1)
+    assert (srt[:, 1:] != srt[:, :-1]).all()
+    assert np.array_equal(gs, pt[r2b[:, None], gi])
+    for i in list(range(0, rows, 331)) + [8191, 8192, rows - 1]:
+        n = int(seq_lens[i])
+        w = W.packed_extend_window(3, i, n)
+        rs, ri = oracle_topk(w[None, :], np.array([n]), pt[[r2b[i]]], 1, 512)
+        assert np.array_equal(gi[i], ri[0]), i
+        assert np.array_equal(gs[i], rs[0]), i

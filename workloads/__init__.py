@@ -18,4 +18,6 @@ from .gen import (  # noqa: F401
     packed_extend_window,
     fused_decode,
     fused_prefill,
+    page_table_perm,
+    fill_rows,
 )

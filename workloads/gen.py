@@ -160,10 +160,33 @@ def make_topk_inputs(
     else:
         for i in range(rows):
             fill_row(i)
-    pt_rows, pt_stride = pt_shape
-    pt = _rng(seed, 202).permutation(pt_rows * pt_stride).astype(np.int32).reshape(pt_rows, pt_stride)
+    pt = page_table_perm(seed, pt_shape)
     r2b = None if row_to_batch is None else np.asarray(row_to_batch, dtype=np.int32)
     return TopkInputs(scores, seq_lens, pt, page_size, k, starts, r2b, name)
+
+
+def page_table_perm(seed: int, pt_shape) -> np.ndarray:
+    """One random permutation of the slot ids, reshaped to ``pt_shape``."""
+    pt_rows, pt_stride = pt_shape
+    return _rng(seed, 202).permutation(pt_rows * pt_stride).astype(np.int32).reshape(pt_rows, pt_stride)
+
+
+def fill_rows(dst: np.ndarray, r0: int, seed: int, row_starts, seq_lens, kind: str = "normal",
+              fill: float = 0.0, threads: int = 0) -> None:
+    """Write score rows ``r0 .. r0 + len(dst) - 1`` of a buffer into ``dst``
+    (same values as ``make_topk_inputs`` gives those rows)."""
+    def one(j: int) -> None:
+        i = r0 + j
+        n = int(seq_lens[i])
+        s = 0 if row_starts is None else int(row_starts[i])
+        dst[j, :s] = fill
+        dst[j, s + max(n, 0):] = fill
+        if n > 0:
+            dst[j, s:s + n] = _row_values(seed, i, n, kind)
+
+    nthreads = threads or min(16, os.cpu_count() or 1)
+    with _cf.ThreadPoolExecutor(nthreads) as ex:
+        list(ex.map(one, range(dst.shape[0])))
 
 
 def tiny_decode(seed: int = 1) -> TopkInputs:
