@@ -111,10 +111,10 @@ def test_indices_only_without_page_table():
 def test_bad_row_metadata_is_flagged_and_emptied():
     import sparse_attention_indexer_top_gb300 as sai
 
-    inp = W.make_topk_inputs(5, [100, 600, 700], 1000, 1, (3, 1000), row_starts=[0, 500, 0])
-    # row 1: start 500 + 600 > stride 1000 -> rejected on the device
+    inp = W.make_topk_inputs(5, [100, 600, 700], 1000, 1, (3, 1000), row_starts=[0, 0, 0])
+    bad_starts = np.array([0, 500, 0], np.int32)  # row 1: 500 + 600 > stride 1000
     slots, idx = sai.topk_transform(_t(inp.scores), _t(inp.seq_lens), _t(inp.page_tables),
-                                    row_starts=_t(inp.row_starts), want_indices=True)
+                                    row_starts=_t(bad_starts), want_indices=True)
     bits = sai.device_status(clear=True)
     assert bits & 1
     ref = _oracle(inp, rows=[0, 2])
