@@ -109,6 +109,40 @@ int sai_topk_transform(const float* scores, int64_t rows, int64_t score_stride, 
                        const int32_t* row_to_batch, int32_t page_size, int32_t k, int32_t* out_slots,
                        int32_t* out_indices, void* workspace, size_t workspace_bytes, sai_stream_t stream);
 
+/*
+ * Size of the library-owned device scratch used by
+ * sai_topk_transform_noalloc: 8 MiB, held on every GPU that loads the
+ * library until the process exits.
+ */
+#define SAI_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * sai_topk_transform_noalloc -- sai_topk_transform without a workspace
+ * argument, for callers that cannot allocate device memory where they need
+ * the top-k (inside an allocator callback or a region that forbids
+ * allocation, a pool owner whose memory is all handed out, or code with no
+ * allocator beyond its fixed input and output buffers). The paper has no
+ * counterpart: this entry point exists only for such callers.
+ *
+ * Arguments, outputs, ordering and errors are those of sai_topk_transform.
+ * Instead of a caller workspace, the split path for few long rows uses a
+ * fixed library-owned device array of SAI_NOALLOC_SCRATCH_BYTES. Calls
+ * whose sizes need more scratch than that (as reported by
+ * sai_topk_transform_workspace) are rejected with SAI_ERR_WORKSPACE before
+ * anything is launched. Nothing is allocated: no cudaMalloc, no cudaFree.
+ *
+ * The first call on a device looks up the array's device address with that
+ * device current; make that first call before any stream capture. All calls
+ * on a device share the one array and it keeps the previous call's contents
+ * (nothing in it needs to start at zero). Calls that can overlap on the GPU
+ * (different streams without ordering between them) race on the array and
+ * must be serialized by the caller.
+ */
+int sai_topk_transform_noalloc(const float* scores, int64_t rows, int64_t score_stride, const int32_t* row_starts,
+                               const int32_t* seq_lens, const int32_t* page_tables, int64_t pt_rows,
+                               int64_t pt_stride, const int32_t* row_to_batch, int32_t page_size, int32_t k,
+                               int32_t* out_slots, int32_t* out_indices, sai_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -93,3 +93,24 @@ def topk_transform(scores: torch.Tensor, seq_lens: torch.Tensor, page_tables: Op
     if out_slots is None:
         return out_indices
     return (out_slots, out_indices) if (want_indices or out_indices is not None) else out_slots
+
+
+def topk_transform_noalloc(scores: torch.Tensor, seq_lens: torch.Tensor, page_tables: torch.Tensor, *,
+                           out_slots: torch.Tensor, out_indices: Optional[torch.Tensor] = None, page_size: int = 1,
+                           k: int = TOPK, row_starts: Optional[torch.Tensor] = None,
+                           row_to_batch: Optional[torch.Tensor] = None, stream=None) -> None:
+    """``topk_transform`` for callers that cannot allocate device memory.
+
+    The caller supplies the output buffers; the split path's scratch is a
+    fixed library-owned device array, so this wrapper allocates nothing.
+    Calls that would need more scratch than that array holds raise
+    ``SaiError`` (workspace). Calls that may overlap on the GPU share the
+    array and must be serialized by the caller.
+    """
+    rows = scores.shape[0]
+    stride = scores.stride(0) if rows > 1 else max(scores.shape[1], 1)
+    st = load().sai_topk_transform_noalloc(
+        _ptr(scores), rows, stride, _ptr(row_starts), _ptr(seq_lens), _ptr(page_tables), page_tables.shape[0],
+        page_tables.stride(0), _ptr(row_to_batch), int(page_size), int(k), _ptr(out_slots), _ptr(out_indices),
+        _stream(stream))
+    check(st, "sai_topk_transform_noalloc")
