@@ -104,12 +104,12 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- workload
-def build_inputs(pinned: bool):
+def build_inputs(pinned: bool, new_tokens: int = 8192):
     import torch
 
     import workloads as W
 
-    row_starts, seq_lens, r2b, width = W.packed_extend_meta()
+    row_starts, seq_lens, r2b, width = W.packed_extend_meta(new_tokens=new_tokens)
     rows = int(seq_lens.size)
     host = torch.empty((rows, width), dtype=torch.float32, pin_memory=pinned)
     hn = host.numpy()
@@ -192,7 +192,7 @@ def run_gpu(args):
     sai.load()
     hbm_peak, _, peak_kind = _peaks()
 
-    host, meta = build_inputs(pinned=True)
+    host, meta = build_inputs(pinned=True, new_tokens=args.new_tokens)
     rows, width = meta["rows"], meta["width"]
     scores = torch.empty((rows, width), dtype=torch.float32, device=dev)
     scores.copy_(host, non_blocking=False)
@@ -237,7 +237,7 @@ def run_gpu(args):
     keys = float(meta["seq_lens"].astype(np.int64).sum())
 
     # end to end: pinned host scores -> device, kernel, slots -> host
-    e2e_steps = max(1, min(3, args.steps))
+    e2e_steps = 0 if args.no_e2e else max(1, min(3, args.steps))
     host_out = torch.empty((rows, K), dtype=torch.int32, pin_memory=True)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -250,7 +250,7 @@ def run_gpu(args):
             host_out.copy_(out_slots, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_ms = e0.elapsed_time(e1) / max(1, e2e_steps)
     h2d = host.numel() * 4
     d2h = rows * K * 4
 
@@ -271,7 +271,8 @@ def run_gpu(args):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "traffic": None, "peak_kind": peak_kind,
                          "kernel": "topk_stream_kernel"},
-            "e2e": {"value": rows / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "e2e": None if args.no_e2e else {"value": rows / (e2e_ms * 1e-3), "unit": UNIT,
+                                             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
@@ -289,6 +290,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--new-tokens", type=int, default=8192,
+                    help="query rows per request (8192 = the full packed-extend chunk; smaller for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
