@@ -104,12 +104,16 @@ __device__ Threshold radix_threshold(int n, uint32_t need, SelectScratch& sc, in
     const uint32_t dmask = (1u << dbits) - 1u;
     for (int i = tid; i < 256; i += NT) sc.hist[i] = 0;
     named_bar(bar, NT);
-    for (int j = tid; j < n; j += NT) {
-      uint32_t v;
-      if (get(j, v)) {
+    for (int j0 = 0; j0 < n; j0 += NT) {
+      const int j = j0 + tid;
+      uint32_t v, bin = 0xFFFFFFFFu;
+      if (j < n && get(j, v)) {
         const uint32_t o = v - t.base;
-        if (shr64(o, t.lo) == t.prefix) atomicAdd(&sc.hist[(o >> dlo) & dmask], 1u);
+        if (shr64(o, t.lo) == t.prefix) bin = (o >> dlo) & dmask;
       }
+      // one shared atomic per distinct bin in the warp
+      const uint32_t peers = __match_any_sync(0xFFFFFFFFu, bin);
+      if (bin != 0xFFFFFFFFu && lane == __ffs(peers) - 1) atomicAdd(&sc.hist[bin], (uint32_t)__popc(peers));
     }
     named_bar(bar, NT);
     if (warp == 0) {

@@ -201,7 +201,9 @@ __device__ void consumers(const TopkLaunch& p, Smem& S, int tid) {
   while (true) {
     const int slot = it % kNStage;
     const uint32_t ph = (it / kNStage) & 1u;
-    const bool ok = named_bar_and(kBarConsumers, kConsumers, mbar_wait(&S.full[slot], ph));
+    // One thread polls the mbarrier; the others sleep in the named barrier,
+    // which also publishes the stage (and any timeout) to all consumers.
+    const bool ok = named_bar_and(kBarConsumers, kConsumers, tid == 0 ? mbar_wait(&S.full[slot], ph) : true);
     if (!ok) {
       if (tid == 0) atomicOr(p.status, kDevWaitTimeout);
       return;
