@@ -280,4 +280,236 @@ __device__ __forceinline__ unsigned long long bitonic_desc512(unsigned long long
   return v;
 }
 
+// ------------------------------------------------------------------------
+// Block-wide helpers for a 512-thread group (named barrier `bar`).
+
+// Exclusive prefix sum of `c` over the group; *total receives the sum.
+__device__ __forceinline__ int block_exscan512(int c, int* total, uint32_t* wsum, int tid, int bar) {
+  const int lane = tid & 31, warp = tid >> 5;
+  int incl = c;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += o;
+  }
+  if (lane == 31) wsum[warp] = (uint32_t)incl;
+  named_bar(bar, 512);
+  int off = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < 16; ++w) {
+    const int v = (int)wsum[w];
+    off += w < warp ? v : 0;
+    tot += v;
+  }
+  *total = tot;
+  return off + incl - c;
+}
+
+// Threshold bin over a 4096-bin histogram of key >> 20 (8 bins per thread):
+// the bin B with count(bins > B) < need <= count(bins >= B). Returns -1 if
+// the histogram holds fewer than `need`. *need_in_bin / *bin_count describe
+// the cut inside B. Two barriers; `wsum` needs 16 words.
+struct BinCut {
+  int bin;
+  uint32_t need_in_bin;
+  uint32_t bin_count;
+};
+
+__device__ __forceinline__ BinCut hist_cut4096(const uint32_t* hist, uint32_t need, uint32_t* wsum, uint32_t* bcast,
+                                               int tid, int bar) {
+  const int lane = tid & 31, warp = tid >> 5;
+  const uint4 a = reinterpret_cast<const uint4*>(hist)[2 * tid];
+  const uint4 b = reinterpret_cast<const uint4*>(hist)[2 * tid + 1];
+  const uint32_t h[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t s = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) s += h[i];
+  // inclusive suffix sum across lanes (higher lanes own higher bins)
+  uint32_t suf = s;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t o = __shfl_down_sync(0xFFFFFFFFu, suf, d);
+    if (lane + d < 32) suf += o;
+  }
+  if (lane == 0) wsum[warp] = suf;  // warp total
+  if (tid == 0) bcast[0] = 0xFFFFFFFFu;
+  named_bar(bar, 512);
+  uint32_t above_w = 0;
+#pragma unroll
+  for (int w = 0; w < 16; ++w) above_w += w > warp ? wsum[w] : 0u;
+  uint32_t above = above_w + suf - s;
+  if (above < need && need <= above + s) {
+#pragma unroll
+    for (int i = 7; i >= 0; --i) {
+      if (above < need && need <= above + h[i]) {
+        bcast[0] = (uint32_t)(8 * tid + i);
+        bcast[1] = need - above;
+        bcast[2] = h[i];
+      }
+      above += h[i];
+    }
+  }
+  named_bar(bar, 512);
+  BinCut c;
+  c.bin = bcast[0] == 0xFFFFFFFFu ? -1 : (int)bcast[0];
+  c.need_in_bin = bcast[1];
+  c.bin_count = bcast[2];
+  return c;
+}
+
+// Keep the entries of ckey/cidx[0, n) with key >= tau, compacted to the
+// front (order not kept). Returns the new count. CAPT bounds n.
+template <int CAPT>
+__device__ __forceinline__ int compact_ge(uint32_t* ckey, int32_t* cidx, int n, uint32_t tau, uint32_t* wsum,
+                                          int tid, int bar) {
+  constexpr int M = (CAPT + 511) / 512;
+  uint32_t k[M];
+  int32_t ix[M];
+  uint32_t keep = 0;
+  int c = 0;
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    const int j = tid + 512 * m;
+    k[m] = 0;
+    ix[m] = 0;
+    if (j < n) {
+      k[m] = ckey[j];
+      ix[m] = cidx[j];
+      if (k[m] >= tau) {
+        keep |= 1u << m;
+        ++c;
+      }
+    }
+  }
+  int total;
+  int pos = block_exscan512(c, &total, wsum, tid, bar);  // its barrier orders all reads before the writes
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    if (keep & (1u << m)) {
+      ckey[pos] = k[m];
+      cidx[pos] = ix[m];
+      ++pos;
+    }
+  }
+  named_bar(bar, 512);
+  return total;
+}
+
+// Exact top-K (K = 512) of ckey/cidx[0, n), n > K, by (key desc, index asc),
+// written to aux_key/aux_idx[0, K). `hist` (4096 words) is scratch and is
+// left zeroed. CAPT bounds n.
+template <int CAPT>
+__device__ void fast_select512(const uint32_t* ckey, const int32_t* cidx, int n, uint32_t* hist, uint32_t* aux_key,
+                               int32_t* aux_idx, SelectScratch& sc, uint32_t* bcast, int tid, int bar) {
+  constexpr int K = kTopK;
+  constexpr int M = (CAPT + 511) / 512;
+  for (int j = tid; j < n; j += 512) atomicAdd(&hist[ckey[j] >> 20], 1u);
+  named_bar(bar, 512);
+  const BinCut cut = hist_cut4096(hist, K, sc.wmin, bcast, tid, bar);
+  const uint32_t B = (uint32_t)cut.bin;
+  // inside the threshold bin: exact cut by key, then by index for ties
+  Threshold t{};
+  t.all_eq = cut.bin_count == cut.need_in_bin;
+  Threshold ti{};
+  bool ties = false;
+  if (!t.all_eq) {
+    t = radix_threshold<512>(n, cut.need_in_bin, sc, tid, bar, [&](int j, uint32_t& v) {
+      v = ckey[j];
+      return (v >> 20) == B;
+    });
+    ties = !t.all_eq;
+    if (ties) {
+      ti = radix_threshold<512>(n, t.need, sc, tid, bar, [&](int j, uint32_t& v) {
+        v = 0x7FFFFFFFu - static_cast<uint32_t>(cidx[j]);
+        return (ckey[j] >> 20) == B && thr_cmp(t, ckey[j]) == 0;
+      });
+    }
+  }
+  // clear the histogram for the next user (8 words per thread)
+  reinterpret_cast<uint4*>(hist)[2 * tid] = make_uint4(0, 0, 0, 0);
+  reinterpret_cast<uint4*>(hist)[2 * tid + 1] = make_uint4(0, 0, 0, 0);
+  uint32_t selm = 0;
+  int c = 0;
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    const int j = tid + 512 * m;
+    if (j < n) {
+      const uint32_t key = ckey[j];
+      const uint32_t hb = key >> 20;
+      bool sel = hb > B;
+      if (hb == B) {
+        if (cut.bin_count == cut.need_in_bin) {
+          sel = true;
+        } else {
+          const int cc = thr_cmp(t, key);
+          sel = cc > 0 ||
+                (cc == 0 && (!ties || thr_cmp(ti, 0x7FFFFFFFu - static_cast<uint32_t>(cidx[j])) >= 0));
+        }
+      }
+      if (sel) {
+        selm |= 1u << m;
+        ++c;
+      }
+    }
+  }
+  int total;
+  int pos = block_exscan512(c, &total, sc.wcnt, tid, bar);
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    if (selm & (1u << m)) {
+      const int j = tid + 512 * m;
+      if (pos < K) {
+        aux_key[pos] = ckey[j];
+        aux_idx[pos] = cidx[j];
+      }
+      ++pos;
+    }
+  }
+  named_bar(bar, 512);
+}
+
+// Sort the `cnt` (<= 512) entries of aux_key/aux_idx by (key desc, index
+// asc). Each thread returns its entry's composite and its output rank;
+// threads tid >= cnt get composite 0 and rank tid (the padding positions).
+// `runs` needs 512 entries.
+__device__ __forceinline__ int rank_sort512(const uint32_t* aux_key, const int32_t* aux_idx, int cnt,
+                                            unsigned long long* runs, unsigned long long* out_v, int tid, int bar) {
+  const int lane = tid & 31, warp = tid >> 5;
+  unsigned long long v = tid < cnt ? composite(aux_key[tid], aux_idx[tid]) : 0ull;
+  // sort each warp's 32 entries descending
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+    const bool asc = (lane & size) != 0 && size < 32;
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const unsigned long long p = __shfl_xor_sync(0xFFFFFFFFu, v, stride);
+      const bool lower = (lane & stride) == 0;
+      const bool keep_max = (lower != asc);
+      v = keep_max ? (v > p ? v : p) : (v < p ? v : p);
+    }
+  }
+  runs[tid] = v;
+  named_bar(bar, 512);
+  int rank = lane;
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    if (r == warp) continue;
+    const unsigned long long* run = runs + 32 * r;
+    int pos = 0;
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1)
+      if (run[pos + s - 1] > v) pos += s;
+    rank += pos;
+  }
+  named_bar(bar, 512);  // runs may be reused after this
+  *out_v = v;
+  return rank;  // meaningful only when v != 0
+}
+
+// Float threshold equivalent to "order key >= tau" for every non-NaN x.
+__device__ __forceinline__ float tau_float(uint32_t tau) {
+  if (tau <= 0x007FFFFFu) return __int_as_float(0xFF800000);  // -inf: everything passes
+  return key_to_float(tau);
+}
+
 }  // namespace sai

@@ -41,14 +41,17 @@ namespace {
 
 constexpr int kConsumers = 512;                 // 16 consumer warps
 constexpr int kThreads = kConsumers + 32;       // + 1 producer warp
-constexpr int kStage = 2048;                    // floats per stage (8 KB)
-constexpr int kNStage = 6;                      // 48 KB in flight per CTA
-constexpr int kCap = 6144;                      // candidate capacity
+constexpr int kStage = 2048;                    // floats per stage (8 KB): one float4 per consumer
+constexpr int kNStage = 5;                      // 40 KB in flight per CTA
 constexpr int kExtra = 8;                       // scalar elements per descriptor
-constexpr int kCompactAt = kCap - kStage - kExtra;
+constexpr int kPruneAt = 2048;                  // prune the candidate list above this size
+constexpr int kCap = 4352;                      // >= kPruneAt + kStage + kExtra
+constexpr int kScanEvery = 256;                 // raise the threshold after this many appends
 constexpr int kBarConsumers = 1;                // named barrier id
 
 static_assert(kTopK == kConsumers, "the final sort keeps one entry per consumer thread");
+static_assert(kCap >= kPruneAt + kStage + kExtra, "candidate list overflow");
+static_assert(kStage == 4 * kConsumers, "one float4 per consumer per stage");
 
 struct StageDesc {
   int unit;   // -1: no more work
@@ -65,19 +68,21 @@ struct StageDesc {
 
 struct __align__(128) Smem {
   float stage[kNStage][kStage];
-  uint32_t ckey[kCap];
-  int32_t cidx[kCap];
   union {
     struct {
-      uint32_t key[kTopK];
-      int32_t idx[kTopK];
-    } aux;
-    unsigned long long sortbuf[kTopK];
-  } u;
+      uint32_t key[kCap];
+      int32_t idx[kCap];
+    } c;
+    unsigned long long runs[kTopK];  // final sort (the list is dead by then)
+  } cand;
+  uint32_t hist[4096];  // running histogram of key >> 20 of every appended element
+  uint32_t aux_key[kTopK];
+  int32_t aux_idx[kTopK];
   StageDesc desc[kNStage];
   uint64_t full[kNStage];
   uint64_t empty[kNStage];
   SelectScratch sc;
+  uint32_t bcast[4];
   int add[3];
 };
 
@@ -173,35 +178,73 @@ __device__ void producer(const TopkLaunch& p, Smem& S) {
 }
 
 // ---------------------------------------------------------------- consumers
-// Write output positions [0, 512) of one row from its sorted composite.
-__device__ __forceinline__ void emit_row(long long row, int batch, unsigned long long v, int cnt, int tid,
-                                         const int* pt, long long pt_stride, int ps, int* out_slots, int* out_idx,
-                                         float* out_scores) {
-  int idx = -1, slot = -1;
-  float score = __int_as_float(0x7FC00000);  // NaN padding for scores
-  if (tid < cnt) {
-    idx = static_cast<int>(~static_cast<uint32_t>(v & 0xFFFFFFFFull));
-    score = key_to_float(static_cast<uint32_t>(v >> 32));
-    if (pt) {
-      const long long page = pt[(long long)batch * pt_stride + (ps == 1 ? idx : idx / ps)];
-      slot = static_cast<int>(ps == 1 ? page : page * ps + idx % ps);
+// Append the elements whose bit is set in `mask` (order keys computed here)
+// and count them in the running histogram; one shared atomic per warp for
+// the positions.
+__device__ __forceinline__ void append_pass(uint32_t* ckey, int32_t* cidx, uint32_t* hist, int base, int* counter,
+                                            const float (&vals)[5], const int32_t (&idxs)[5], uint32_t mask,
+                                            int lane) {
+  const int m = __popc(mask);
+  if (!__any_sync(0xFFFFFFFFu, m > 0)) return;
+  int incl = m;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += o;
+  }
+  int start = 0;
+  if (lane == 31) start = atomicAdd(counter, incl);
+  int pos = __shfl_sync(0xFFFFFFFFu, start, 31) + base + incl - m;
+#pragma unroll
+  for (int i = 0; i < 5; ++i) {
+    if (mask & (1u << i)) {
+      const uint32_t key = order_key(vals[i]);
+      ckey[pos] = key;
+      cidx[pos] = idxs[i];
+      atomicAdd(&hist[key >> 20], 1u);
+      ++pos;
     }
   }
-  const long long o = row * kTopK + tid;
-  if (out_idx) out_idx[o] = idx;
-  if (out_slots) out_slots[o] = slot;
-  if (out_scores) out_scores[o] = score;
+}
+
+// Write one row's output: entry of composite v goes to position `rank`;
+// threads tid >= cnt write the -1 padding at position tid.
+__device__ __forceinline__ void emit_ranked(long long row, int batch, unsigned long long v, int rank, int cnt,
+                                            int tid, const int* pt, long long pt_stride, int ps, int* out_slots,
+                                            int* out_idx, float* out_scores) {
+  const long long o = row * kTopK;
+  if (v != 0ull) {
+    const int idx = static_cast<int>(~static_cast<uint32_t>(v & 0xFFFFFFFFull));
+    if (out_idx) out_idx[o + rank] = idx;
+    if (out_scores) out_scores[o + rank] = key_to_float(static_cast<uint32_t>(v >> 32));
+    if (out_slots) {
+      int slot = -1;
+      if (pt) {
+        const long long page = pt[(long long)batch * pt_stride + (ps == 1 ? idx : idx / ps)];
+        slot = static_cast<int>(ps == 1 ? page : page * ps + idx % ps);
+      }
+      out_slots[o + rank] = slot;
+    }
+  }
+  if (tid >= cnt) {
+    if (out_idx) out_idx[o + tid] = -1;
+    if (out_slots) out_slots[o + tid] = -1;
+    if (out_scores) out_scores[o + tid] = __int_as_float(0x7FC00000);
+  }
 }
 
 __device__ void consumers(const TopkLaunch& p, Smem& S, int tid) {
   const int lane = tid & 31;
+  uint32_t* const ckey = S.cand.c.key;
+  int32_t* const cidx = S.cand.c.idx;
   uint32_t it = 0;
   int cnt = 0;       // candidates held before the current stage (uniform)
-  uint32_t tau = 0;  // strict filter: keep key > tau (0 is below every non-NaN key)
+  int since = 0;     // appends since the last threshold update
+  uint32_t tau = 0;  // keep elements whose order key >= tau
   while (true) {
     const int slot = it % kNStage;
     const uint32_t ph = (it / kNStage) & 1u;
-    // One thread polls the mbarrier; the others sleep in the named barrier,
+    // One thread polls the mbarrier; the others wait in the named barrier,
     // which also publishes the stage (and any timeout) to all consumers.
     const bool ok = named_bar_and(kBarConsumers, kConsumers, tid == 0 ? mbar_wait(&S.full[slot], ph) : true);
     if (!ok) {
@@ -214,55 +257,78 @@ __device__ void consumers(const TopkLaunch& p, Smem& S, int tid) {
     const int flags = d.flags, nvec = d.nvec, nextra = d.nextra, base = d.base, row = d.row, batch = d.batch;
     if (flags & 1) {
       cnt = 0;
+      since = 0;
       tau = 0;
     }
-    uint32_t keys[5];
+    const float tf = tau_float(tau);
+    float vals[5];
     int32_t idxs[5];
     uint32_t mask = 0;
     if (4 * tid < nvec) {
       const float4 v = reinterpret_cast<const float4*>(S.stage[slot])[tid];
-      keys[0] = order_key(v.x);
-      keys[1] = order_key(v.y);
-      keys[2] = order_key(v.z);
-      keys[3] = order_key(v.w);
+      vals[0] = v.x;
+      vals[1] = v.y;
+      vals[2] = v.z;
+      vals[3] = v.w;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         idxs[i] = base + 4 * tid + i;
-        mask |= (keys[i] > tau ? 1u : 0u) << i;
+        mask |= (vals[i] >= tf ? 1u : 0u) << i;
       }
     }
     if (tid < nextra) {
-      keys[4] = order_key(d.extra_val[tid]);
+      vals[4] = d.extra_val[tid];
       idxs[4] = d.extra_idx[tid];
-      mask |= (keys[4] > tau ? 1u : 0u) << 4;
+      mask |= (vals[4] >= tf ? 1u : 0u) << 4;
     }
-    append_masked<5>(S.ckey, S.cidx, cnt, &S.add[it % 3], keys, idxs, mask, lane);
+    append_pass(ckey, cidx, S.hist, cnt, &S.add[it % 3], vals, idxs, mask, lane);
     named_bar(kBarConsumers, kConsumers);
     if (tid == 0) {
       mbar_arrive(&S.empty[slot]);  // stage data and descriptor are no longer read
       S.add[(it + 2) % 3] = 0;      // counter of stage it+2; last read before this barrier
     }
-    cnt += S.add[it % 3];
-    if (cnt > kCompactAt) {
-      tau = select_topk<kConsumers>(S.ckey, S.cidx, cnt, kTopK, S.u.aux.key, S.u.aux.idx, S.sc, tid,
-                                    kBarConsumers);
-      cnt = kTopK;
+    const int added = S.add[it % 3];
+    cnt += added;
+    since += added;
+    if (since >= kScanEvery || cnt > kPruneAt) {
+      since = 0;
+      const BinCut c = hist_cut4096(S.hist, kTopK, S.sc.wmin, S.bcast, tid, kBarConsumers);
+      if (c.bin >= 0) tau = max(tau, static_cast<uint32_t>(c.bin) << 20);
+      if (cnt > kPruneAt) {
+        cnt = compact_ge<kCap>(ckey, cidx, cnt, tau, S.sc.wcnt, tid, kBarConsumers);
+        if (cnt > kPruneAt) {  // the threshold bin alone is too full: exact cut
+          const uint32_t t2 = select_topk<kConsumers>(ckey, cidx, cnt, kTopK, S.aux_key, S.aux_idx, S.sc, tid,
+                                                      kBarConsumers);
+          tau = max(tau, t2);
+          cnt = kTopK;
+        }
+      }
     }
     if (flags & 2) {
+      // the running histogram counts pruned elements too: start a fresh one
+      reinterpret_cast<uint4*>(S.hist)[2 * tid] = make_uint4(0, 0, 0, 0);
+      reinterpret_cast<uint4*>(S.hist)[2 * tid + 1] = make_uint4(0, 0, 0, 0);
+      named_bar(kBarConsumers, kConsumers);
       if (cnt > kTopK) {
-        select_topk<kConsumers>(S.ckey, S.cidx, cnt, kTopK, S.u.aux.key, S.u.aux.idx, S.sc, tid, kBarConsumers);
+        fast_select512<kCap>(ckey, cidx, cnt, S.hist, S.aux_key, S.aux_idx, S.sc, S.bcast, tid, kBarConsumers);
         cnt = kTopK;
+      } else {
+        if (tid < cnt) {
+          S.aux_key[tid] = ckey[tid];
+          S.aux_idx[tid] = cidx[tid];
+        }
+        named_bar(kBarConsumers, kConsumers);
       }
       if (p.chunks == 1) {
-        unsigned long long v = tid < cnt ? composite(S.ckey[tid], S.cidx[tid]) : 0ull;
-        v = bitonic_desc512(v, S.u.sortbuf, tid, kBarConsumers);
-        emit_row(row, batch, v, cnt, tid, p.page_tables, p.pt_stride, p.page_size, p.out_slots, p.out_idx,
-                 nullptr);
+        unsigned long long v;
+        const int rank = rank_sort512(S.aux_key, S.aux_idx, cnt, S.cand.runs, &v, tid, kBarConsumers);
+        emit_ranked(row, batch, v, rank, cnt, tid, p.page_tables, p.pt_stride, p.page_size, p.out_slots, p.out_idx,
+                    nullptr);
       } else {
         const long long o = (long long)unit * kTopK;
-        for (int j = tid; j < cnt; j += kConsumers) {
-          p.part_key[o + j] = S.ckey[j];
-          p.part_idx[o + j] = S.cidx[j];
+        if (tid < cnt) {
+          p.part_key[o + tid] = S.aux_key[tid];
+          p.part_idx[o + tid] = S.aux_idx[tid];
         }
         if (tid == 0) p.part_cnt[unit] = cnt;
         named_bar(kBarConsumers, kConsumers);
@@ -285,6 +351,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_stream_kernel(const __grid_c
     S.add[0] = S.add[1] = S.add[2] = 0;
     fence_mbar_init();
   }
+  for (int i = tid; i < 4096; i += kThreads) S.hist[i] = 0;
   __syncthreads();
   if (tid >= kConsumers) {
     if (tid == kConsumers) producer(p, S);
@@ -298,16 +365,18 @@ constexpr int kMergeUnits = 12;
 constexpr int kMergeCap = kMergeUnits * kTopK;
 
 struct __align__(16) MergeSmem {
-  uint32_t ckey[kMergeCap];
-  int32_t cidx[kMergeCap];
   union {
     struct {
-      uint32_t key[kTopK];
-      int32_t idx[kTopK];
-    } aux;
-    unsigned long long sortbuf[kTopK];
-  } u;
+      uint32_t key[kMergeCap];
+      int32_t idx[kMergeCap];
+    } c;
+    unsigned long long runs[kTopK];
+  } cand;
+  uint32_t hist[4096];
+  uint32_t aux_key[kTopK];
+  int32_t aux_idx[kTopK];
   SelectScratch sc;
+  uint32_t bcast[4];
 };
 
 __global__ void __launch_bounds__(kTopK, 1) merge_kernel(const __grid_constant__ MergeLaunch p) {
@@ -315,26 +384,35 @@ __global__ void __launch_bounds__(kTopK, 1) merge_kernel(const __grid_constant__
   MergeSmem& S = *reinterpret_cast<MergeSmem*>(smem_raw);
   const int tid = threadIdx.x;
   const long long row = blockIdx.x;
+  reinterpret_cast<uint4*>(S.hist)[2 * tid] = make_uint4(0, 0, 0, 0);
+  reinterpret_cast<uint4*>(S.hist)[2 * tid + 1] = make_uint4(0, 0, 0, 0);
   int total = 0;
   for (int c = 0; c < p.units_per_row; ++c) {
     const long long unit = row * p.units_per_row + c;
     const int n = min(p.part_cnt[unit], kTopK);
-    for (int j = tid; j < n; j += kTopK) {
-      S.ckey[total + j] = p.part_key[unit * kTopK + j];
-      S.cidx[total + j] = p.part_idx[unit * kTopK + j];
+    if (tid < n) {
+      S.cand.c.key[total + tid] = p.part_key[unit * kTopK + tid];
+      S.cand.c.idx[total + tid] = p.part_idx[unit * kTopK + tid];
     }
     total += n;
   }
   __syncthreads();
   int cnt = total;
   if (cnt > kTopK) {
-    select_topk<kTopK>(S.ckey, S.cidx, cnt, kTopK, S.u.aux.key, S.u.aux.idx, S.sc, tid, 1);
+    fast_select512<kMergeCap>(S.cand.c.key, S.cand.c.idx, cnt, S.hist, S.aux_key, S.aux_idx, S.sc, S.bcast, tid, 1);
     cnt = kTopK;
+  } else {
+    if (tid < cnt) {
+      S.aux_key[tid] = S.cand.c.key[tid];
+      S.aux_idx[tid] = S.cand.c.idx[tid];
+    }
+    __syncthreads();
   }
-  unsigned long long v = tid < cnt ? composite(S.ckey[tid], S.cidx[tid]) : 0ull;
-  v = bitonic_desc512(v, S.u.sortbuf, tid, 1);
+  unsigned long long v;
+  const int rank = rank_sort512(S.aux_key, S.aux_idx, cnt, S.cand.runs, &v, tid, 1);
   const int batch = cnt > 0 ? (p.row_to_batch ? p.row_to_batch[row] : (int)row) : 0;
-  emit_row(row, batch, v, cnt, tid, p.page_tables, p.pt_stride, p.page_size, p.out_slots, p.out_idx, p.out_scores);
+  emit_ranked(row, batch, v, rank, cnt, tid, p.page_tables, p.pt_stride, p.page_size, p.out_slots, p.out_idx,
+              p.out_scores);
 }
 
 bool g_attr_done[64];
