@@ -495,10 +495,11 @@ __device__ __forceinline__ int rank_sort512(const uint32_t* aux_key, const int32
   for (int r = 0; r < 16; ++r) {
     if (r == warp) continue;
     const unsigned long long* run = runs + 32 * r;
-    int pos = 0;
+    // number of entries of the descending run that are > v (0..32)
+    int pos = run[31] > v ? 32 : 0;
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1)
-      if (run[pos + s - 1] > v) pos += s;
+      if (pos + s <= 31 && run[pos + s - 1] > v) pos += s;
     rank += pos;
   }
   named_bar(bar, 512);  // runs may be reused after this
