@@ -513,4 +513,135 @@ __device__ __forceinline__ float tau_float(uint32_t tau) {
   return key_to_float(tau);
 }
 
+// ------------------------------------------------------------------------
+// Helpers for a group of NT threads (NT a multiple of 32, NT <= 512).
+
+template <int NT>
+__device__ __forceinline__ int block_exscan(int c, int* total, uint32_t* wsum, int tid, int bar) {
+  constexpr int NW = NT / 32;
+  const int lane = tid & 31, warp = tid >> 5;
+  int incl = c;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += o;
+  }
+  if (lane == 31) wsum[warp] = (uint32_t)incl;
+  named_bar(bar, NT);
+  int off = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    const int v = (int)wsum[w];
+    off += w < warp ? v : 0;
+    tot += v;
+  }
+  *total = tot;
+  return off + incl - c;
+}
+
+// Exact top-K (K = 512) of ckey/cidx[0, n), n > K, by (key desc, index
+// asc) into aux_key/aux_idx[0, K) (unordered; ckey/cidx are left intact).
+// Returns the lowest key of the final threshold bin, a value <= the K-th
+// key (so "key >= returned value" is a valid filter for later elements).
+template <int NT, int CAPT>
+__device__ uint32_t select512_to_aux(const uint32_t* ckey, const int32_t* cidx, int n, uint32_t* aux_key,
+                                     int32_t* aux_idx, SelectScratch& sc, int tid, int bar) {
+  constexpr int K = kTopK;
+  constexpr int M = (CAPT + NT - 1) / NT;
+  const Threshold t = radix_threshold<NT>(n, (uint32_t)K, sc, tid, bar, [&](int j, uint32_t& v) {
+    v = ckey[j];
+    return true;
+  });
+  Threshold ti{};
+  const bool ties = !t.all_eq;
+  if (ties) {
+    ti = radix_threshold<NT>(n, t.need, sc, tid, bar, [&](int j, uint32_t& v) {
+      v = 0x7FFFFFFFu - static_cast<uint32_t>(cidx[j]);
+      return thr_cmp(t, ckey[j]) == 0;
+    });
+  }
+  uint32_t selm = 0;
+  int c = 0;
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    const int j = tid + NT * m;
+    if (j < n) {
+      const int cc = thr_cmp(t, ckey[j]);
+      const bool sel =
+          cc > 0 || (cc == 0 && (!ties || thr_cmp(ti, 0x7FFFFFFFu - static_cast<uint32_t>(cidx[j])) >= 0));
+      if (sel) {
+        selm |= 1u << m;
+        ++c;
+      }
+    }
+  }
+  int total;
+  int pos = block_exscan<NT>(c, &total, sc.wcnt, tid, bar);
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    if (selm & (1u << m)) {
+      const int j = tid + NT * m;
+      if (pos < K) {
+        aux_key[pos] = ckey[j];
+        aux_idx[pos] = cidx[j];
+      }
+      ++pos;
+    }
+  }
+  named_bar(bar, NT);
+  return t.base + static_cast<uint32_t>(static_cast<uint64_t>(t.prefix) << t.lo);
+}
+
+// Sort the `cnt` (<= 512) entries of aux_key/aux_idx by (key desc, index
+// asc): 16 runs of 32 are sorted by warp shuffles, then each entry's rank is
+// its place in its run plus, for every other run, the number of larger
+// entries (binary search). Thread tid handles runs warp, warp+NW, ...; for
+// each, v[e] is its entry's composite (0 = padding) and rank[e] its output
+// position. `runs` needs 512 entries.
+template <int NT>
+__device__ __forceinline__ void rank_sort(const uint32_t* aux_key, const int32_t* aux_idx, int cnt,
+                                          unsigned long long* runs, unsigned long long (&v)[kTopK / NT],
+                                          int (&rank)[kTopK / NT], int tid, int bar) {
+  constexpr int NW = NT / 32;
+  constexpr int E = kTopK / NT;
+  const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int r = warp + NW * e;
+    const int j = 32 * r + lane;
+    unsigned long long x = j < cnt ? composite(aux_key[j], aux_idx[j]) : 0ull;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+      const bool asc = (lane & size) != 0;
+#pragma unroll
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        const unsigned long long p = __shfl_xor_sync(0xFFFFFFFFu, x, stride);
+        const bool lower = (lane & stride) == 0;
+        x = (lower != asc) ? (x > p ? x : p) : (x < p ? x : p);
+      }
+    }
+    runs[j] = x;
+    v[e] = x;
+  }
+  named_bar(bar, NT);
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int r0 = warp + NW * e;
+    int rk = lane;
+    const unsigned long long x = v[e];
+#pragma unroll 4
+    for (int r = 0; r < 16; ++r) {
+      if (r == r0) continue;
+      const unsigned long long* run = runs + 32 * r;
+      int pos = run[31] > x ? 32 : 0;
+#pragma unroll
+      for (int s = 16; s > 0; s >>= 1)
+        if (pos + s <= 31 && run[pos + s - 1] > x) pos += s;
+      rk += pos;
+    }
+    rank[e] = rk;
+  }
+  named_bar(bar, NT);
+}
+
 }  // namespace sai

@@ -8,23 +8,24 @@
 // addressing inside the top-k kernel is the "merge build sparse block into
 // topk" step of ROCm/ATOM PR #1282.
 //
-// GB300 design. One persistent CTA processes a strided list of work units
-// (a whole row, or one chunk of a long row). Inside the CTA:
-//   * a producer warp streams each unit's window into a ring of shared-memory
-//     stages with 1-D bulk TMA copies (cp.async.bulk + mbarrier
-//     complete_tx), evict-first in L2 since each score is read once. The
-//     16-byte-aligned interior of the window goes through TMA; the <= 3
-//     leading and <= 3 trailing elements (any row stride or row start) are
-//     read by the producer with plain loads and handed over in the stage
-//     descriptor. This is the scalar path the pages require when the stride
-//     is not a multiple of 4, folded into every row instead of a fallback;
-//   * 16 consumer warps turn each stage into order keys and keep a running
-//     threshold tau: only keys > tau are appended (warp-aggregated) to a
-//     shared candidate buffer. When the buffer nears capacity it is cut back
-//     to the exact top 512 (radix select in shared memory) and tau rises.
-//     Every later element has a larger index than all kept ones, so the
-//     strict filter never drops a winner;
-//   * at the end of a unit the candidates are cut to 512, bitonic-sorted by
+// GB300 design: many small persistent CTAs (4 warps, ~34 KB of shared
+// memory, six per SM), each streaming one work unit (a row, or a chunk of a
+// long row) at a time, so that the serial latency of one CTA's
+// stage -> filter -> barrier chain is hidden by the other CTAs on the SM.
+//   * Thread 0 keeps a ring of shared-memory stages filled with 1-D bulk TMA
+//     copies (cp.async.bulk + mbarrier complete_tx, evict-first in L2: every
+//     score is read once). The 16-byte-aligned interior of each window goes
+//     through TMA; its <= 3 leading and <= 3 trailing elements (any row
+//     stride, any row start) are read with scalar loads. This is the scalar
+//     path the pages require for strides that are not a multiple of 4,
+//     folded into every row instead of a separate fallback kernel.
+//   * Each thread compares its 8 scores of a stage against the running
+//     threshold tau (as a float) and appends the survivors (order key,
+//     row-local index) to a shared candidate list. When the list fills up it
+//     is cut to the exact top 512 (radix select in shared memory) and tau
+//     rises to that cut, so the filter stays exact: every dropped element is
+//     beaten by 512 kept ones.
+//   * At the end of a unit the candidates are cut to 512, sorted by
 //     (score desc, index asc), page-transformed and written (one unit per
 //     row), or written as a partial list for the merge kernel (split rows).
 #include <cuda_runtime.h>
@@ -39,31 +40,28 @@
 namespace sai {
 namespace {
 
-constexpr int kConsumers = 512;                 // 16 consumer warps
-constexpr int kThreads = kConsumers + 32;       // + 1 producer warp
-constexpr int kStage = 2048;                    // floats per stage (8 KB): one float4 per consumer
-constexpr int kNStage = 5;                      // 40 KB in flight per CTA
-constexpr int kExtra = 8;                       // scalar elements per descriptor
-constexpr int kPruneAt = 2048;                  // prune the candidate list above this size
-constexpr int kCap = 4352;                      // >= kPruneAt + kStage + kExtra
-constexpr int kScanEvery = 256;                 // raise the threshold after this many appends
-constexpr int kBarConsumers = 1;                // named barrier id
+constexpr int kThreads = 128;                    // 4 warps per CTA
+constexpr int kStage = 1024;                     // floats per stage (4 KB): two float4 per thread
+constexpr int kNStage = 3;                       // 12 KB in flight per CTA
+constexpr int kCap = 2048;                       // candidate capacity
+constexpr int kMaxExtra = 8;                     // scalar head/tail elements of a window
+constexpr int kPruneAt = kCap - kStage - kMaxExtra;
+constexpr int kBar = 1;                          // named barrier id (all 128 threads)
+constexpr int kCtasPerSm = 6;
 
-static_assert(kTopK == kConsumers, "the final sort keeps one entry per consumer thread");
-static_assert(kCap >= kPruneAt + kStage + kExtra, "candidate list overflow");
-static_assert(kStage == 4 * kConsumers, "one float4 per consumer per stage");
+static_assert(kStage == 8 * kThreads, "two float4 per thread per stage");
+static_assert(kPruneAt > kTopK, "room to keep the top 512 and append one stage");
 
 struct StageDesc {
-  int unit;   // -1: no more work
+  int unit;          // -1: no more work
   int row;
-  int base;   // row-local index of stage element 0
-  int nvec;   // TMA elements in this stage (multiple of 4)
-  int nextra;
-  int flags;  // 1: first stage of the unit, 2: last stage of the unit
-  int batch;  // page-table row
-  int pad_;
-  int extra_idx[kExtra];
-  float extra_val[kExtra];
+  int batch;         // page-table row
+  int base;          // row-local index of stage element 0
+  int nvec;          // TMA elements in this stage (multiple of 4)
+  int flags;         // 1: first stage of the unit, 2: last stage of the unit
+  int head, tail;    // scalar elements: [lo, lo+head) and [tail_at, tail_at+tail)
+  int lo, tail_at;
+  long long woff;    // element offset of the row's window start in `scores`
 };
 
 struct __align__(128) Smem {
@@ -75,14 +73,11 @@ struct __align__(128) Smem {
     } c;
     unsigned long long runs[kTopK];  // final sort (the list is dead by then)
   } cand;
-  uint32_t hist[4096];  // running histogram of key >> 20 of every appended element
   uint32_t aux_key[kTopK];
   int32_t aux_idx[kTopK];
   StageDesc desc[kNStage];
   uint64_t full[kNStage];
-  uint64_t empty[kNStage];
   SelectScratch sc;
-  uint32_t bcast[4];
   int add[3];
 };
 
@@ -94,95 +89,90 @@ __device__ __forceinline__ Smem& smem_ref(unsigned char* raw) {
   return *reinterpret_cast<Smem*>(a);
 }
 
-// ---------------------------------------------------------------- producer
-__device__ void producer(const TopkLaunch& p, Smem& S) {
-  const uint64_t policy = l2_policy_evict_first();
+// Work-unit walker owned by thread 0: yields the stages to issue, in order.
+struct Cursor {
+  int unit;      // current unit (>= units: done)
+  int s, nst;    // stage index within the unit, stage count
+  int row, batch;
+  long long woff;
+  int lo, head, body, tail;
+};
+
+__device__ void cursor_load(const TopkLaunch& p, Cursor& c) {
   const int units = p.rows * p.chunks;
-  uint32_t it = 0;
-  for (int u = blockIdx.x;; u += gridDim.x) {
-    const bool done = u >= units;
-    int row = 0, b = 0, lo = 0, hi = 0;
-    const float* win = p.scores;
-    if (!done) {
-      row = u / p.chunks;
-      const int ch = u - row * p.chunks;
-      int n = p.seq_lens[row];
-      const long long start = p.row_starts ? p.row_starts[row] : 0;
-      b = p.row_to_batch ? p.row_to_batch[row] : row;
-      bool bad = n < 0 || start < 0 || start + n > p.stride;
-      if (p.page_tables) {
-        bad = bad || b < 0 || b >= p.pt_rows || (n > 0 && (long long)(n - 1) / p.page_size >= p.pt_stride);
-      }
-      if (bad) {
-        atomicOr(p.status, kDevBadRowMeta);
-        n = 0;
-        b = 0;
-      }
-      win = p.scores + (long long)row * p.stride + (bad ? 0 : start);
-      lo = p.chunks > 1 ? ch * p.chunk_len : 0;
-      hi = p.chunks > 1 ? min(n, lo + p.chunk_len) : n;
-      if (lo > hi) lo = hi;
-    }
-    // split [lo, hi) into scalar head, 16-byte aligned body, scalar tail
-    const int len = hi - lo;
-    int head = (int)(((16u - (reinterpret_cast<uintptr_t>(win + lo) & 15u)) & 15u) >> 2);
-    int body = 0;
-    if (len <= kExtra || head > len) {
-      head = len;
-    } else {
-      body = (len - head) & ~3;
-    }
-    const int tail = len - head - body;
-    const int nst = done ? 1 : max(1, (body + kStage - 1) / kStage);
-    for (int s = 0; s < nst; ++s, ++it) {
-      const int slot = it % kNStage;
-      const uint32_t ph = (it / kNStage) & 1u;
-      if (!mbar_wait(&S.empty[slot], ph ^ 1u)) {
-        atomicOr(p.status, kDevWaitTimeout);
-        return;  // consumers time out on the full barrier and stop too
-      }
-      StageDesc& d = S.desc[slot];
-      if (done) {
-        d.unit = -1;
-        mbar_arrive(&S.full[slot]);
-        return;
-      }
-      d.unit = u;
-      d.row = row;
-      d.batch = b;
-      d.flags = (s == 0 ? 1 : 0) | (s == nst - 1 ? 2 : 0);
-      d.base = lo + head + s * kStage;
-      d.nvec = min(kStage, body - s * kStage);
-      d.nextra = 0;
-      if (s == 0) {
-        int e = 0;
-        for (int i = 0; i < head; ++i, ++e) {
-          d.extra_idx[e] = lo + i;
-          d.extra_val[e] = __ldg(win + lo + i);
-        }
-        for (int i = 0; i < tail; ++i, ++e) {
-          const int j = lo + head + body + i;
-          d.extra_idx[e] = j;
-          d.extra_val[e] = __ldg(win + j);
-        }
-        d.nextra = e;
-      }
-      if (d.nvec > 0) {
-        mbar_arrive_expect_tx(&S.full[slot], (uint32_t)d.nvec * 4u);
-        bulk_g2s_stream(S.stage[slot], win + d.base, (uint32_t)d.nvec * 4u, &S.full[slot], policy);
-      } else {
-        mbar_arrive(&S.full[slot]);
-      }
-    }
+  c.s = 0;
+  if (c.unit >= units) return;
+  const int row = c.unit / p.chunks;
+  const int ch = c.unit - row * p.chunks;
+  int n = p.seq_lens[row];
+  const long long start = p.row_starts ? p.row_starts[row] : 0;
+  int b = p.row_to_batch ? p.row_to_batch[row] : row;
+  bool bad = n < 0 || start < 0 || start + n > p.stride;
+  if (p.page_tables)
+    bad = bad || b < 0 || b >= p.pt_rows || (n > 0 && (long long)(n - 1) / p.page_size >= p.pt_stride);
+  if (bad) {
+    atomicOr(p.status, kDevBadRowMeta);
+    n = 0;
+    b = 0;
+  }
+  c.row = row;
+  c.batch = b;
+  c.woff = (long long)row * p.stride + (bad ? 0 : start);
+  int lo = p.chunks > 1 ? ch * p.chunk_len : 0;
+  const int hi = p.chunks > 1 ? min(n, lo + p.chunk_len) : n;
+  if (lo > hi) lo = hi;
+  const int len = hi - lo;
+  int head = (int)(((16u - (reinterpret_cast<uintptr_t>(p.scores + c.woff + lo) & 15u)) & 15u) >> 2);
+  int body = 0;
+  if (len <= kMaxExtra || head > len) {
+    head = len;
+  } else {
+    body = (len - head) & ~3;
+  }
+  c.lo = lo;
+  c.head = head;
+  c.body = body;
+  c.tail = len - head - body;
+  c.nst = max(1, (body + kStage - 1) / kStage);
+}
+
+// Issue the cursor's next stage into `slot` (thread 0 only) and advance.
+__device__ void issue_stage(const TopkLaunch& p, Smem& S, Cursor& c, int slot, uint64_t policy) {
+  const int units = p.rows * p.chunks;
+  StageDesc& d = S.desc[slot];
+  if (c.unit >= units) {
+    d.unit = -1;
+    mbar_arrive(&S.full[slot]);
+    return;
+  }
+  d.unit = c.unit;
+  d.row = c.row;
+  d.batch = c.batch;
+  d.flags = (c.s == 0 ? 1 : 0) | (c.s == c.nst - 1 ? 2 : 0);
+  d.base = c.lo + c.head + c.s * kStage;
+  d.nvec = min(kStage, c.body - c.s * kStage);
+  d.head = c.s == 0 ? c.head : 0;
+  d.tail = c.s == 0 ? c.tail : 0;
+  d.lo = c.lo;
+  d.tail_at = c.lo + c.head + c.body;
+  d.woff = c.woff;
+  if (d.nvec > 0) {
+    mbar_arrive_expect_tx(&S.full[slot], (uint32_t)d.nvec * 4u);
+    bulk_g2s_stream(S.stage[slot], p.scores + c.woff + d.base, (uint32_t)d.nvec * 4u, &S.full[slot], policy);
+  } else {
+    mbar_arrive(&S.full[slot]);
+  }
+  if (++c.s >= c.nst) {
+    c.unit += gridDim.x;
+    cursor_load(p, c);
   }
 }
 
-// ---------------------------------------------------------------- consumers
-// Append the elements whose bit is set in `mask` (order keys computed here)
-// and count them in the running histogram; one shared atomic per warp for
-// the positions.
-__device__ __forceinline__ void append_pass(uint32_t* ckey, int32_t* cidx, uint32_t* hist, int base, int* counter,
-                                            const float (&vals)[5], const int32_t (&idxs)[5], uint32_t mask,
+// Append the elements whose bit is set in `mask` at positions base +
+// running count; one shared atomic per warp.
+template <int M>
+__device__ __forceinline__ void append_keys(uint32_t* ckey, int32_t* cidx, int base, int* counter,
+                                            const float (&vals)[M], const int32_t (&idxs)[M], uint32_t mask,
                                             int lane) {
   const int m = __popc(mask);
   if (!__any_sync(0xFFFFFFFFu, m > 0)) return;
@@ -196,19 +186,17 @@ __device__ __forceinline__ void append_pass(uint32_t* ckey, int32_t* cidx, uint3
   if (lane == 31) start = atomicAdd(counter, incl);
   int pos = __shfl_sync(0xFFFFFFFFu, start, 31) + base + incl - m;
 #pragma unroll
-  for (int i = 0; i < 5; ++i) {
+  for (int i = 0; i < M; ++i) {
     if (mask & (1u << i)) {
-      const uint32_t key = order_key(vals[i]);
-      ckey[pos] = key;
+      ckey[pos] = order_key(vals[i]);
       cidx[pos] = idxs[i];
-      atomicAdd(&hist[key >> 20], 1u);
       ++pos;
     }
   }
 }
 
-// Write one row's output: entry of composite v goes to position `rank`;
-// threads tid >= cnt write the -1 padding at position tid.
+// Write one row's output from a 512-thread group: the entry of composite v
+// goes to position `rank`; threads tid >= cnt write the -1 padding at tid.
 __device__ __forceinline__ void emit_ranked(long long row, int batch, unsigned long long v, int rank, int cnt,
                                             int tid, const int* pt, long long pt_stride, int ps, int* out_slots,
                                             int* out_idx, float* out_scores) {
@@ -233,131 +221,157 @@ __device__ __forceinline__ void emit_ranked(long long row, int batch, unsigned l
   }
 }
 
-__device__ void consumers(const TopkLaunch& p, Smem& S, int tid) {
-  const int lane = tid & 31;
+__device__ __forceinline__ void emit_one(long long o, int batch, unsigned long long v, int rank,
+                                         const TopkLaunch& p) {
+  if (v == 0ull) return;
+  const int idx = static_cast<int>(~static_cast<uint32_t>(v & 0xFFFFFFFFull));
+  if (p.out_idx) p.out_idx[o + rank] = idx;
+  if (p.out_slots) {
+    const int ps = p.page_size;
+    const long long page = p.page_tables[(long long)batch * p.pt_stride + (ps == 1 ? idx : idx / ps)];
+    p.out_slots[o + rank] = static_cast<int>(ps == 1 ? page : page * ps + idx % ps);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const __grid_constant__ TopkLaunch p) {
+  extern __shared__ unsigned char smem_raw[];
+  Smem& S = smem_ref(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31;
   uint32_t* const ckey = S.cand.c.key;
   int32_t* const cidx = S.cand.c.idx;
+  Cursor cur{};
+  uint64_t policy = 0;
+  bool issuing = false;
+  if (tid == 0) {
+    for (int i = 0; i < kNStage; ++i) mbar_init(&S.full[i], 1);
+    S.add[0] = S.add[1] = S.add[2] = 0;
+    fence_mbar_init();
+    policy = l2_policy_evict_first();
+    cur.unit = blockIdx.x;
+    cursor_load(p, cur);
+    issuing = true;
+    const int units = p.rows * p.chunks;
+    for (int i = 0; i < kNStage && issuing; ++i) {
+      issuing = cur.unit < units;
+      issue_stage(p, S, cur, i, policy);
+    }
+  }
+  __syncthreads();
   uint32_t it = 0;
   int cnt = 0;       // candidates held before the current stage (uniform)
-  int since = 0;     // appends since the last threshold update
   uint32_t tau = 0;  // keep elements whose order key >= tau
   while (true) {
     const int slot = it % kNStage;
     const uint32_t ph = (it / kNStage) & 1u;
-    // One thread polls the mbarrier; the others wait in the named barrier,
-    // which also publishes the stage (and any timeout) to all consumers.
-    const bool ok = named_bar_and(kBarConsumers, kConsumers, tid == 0 ? mbar_wait(&S.full[slot], ph) : true);
-    if (!ok) {
-      if (tid == 0) atomicOr(p.status, kDevWaitTimeout);
-      return;
-    }
+    const bool ok = mbar_wait(&S.full[slot], ph);
     const StageDesc& d = S.desc[slot];
-    const int unit = d.unit;
-    if (unit < 0) return;
-    const int flags = d.flags, nvec = d.nvec, nextra = d.nextra, base = d.base, row = d.row, batch = d.batch;
+    // after a timeout the descriptor is not trusted: process nothing, then
+    // leave together at the barrier below
+    const int unit = ok ? d.unit : 0;
+    if (unit < 0) break;
+    const int flags = ok ? d.flags : 0, nvec = ok ? d.nvec : 0, base = d.base, row = d.row, batch = d.batch;
+    const int head = ok ? d.head : 0, tail = ok ? d.tail : 0, lo = d.lo, tail_at = d.tail_at;
+    const long long woff = d.woff;
     if (flags & 1) {
       cnt = 0;
-      since = 0;
       tau = 0;
     }
     const float tf = tau_float(tau);
-    float vals[5];
-    int32_t idxs[5];
+    float vals[9];
+    int32_t idxs[9];
     uint32_t mask = 0;
     if (4 * tid < nvec) {
-      const float4 v = reinterpret_cast<const float4*>(S.stage[slot])[tid];
-      vals[0] = v.x;
-      vals[1] = v.y;
-      vals[2] = v.z;
-      vals[3] = v.w;
+      const float4 a = reinterpret_cast<const float4*>(S.stage[slot])[tid];
+      vals[0] = a.x;
+      vals[1] = a.y;
+      vals[2] = a.z;
+      vals[3] = a.w;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         idxs[i] = base + 4 * tid + i;
         mask |= (vals[i] >= tf ? 1u : 0u) << i;
       }
     }
-    if (tid < nextra) {
-      vals[4] = d.extra_val[tid];
-      idxs[4] = d.extra_idx[tid];
-      mask |= (vals[4] >= tf ? 1u : 0u) << 4;
-    }
-    append_pass(ckey, cidx, S.hist, cnt, &S.add[it % 3], vals, idxs, mask, lane);
-    named_bar(kBarConsumers, kConsumers);
-    if (tid == 0) {
-      mbar_arrive(&S.empty[slot]);  // stage data and descriptor are no longer read
-      S.add[(it + 2) % 3] = 0;      // counter of stage it+2; last read before this barrier
-    }
-    const int added = S.add[it % 3];
-    cnt += added;
-    since += added;
-    if (since >= kScanEvery || cnt > kPruneAt) {
-      since = 0;
-      const BinCut c = hist_cut4096(S.hist, kTopK, S.sc.wmin, S.bcast, tid, kBarConsumers);
-      if (c.bin >= 0) tau = max(tau, static_cast<uint32_t>(c.bin) << 20);
-      if (cnt > kPruneAt) {
-        cnt = compact_ge<kCap>(ckey, cidx, cnt, tau, S.sc.wcnt, tid, kBarConsumers);
-        if (cnt > kPruneAt) {  // the threshold bin alone is too full: exact cut
-          const uint32_t t2 = select_topk<kConsumers>(ckey, cidx, cnt, kTopK, S.aux_key, S.aux_idx, S.sc, tid,
-                                                      kBarConsumers);
-          tau = max(tau, t2);
-          cnt = kTopK;
-        }
+    if (4 * (kThreads + tid) < nvec) {
+      const float4 b = reinterpret_cast<const float4*>(S.stage[slot])[kThreads + tid];
+      vals[4] = b.x;
+      vals[5] = b.y;
+      vals[6] = b.z;
+      vals[7] = b.w;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        idxs[4 + i] = base + 4 * (kThreads + tid) + i;
+        mask |= (vals[4 + i] >= tf ? 1u : 0u) << (4 + i);
       }
+    }
+    if (tid < head + tail) {  // scalar ends of the window (first stage of a unit)
+      const int j = tid < head ? lo + tid : tail_at + (tid - head);
+      vals[8] = __ldg(p.scores + woff + j);
+      idxs[8] = j;
+      mask |= (vals[8] >= tf ? 1u : 0u) << 8;
+    }
+    append_keys<9>(ckey, cidx, cnt, &S.add[it % 3], vals, idxs, mask, lane);
+    if (!named_bar_and(kBar, kThreads, ok)) {
+      if (tid == 0) {
+        atomicOr(p.status, kDevWaitTimeout);
+        // let the copies already issued land before the CTA exits (bounded)
+        for (int k = 1; k < kNStage; ++k) mbar_wait(&S.full[(it + k) % kNStage], ((it + k) / kNStage) & 1u);
+      }
+      break;
+    }
+    if (tid == 0) {
+      S.add[(it + 2) % 3] = 0;  // counter of stage it+2; last read before this barrier
+      if (issuing) {            // refill the slot just consumed
+        fence_proxy_async_smem();
+        issuing = cur.unit < p.rows * p.chunks;
+        issue_stage(p, S, cur, slot, policy);
+      }
+    }
+    cnt += S.add[it % 3];
+    if (cnt > kPruneAt) {
+      tau = max(tau, select512_to_aux<kThreads, kCap>(ckey, cidx, cnt, S.aux_key, S.aux_idx, S.sc, tid, kBar));
+      for (int j = tid; j < kTopK; j += kThreads) {
+        ckey[j] = S.aux_key[j];
+        cidx[j] = S.aux_idx[j];
+      }
+      named_bar(kBar, kThreads);
+      cnt = kTopK;
     }
     if (flags & 2) {
-      // the running histogram counts pruned elements too: start a fresh one
-      reinterpret_cast<uint4*>(S.hist)[2 * tid] = make_uint4(0, 0, 0, 0);
-      reinterpret_cast<uint4*>(S.hist)[2 * tid + 1] = make_uint4(0, 0, 0, 0);
-      named_bar(kBarConsumers, kConsumers);
       if (cnt > kTopK) {
-        fast_select512<kCap>(ckey, cidx, cnt, S.hist, S.aux_key, S.aux_idx, S.sc, S.bcast, tid, kBarConsumers);
+        select512_to_aux<kThreads, kCap>(ckey, cidx, cnt, S.aux_key, S.aux_idx, S.sc, tid, kBar);
         cnt = kTopK;
       } else {
-        if (tid < cnt) {
-          S.aux_key[tid] = ckey[tid];
-          S.aux_idx[tid] = cidx[tid];
+        for (int j = tid; j < cnt; j += kThreads) {
+          S.aux_key[j] = ckey[j];
+          S.aux_idx[j] = cidx[j];
         }
-        named_bar(kBarConsumers, kConsumers);
+        named_bar(kBar, kThreads);
       }
       if (p.chunks == 1) {
-        unsigned long long v;
-        const int rank = rank_sort512(S.aux_key, S.aux_idx, cnt, S.cand.runs, &v, tid, kBarConsumers);
-        emit_ranked(row, batch, v, rank, cnt, tid, p.page_tables, p.pt_stride, p.page_size, p.out_slots, p.out_idx,
-                    nullptr);
+        unsigned long long v[kTopK / kThreads];
+        int rk[kTopK / kThreads];
+        rank_sort<kThreads>(S.aux_key, S.aux_idx, cnt, S.cand.runs, v, rk, tid, kBar);
+        const long long o = (long long)row * kTopK;
+#pragma unroll
+        for (int e = 0; e < kTopK / kThreads; ++e) emit_one(o, batch, v[e], rk[e], p);
+        for (int j = cnt + tid; j < kTopK; j += kThreads) {
+          if (p.out_idx) p.out_idx[o + j] = -1;
+          if (p.out_slots) p.out_slots[o + j] = -1;
+        }
       } else {
         const long long o = (long long)unit * kTopK;
-        if (tid < cnt) {
-          p.part_key[o + tid] = S.aux_key[tid];
-          p.part_idx[o + tid] = S.aux_idx[tid];
+        for (int j = tid; j < cnt; j += kThreads) {
+          p.part_key[o + j] = S.aux_key[j];
+          p.part_idx[o + j] = S.aux_idx[j];
         }
         if (tid == 0) p.part_cnt[unit] = cnt;
-        named_bar(kBarConsumers, kConsumers);
+        named_bar(kBar, kThreads);
       }
       cnt = 0;
     }
     ++it;
   }
-}
-
-__global__ void __launch_bounds__(kThreads, 2) topk_stream_kernel(const __grid_constant__ TopkLaunch p) {
-  extern __shared__ unsigned char smem_raw[];
-  Smem& S = smem_ref(smem_raw);
-  const int tid = threadIdx.x;
-  if (tid == 0) {
-    for (int i = 0; i < kNStage; ++i) {
-      mbar_init(&S.full[i], 1);
-      mbar_init(&S.empty[i], 1);
-    }
-    S.add[0] = S.add[1] = S.add[2] = 0;
-    fence_mbar_init();
-  }
-  for (int i = tid; i < 4096; i += kThreads) S.hist[i] = 0;
-  __syncthreads();
-  if (tid >= kConsumers) {
-    if (tid == kConsumers) producer(p, S);
-    return;
-  }
-  consumers(p, S, tid);
 }
 
 // ---------------------------------------------------------------- merge
@@ -465,8 +479,15 @@ cudaError_t launch_topk_transform(const TopkLaunch& p, int num_sms, cudaStream_t
     if (e != cudaSuccess) return e;
     g_attr_done[dev] = true;
   }
+  static int ctas_per_sm[64];
+  if (dev < 64 && ctas_per_sm[dev] == 0) {
+    int nb = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, topk_stream_kernel, kThreads, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    ctas_per_sm[dev] = nb > 0 ? nb : 1;
+  }
   const long long units = (long long)p.rows * p.chunks;
-  const int grid = (int)std::min<long long>(units, 2LL * num_sms);
+  const int grid = (int)std::min<long long>(units, (long long)(dev < 64 ? ctas_per_sm[dev] : 1) * num_sms);
   topk_stream_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.chunks == 1) return e;
