@@ -254,31 +254,6 @@ __device__ __forceinline__ unsigned long long composite(uint32_t key, int32_t id
   return (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(idx));
 }
 
-// Sort 512 composites into descending order, one per thread (tid < 512),
-// using warp shuffles for strides < 32 and `buf` (512 entries) otherwise.
-__device__ __forceinline__ unsigned long long bitonic_desc512(unsigned long long v, unsigned long long* buf, int tid,
-                                                              int bar) {
-#pragma unroll 1
-  for (int size = 2; size <= 512; size <<= 1) {
-    const bool asc = (tid & size) != 0;
-#pragma unroll 1
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      unsigned long long p;
-      if (stride >= 32) {
-        buf[tid] = v;
-        named_bar(bar, 512);
-        p = buf[tid ^ stride];
-        named_bar(bar, 512);
-      } else {
-        p = __shfl_xor_sync(0xFFFFFFFFu, v, stride);
-      }
-      const bool lower = (tid & stride) == 0;
-      const bool keep_max = (lower != asc);
-      v = keep_max ? (v > p ? v : p) : (v < p ? v : p);
-    }
-  }
-  return v;
-}
 
 // ------------------------------------------------------------------------
 // Block-wide helpers for a 512-thread group (named barrier `bar`).
@@ -468,45 +443,6 @@ __device__ void fast_select512(const uint32_t* ckey, const int32_t* cidx, int n,
   named_bar(bar, 512);
 }
 
-// Sort the `cnt` (<= 512) entries of aux_key/aux_idx by (key desc, index
-// asc). Each thread returns its entry's composite and its output rank;
-// threads tid >= cnt get composite 0 and rank tid (the padding positions).
-// `runs` needs 512 entries.
-__device__ __forceinline__ int rank_sort512(const uint32_t* aux_key, const int32_t* aux_idx, int cnt,
-                                            unsigned long long* runs, unsigned long long* out_v, int tid, int bar) {
-  const int lane = tid & 31, warp = tid >> 5;
-  unsigned long long v = tid < cnt ? composite(aux_key[tid], aux_idx[tid]) : 0ull;
-  // sort each warp's 32 entries descending
-#pragma unroll
-  for (int size = 2; size <= 32; size <<= 1) {
-    const bool asc = (lane & size) != 0 && size < 32;
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const unsigned long long p = __shfl_xor_sync(0xFFFFFFFFu, v, stride);
-      const bool lower = (lane & stride) == 0;
-      const bool keep_max = (lower != asc);
-      v = keep_max ? (v > p ? v : p) : (v < p ? v : p);
-    }
-  }
-  runs[tid] = v;
-  named_bar(bar, 512);
-  int rank = lane;
-#pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    if (r == warp) continue;
-    const unsigned long long* run = runs + 32 * r;
-    // number of entries of the descending run that are > v (0..32)
-    int pos = run[31] > v ? 32 : 0;
-#pragma unroll
-    for (int s = 16; s > 0; s >>= 1)
-      if (pos + s <= 31 && run[pos + s - 1] > v) pos += s;
-    rank += pos;
-  }
-  named_bar(bar, 512);  // runs may be reused after this
-  *out_v = v;
-  return rank;  // meaningful only when v != 0
-}
-
 // Float threshold equivalent to "order key >= tau" for every non-NaN x.
 __device__ __forceinline__ float tau_float(uint32_t tau) {
   if (tau <= 0x007FFFFFu) return __int_as_float(0xFF800000);  // -inf: everything passes
@@ -594,14 +530,16 @@ __device__ uint32_t select512_to_aux(const uint32_t* ckey, const int32_t* cidx, 
 
 // Sort the `cnt` (<= 512) entries of aux_key/aux_idx by (key desc, index
 // asc): 16 runs of 32 are sorted by warp shuffles, then each entry's rank is
-// its place in its run plus, for every other run, the number of larger
-// entries (binary search). Thread tid handles runs warp, warp+NW, ...; for
-// each, v[e] is its entry's composite (0 = padding) and rank[e] its output
-// position. `runs` needs 512 entries.
+// its place in its run plus, for every other run, the number of entries
+// before it (binary search over the run's 32-bit keys: a run spans the 32
+// banks once, so the search is conflict-free; equal keys are then ordered
+// by index). Thread tid handles runs warp, warp+NW, ...; for each, k/ix[e]
+// is its entry (ix = -1: padding) and rank[e] its output position.
+// `runs_key` / `runs_idx` need 512 entries each.
 template <int NT>
 __device__ __forceinline__ void rank_sort(const uint32_t* aux_key, const int32_t* aux_idx, int cnt,
-                                          unsigned long long* runs, unsigned long long (&v)[kTopK / NT],
-                                          int (&rank)[kTopK / NT], int tid, int bar) {
+                                          uint32_t* runs_key, int32_t* runs_idx, uint32_t (&k)[kTopK / NT],
+                                          int32_t (&ix)[kTopK / NT], int (&rank)[kTopK / NT], int tid, int bar) {
   constexpr int NW = NT / 32;
   constexpr int E = kTopK / NT;
   const int lane = tid & 31, warp = tid >> 5;
@@ -620,23 +558,28 @@ __device__ __forceinline__ void rank_sort(const uint32_t* aux_key, const int32_t
         x = (lower != asc) ? (x > p ? x : p) : (x < p ? x : p);
       }
     }
-    runs[j] = x;
-    v[e] = x;
+    k[e] = static_cast<uint32_t>(x >> 32);
+    ix[e] = x ? static_cast<int32_t>(~static_cast<uint32_t>(x & 0xFFFFFFFFull)) : -1;
+    runs_key[j] = k[e];
+    runs_idx[j] = ix[e];
   }
   named_bar(bar, NT);
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const int r0 = warp + NW * e;
     int rk = lane;
-    const unsigned long long x = v[e];
+    const uint32_t xk = k[e];
+    const int32_t xi = ix[e];
 #pragma unroll 4
     for (int r = 0; r < 16; ++r) {
       if (r == r0) continue;
-      const unsigned long long* run = runs + 32 * r;
-      int pos = run[31] > x ? 32 : 0;
+      const uint32_t* run = runs_key + 32 * r;
+      int pos = run[31] > xk ? 32 : 0;
 #pragma unroll
       for (int s = 16; s > 0; s >>= 1)
-        if (pos + s <= 31 && run[pos + s - 1] > x) pos += s;
+        if (pos + s <= 31 && run[pos + s - 1] > xk) pos += s;
+      // padding entries (key 0, index -1) never precede a real entry
+      while (pos < 32 && run[pos] == xk && runs_idx[32 * r + pos] >= 0 && runs_idx[32 * r + pos] < xi) ++pos;
       rk += pos;
     }
     rank[e] = rk;

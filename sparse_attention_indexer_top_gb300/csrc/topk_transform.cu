@@ -61,6 +61,7 @@ struct StageDesc {
   int flags;         // 1: first stage of the unit, 2: last stage of the unit
   int head, tail;    // scalar elements: [lo, lo+head) and [tail_at, tail_at+tail)
   int lo, tail_at;
+  int len;           // elements of the unit's window range [lo, lo+len)
   long long woff;    // element offset of the row's window start in `scores`
 };
 
@@ -71,13 +72,17 @@ struct __align__(128) Smem {
       uint32_t key[kCap];
       int32_t idx[kCap];
     } c;
-    unsigned long long runs[kTopK];  // final sort (the list is dead by then)
+    struct {
+      uint32_t key[kTopK];
+      int32_t idx[kTopK];
+    } runs;  // final sort (the list is dead by then)
   } cand;
   uint32_t aux_key[kTopK];
   int32_t aux_idx[kTopK];
   StageDesc desc[kNStage];
   uint64_t full[kNStage];
   SelectScratch sc;
+  uint32_t spec_keys[2];  // keys at ranks 256 and 512 of the last finished unit
   int add[3];
 };
 
@@ -155,6 +160,7 @@ __device__ void issue_stage(const TopkLaunch& p, Smem& S, Cursor& c, int slot, u
   d.tail = c.s == 0 ? c.tail : 0;
   d.lo = c.lo;
   d.tail_at = c.lo + c.head + c.body;
+  d.len = c.head + c.body + c.tail;
   d.woff = c.woff;
   if (d.nvec > 0) {
     mbar_arrive_expect_tx(&S.full[slot], (uint32_t)d.nvec * 4u);
@@ -195,48 +201,36 @@ __device__ __forceinline__ void append_keys(uint32_t* ckey, int32_t* cidx, int b
   }
 }
 
-// Write one row's output from a 512-thread group: the entry of composite v
-// goes to position `rank`; threads tid >= cnt write the -1 padding at tid.
-__device__ __forceinline__ void emit_ranked(long long row, int batch, unsigned long long v, int rank, int cnt,
-                                            int tid, const int* pt, long long pt_stride, int ps, int* out_slots,
-                                            int* out_idx, float* out_scores) {
-  const long long o = row * kTopK;
-  if (v != 0ull) {
-    const int idx = static_cast<int>(~static_cast<uint32_t>(v & 0xFFFFFFFFull));
-    if (out_idx) out_idx[o + rank] = idx;
-    if (out_scores) out_scores[o + rank] = key_to_float(static_cast<uint32_t>(v >> 32));
-    if (out_slots) {
-      int slot = -1;
-      if (pt) {
-        const long long page = pt[(long long)batch * pt_stride + (ps == 1 ? idx : idx / ps)];
-        slot = static_cast<int>(ps == 1 ? page : page * ps + idx % ps);
-      }
-      out_slots[o + rank] = slot;
+// Append a block of up to 9 elements per thread (bit i of `mask`: element
+// i passes the filter), then cut the list back to the top 512 when it is
+// nearly full. `rot` rotates the three shared append counters; all 128
+// threads call this with uniform cnt/tau/rot.
+__device__ __forceinline__ void add_block(Smem& S, const float (&vals)[9], const int32_t (&idxs)[9], uint32_t mask,
+                                          int& cnt, uint32_t& tau, uint32_t& rot, int& appended, int tid) {
+  append_keys<9>(S.cand.c.key, S.cand.c.idx, cnt, &S.add[rot % 3], vals, idxs, mask, tid & 31);
+  named_bar(kBar, kThreads);
+  if (tid == 0) S.add[(rot + 2) % 3] = 0;  // counter of block rot+2; last read before this barrier
+  const int added = S.add[rot % 3];
+  ++rot;
+  cnt += added;
+  appended += added;
+  if (cnt > kPruneAt) {
+    uint32_t* const ckey = S.cand.c.key;
+    int32_t* const cidx = S.cand.c.idx;
+    tau = max(tau, select512_to_aux<kThreads, kCap>(ckey, cidx, cnt, S.aux_key, S.aux_idx, S.sc, tid, kBar));
+    for (int j = tid; j < kTopK; j += kThreads) {
+      ckey[j] = S.aux_key[j];
+      cidx[j] = S.aux_idx[j];
     }
-  }
-  if (tid >= cnt) {
-    if (out_idx) out_idx[o + tid] = -1;
-    if (out_slots) out_slots[o + tid] = -1;
-    if (out_scores) out_scores[o + tid] = __int_as_float(0x7FC00000);
-  }
-}
-
-__device__ __forceinline__ void emit_one(long long o, int batch, unsigned long long v, int rank,
-                                         const TopkLaunch& p) {
-  if (v == 0ull) return;
-  const int idx = static_cast<int>(~static_cast<uint32_t>(v & 0xFFFFFFFFull));
-  if (p.out_idx) p.out_idx[o + rank] = idx;
-  if (p.out_slots) {
-    const int ps = p.page_size;
-    const long long page = p.page_tables[(long long)batch * p.pt_stride + (ps == 1 ? idx : idx / ps)];
-    p.out_slots[o + rank] = static_cast<int>(ps == 1 ? page : page * ps + idx % ps);
+    named_bar(kBar, kThreads);
+    cnt = kTopK;
   }
 }
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const __grid_constant__ TopkLaunch p) {
   extern __shared__ unsigned char smem_raw[];
   Smem& S = smem_ref(smem_raw);
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x;
   uint32_t* const ckey = S.cand.c.key;
   int32_t* const cidx = S.cand.c.idx;
   Cursor cur{};
@@ -257,9 +251,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
     }
   }
   __syncthreads();
-  uint32_t it = 0;
-  int cnt = 0;       // candidates held before the current stage (uniform)
-  uint32_t tau = 0;  // keep elements whose order key >= tau
+  uint32_t it = 0, rot = 0;
+  int cnt = 0;        // candidates held (uniform)
+  int appended = 0;   // elements that passed the filter in this unit
+  uint32_t tau = 0;   // keep elements whose order key >= tau
+  uint32_t spec = 0;  // speculative starting threshold for the next unit (0: none)
+  uint32_t spec_used = 0;
   while (true) {
     const int slot = it % kNStage;
     const uint32_t ph = (it / kNStage) & 1u;
@@ -270,11 +267,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
     const int unit = ok ? d.unit : 0;
     if (unit < 0) break;
     const int flags = ok ? d.flags : 0, nvec = ok ? d.nvec : 0, base = d.base, row = d.row, batch = d.batch;
-    const int head = ok ? d.head : 0, tail = ok ? d.tail : 0, lo = d.lo, tail_at = d.tail_at;
+    const int head = ok ? d.head : 0, tail = ok ? d.tail : 0, lo = d.lo, tail_at = d.tail_at, len = d.len;
     const long long woff = d.woff;
     if (flags & 1) {
       cnt = 0;
-      tau = 0;
+      appended = 0;
+      // Start from the previous unit's threshold estimate; whether it was
+      // low enough is checked exactly when the unit ends.
+      tau = spec;
+      spec_used = spec;
     }
     const float tf = tau_float(tau);
     float vals[9];
@@ -310,7 +311,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
       idxs[8] = j;
       mask |= (vals[8] >= tf ? 1u : 0u) << 8;
     }
-    append_keys<9>(ckey, cidx, cnt, &S.add[it % 3], vals, idxs, mask, lane);
     if (!named_bar_and(kBar, kThreads, ok)) {
       if (tid == 0) {
         atomicOr(p.status, kDevWaitTimeout);
@@ -319,25 +319,37 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
       }
       break;
     }
-    if (tid == 0) {
-      S.add[(it + 2) % 3] = 0;  // counter of stage it+2; last read before this barrier
-      if (issuing) {            // refill the slot just consumed
-        fence_proxy_async_smem();
-        issuing = cur.unit < p.rows * p.chunks;
-        issue_stage(p, S, cur, slot, policy);
-      }
+    if (tid == 0 && issuing) {  // the slot's data is in registers: refill it now
+      fence_proxy_async_smem();
+      issuing = cur.unit < p.rows * p.chunks;
+      issue_stage(p, S, cur, slot, policy);
     }
-    cnt += S.add[it % 3];
-    if (cnt > kPruneAt) {
-      tau = max(tau, select512_to_aux<kThreads, kCap>(ckey, cidx, cnt, S.aux_key, S.aux_idx, S.sc, tid, kBar));
-      for (int j = tid; j < kTopK; j += kThreads) {
-        ckey[j] = S.aux_key[j];
-        cidx[j] = S.aux_idx[j];
-      }
-      named_bar(kBar, kThreads);
-      cnt = kTopK;
-    }
+    add_block(S, vals, idxs, mask, cnt, tau, rot, appended, tid);
     if (flags & 2) {
+      if (spec_used && appended < min(len, kTopK)) {
+        // The starting threshold was too high for this unit: redo it from
+        // global memory with no threshold (exact again, just slower).
+        cnt = 0;
+        appended = 0;
+        tau = 0;
+        for (int b0 = 0; b0 < len; b0 += 8 * kThreads) {
+          const float tf0 = tau_float(tau);
+          float rv[9];
+          int32_t ri[9];
+          uint32_t rm = 0;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int j = b0 + k * kThreads + tid;
+            if (j < len) {
+              rv[k] = __ldg(p.scores + woff + lo + j);
+              ri[k] = lo + j;
+              rm |= (rv[k] >= tf0 ? 1u : 0u) << k;
+            }
+          }
+          add_block(S, rv, ri, rm, cnt, tau, rot, appended, tid);
+        }
+        spec_used = 0;
+      }
       if (cnt > kTopK) {
         select512_to_aux<kThreads, kCap>(ckey, cidx, cnt, S.aux_key, S.aux_idx, S.sc, tid, kBar);
         cnt = kTopK;
@@ -348,25 +360,52 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
         }
         named_bar(kBar, kThreads);
       }
+      uint32_t k[kTopK / kThreads];
+      int32_t ix[kTopK / kThreads];
+      int rk[kTopK / kThreads];
+      rank_sort<kThreads>(S.aux_key, S.aux_idx, cnt, S.cand.runs.key, S.cand.runs.idx, k, ix, rk, tid, kBar);
+      if (tid == 0) S.spec_keys[0] = S.spec_keys[1] = 0;
+      named_bar(kBar, kThreads);
+#pragma unroll
+      for (int e = 0; e < kTopK / kThreads; ++e) {
+        if (ix[e] >= 0 && rk[e] == kTopK / 2 - 1) S.spec_keys[0] = k[e];
+        if (ix[e] >= 0 && rk[e] == kTopK - 1) S.spec_keys[1] = k[e];
+      }
       if (p.chunks == 1) {
-        unsigned long long v[kTopK / kThreads];
-        int rk[kTopK / kThreads];
-        rank_sort<kThreads>(S.aux_key, S.aux_idx, cnt, S.cand.runs, v, rk, tid, kBar);
         const long long o = (long long)row * kTopK;
 #pragma unroll
-        for (int e = 0; e < kTopK / kThreads; ++e) emit_one(o, batch, v[e], rk[e], p);
+        for (int e = 0; e < kTopK / kThreads; ++e) {
+          if (ix[e] < 0) continue;
+          if (p.out_idx) p.out_idx[o + rk[e]] = ix[e];
+          if (p.out_slots) {
+            const int ps = p.page_size;
+            const long long page = p.page_tables[(long long)batch * p.pt_stride + (ps == 1 ? ix[e] : ix[e] / ps)];
+            p.out_slots[o + rk[e]] = static_cast<int>(ps == 1 ? page : page * ps + ix[e] % ps);
+          }
+        }
         for (int j = cnt + tid; j < kTopK; j += kThreads) {
           if (p.out_idx) p.out_idx[o + j] = -1;
           if (p.out_slots) p.out_slots[o + j] = -1;
         }
       } else {
         const long long o = (long long)unit * kTopK;
-        for (int j = tid; j < cnt; j += kThreads) {
-          p.part_key[o + j] = S.aux_key[j];
-          p.part_idx[o + j] = S.aux_idx[j];
+#pragma unroll
+        for (int e = 0; e < kTopK / kThreads; ++e) {
+          if (ix[e] < 0) continue;
+          p.part_key[o + rk[e]] = k[e];
+          p.part_idx[o + rk[e]] = ix[e];
         }
         if (tid == 0) p.part_cnt[unit] = cnt;
-        named_bar(kBar, kThreads);
+      }
+      named_bar(kBar, kThreads);
+      // Next unit's starting threshold: extrapolate the tail one octave of
+      // rank down, t = 2*v(512) - v(256), which keeps about twice the
+      // needed count when neighbouring rows look alike.
+      spec = 0;
+      if (S.spec_keys[1] != 0) {
+        const float v256 = key_to_float(S.spec_keys[0]), v512 = key_to_float(S.spec_keys[1]);
+        const float t = 2.0f * v512 - v256;
+        if (isfinite(t) && isfinite(v256) && isfinite(v512)) spec = order_key(t);
       }
       cnt = 0;
     }
@@ -384,7 +423,10 @@ struct __align__(16) MergeSmem {
       uint32_t key[kMergeCap];
       int32_t idx[kMergeCap];
     } c;
-    unsigned long long runs[kTopK];
+    struct {
+      uint32_t key[kTopK];
+      int32_t idx[kTopK];
+    } runs;
   } cand;
   uint32_t hist[4096];
   uint32_t aux_key[kTopK];
@@ -422,11 +464,26 @@ __global__ void __launch_bounds__(kTopK, 1) merge_kernel(const __grid_constant__
     }
     __syncthreads();
   }
-  unsigned long long v;
-  const int rank = rank_sort512(S.aux_key, S.aux_idx, cnt, S.cand.runs, &v, tid, 1);
-  const int batch = cnt > 0 ? (p.row_to_batch ? p.row_to_batch[row] : (int)row) : 0;
-  emit_ranked(row, batch, v, rank, cnt, tid, p.page_tables, p.pt_stride, p.page_size, p.out_slots, p.out_idx,
-              p.out_scores);
+  uint32_t k[1];
+  int32_t ix[1];
+  int rk[1];
+  rank_sort<kTopK>(S.aux_key, S.aux_idx, cnt, S.cand.runs.key, S.cand.runs.idx, k, ix, rk, tid, 1);
+  const long long o = row * kTopK;
+  if (ix[0] >= 0) {
+    if (p.out_idx) p.out_idx[o + rk[0]] = ix[0];
+    if (p.out_scores) p.out_scores[o + rk[0]] = key_to_float(k[0]);
+    if (p.out_slots) {
+      const int batch = p.row_to_batch ? p.row_to_batch[row] : (int)row;
+      const int ps = p.page_size;
+      const long long page = p.page_tables[(long long)batch * p.pt_stride + (ps == 1 ? ix[0] : ix[0] / ps)];
+      p.out_slots[o + rk[0]] = static_cast<int>(ps == 1 ? page : page * ps + ix[0] % ps);
+    }
+  }
+  if (tid >= cnt) {
+    if (p.out_idx) p.out_idx[o + tid] = -1;
+    if (p.out_slots) p.out_slots[o + tid] = -1;
+    if (p.out_scores) p.out_scores[o + tid] = __int_as_float(0x7FC00000);
+  }
 }
 
 bool g_attr_done[64];

@@ -72,6 +72,16 @@ def test_packed_extend_ragged(stride_pad):
     _assert_equal(_run(inp, force_single=True), _oracle(inp), f"packed single pad={stride_pad}")
 
 
+@pytest.mark.parametrize("single", [False, True])
+def test_row_to_row_scale_changes(single):
+    # Rows whose scale jumps by 1e3 between neighbours: a threshold carried
+    # over from one row to the next is often far too high or too low.
+    lens = np.random.default_rng(3).integers(0, 3000, size=2500).astype(np.int32)
+    lens[::7] = 512
+    inp = W.make_topk_inputs(33, lens, 3001, 1, (2500, 3001), kind="scaled", fill=np.inf)
+    _assert_equal(_run(inp, force_single=single), _oracle(inp), "scaled rows")
+
+
 def test_unaligned_base_pointer():
     inp = W.packed_extend(seed=13, reqs=2, new_tokens=50, kv_len=7001, fill=np.inf)
     big = np.full((inp.rows, inp.scores.shape[1] + 1), np.inf, np.float32)

@@ -87,6 +87,8 @@ def _row_values(seed: int, row: int, n: int, kind: str) -> np.ndarray:
         v[u < 0.002] = np.inf
         v[(u >= 0.002) & (u < 0.004)] = -np.inf
         return v
+    if kind == "scaled":  # N(0,1) times 1e-3, 1 or 1e3, varying from row to row
+        return g.standard_normal(n, dtype=np.float32) * np.float32(10.0 ** (3 * ((row * 7919) % 3 - 1)))
     if kind == "ascending":  # worst order for a streaming filter
         return np.sort(g.standard_normal(n, dtype=np.float32))
     if kind == "descending":
