@@ -84,6 +84,13 @@ struct __align__(128) Smem {
   SelectScratch sc;
   uint32_t spec_keys[2];  // keys at ranks 256 and 512 of the last finished unit
   int add[3];
+  struct Cursor {         // thread 0's walk over its work units (issue side)
+    int unit;             // current unit (>= units: done)
+    int s, nst;           // stage index within the unit, stage count
+    int row, batch;
+    int lo, head, body, tail;
+    long long woff;
+  } cur;
 };
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 128;  // + alignment slack
@@ -94,14 +101,7 @@ __device__ __forceinline__ Smem& smem_ref(unsigned char* raw) {
   return *reinterpret_cast<Smem*>(a);
 }
 
-// Work-unit walker owned by thread 0: yields the stages to issue, in order.
-struct Cursor {
-  int unit;      // current unit (>= units: done)
-  int s, nst;    // stage index within the unit, stage count
-  int row, batch;
-  long long woff;
-  int lo, head, body, tail;
-};
+using Cursor = Smem::Cursor;
 
 __device__ void cursor_load(const TopkLaunch& p, Cursor& c) {
   const int units = p.rows * p.chunks;
@@ -142,13 +142,15 @@ __device__ void cursor_load(const TopkLaunch& p, Cursor& c) {
 }
 
 // Issue the cursor's next stage into `slot` (thread 0 only) and advance.
-__device__ void issue_stage(const TopkLaunch& p, Smem& S, Cursor& c, int slot, uint64_t policy) {
+// Returns false once the terminal descriptor has been issued.
+__device__ bool issue_stage(const TopkLaunch& p, Smem& S, int slot, uint64_t policy) {
+  Cursor& c = S.cur;
   const int units = p.rows * p.chunks;
   StageDesc& d = S.desc[slot];
   if (c.unit >= units) {
     d.unit = -1;
     mbar_arrive(&S.full[slot]);
-    return;
+    return false;
   }
   d.unit = c.unit;
   d.row = c.row;
@@ -172,42 +174,42 @@ __device__ void issue_stage(const TopkLaunch& p, Smem& S, Cursor& c, int slot, u
     c.unit += gridDim.x;
     cursor_load(p, c);
   }
+  return true;
 }
 
-// Append the elements whose bit is set in `mask` at positions base +
-// running count; one shared atomic per warp.
-template <int M>
-__device__ __forceinline__ void append_keys(uint32_t* ckey, int32_t* cidx, int base, int* counter,
-                                            const float (&vals)[M], const int32_t (&idxs)[M], uint32_t mask,
-                                            int lane) {
+// One block of up to 9 elements per thread: a = elements base+4t..+3,
+// b = elements base+512+4t..+3, x = one scalar element at index xi; bit i
+// of `mask` says element i passes the filter. Survivors are appended to the
+// candidate list (one shared atomic per warp), and the list is cut back to
+// the top 512 when it is nearly full. `rot` rotates the three shared append
+// counters; all 128 threads call this with uniform cnt/tau/rot.
+__device__ __forceinline__ void add_block(Smem& S, const float4& a, const float4& b, float x, int xi, int base,
+                                          uint32_t mask, int& cnt, uint32_t& tau, uint32_t& rot, int& appended,
+                                          int tid) {
+  const int lane = tid & 31;
   const int m = __popc(mask);
-  if (!__any_sync(0xFFFFFFFFu, m > 0)) return;
-  int incl = m;
+  if (__any_sync(0xFFFFFFFFu, m > 0)) {
+    int incl = m;
 #pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-    if (lane >= d) incl += o;
-  }
-  int start = 0;
-  if (lane == 31) start = atomicAdd(counter, incl);
-  int pos = __shfl_sync(0xFFFFFFFFu, start, 31) + base + incl - m;
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+      if (lane >= d) incl += o;
+    }
+    int start = 0;
+    if (lane == 31) start = atomicAdd(&S.add[rot % 3], incl);
+    int pos = __shfl_sync(0xFFFFFFFFu, start, 31) + cnt + incl - m;
+    if (mask) {
+      const float v[9] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, x};
 #pragma unroll
-  for (int i = 0; i < M; ++i) {
-    if (mask & (1u << i)) {
-      ckey[pos] = order_key(vals[i]);
-      cidx[pos] = idxs[i];
-      ++pos;
+      for (int i = 0; i < 9; ++i) {
+        if (mask & (1u << i)) {
+          S.cand.c.key[pos] = order_key(v[i]);
+          S.cand.c.idx[pos] = i < 4 ? base + 4 * tid + i : (i < 8 ? base + 4 * (kThreads + tid) + (i - 4) : xi);
+          ++pos;
+        }
+      }
     }
   }
-}
-
-// Append a block of up to 9 elements per thread (bit i of `mask`: element
-// i passes the filter), then cut the list back to the top 512 when it is
-// nearly full. `rot` rotates the three shared append counters; all 128
-// threads call this with uniform cnt/tau/rot.
-__device__ __forceinline__ void add_block(Smem& S, const float (&vals)[9], const int32_t (&idxs)[9], uint32_t mask,
-                                          int& cnt, uint32_t& tau, uint32_t& rot, int& appended, int tid) {
-  append_keys<9>(S.cand.c.key, S.cand.c.idx, cnt, &S.add[rot % 3], vals, idxs, mask, tid & 31);
   named_bar(kBar, kThreads);
   if (tid == 0) S.add[(rot + 2) % 3] = 0;  // counter of block rot+2; last read before this barrier
   const int added = S.add[rot % 3];
@@ -227,13 +229,16 @@ __device__ __forceinline__ void add_block(Smem& S, const float (&vals)[9], const
   }
 }
 
+__device__ __forceinline__ uint32_t pass4(const float4& v, float tf) {
+  return (v.x >= tf ? 1u : 0u) | (v.y >= tf ? 2u : 0u) | (v.z >= tf ? 4u : 0u) | (v.w >= tf ? 8u : 0u);
+}
+
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const __grid_constant__ TopkLaunch p) {
   extern __shared__ unsigned char smem_raw[];
   Smem& S = smem_ref(smem_raw);
   const int tid = threadIdx.x;
   uint32_t* const ckey = S.cand.c.key;
   int32_t* const cidx = S.cand.c.idx;
-  Cursor cur{};
   uint64_t policy = 0;
   bool issuing = false;
   if (tid == 0) {
@@ -241,14 +246,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
     S.add[0] = S.add[1] = S.add[2] = 0;
     fence_mbar_init();
     policy = l2_policy_evict_first();
-    cur.unit = blockIdx.x;
-    cursor_load(p, cur);
+    S.cur.unit = blockIdx.x;
+    cursor_load(p, S.cur);
     issuing = true;
-    const int units = p.rows * p.chunks;
-    for (int i = 0; i < kNStage && issuing; ++i) {
-      issuing = cur.unit < units;
-      issue_stage(p, S, cur, i, policy);
-    }
+    for (int i = 0; i < kNStage && issuing; ++i) issuing = issue_stage(p, S, i, policy);
   }
   __syncthreads();
   uint32_t it = 0, rot = 0;
@@ -278,38 +279,22 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
       spec_used = spec;
     }
     const float tf = tau_float(tau);
-    float vals[9];
-    int32_t idxs[9];
+    float4 va = make_float4(0.f, 0.f, 0.f, 0.f), vb = va;
+    float vx = 0.f;
+    int xi = 0;
     uint32_t mask = 0;
     if (4 * tid < nvec) {
-      const float4 a = reinterpret_cast<const float4*>(S.stage[slot])[tid];
-      vals[0] = a.x;
-      vals[1] = a.y;
-      vals[2] = a.z;
-      vals[3] = a.w;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        idxs[i] = base + 4 * tid + i;
-        mask |= (vals[i] >= tf ? 1u : 0u) << i;
-      }
+      va = reinterpret_cast<const float4*>(S.stage[slot])[tid];
+      mask = pass4(va, tf);
     }
     if (4 * (kThreads + tid) < nvec) {
-      const float4 b = reinterpret_cast<const float4*>(S.stage[slot])[kThreads + tid];
-      vals[4] = b.x;
-      vals[5] = b.y;
-      vals[6] = b.z;
-      vals[7] = b.w;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        idxs[4 + i] = base + 4 * (kThreads + tid) + i;
-        mask |= (vals[4 + i] >= tf ? 1u : 0u) << (4 + i);
-      }
+      vb = reinterpret_cast<const float4*>(S.stage[slot])[kThreads + tid];
+      mask |= pass4(vb, tf) << 4;
     }
     if (tid < head + tail) {  // scalar ends of the window (first stage of a unit)
-      const int j = tid < head ? lo + tid : tail_at + (tid - head);
-      vals[8] = __ldg(p.scores + woff + j);
-      idxs[8] = j;
-      mask |= (vals[8] >= tf ? 1u : 0u) << 8;
+      xi = tid < head ? lo + tid : tail_at + (tid - head);
+      vx = __ldg(p.scores + woff + xi);
+      mask |= (vx >= tf ? 1u : 0u) << 8;
     }
     if (!named_bar_and(kBar, kThreads, ok)) {
       if (tid == 0) {
@@ -321,10 +306,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
     }
     if (tid == 0 && issuing) {  // the slot's data is in registers: refill it now
       fence_proxy_async_smem();
-      issuing = cur.unit < p.rows * p.chunks;
-      issue_stage(p, S, cur, slot, policy);
+      issuing = issue_stage(p, S, slot, policy);
     }
-    add_block(S, vals, idxs, mask, cnt, tau, rot, appended, tid);
+    add_block(S, va, vb, vx, xi, base, mask, cnt, tau, rot, appended, tid);
     if (flags & 2) {
       if (spec_used && appended < min(len, kTopK)) {
         // The starting threshold was too high for this unit: redo it from
@@ -332,21 +316,22 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
         cnt = 0;
         appended = 0;
         tau = 0;
-        for (int b0 = 0; b0 < len; b0 += 8 * kThreads) {
+        for (int b0 = 0; b0 < len; b0 += kStage) {
           const float tf0 = tau_float(tau);
-          float rv[9];
-          int32_t ri[9];
+          const float* src = p.scores + woff + lo + b0;
+          float r[8];
           uint32_t rm = 0;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const int j = b0 + k * kThreads + tid;
-            if (j < len) {
-              rv[k] = __ldg(p.scores + woff + lo + j);
-              ri[k] = lo + j;
-              rm |= (rv[k] >= tf0 ? 1u : 0u) << k;
+            const int j = (k < 4 ? 4 * tid + k : 4 * (kThreads + tid) + (k - 4));
+            r[k] = 0.f;
+            if (b0 + j < len) {
+              r[k] = __ldg(src + j);
+              rm |= (r[k] >= tf0 ? 1u : 0u) << k;
             }
           }
-          add_block(S, rv, ri, rm, cnt, tau, rot, appended, tid);
+          add_block(S, make_float4(r[0], r[1], r[2], r[3]), make_float4(r[4], r[5], r[6], r[7]), 0.f, 0, lo + b0,
+                    rm, cnt, tau, rot, appended, tid);
         }
         spec_used = 0;
       }
