@@ -111,9 +111,7 @@ __device__ Threshold radix_threshold(int n, uint32_t need, SelectScratch& sc, in
         const uint32_t o = v - t.base;
         if (shr64(o, t.lo) == t.prefix) bin = (o >> dlo) & dmask;
       }
-      // one shared atomic per distinct bin in the warp
-      const uint32_t peers = __match_any_sync(0xFFFFFFFFu, bin);
-      if (bin != 0xFFFFFFFFu && lane == __ffs(peers) - 1) atomicAdd(&sc.hist[bin], (uint32_t)__popc(peers));
+      if (bin != 0xFFFFFFFFu) atomicAdd(&sc.hist[bin], 1u);
     }
     named_bar(bar, NT);
     if (warp == 0) {

@@ -177,38 +177,50 @@ __device__ bool issue_stage(const TopkLaunch& p, Smem& S, int slot, uint64_t pol
   return true;
 }
 
-// One block of up to 9 elements per thread: a = elements base+4t..+3,
-// b = elements base+512+4t..+3, x = one scalar element at index xi; bit i
-// of `mask` says element i passes the filter. Survivors are appended to the
-// candidate list (one shared atomic per warp), and the list is cut back to
-// the top 512 when it is nearly full. `rot` rotates the three shared append
-// counters; all 128 threads call this with uniform cnt/tau/rot.
+// One block of up to 9 elements per thread. Thread (warp w, lane l) holds
+// a = elements base + 4*(64w + l) + 0..3, b = elements base + 4*(64w + 32 +
+// l) + 0..3 and one scalar element x at index xi; bit i of `mask` says
+// element i passes the filter. Survivors are appended to the candidate list
+// with one ballot per element slot and one shared atomic per warp; when the
+// list is nearly full it is cut back to the top 512. `rot` rotates the
+// three shared append counters; all 128 threads call this with uniform
+// cnt/tau/rot.
 __device__ __forceinline__ void add_block(Smem& S, const float4& a, const float4& b, float x, int xi, int base,
                                           uint32_t mask, int& cnt, uint32_t& tau, uint32_t& rot, int& appended,
                                           int tid) {
-  const int lane = tid & 31;
-  const int m = __popc(mask);
-  if (__any_sync(0xFFFFFFFFu, m > 0)) {
-    int incl = m;
+  const int lane = tid & 31, warp = tid >> 5;
+  if (__any_sync(0xFFFFFFFFu, mask != 0)) {
+    uint32_t bal[9];
+    int total = 0;
 #pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-      if (lane >= d) incl += o;
+    for (int i = 0; i < 9; ++i) {
+      bal[i] = __ballot_sync(0xFFFFFFFFu, (mask >> i) & 1u);
+      total += __popc(bal[i]);
     }
     int start = 0;
-    if (lane == 31) start = atomicAdd(&S.add[rot % 3], incl);
-    int pos = __shfl_sync(0xFFFFFFFFu, start, 31) + cnt + incl - m;
-    if (mask) {
-      const float v[9] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, x};
-#pragma unroll
-      for (int i = 0; i < 9; ++i) {
-        if (mask & (1u << i)) {
-          S.cand.c.key[pos] = order_key(v[i]);
-          S.cand.c.idx[pos] = i < 4 ? base + 4 * tid + i : (i < 8 ? base + 4 * (kThreads + tid) + (i - 4) : xi);
-          ++pos;
-        }
-      }
+    if (lane == 0) start = atomicAdd(&S.add[rot % 3], total);
+    int pos = __shfl_sync(0xFFFFFFFFu, start, 0) + cnt;
+    const uint32_t lt = (1u << lane) - 1u;
+    const int i0 = base + 4 * (64 * warp + lane), i1 = base + 4 * (64 * warp + 32 + lane);
+#define SAI_PUT(I, V, IDX)                                           \
+    if (bal[I]) {                                                    \
+      if ((mask >> (I)) & 1u) {                                      \
+        const int q = pos + __popc(bal[I] & lt);                     \
+        S.cand.c.key[q] = order_key(V);                              \
+        S.cand.c.idx[q] = (IDX);                                     \
+      }                                                              \
+      pos += __popc(bal[I]);                                         \
     }
+    SAI_PUT(0, a.x, i0 + 0)
+    SAI_PUT(1, a.y, i0 + 1)
+    SAI_PUT(2, a.z, i0 + 2)
+    SAI_PUT(3, a.w, i0 + 3)
+    SAI_PUT(4, b.x, i1 + 0)
+    SAI_PUT(5, b.y, i1 + 1)
+    SAI_PUT(6, b.z, i1 + 2)
+    SAI_PUT(7, b.w, i1 + 3)
+    SAI_PUT(8, x, xi)
+#undef SAI_PUT
   }
   named_bar(kBar, kThreads);
   if (tid == 0) S.add[(rot + 2) % 3] = 0;  // counter of block rot+2; last read before this barrier
@@ -283,12 +295,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
     float vx = 0.f;
     int xi = 0;
     uint32_t mask = 0;
-    if (4 * tid < nvec) {
-      va = reinterpret_cast<const float4*>(S.stage[slot])[tid];
+    const int q0 = 64 * (tid >> 5) + (tid & 31);  // float4 index of `va`; `vb` is q0 + 32
+    if (4 * q0 < nvec) {
+      va = reinterpret_cast<const float4*>(S.stage[slot])[q0];
       mask = pass4(va, tf);
     }
-    if (4 * (kThreads + tid) < nvec) {
-      vb = reinterpret_cast<const float4*>(S.stage[slot])[kThreads + tid];
+    if (4 * (q0 + 32) < nvec) {
+      vb = reinterpret_cast<const float4*>(S.stage[slot])[q0 + 32];
       mask |= pass4(vb, tf) << 4;
     }
     if (tid < head + tail) {  // scalar ends of the window (first stage of a unit)
@@ -321,9 +334,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
           const float* src = p.scores + woff + lo + b0;
           float r[8];
           uint32_t rm = 0;
+          const int q0 = 64 * (tid >> 5) + (tid & 31);
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const int j = (k < 4 ? 4 * tid + k : 4 * (kThreads + tid) + (k - 4));
+            const int j = (k < 4 ? 4 * q0 + k : 4 * (q0 + 32) + (k - 4));
             r[k] = 0.f;
             if (b0 + j < len) {
               r[k] = __ldg(src + j);
