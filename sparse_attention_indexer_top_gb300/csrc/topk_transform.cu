@@ -40,7 +40,8 @@
 namespace sai {
 namespace {
 
-constexpr int kThreads = 128;                    // 4 warps per CTA
+constexpr int kThreads = 128;                    // 4 consumer warps per CTA
+constexpr int kCtaThreads = kThreads + 32;       // + 1 producer warp
 constexpr int kStage = 1024;                     // floats per stage (4 KB): two float4 per thread
 constexpr int kNStage = 3;                       // 12 KB in flight per CTA
 constexpr int kCap = 2048;                       // candidate capacity
@@ -63,6 +64,7 @@ struct StageDesc {
   int lo, tail_at;
   int len;           // elements of the unit's window range [lo, lo+len)
   long long woff;    // element offset of the row's window start in `scores`
+  float extra_val[kMaxExtra];  // the scalar elements themselves (first stage only)
 };
 
 struct __align__(128) Smem {
@@ -81,6 +83,7 @@ struct __align__(128) Smem {
   int32_t aux_idx[kTopK];
   StageDesc desc[kNStage];
   uint64_t full[kNStage];
+  uint64_t empty[kNStage];  // one arrival per consumer warp once the slot is in registers
   SelectScratch sc;
   uint32_t spec_keys[2];  // keys at ranks 256 and 512 of the last finished unit
   int add[3];
@@ -164,6 +167,10 @@ __device__ bool issue_stage(const TopkLaunch& p, Smem& S, int slot, uint64_t pol
   d.tail_at = c.lo + c.head + c.body;
   d.len = c.head + c.body + c.tail;
   d.woff = c.woff;
+  for (int e = 0; e < d.head + d.tail; ++e) {
+    const int j = e < d.head ? d.lo + e : d.tail_at + (e - d.head);
+    d.extra_val[e] = __ldg(p.scores + c.woff + j);
+  }
   if (d.nvec > 0) {
     mbar_arrive_expect_tx(&S.full[slot], (uint32_t)d.nvec * 4u);
     bulk_g2s_stream(S.stage[slot], p.scores + c.woff + d.base, (uint32_t)d.nvec * 4u, &S.full[slot], policy);
@@ -245,25 +252,37 @@ __device__ __forceinline__ uint32_t pass4(const float4& v, float tf) {
   return (v.x >= tf ? 1u : 0u) | (v.y >= tf ? 2u : 0u) | (v.z >= tf ? 4u : 0u) | (v.w >= tf ? 8u : 0u);
 }
 
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const __grid_constant__ TopkLaunch p) {
+__global__ void __launch_bounds__(kCtaThreads, kCtasPerSm) topk_stream_kernel(const __grid_constant__ TopkLaunch p) {
   extern __shared__ unsigned char smem_raw[];
   Smem& S = smem_ref(smem_raw);
   const int tid = threadIdx.x;
   uint32_t* const ckey = S.cand.c.key;
   int32_t* const cidx = S.cand.c.idx;
-  uint64_t policy = 0;
-  bool issuing = false;
   if (tid == 0) {
-    for (int i = 0; i < kNStage; ++i) mbar_init(&S.full[i], 1);
+    for (int i = 0; i < kNStage; ++i) {
+      mbar_init(&S.full[i], 1);
+      mbar_init(&S.empty[i], kThreads / 32);
+    }
     S.add[0] = S.add[1] = S.add[2] = 0;
     fence_mbar_init();
-    policy = l2_policy_evict_first();
-    S.cur.unit = blockIdx.x;
-    cursor_load(p, S.cur);
-    issuing = true;
-    for (int i = 0; i < kNStage && issuing; ++i) issuing = issue_stage(p, S, i, policy);
   }
   __syncthreads();
+  if (tid >= kThreads) {  // producer warp: one lane walks the units and fills the ring
+    if (tid == kThreads) {
+      const uint64_t policy = l2_policy_evict_first();
+      S.cur.unit = blockIdx.x;
+      cursor_load(p, S.cur);
+      for (uint32_t j = 0;; ++j) {
+        const int slot = j % kNStage;
+        if (!mbar_wait(&S.empty[slot], ((j / kNStage) & 1u) ^ 1u)) {
+          atomicOr(p.status, kDevWaitTimeout);
+          break;  // the consumers then time out on `full` and stop too
+        }
+        if (!issue_stage(p, S, slot, policy)) break;
+      }
+    }
+    return;
+  }
   uint32_t it = 0, rot = 0;
   int cnt = 0;        // candidates held (uniform)
   int appended = 0;   // elements that passed the filter in this unit
@@ -306,20 +325,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
     }
     if (tid < head + tail) {  // scalar ends of the window (first stage of a unit)
       xi = tid < head ? lo + tid : tail_at + (tid - head);
-      vx = __ldg(p.scores + woff + xi);
+      vx = d.extra_val[tid];
       mask |= (vx >= tf ? 1u : 0u) << 8;
     }
+    __syncwarp();
+    if ((tid & 31) == 0 && ok) mbar_arrive(&S.empty[slot]);  // this warp is done with the slot
     if (!named_bar_and(kBar, kThreads, ok)) {
-      if (tid == 0) {
-        atomicOr(p.status, kDevWaitTimeout);
-        // let the copies already issued land before the CTA exits (bounded)
-        for (int k = 1; k < kNStage; ++k) mbar_wait(&S.full[(it + k) % kNStage], ((it + k) / kNStage) & 1u);
-      }
+      if (tid == 0) atomicOr(p.status, kDevWaitTimeout);
       break;
-    }
-    if (tid == 0 && issuing) {  // the slot's data is in registers: refill it now
-      fence_proxy_async_smem();
-      issuing = issue_stage(p, S, slot, policy);
     }
     add_block(S, va, vb, vx, xi, base, mask, cnt, tau, rot, appended, tid);
     if (flags & 2) {
@@ -538,13 +551,13 @@ cudaError_t launch_topk_transform(const TopkLaunch& p, int num_sms, cudaStream_t
   static int ctas_per_sm[64];
   if (dev < 64 && ctas_per_sm[dev] == 0) {
     int nb = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, topk_stream_kernel, kThreads, kSmemBytes);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, topk_stream_kernel, kCtaThreads, kSmemBytes);
     if (e != cudaSuccess) return e;
     ctas_per_sm[dev] = nb > 0 ? nb : 1;
   }
   const long long units = (long long)p.rows * p.chunks;
   const int grid = (int)std::min<long long>(units, (long long)(dev < 64 ? ctas_per_sm[dev] : 1) * num_sms);
-  topk_stream_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
+  topk_stream_kernel<<<grid, kCtaThreads, kSmemBytes, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.chunks == 1) return e;
   MergeLaunch m{};
