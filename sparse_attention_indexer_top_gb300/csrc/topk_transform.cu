@@ -8,33 +8,26 @@
 // addressing inside the top-k kernel is the "merge build sparse block into
 // topk" step of ROCm/ATOM PR #1282.
 //
-// GB300 design: one warp owns one work unit (a row, or a chunk of a long
-// row) at a time, with no synchronisation beyond the warp, so an SM runs a
-// dozen fully independent streams and hides each one's latency with the
-// others.
-//   * Each warp (a one-warp CTA) keeps its own ring of six 1 KB shared-memory
-//     stages filled with 1-D bulk TMA copies (cp.async.bulk + mbarrier
-//     complete_tx, evict-first in L2: every score is read once). The
-//     16-byte-aligned interior of each window goes through TMA; its <= 3
-//     leading and <= 3 trailing elements (any row stride, any row start) are
-//     read with scalar loads. This is the scalar path the pages require for
-//     strides that are not a multiple of 4, folded into every row instead of
-//     a separate fallback kernel.
-//   * Each lane compares its 8 scores of a stage against the running
-//     threshold tau and the warp appends the survivors (order key, row-local
-//     index) to its candidate list with one ballot per element slot. When
-//     the list is nearly full it is cut to the exact top 512 (warp radix
-//     select in shared memory) and tau rises to that cut, so the filter
-//     stays exact: every dropped element is beaten by 512 kept ones.
-//   * A unit starts from a threshold extrapolated from the warp's previous
-//     unit. Whether it was low enough is checked exactly at the unit end (at
-//     least min(n, 512) elements must have passed); if not, the unit is redone
-//     from global memory with no threshold.
+// GB300 design: many small persistent CTAs (4 warps, ~34 KB of shared
+// memory, six per SM), each streaming one work unit (a row, or a chunk of a
+// long row) at a time, so that the serial latency of one CTA's
+// stage -> filter -> barrier chain is hidden by the other CTAs on the SM.
+//   * Thread 0 keeps a ring of shared-memory stages filled with 1-D bulk TMA
+//     copies (cp.async.bulk + mbarrier complete_tx, evict-first in L2: every
+//     score is read once). The 16-byte-aligned interior of each window goes
+//     through TMA; its <= 3 leading and <= 3 trailing elements (any row
+//     stride, any row start) are read with scalar loads. This is the scalar
+//     path the pages require for strides that are not a multiple of 4,
+//     folded into every row instead of a separate fallback kernel.
+//   * Each thread compares its 8 scores of a stage against the running
+//     threshold tau (as a float) and appends the survivors (order key,
+//     row-local index) to a shared candidate list. When the list fills up it
+//     is cut to the exact top 512 (radix select in shared memory) and tau
+//     rises to that cut, so the filter stays exact: every dropped element is
+//     beaten by 512 kept ones.
 //   * At the end of a unit the candidates are cut to 512, sorted by
-//     (score desc, index asc) with a 512-element warp bitonic network (16 per
-//     lane, registers and shuffles), page-transformed and written (one unit
-//     per row), or written as a partial list for the merge kernel (split
-//     rows).
+//     (score desc, index asc), page-transformed and written (one unit per
+//     row), or written as a partial list for the merge kernel (split rows).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -47,51 +40,68 @@
 namespace sai {
 namespace {
 
-constexpr int kWS = 256;                         // floats per stage (1 KB): two float4 per lane
-constexpr int kNS = 6;                           // stages in flight per warp
-constexpr int kWCap = 1024;                      // candidate list per warp
+constexpr int kThreads = 128;                    // 4 warps per CTA
+constexpr int kStage = 1024;                     // floats per stage (4 KB): two float4 per thread
+constexpr int kNStage = 3;                       // 12 KB in flight per CTA
+constexpr int kCap = 2048;                       // candidate capacity
 constexpr int kMaxExtra = 8;                     // scalar head/tail elements of a window
-constexpr int kPruneAt = kWCap - kWS - kMaxExtra;
+constexpr int kPruneAt = kCap - kStage - kMaxExtra;
+constexpr int kBar = 1;                          // named barrier id (all 128 threads)
+constexpr int kCtasPerSm = 6;
 
-static_assert(kPruneAt >= kTopK, "room to keep the top 512 and append one stage");
-static_assert(kWCap % 32 == 0, "whole warp chunks");
+static_assert(kStage == 8 * kThreads, "two float4 per thread per stage");
+static_assert(kPruneAt > kTopK, "room to keep the top 512 and append one stage");
 
-struct SlotInfo {
-  int unit;  // -1: no more work
-  int row, batch;
-  int base, nvec;  // row-local index of stage element 0; TMA elements (multiple of 4)
-  int flags;       // 1: first stage of the unit, 2: last stage of the unit
-  int lo, len;     // the unit's range of the window: [lo, lo + len)
-  int nextra;      // scalar elements (first stage only)
-  int pad_;
-  long long woff;  // element offset of the row's window start in `scores`
-  int extra_idx[kMaxExtra];
-  float extra_val[kMaxExtra];
+struct StageDesc {
+  int unit;          // -1: no more work
+  int row;
+  int batch;         // page-table row
+  int base;          // row-local index of stage element 0
+  int nvec;          // TMA elements in this stage (multiple of 4)
+  int flags;         // 1: first stage of the unit, 2: last stage of the unit
+  int head, tail;    // scalar elements: [lo, lo+head) and [tail_at, tail_at+tail)
+  int lo, tail_at;
+  int len;           // elements of the unit's window range [lo, lo+len)
+  long long woff;    // element offset of the row's window start in `scores`
 };
 
-struct __align__(128) WarpSmem {
-  float stage[kNS][kWS];
-  uint32_t ckey[kWCap];
-  int32_t cidx[kWCap];
-  uint32_t hist[256];
-  SlotInfo info[kNS];
-  uint64_t full[kNS];
+struct __align__(128) Smem {
+  float stage[kNStage][kStage];
+  union {
+    struct {
+      uint32_t key[kCap];
+      int32_t idx[kCap];
+    } c;
+    struct {
+      uint32_t key[kTopK];
+      int32_t idx[kTopK];
+    } runs;  // final sort (the list is dead by then)
+  } cand;
+  uint32_t aux_key[kTopK];
+  int32_t aux_idx[kTopK];
+  StageDesc desc[kNStage];
+  uint64_t full[kNStage];
+  SelectScratch sc;
+  uint32_t spec_keys[2];  // keys at ranks 256 and 512 of the last finished unit
+  int add[3];
+  struct Cursor {         // thread 0's walk over its work units (issue side)
+    int unit;             // current unit (>= units: done)
+    int s, nst;           // stage index within the unit, stage count
+    int row, batch;
+    int lo, head, body, tail;
+    long long woff;
+  } cur;
 };
 
-constexpr size_t kSmemBytes = sizeof(WarpSmem) + 128;  // + alignment slack
+constexpr size_t kSmemBytes = sizeof(Smem) + 128;  // + alignment slack
 
-__device__ __forceinline__ WarpSmem& smem_ref(unsigned char* raw) {
+__device__ __forceinline__ Smem& smem_ref(unsigned char* raw) {
   uintptr_t a = reinterpret_cast<uintptr_t>(raw);
   a = (a + 127) & ~static_cast<uintptr_t>(127);
-  return *reinterpret_cast<WarpSmem*>(a);
+  return *reinterpret_cast<Smem*>(a);
 }
 
-// The warp's walk over its work units (warp-uniform registers).
-struct Cursor {
-  int unit, s, nst;
-  int row, batch, lo, head, body, tail;
-  long long woff;
-};
+using Cursor = Smem::Cursor;
 
 __device__ void cursor_load(const TopkLaunch& p, Cursor& c) {
   const int units = p.rows * p.chunks;
@@ -106,7 +116,7 @@ __device__ void cursor_load(const TopkLaunch& p, Cursor& c) {
   if (p.page_tables)
     bad = bad || b < 0 || b >= p.pt_rows || (n > 0 && (long long)(n - 1) / p.page_size >= p.pt_stride);
   if (bad) {
-    if ((threadIdx.x & 31) == 0) atomicOr(p.status, kDevBadRowMeta);
+    atomicOr(p.status, kDevBadRowMeta);
     n = 0;
     b = 0;
   }
@@ -128,50 +138,37 @@ __device__ void cursor_load(const TopkLaunch& p, Cursor& c) {
   c.head = head;
   c.body = body;
   c.tail = len - head - body;
-  c.nst = max(1, (body + kWS - 1) / kWS);
+  c.nst = max(1, (body + kStage - 1) / kStage);
 }
 
-// Issue the cursor's next stage into `slot` (whole warp) and advance.
+// Issue the cursor's next stage into `slot` (thread 0 only) and advance.
 // Returns false once the terminal descriptor has been issued.
-__device__ bool issue_stage(const TopkLaunch& p, WarpSmem& S, Cursor& c, int slot, uint64_t policy, int lane) {
+__device__ bool issue_stage(const TopkLaunch& p, Smem& S, int slot, uint64_t policy) {
+  Cursor& c = S.cur;
   const int units = p.rows * p.chunks;
-  SlotInfo& d = S.info[slot];
+  StageDesc& d = S.desc[slot];
   if (c.unit >= units) {
-    __syncwarp();
-    if (lane == 0) {
-      d.unit = -1;
-      mbar_arrive(&S.full[slot]);
-    }
+    d.unit = -1;
+    mbar_arrive(&S.full[slot]);
     return false;
   }
-  const int base = c.lo + c.head + c.s * kWS;
-  const int nvec = min(kWS, c.body - c.s * kWS);
-  const int nextra = c.s == 0 ? c.head + c.tail : 0;
-  if (lane < nextra) {
-    const int j = lane < c.head ? c.lo + lane : c.lo + c.head + c.body + (lane - c.head);
-    d.extra_idx[lane] = j;
-    d.extra_val[lane] = __ldg(p.scores + c.woff + j);
-  }
-  if (lane == 0) {
-    d.unit = c.unit;
-    d.row = c.row;
-    d.batch = c.batch;
-    d.base = base;
-    d.nvec = nvec;
-    d.flags = (c.s == 0 ? 1 : 0) | (c.s == c.nst - 1 ? 2 : 0);
-    d.lo = c.lo;
-    d.len = c.head + c.body + c.tail;
-    d.nextra = nextra;
-    d.woff = c.woff;
-  }
-  __syncwarp();
-  if (lane == 0) {
-    if (nvec > 0) {
-      mbar_arrive_expect_tx(&S.full[slot], (uint32_t)nvec * 4u);
-      bulk_g2s_stream(S.stage[slot], p.scores + c.woff + base, (uint32_t)nvec * 4u, &S.full[slot], policy);
-    } else {
-      mbar_arrive(&S.full[slot]);
-    }
+  d.unit = c.unit;
+  d.row = c.row;
+  d.batch = c.batch;
+  d.flags = (c.s == 0 ? 1 : 0) | (c.s == c.nst - 1 ? 2 : 0);
+  d.base = c.lo + c.head + c.s * kStage;
+  d.nvec = min(kStage, c.body - c.s * kStage);
+  d.head = c.s == 0 ? c.head : 0;
+  d.tail = c.s == 0 ? c.tail : 0;
+  d.lo = c.lo;
+  d.tail_at = c.lo + c.head + c.body;
+  d.len = c.head + c.body + c.tail;
+  d.woff = c.woff;
+  if (d.nvec > 0) {
+    mbar_arrive_expect_tx(&S.full[slot], (uint32_t)d.nvec * 4u);
+    bulk_g2s_stream(S.stage[slot], p.scores + c.woff + d.base, (uint32_t)d.nvec * 4u, &S.full[slot], policy);
+  } else {
+    mbar_arrive(&S.full[slot]);
   }
   if (++c.s >= c.nst) {
     c.unit += gridDim.x;
@@ -180,168 +177,55 @@ __device__ bool issue_stage(const TopkLaunch& p, WarpSmem& S, Cursor& c, int slo
   return true;
 }
 
-// ---------------------------------------------------------------- warp select
-// Threshold bin of the `need` largest values among the active entries j in
-// [0, n) (active/value from `get(j, v)`), by 8-bit radix digits over the
-// value range, for one warp. `need` must not exceed the active count.
-template <typename Get>
-__device__ Threshold warp_threshold(int n, uint32_t need, uint32_t* hist, int lane, Get get) {
-  uint32_t lmin = 0xFFFFFFFFu, lmax = 0u, lcnt = 0u;
-  for (int j = lane; j < n; j += 32) {
-    uint32_t v;
-    if (get(j, v)) {
-      lmin = min(lmin, v);
-      lmax = max(lmax, v);
-      ++lcnt;
-    }
-  }
-  Threshold t;
-  t.base = __reduce_min_sync(0xFFFFFFFFu, lmin);
-  const uint32_t span = __reduce_max_sync(0xFFFFFFFFu, lmax) - t.base;
-  const uint32_t nact = __reduce_add_sync(0xFFFFFFFFu, lcnt);
-  t.lo = span ? 32 - __clz(span) : 0;
-  t.prefix = 0;
-  t.need = need;
-  t.all_eq = (nact == need);
-  while (t.lo > 0 && !t.all_eq) {
-    const int dlo = t.lo > 8 ? t.lo - 8 : 0;
-    const int dbits = t.lo - dlo;
-    const uint32_t dmask = (1u << dbits) - 1u;
-    reinterpret_cast<uint4*>(hist)[2 * lane] = make_uint4(0, 0, 0, 0);
-    reinterpret_cast<uint4*>(hist)[2 * lane + 1] = make_uint4(0, 0, 0, 0);
-    __syncwarp();
-    for (int j = lane; j < n; j += 32) {
-      uint32_t v;
-      if (get(j, v)) {
-        const uint32_t o = v - t.base;
-        if (shr64(o, t.lo) == t.prefix) atomicAdd(&hist[(o >> dlo) & dmask], 1u);
-      }
-    }
-    __syncwarp();
-    const uint4 a = reinterpret_cast<const uint4*>(hist)[2 * lane];
-    const uint4 b = reinterpret_cast<const uint4*>(hist)[2 * lane + 1];
-    const uint32_t h[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    uint32_t tot = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) tot += h[i];
-    uint32_t suf = tot;
+// One block of up to 9 elements per thread: a = elements base+4t..+3,
+// b = elements base+512+4t..+3, x = one scalar element at index xi; bit i
+// of `mask` says element i passes the filter. Survivors are appended to the
+// candidate list (one shared atomic per warp), and the list is cut back to
+// the top 512 when it is nearly full. `rot` rotates the three shared append
+// counters; all 128 threads call this with uniform cnt/tau/rot.
+__device__ __forceinline__ void add_block(Smem& S, const float4& a, const float4& b, float x, int xi, int base,
+                                          uint32_t mask, int& cnt, uint32_t& tau, uint32_t& rot, int& appended,
+                                          int tid) {
+  const int lane = tid & 31;
+  const int m = __popc(mask);
+  if (__any_sync(0xFFFFFFFFu, m > 0)) {
+    int incl = m;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-      const uint32_t o = __shfl_down_sync(0xFFFFFFFFu, suf, d);
-      if (lane + d < 32) suf += o;
+      const int o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+      if (lane >= d) incl += o;
     }
-    uint32_t above = suf - tot;
-    const uint32_t nd = t.need;
-    uint32_t bin = 0, need_after = 0, bcount = 0;
-    const bool mine = above < nd && nd <= suf;
-    if (mine) {
+    int start = 0;
+    if (lane == 31) start = atomicAdd(&S.add[rot % 3], incl);
+    int pos = __shfl_sync(0xFFFFFFFFu, start, 31) + cnt + incl - m;
+    if (mask) {
+      const float v[9] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, x};
 #pragma unroll
-      for (int i = 7; i >= 0; --i) {
-        if (above < nd && nd <= above + h[i]) {
-          bin = lane * 8 + i;
-          need_after = nd - above;
-          bcount = h[i];
-        }
-        above += h[i];
-      }
-    }
-    const int src = __ffs(__ballot_sync(0xFFFFFFFFu, mine)) - 1;
-    bin = __shfl_sync(0xFFFFFFFFu, bin, src);
-    need_after = __shfl_sync(0xFFFFFFFFu, need_after, src);
-    bcount = __shfl_sync(0xFFFFFFFFu, bcount, src);
-    t.prefix = (t.prefix << dbits) | bin;
-    t.need = need_after;
-    t.all_eq = (bcount == t.need);
-    t.lo = dlo;
-    __syncwarp();
-  }
-  return t;
-}
-
-// Cut the warp's list ckey/cidx[0, n), n > 512, to its top 512 by (key
-// desc, index asc), compacted in place to [0, 512). Returns the lowest key
-// of the final threshold bin (<= the 512th key): "key >= returned value" is
-// a valid filter for later elements.
-__device__ uint32_t warp_select512(WarpSmem& S, int n, int lane) {
-  uint32_t* const ckey = S.ckey;
-  int32_t* const cidx = S.cidx;
-  const Threshold t = warp_threshold(n, (uint32_t)kTopK, S.hist, lane, [&](int j, uint32_t& v) {
-    v = ckey[j];
-    return true;
-  });
-  Threshold ti{};
-  const bool ties = !t.all_eq;
-  if (ties) {
-    ti = warp_threshold(n, t.need, S.hist, lane, [&](int j, uint32_t& v) {
-      v = 0x7FFFFFFFu - static_cast<uint32_t>(cidx[j]);
-      return thr_cmp(t, ckey[j]) == 0;
-    });
-  }
-  // In-place compaction: chunk c is read before any of its selected entries
-  // is written, and a write position never exceeds its read position.
-  int out = 0;
-  const uint32_t lt = (1u << lane) - 1u;
-  for (int j0 = 0; j0 < n; j0 += 32) {
-    const int j = j0 + lane;
-    bool sel = false;
-    uint32_t key = 0;
-    int32_t idx = 0;
-    if (j < n) {
-      key = ckey[j];
-      idx = cidx[j];
-      const int cc = thr_cmp(t, key);
-      sel = cc > 0 || (cc == 0 && (!ties || thr_cmp(ti, 0x7FFFFFFFu - static_cast<uint32_t>(idx)) >= 0));
-    }
-    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, sel);
-    __syncwarp();
-    if (sel) {
-      const int pos = out + __popc(bal & lt);
-      if (pos < kTopK) {
-        ckey[pos] = key;
-        cidx[pos] = idx;
-      }
-    }
-    out += __popc(bal);
-    __syncwarp();
-  }
-  return t.base + static_cast<uint32_t>(static_cast<uint64_t>(t.prefix) << t.lo);
-}
-
-// Sort the warp's list ckey/cidx[0, cnt), cnt <= 512, by (key desc, index
-// asc): bitonic network over the virtual index vi = 16*lane + s, so that on
-// return v[s] holds the entry of output rank 16*lane + s (0 = padding).
-__device__ __forceinline__ void warp_sort512(const WarpSmem& S, int cnt, unsigned long long (&v)[16], int lane) {
-#pragma unroll
-  for (int s = 0; s < 16; ++s) {
-    const int e = 32 * s + lane;  // any placement works: everything gets sorted
-    v[s] = e < cnt ? composite(S.ckey[e], S.cidx[e]) : 0ull;
-  }
-#pragma unroll
-  for (int size = 2; size <= 512; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      if (stride < 16) {
-#pragma unroll
-        for (int s = 0; s < 16; ++s) {
-          if (s & stride) continue;
-          const int s2 = s | stride;
-          const bool asc = ((16 * lane + s) & size) != 0;
-          const unsigned long long x = v[s], y = v[s2];
-          const unsigned long long hi = x > y ? x : y, lo = x > y ? y : x;
-          v[s] = asc ? lo : hi;
-          v[s2] = asc ? hi : lo;
-        }
-      } else {
-        const int d = stride >> 4;
-        const bool lower = (lane & d) == 0;
-        const bool asc = (lane & (size >> 4)) != 0;
-#pragma unroll
-        for (int s = 0; s < 16; ++s) {
-          const unsigned long long p = __shfl_xor_sync(0xFFFFFFFFu, v[s], d);
-          v[s] = (lower != asc) ? (v[s] > p ? v[s] : p) : (v[s] < p ? v[s] : p);
+      for (int i = 0; i < 9; ++i) {
+        if (mask & (1u << i)) {
+          S.cand.c.key[pos] = order_key(v[i]);
+          S.cand.c.idx[pos] = i < 4 ? base + 4 * tid + i : (i < 8 ? base + 4 * (kThreads + tid) + (i - 4) : xi);
+          ++pos;
         }
       }
     }
+  }
+  named_bar(kBar, kThreads);
+  if (tid == 0) S.add[(rot + 2) % 3] = 0;  // counter of block rot+2; last read before this barrier
+  const int added = S.add[rot % 3];
+  ++rot;
+  cnt += added;
+  appended += added;
+  if (cnt > kPruneAt) {
+    uint32_t* const ckey = S.cand.c.key;
+    int32_t* const cidx = S.cand.c.idx;
+    tau = max(tau, select512_to_aux<kThreads, kCap>(ckey, cidx, cnt, S.aux_key, S.aux_idx, S.sc, tid, kBar));
+    for (int j = tid; j < kTopK; j += kThreads) {
+      ckey[j] = S.aux_key[j];
+      cidx[j] = S.aux_idx[j];
+    }
+    named_bar(kBar, kThreads);
+    cnt = kTopK;
   }
 }
 
@@ -349,84 +233,48 @@ __device__ __forceinline__ uint32_t pass4(const float4& v, float tf) {
   return (v.x >= tf ? 1u : 0u) | (v.y >= tf ? 2u : 0u) | (v.z >= tf ? 4u : 0u) | (v.w >= tf ? 8u : 0u);
 }
 
-// Append the elements whose bit is set in `mask` to the warp's list: lane
-// holds a = elements base+4*lane+0..3, b = elements base+128+4*lane+0..3 and
-// one scalar element x at index xi. One ballot per element slot.
-__device__ __forceinline__ int warp_append(WarpSmem& S, const float4& a, const float4& b, float x, int xi, int base,
-                                           uint32_t mask, int wcnt, int lane) {
-  if (!__any_sync(0xFFFFFFFFu, mask != 0)) return wcnt;
-  const uint32_t lt = (1u << lane) - 1u;
-  int pos = wcnt;
-  const int i0 = base + 4 * lane, i1 = base + 128 + 4 * lane;
-#define SAI_PUT(I, V, IDX)                                  \
-  {                                                         \
-    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, (mask >> (I)) & 1u); \
-    if (bal) {                                              \
-      if ((mask >> (I)) & 1u) {                             \
-        const int q = pos + __popc(bal & lt);               \
-        S.ckey[q] = order_key(V);                           \
-        S.cidx[q] = (IDX);                                  \
-      }                                                     \
-      pos += __popc(bal);                                   \
-    }                                                       \
-  }
-  SAI_PUT(0, a.x, i0 + 0)
-  SAI_PUT(1, a.y, i0 + 1)
-  SAI_PUT(2, a.z, i0 + 2)
-  SAI_PUT(3, a.w, i0 + 3)
-  SAI_PUT(4, b.x, i1 + 0)
-  SAI_PUT(5, b.y, i1 + 1)
-  SAI_PUT(6, b.z, i1 + 2)
-  SAI_PUT(7, b.w, i1 + 3)
-  SAI_PUT(8, x, xi)
-#undef SAI_PUT
-  __syncwarp();
-  return pos;
-}
-
-// ---------------------------------------------------------------- kernel
-__global__ void __launch_bounds__(32) topk_stream_kernel(const __grid_constant__ TopkLaunch p) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const __grid_constant__ TopkLaunch p) {
   extern __shared__ unsigned char smem_raw[];
-  WarpSmem& S = smem_ref(smem_raw);
-  const int lane = threadIdx.x;
-  if (lane == 0) {
-    for (int i = 0; i < kNS; ++i) mbar_init(&S.full[i], 1);
+  Smem& S = smem_ref(smem_raw);
+  const int tid = threadIdx.x;
+  uint32_t* const ckey = S.cand.c.key;
+  int32_t* const cidx = S.cand.c.idx;
+  uint64_t policy = 0;
+  bool issuing = false;
+  if (tid == 0) {
+    for (int i = 0; i < kNStage; ++i) mbar_init(&S.full[i], 1);
+    S.add[0] = S.add[1] = S.add[2] = 0;
     fence_mbar_init();
+    policy = l2_policy_evict_first();
+    S.cur.unit = blockIdx.x;
+    cursor_load(p, S.cur);
+    issuing = true;
+    for (int i = 0; i < kNStage && issuing; ++i) issuing = issue_stage(p, S, i, policy);
   }
-  __syncwarp();
-  const uint64_t policy = l2_policy_evict_first();
-  Cursor cur{};
-  cur.unit = blockIdx.x;
-  cursor_load(p, cur);
-  bool issuing = true;
-  for (int i = 0; i < kNS && issuing; ++i) issuing = issue_stage(p, S, cur, i, policy, lane);
-
-  uint32_t it = 0;
-  int wcnt = 0;        // entries in the candidate list
-  int wapp = 0;        // elements that passed the filter in this unit
-  uint32_t tau = 0;    // keep elements whose order key >= tau
-  uint32_t spec = 0;   // starting threshold for the next unit (0: none)
+  __syncthreads();
+  uint32_t it = 0, rot = 0;
+  int cnt = 0;        // candidates held (uniform)
+  int appended = 0;   // elements that passed the filter in this unit
+  uint32_t tau = 0;   // keep elements whose order key >= tau
+  uint32_t spec = 0;  // speculative starting threshold for the next unit (0: none)
   uint32_t spec_used = 0;
   while (true) {
-    const int slot = it % kNS;
-    const uint32_t ph = (it / kNS) & 1u;
-    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&S.full[slot], ph))) {
-      if (lane == 0) {
-        atomicOr(p.status, kDevWaitTimeout);
-        // let copies already issued land before the CTA exits (bounded)
-        for (int k = 1; k < kNS; ++k) mbar_wait(&S.full[(it + k) % kNS], ((it + k) / kNS) & 1u);
-      }
-      break;
-    }
-    const SlotInfo& d = S.info[slot];
-    const int unit = d.unit;
+    const int slot = it % kNStage;
+    const uint32_t ph = (it / kNStage) & 1u;
+    const bool ok = mbar_wait(&S.full[slot], ph);
+    const StageDesc& d = S.desc[slot];
+    // after a timeout the descriptor is not trusted: process nothing, then
+    // leave together at the barrier below
+    const int unit = ok ? d.unit : 0;
     if (unit < 0) break;
-    const int flags = d.flags, nvec = d.nvec, base = d.base, row = d.row, batch = d.batch;
-    const int lo = d.lo, len = d.len, nextra = d.nextra;
+    const int flags = ok ? d.flags : 0, nvec = ok ? d.nvec : 0, base = d.base, row = d.row, batch = d.batch;
+    const int head = ok ? d.head : 0, tail = ok ? d.tail : 0, lo = d.lo, tail_at = d.tail_at, len = d.len;
     const long long woff = d.woff;
     if (flags & 1) {
-      wcnt = 0;
-      wapp = 0;
+      cnt = 0;
+      appended = 0;
+      // Start from the previous unit's threshold estimate; whether it was
+      // low enough is checked exactly when the unit ends.
       tau = spec;
       spec_used = spec;
     }
@@ -435,128 +283,116 @@ __global__ void __launch_bounds__(32) topk_stream_kernel(const __grid_constant__
     float vx = 0.f;
     int xi = 0;
     uint32_t mask = 0;
-    if (4 * lane < nvec) {
-      va = reinterpret_cast<const float4*>(S.stage[slot])[lane];
+    if (4 * tid < nvec) {
+      va = reinterpret_cast<const float4*>(S.stage[slot])[tid];
       mask = pass4(va, tf);
     }
-    if (4 * (lane + 32) < nvec) {
-      vb = reinterpret_cast<const float4*>(S.stage[slot])[lane + 32];
+    if (4 * (kThreads + tid) < nvec) {
+      vb = reinterpret_cast<const float4*>(S.stage[slot])[kThreads + tid];
       mask |= pass4(vb, tf) << 4;
     }
-    if (lane < nextra) {
-      xi = d.extra_idx[lane];
-      vx = d.extra_val[lane];
+    if (tid < head + tail) {  // scalar ends of the window (first stage of a unit)
+      xi = tid < head ? lo + tid : tail_at + (tid - head);
+      vx = __ldg(p.scores + woff + xi);
       mask |= (vx >= tf ? 1u : 0u) << 8;
     }
-    __syncwarp();
-    if (issuing) {  // the slot's data is in registers: refill it
-      if (lane == 0) fence_proxy_async_smem();
-      issuing = issue_stage(p, S, cur, slot, policy, lane);
+    if (!named_bar_and(kBar, kThreads, ok)) {
+      if (tid == 0) {
+        atomicOr(p.status, kDevWaitTimeout);
+        // let the copies already issued land before the CTA exits (bounded)
+        for (int k = 1; k < kNStage; ++k) mbar_wait(&S.full[(it + k) % kNStage], ((it + k) / kNStage) & 1u);
+      }
+      break;
     }
-    const int nw = warp_append(S, va, vb, vx, xi, base, mask, wcnt, lane);
-    wapp += nw - wcnt;
-    wcnt = nw;
-    if (wcnt > kPruneAt) {
-      tau = max(tau, warp_select512(S, wcnt, lane));
-      wcnt = kTopK;
+    if (tid == 0 && issuing) {  // the slot's data is in registers: refill it now
+      fence_proxy_async_smem();
+      issuing = issue_stage(p, S, slot, policy);
     }
+    add_block(S, va, vb, vx, xi, base, mask, cnt, tau, rot, appended, tid);
     if (flags & 2) {
-      if (spec_used && wapp < min(len, kTopK)) {
+      if (spec_used && appended < min(len, kTopK)) {
         // The starting threshold was too high for this unit: redo it from
         // global memory with no threshold (exact again, just slower).
-        wcnt = 0;
-        wapp = 0;
+        cnt = 0;
+        appended = 0;
         tau = 0;
-        for (int b0 = 0; b0 < len; b0 += kWS) {
+        for (int b0 = 0; b0 < len; b0 += kStage) {
           const float tf0 = tau_float(tau);
           const float* src = p.scores + woff + lo + b0;
           float r[8];
           uint32_t rm = 0;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const int j = k < 4 ? 4 * lane + k : 128 + 4 * lane + (k - 4);
+            const int j = (k < 4 ? 4 * tid + k : 4 * (kThreads + tid) + (k - 4));
             r[k] = 0.f;
             if (b0 + j < len) {
               r[k] = __ldg(src + j);
               rm |= (r[k] >= tf0 ? 1u : 0u) << k;
             }
           }
-          const int nw2 = warp_append(S, make_float4(r[0], r[1], r[2], r[3]), make_float4(r[4], r[5], r[6], r[7]),
-                                      0.f, 0, lo + b0, rm, wcnt, lane);
-          wapp += nw2 - wcnt;
-          wcnt = nw2;
-          if (wcnt > kPruneAt) {
-            tau = max(tau, warp_select512(S, wcnt, lane));
-            wcnt = kTopK;
-          }
+          add_block(S, make_float4(r[0], r[1], r[2], r[3]), make_float4(r[4], r[5], r[6], r[7]), 0.f, 0, lo + b0,
+                    rm, cnt, tau, rot, appended, tid);
         }
         spec_used = 0;
       }
-      if (wcnt > kTopK) {
-        warp_select512(S, wcnt, lane);
-        wcnt = kTopK;
+      if (cnt > kTopK) {
+        select512_to_aux<kThreads, kCap>(ckey, cidx, cnt, S.aux_key, S.aux_idx, S.sc, tid, kBar);
+        cnt = kTopK;
+      } else {
+        for (int j = tid; j < cnt; j += kThreads) {
+          S.aux_key[j] = ckey[j];
+          S.aux_idx[j] = cidx[j];
+        }
+        named_bar(kBar, kThreads);
       }
-      unsigned long long v[16];
-      warp_sort512(S, wcnt, v, lane);
-      __syncwarp();
+      uint32_t k[kTopK / kThreads];
+      int32_t ix[kTopK / kThreads];
+      int rk[kTopK / kThreads];
+      rank_sort<kThreads>(S.aux_key, S.aux_idx, cnt, S.cand.runs.key, S.cand.runs.idx, k, ix, rk, tid, kBar);
+      if (tid == 0) S.spec_keys[0] = S.spec_keys[1] = 0;
+      named_bar(kBar, kThreads);
+#pragma unroll
+      for (int e = 0; e < kTopK / kThreads; ++e) {
+        if (ix[e] >= 0 && rk[e] == kTopK / 2 - 1) S.spec_keys[0] = k[e];
+        if (ix[e] >= 0 && rk[e] == kTopK - 1) S.spec_keys[1] = k[e];
+      }
       if (p.chunks == 1) {
-        const long long o = (long long)row * kTopK + 16 * lane;
-        int oi[16], os[16];
+        const long long o = (long long)row * kTopK;
 #pragma unroll
-        for (int s = 0; s < 16; ++s) {
-          const bool real = 16 * lane + s < wcnt;
-          const int idx = real ? static_cast<int>(~static_cast<uint32_t>(v[s] & 0xFFFFFFFFull)) : -1;
-          oi[s] = idx;
-          os[s] = -1;
-          if (real && p.page_tables) {
+        for (int e = 0; e < kTopK / kThreads; ++e) {
+          if (ix[e] < 0) continue;
+          if (p.out_idx) p.out_idx[o + rk[e]] = ix[e];
+          if (p.out_slots) {
             const int ps = p.page_size;
-            const long long page = p.page_tables[(long long)batch * p.pt_stride + (ps == 1 ? idx : idx / ps)];
-            os[s] = static_cast<int>(ps == 1 ? page : page * ps + idx % ps);
+            const long long page = p.page_tables[(long long)batch * p.pt_stride + (ps == 1 ? ix[e] : ix[e] / ps)];
+            p.out_slots[o + rk[e]] = static_cast<int>(ps == 1 ? page : page * ps + ix[e] % ps);
           }
         }
-        const bool vec = ((reinterpret_cast<uintptr_t>(p.out_idx) | reinterpret_cast<uintptr_t>(p.out_slots)) & 15u) == 0;
-        if (p.out_idx) {
-          if (vec) {
-            int4* dst = reinterpret_cast<int4*>(p.out_idx + o);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = make_int4(oi[4 * q], oi[4 * q + 1], oi[4 * q + 2], oi[4 * q + 3]);
-          } else {
-#pragma unroll
-            for (int s = 0; s < 16; ++s) p.out_idx[o + s] = oi[s];
-          }
-        }
-        if (p.out_slots) {
-          if (vec) {
-            int4* dst = reinterpret_cast<int4*>(p.out_slots + o);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = make_int4(os[4 * q], os[4 * q + 1], os[4 * q + 2], os[4 * q + 3]);
-          } else {
-#pragma unroll
-            for (int s = 0; s < 16; ++s) p.out_slots[o + s] = os[s];
-          }
+        for (int j = cnt + tid; j < kTopK; j += kThreads) {
+          if (p.out_idx) p.out_idx[o + j] = -1;
+          if (p.out_slots) p.out_slots[o + j] = -1;
         }
       } else {
-        const long long o = (long long)unit * kTopK + 16 * lane;
+        const long long o = (long long)unit * kTopK;
 #pragma unroll
-        for (int s = 0; s < 16; ++s) {
-          if (16 * lane + s < wcnt) {
-            p.part_key[o + s] = static_cast<uint32_t>(v[s] >> 32);
-            p.part_idx[o + s] = static_cast<int32_t>(~static_cast<uint32_t>(v[s] & 0xFFFFFFFFull));
-          }
+        for (int e = 0; e < kTopK / kThreads; ++e) {
+          if (ix[e] < 0) continue;
+          p.part_key[o + rk[e]] = k[e];
+          p.part_idx[o + rk[e]] = ix[e];
         }
-        if (lane == 0) p.part_cnt[unit] = wcnt;
+        if (tid == 0) p.part_cnt[unit] = cnt;
       }
+      named_bar(kBar, kThreads);
       // Next unit's starting threshold: extrapolate the tail one octave of
       // rank down, t = 2*v(512) - v(256), which keeps about twice the
       // needed count when neighbouring rows look alike.
       spec = 0;
-      const uint32_t k256 = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(v[15] >> 32), 15);
-      const uint32_t k512 = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(v[15] >> 32), 31);
-      if (wcnt >= kTopK && k512 != 0) {
-        const float t = 2.0f * key_to_float(k512) - key_to_float(k256);
-        if (isfinite(t) && isfinite(key_to_float(k256)) && isfinite(key_to_float(k512))) spec = order_key(t);
+      if (S.spec_keys[1] != 0) {
+        const float v256 = key_to_float(S.spec_keys[0]), v512 = key_to_float(S.spec_keys[1]);
+        const float t = 2.0f * v512 - v256;
+        if (isfinite(t) && isfinite(v256) && isfinite(v512)) spec = order_key(t);
       }
-      wcnt = 0;
+      cnt = 0;
     }
     ++it;
   }
@@ -688,13 +524,13 @@ cudaError_t launch_topk_transform(const TopkLaunch& p, int num_sms, cudaStream_t
   static int ctas_per_sm[64];
   if (dev < 64 && ctas_per_sm[dev] == 0) {
     int nb = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, topk_stream_kernel, 32, kSmemBytes);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, topk_stream_kernel, kThreads, kSmemBytes);
     if (e != cudaSuccess) return e;
     ctas_per_sm[dev] = nb > 0 ? nb : 1;
   }
   const long long units = (long long)p.rows * p.chunks;
   const int grid = (int)std::min<long long>(units, (long long)(dev < 64 ? ctas_per_sm[dev] : 1) * num_sms);
-  topk_stream_kernel<<<grid, 32, kSmemBytes, stream>>>(p);
+  topk_stream_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.chunks == 1) return e;
   MergeLaunch m{};
