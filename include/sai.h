@@ -110,6 +110,61 @@ int sai_topk_transform(const float* scores, int64_t rows, int64_t score_stride, 
                        int32_t* out_indices, void* workspace, size_t workspace_bytes, sai_stream_t stream);
 
 /*
+ * Workspace bytes that sai_index_score_topk needs for these sizes on the
+ * current device (the per-(row, KV chunk) candidate lists).
+ */
+size_t sai_index_score_topk_workspace(int64_t rows, int32_t max_seq_len, int32_t group_rows, int32_t k);
+
+/*
+ * sai_index_score_topk -- FP8 index scores and top-k in one pass.
+ *
+ * Follows ROCm/ATOM PR #1473 "enable minimax m3 fp8 index cache and fuse
+ * index_score_kernel with partial_topk kernel" (pull request overview: FP8
+ * index cache, the score computed in FP8, index score and partial top-k fused
+ * so that no score tensor is written; the fused decode kernel walks the
+ * request's block table and masks keys at or beyond the causal length).
+ * For each query row i, with b = row_to_batch ? row_to_batch[i] : i and
+ * n = seq_lens[i]:
+ *   score(t) = kscale[p*128 + o] * sum_h w[i*64 + h] * relu(sum_d q[i,h,d] k[p,o,d])
+ *   for t < n, p = block_table[b*bt_stride + t/128], o = t % 128;
+ * then the top-k keys by (score desc, index asc):
+ *   out_indices[i*512 + j] = t_j, out_slots[...] = p_j*128 + o_j,
+ *   out_scores[...] = score(t_j) (fp32), padded with -1 / NaN.
+ *
+ * q_fp8       e4m3fn [rows, heads, dim], 16-byte aligned.
+ * w           fp32 [rows, heads].
+ * kcache_fp8  e4m3fn [num_blocks, block_size, dim], 16-byte aligned.
+ * kscale      fp32 [num_blocks, block_size].
+ * block_table int32 [bt_rows, bt_stride]; block ids outside [0, num_blocks)
+ *             mask their keys and set status bit 4.
+ * seq_lens    int32 [rows], 0 <= n <= max_seq_len and ceil(n/128) <= bt_stride
+ *             (checked on device; a bad row is emptied and sets bit 1).
+ * heads = 64, dim = 128, block_size = 128, k = 512 (else SAI_ERR_UNSUPPORTED).
+ * group_rows  1, or 4 when every 4 consecutive rows share one row_to_batch
+ *             value (packed prefill): each CTA then scores 4 rows at once.
+ *             A group whose rows differ is emptied and sets bit 1.
+ * out_*       any of the three may be NULL, not all.
+ * workspace   at least sai_index_score_topk_workspace(...) bytes, 16-byte aligned.
+ */
+int sai_index_score_topk(const uint8_t* q_fp8, const float* w, const uint8_t* kcache_fp8, const float* kscale,
+                         int64_t num_blocks, const int32_t* block_table, int64_t bt_rows, int64_t bt_stride,
+                         const int32_t* row_to_batch, const int32_t* seq_lens, int64_t rows, int32_t heads,
+                         int32_t dim, int32_t block_size, int32_t max_seq_len, int32_t group_rows, int32_t k,
+                         int32_t* out_slots, int32_t* out_indices, float* out_scores, void* workspace,
+                         size_t workspace_bytes, sai_stream_t stream);
+
+/*
+ * sai_index_score -- the same FP8 index scores written densely (for tests):
+ * out_scores[i*out_stride + t] = score(i, t) for t < seq_lens[i]; other
+ * cells are not written. out_stride >= max_seq_len. Same argument rules.
+ */
+int sai_index_score(const uint8_t* q_fp8, const float* w, const uint8_t* kcache_fp8, const float* kscale,
+                    int64_t num_blocks, const int32_t* block_table, int64_t bt_rows, int64_t bt_stride,
+                    const int32_t* row_to_batch, const int32_t* seq_lens, int64_t rows, int32_t heads, int32_t dim,
+                    int32_t block_size, int32_t max_seq_len, int32_t group_rows, float* out_scores,
+                    int64_t out_stride, sai_stream_t stream);
+
+/*
  * Size of the library-owned device scratch used by
  * sai_topk_transform_noalloc: 8 MiB, held on every GPU that loads the
  * library until the process exits.

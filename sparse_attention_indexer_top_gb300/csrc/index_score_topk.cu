@@ -1,0 +1,405 @@
+// index_score_topk: FP8 index scores + top-512 in one pass, no score buffer.
+//
+// What is computed (ROCm/ATOM PR #1473 "enable minimax m3 fp8 index cache
+// and fuse index_score_kernel with partial_topk kernel": pull request
+// overview "Changes", the fused decode kernel over (query, index head, key
+// chunk) and its paged block loop in the review diff of index_topk.py):
+//
+//   score(i, t) = kscale[p, o] * sum_h w[i, h] * relu( q[i, h, :] . k[p, o, :] )
+//
+// with p = block_table[b][t / 128], o = t % 128, b = row_to_batch[i] (or i),
+// for every key t < seq_lens[i] (the causal length), then the top-512 keys
+// by (score desc, index asc), mapped to physical slots p*128 + o. The pages
+// name the fused kernel and its FP8 index cache but print no formula; this
+// is the formula the library adopts (scale outside the relu, no 1/sqrt(d)).
+//
+// GB300 design. One CTA takes a group of R query rows (R = 1 for decode,
+// R = 4 when consecutive rows share one request, as in prefill) and a chunk
+// of that request's KV blocks:
+//   * warp 4 streams each 128-token FP8 key block [128 keys x 128 dims]
+//     through a 4-stage shared-memory ring with 2-D TMA tensor loads (128-byte
+//     swizzle; the paged gather is just the block's row coordinate);
+//   * warp 5 issues tcgen05.mma kind::f8f6f4 with the keys as M = 128 and
+//     the group's R x 64 (row, head) query vectors as N, K = 128 dims in four
+//     K = 32 steps, accumulating in FP32 in tensor memory, double-buffered;
+//   * warps 0-3 own TMEM lanes 0-127, i.e. one key each: they load the key's
+//     R x 64 dot products with tcgen05.ld, apply relu, the per-head weights
+//     and the key's scale in FP32, and feed the scores into per-row running
+//     top-k filters (candidate lists cut back to 512 by a radix select in
+//     shared memory when they fill up).
+// The per-(row, chunk) candidate lists go to a workspace; the merge kernel
+// of topk_transform.cu then selects, sorts and page-transforms each row.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+
+#include "sai_internal.h"
+#include "sai_ptx.cuh"
+#include "sai_select.cuh"
+
+namespace sai {
+
+
+namespace {
+
+constexpr int kH = 64;        // index heads
+constexpr int kD = 128;       // head dim (bytes per fp8 row)
+constexpr int kBlk = 128;     // tokens per KV block = MMA M
+constexpr int kNSf = 4;       // K-tile stages
+constexpr int kFCap = 1024;   // candidate list per row
+constexpr int kFPruneAt = kFCap - kBlk;
+constexpr int kEpi = 128;     // epilogue threads (warps 0-3)
+constexpr int kFThreads = kEpi + 64;
+constexpr int kBarEpi = 1;
+
+template <int R>
+struct __align__(1024) FusedSmem {
+  uint8_t kst[kNSf][kBlk * kD];  // 16 KB each, 1024-byte aligned
+  uint8_t q[R * kH * kD];
+  float w[R * kH];
+  uint32_t ckey[R][kFCap];
+  int32_t cidx[R][kFCap];
+  uint32_t aux_key[kTopK];
+  int32_t aux_idx[kTopK];
+  SelectScratch sc;
+  uint64_t full[kNSf], empty[kNSf], tfull[2], tempty[2], qfull;
+  uint32_t tmem_base;
+  int add[R][3];
+};
+
+template <int R>
+constexpr size_t fused_smem_bytes() {
+  return sizeof(FusedSmem<R>) + 1024;
+}
+
+template <int R>
+__device__ __forceinline__ FusedSmem<R>& fused_smem(unsigned char* raw) {
+  uintptr_t a = reinterpret_cast<uintptr_t>(raw);
+  a = (a + 1023) & ~static_cast<uintptr_t>(1023);
+  return *reinterpret_cast<FusedSmem<R>*>(a);
+}
+
+// Row group metadata, recomputed identically by every thread.
+struct GroupMeta {
+  int row0, nrows;  // rows [row0, row0 + nrows)
+  int batch;
+  int nblk;         // blocks to visit for the group (max over its rows)
+  int blk0, blk1;   // this unit's block range
+};
+
+template <int R>
+__device__ GroupMeta group_meta(const FusedLaunch& p, int g, int c, int (&n)[R], bool report) {
+  GroupMeta m;
+  m.row0 = g * R;
+  m.nrows = min(R, p.rows - m.row0);
+  m.batch = p.row_to_batch ? p.row_to_batch[m.row0] : m.row0;
+  bool bad_batch = m.batch < 0 || m.batch >= p.bt_rows;
+  int nmax = 0;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    n[r] = 0;
+    if (r < m.nrows) {
+      const int row = m.row0 + r;
+      int nr = p.seq_lens[row];
+      const int br = p.row_to_batch ? p.row_to_batch[row] : row;
+      const bool bad = bad_batch || nr < 0 || nr > p.max_len || br != m.batch ||
+                       (long long)(nr + kBlk - 1) / kBlk > p.bt_stride;
+      if (bad) {
+        if (report) atomicOr(p.status, kDevBadRowMeta);
+        nr = 0;
+      }
+      n[r] = nr;
+      nmax = max(nmax, nr);
+    }
+  }
+  if (bad_batch) m.batch = 0;
+  m.nblk = (nmax + kBlk - 1) / kBlk;
+  m.blk0 = min(m.nblk, c * p.chunk_blocks);
+  m.blk1 = min(m.nblk, m.blk0 + p.chunk_blocks);
+  return m;
+}
+
+template <int R, bool DENSE>
+__global__ void __launch_bounds__(kFThreads, 1)
+    fused_score_topk_kernel(const __grid_constant__ FusedLaunch p, const __grid_constant__ CUtensorMap kmap,
+                            const __grid_constant__ CUtensorMap qmap) {
+  extern __shared__ unsigned char smem_raw[];
+  FusedSmem<R>& S = fused_smem<R>(smem_raw);
+  constexpr int N = R * kH;          // MMA N
+  constexpr uint32_t kCols = 2 * N;  // two accumulator buffers
+  constexpr uint32_t kIdesc = umma_idesc_e4m3(kBlk, N);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = blockIdx.x / p.chunks, c = blockIdx.x - g * p.chunks;
+  int n[R];
+  const GroupMeta m = group_meta<R>(p, g, c, n, tid == 0 && c == 0);
+  const int ntiles = m.blk1 - m.blk0;
+
+  if (tid == 0) {
+    for (int i = 0; i < kNSf; ++i) {
+      mbar_init(&S.full[i], 1);
+      mbar_init(&S.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.tfull[i], 1);
+      mbar_init(&S.tempty[i], kEpi / 32);
+    }
+    mbar_init(&S.qfull, 1);
+    for (int r = 0; r < R; ++r) S.add[r][0] = S.add[r][1] = S.add[r][2] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&S.tmem_base, kCols);
+    tmem_relinquish();
+  }
+  for (int i = tid; i < R * kH; i += kFThreads) {
+    const int r = i / kH;
+    S.w[i] = r < m.nrows ? p.w[(long long)(m.row0 + r) * kH + (i - r * kH)] : 0.f;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  bool ok = true;
+
+  if (warp == 4) {
+    // ---------------- TMA producer
+    if (lane == 0 && ntiles > 0) {
+      prefetch_tmap(&kmap);
+      prefetch_tmap(&qmap);
+      const uint64_t keep = l2_policy_evict_last();   // q and K are re-read by other CTAs
+      mbar_arrive_expect_tx(&S.qfull, (uint32_t)(N * kD));
+      tma_load_2d(S.q, &qmap, 0, m.row0 * kH, &S.qfull, keep);
+      for (int i = 0; i < ntiles; ++i) {
+        const int s = i % kNSf;
+        if (!mbar_wait(&S.empty[s], ((i / kNSf) & 1u) ^ 1u)) {
+          atomicOr(p.status, kDevWaitTimeout);
+          break;
+        }
+        int page = p.block_table[(long long)m.batch * p.bt_stride + m.blk0 + i];
+        if (page < 0 || page >= p.num_blocks) page = 0;  // the epilogue masks this block
+        mbar_arrive_expect_tx(&S.full[s], (uint32_t)(kBlk * kD));
+        tma_load_2d(S.kst[s], &kmap, 0, page * kBlk, &S.full[s], keep);
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------- MMA issuer
+    if (lane == 0 && ntiles > 0) {
+      bool run = mbar_wait(&S.qfull, 0);
+      const uint64_t bdesc = umma_desc_sw128_kmajor(smem_u32(S.q));
+      for (int i = 0; i < ntiles && run; ++i) {
+        const int s = i % kNSf, buf = i & 1;
+        run = mbar_wait(&S.full[s], (i / kNSf) & 1u) && mbar_wait(&S.tempty[buf], ((i >> 1) & 1u) ^ 1u);
+        if (!run) {
+          atomicOr(p.status, kDevWaitTimeout);
+          break;
+        }
+        tc_fence_after();
+        const uint64_t adesc = umma_desc_sw128_kmajor(smem_u32(S.kst[s]));
+#pragma unroll
+        for (int k = 0; k < kD / 32; ++k)
+          umma_f8(tmem + buf * N, adesc + 2 * k, bdesc + 2 * k, kIdesc, k > 0 ? 1u : 0u);
+        umma_commit(&S.empty[s]);
+        umma_commit(&S.tfull[buf]);
+      }
+    }
+  } else {
+    // ---------------- epilogue: one key (TMEM lane) per thread
+    uint32_t rot = 0;
+    int cnt[R];
+    uint32_t tau[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      cnt[r] = 0;
+      tau[r] = 0;
+    }
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    for (int i = 0; i < ntiles; ++i) {
+      const int blk = m.blk0 + i, buf = i & 1;
+      const int t = blk * kBlk + tid;
+      const int page = p.block_table[(long long)m.batch * p.bt_stride + blk];
+      const bool page_ok = page >= 0 && page < p.num_blocks;
+      const float ks = page_ok ? __ldg(p.kscale + (long long)page * kBlk + tid) : 0.f;
+      if (!page_ok && tid == 0) atomicOr(p.status, kDevBadPage);
+      ok = mbar_wait(&S.tfull[buf], (i >> 1) & 1u);
+      float score[R];
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          uint32_t a[32], b[32];
+          const uint32_t col = tmem + lane_base + static_cast<uint32_t>(buf * N + r * kH);
+          tmem_ld32(col, a);
+          tmem_ld32(col + 32, b);
+          tmem_ld_wait();
+          const float4* w4 = reinterpret_cast<const float4*>(S.w + r * kH);
+          float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+          for (int h4 = 0; h4 < 8; ++h4) {
+            const float4 wa = w4[h4], wb = w4[8 + h4];
+            acc0 = fmaf(wa.x, fmaxf(__uint_as_float(a[4 * h4 + 0]), 0.f), acc0);
+            acc1 = fmaf(wa.y, fmaxf(__uint_as_float(a[4 * h4 + 1]), 0.f), acc1);
+            acc0 = fmaf(wa.z, fmaxf(__uint_as_float(a[4 * h4 + 2]), 0.f), acc0);
+            acc1 = fmaf(wa.w, fmaxf(__uint_as_float(a[4 * h4 + 3]), 0.f), acc1);
+            acc0 = fmaf(wb.x, fmaxf(__uint_as_float(b[4 * h4 + 0]), 0.f), acc0);
+            acc1 = fmaf(wb.y, fmaxf(__uint_as_float(b[4 * h4 + 1]), 0.f), acc1);
+            acc0 = fmaf(wb.z, fmaxf(__uint_as_float(b[4 * h4 + 2]), 0.f), acc0);
+            acc1 = fmaf(wb.w, fmaxf(__uint_as_float(b[4 * h4 + 3]), 0.f), acc1);
+          }
+          score[r] = (acc0 + acc1) * ks;
+        }
+        tc_fence_before();
+      }
+      __syncwarp();
+      if (lane == 0 && ok) mbar_arrive(&S.tempty[buf]);
+      if (!named_bar_and(kBarEpi, kEpi, ok)) {
+        if (tid == 0) atomicOr(p.status, kDevWaitTimeout);
+        ok = false;
+        break;
+      }
+      if constexpr (DENSE) {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          if (r < m.nrows && t < n[r] && page_ok) p.dense[(long long)(m.row0 + r) * p.dense_stride + t] = score[r];
+      } else {
+        // running top-k filter per row: one ballot and one shared atomic per warp
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const bool pass = page_ok && t < n[r] && score[r] >= tau_float(tau[r]);
+          const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass);
+          if (bal) {
+            int start = 0;
+            if (lane == 0) start = atomicAdd(&S.add[r][rot % 3], __popc(bal));
+            start = __shfl_sync(0xFFFFFFFFu, start, 0);
+            if (pass) {
+              const int q = cnt[r] + start + __popc(bal & ((1u << lane) - 1u));
+              S.ckey[r][q] = order_key(score[r]);
+              S.cidx[r][q] = t;
+            }
+          }
+        }
+        named_bar(kBarEpi, kEpi);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          if (tid == 0) S.add[r][(rot + 2) % 3] = 0;
+          cnt[r] += S.add[r][rot % 3];
+          if (cnt[r] > kFPruneAt) {
+            tau[r] = max(tau[r], select512_to_aux<kEpi, kFCap>(S.ckey[r], S.cidx[r], cnt[r], S.aux_key, S.aux_idx,
+                                                               S.sc, tid, kBarEpi));
+            for (int j = tid; j < kTopK; j += kEpi) {
+              S.ckey[r][j] = S.aux_key[j];
+              S.cidx[r][j] = S.aux_idx[j];
+            }
+            named_bar(kBarEpi, kEpi);
+            cnt[r] = kTopK;
+          }
+        }
+        ++rot;
+      }
+    }
+    if constexpr (!DENSE) {
+      // unit end: cut each row's list to 512 and write it as a partial list
+      for (int r = 0; r < m.nrows; ++r) {
+        const long long unit = (long long)(m.row0 + r) * p.chunks + c;
+        int cr = ok ? cnt[r] : 0;
+        const uint32_t* src_k = S.ckey[r];
+        const int32_t* src_i = S.cidx[r];
+        if (cr > kTopK) {
+          select512_to_aux<kEpi, kFCap>(S.ckey[r], S.cidx[r], cr, S.aux_key, S.aux_idx, S.sc, tid, kBarEpi);
+          cr = kTopK;
+          src_k = S.aux_key;
+          src_i = S.aux_idx;
+        }
+        for (int j = tid; j < cr; j += kEpi) {
+          p.part_key[unit * kTopK + j] = src_k[j];
+          p.part_idx[unit * kTopK + j] = src_i[j];
+        }
+        if (tid == 0) p.part_cnt[unit] = cr;
+        named_bar(kBarEpi, kEpi);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// 2-D uint8 map over [rows, 128] with a [box_rows, 128] box, 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* base, long long rows, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kD), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int R, bool DENSE>
+cudaError_t launch_fused_t(const FusedLaunch& p, const uint8_t* kcache, cudaStream_t stream) {
+  CUtensorMap kmap, qmap;
+  if (!make_map(&kmap, kcache, p.num_blocks * kBlk, kBlk)) return cudaErrorInvalidValue;
+  if (!make_map(&qmap, p.q, (long long)p.rows * kH, R * kH)) return cudaErrorInvalidValue;
+  static bool attr_done[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  constexpr size_t smem = fused_smem_bytes<R>();
+  if (dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(fused_score_topk_kernel<R, DENSE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  const int groups = (p.rows + R - 1) / R;
+  fused_score_topk_kernel<R, DENSE><<<groups * p.chunks, kFThreads, smem, stream>>>(p, kmap, qmap);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+FusedPlan fused_plan(long long rows, int max_seq_len, int group_rows, int num_sms) {
+  FusedPlan pl{1, 1, 1, 0};
+  pl.group = (group_rows == 4 && rows >= 4) ? 4 : 1;
+  const long long max_blocks = std::max<long long>(1, ((long long)max_seq_len + kBlk - 1) / kBlk);
+  const long long groups = (rows + pl.group - 1) / pl.group;
+  const long long target = 4LL * num_sms;
+  long long chunks = groups > 0 ? (target + groups - 1) / groups : 1;
+  chunks = std::max<long long>(1, std::min<long long>({chunks, 12LL, max_blocks}));
+  const long long cb = (max_blocks + chunks - 1) / chunks;
+  pl.chunk_blocks = static_cast<int>(cb);
+  pl.chunks = static_cast<int>((max_blocks + cb - 1) / cb);
+  pl.workspace_bytes = static_cast<size_t>(rows) * pl.chunks * (kTopK * 8 + 4) + 256;
+  return pl;
+}
+
+cudaError_t launch_fused(const FusedLaunch& p, int group, bool dense, const uint8_t* kcache, cudaStream_t stream) {
+  if (group == 4) return dense ? launch_fused_t<4, true>(p, kcache, stream) : launch_fused_t<4, false>(p, kcache, stream);
+  return dense ? launch_fused_t<1, true>(p, kcache, stream) : launch_fused_t<1, false>(p, kcache, stream);
+}
+
+}  // namespace sai

@@ -64,4 +64,33 @@ struct MergeLaunch {
 };
 cudaError_t launch_merge(const MergeLaunch& p, cudaStream_t stream);
 
+struct FusedLaunch {
+  const uint8_t* q;        // [rows, 64, 128] e4m3
+  const float* w;          // [rows, 64]
+  const float* kscale;     // [num_blocks, 128]
+  long long num_blocks;
+  const int* block_table;  // [bt_rows, bt_stride]
+  long long bt_rows, bt_stride;
+  const int* row_to_batch;
+  const int* seq_lens;
+  int rows;
+  int max_len;       // caller's bound on seq_lens (checked per row)
+  int chunks;        // work units per row group
+  int chunk_blocks;  // KV blocks per unit
+  uint32_t* part_key;
+  int32_t* part_idx;
+  int* part_cnt;     // [rows * chunks]
+  float* dense;      // scores-only mode: [rows, dense_stride]
+  long long dense_stride;
+  int* status;
+};
+struct FusedPlan {
+  int group;         // query rows per CTA (1 or 4)
+  int chunks;        // KV chunks per row group
+  int chunk_blocks;  // KV blocks per chunk
+  size_t workspace_bytes;
+};
+FusedPlan fused_plan(long long rows, int max_seq_len, int group_rows, int num_sms);
+cudaError_t launch_fused(const FusedLaunch& p, int group, bool dense, const uint8_t* kcache, cudaStream_t stream);
+
 }  // namespace sai

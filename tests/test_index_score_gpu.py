@@ -1,0 +1,166 @@
+"""GPU parity of the fused FP8 index score (+ top-k) against the CPU oracle.
+
+Scores: the oracle forms the FP8 dot products exactly, the kernel in FP32 on
+the tensor cores; they must agree within 1e-3 relative (floored at the row's
+k-th score). Integer-valued inputs make every score an exact integer on both
+sides, so there the comparison is bit-exact and pins the MMA operand layout.
+Selection: a GPU pick is accepted when its oracle score is at least the
+oracle's k-th score minus that tolerance; the count, distinctness, order and
+the slot transform of the GPU's own indices are checked exactly.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle.score import index_scores
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+TOL = 1e-3
+
+
+def _t(a):
+    return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def _dev_inputs(inp):
+    return dict(q=_t(inp.q), w=_t(inp.w), kcache=_t(inp.kcache), kscale=_t(inp.kscale),
+                block_table=_t(inp.block_table), seq_lens=_t(inp.seq_lens), row_to_batch=_t(inp.row_to_batch))
+
+
+def _dense(inp, group_rows=1):
+    import sparse_attention_indexer_top_gb300 as sai
+
+    d = _dev_inputs(inp)
+    max_len = int(inp.seq_lens.max()) if inp.rows else 0
+    out = sai.index_score(d["q"], d["w"], d["kcache"], d["kscale"], d["block_table"], d["seq_lens"],
+                          max_seq_len=max_len, row_to_batch=d["row_to_batch"], group_rows=group_rows)
+    torch.cuda.synchronize()
+    assert sai.device_status() == 0
+    return out.cpu().numpy()
+
+
+def _fused(inp, group_rows=1):
+    import sparse_attention_indexer_top_gb300 as sai
+
+    d = _dev_inputs(inp)
+    max_len = int(inp.seq_lens.max()) if inp.rows else 0
+    slots, idx, scores = sai.index_score_topk(d["q"], d["w"], d["kcache"], d["kscale"], d["block_table"],
+                                              d["seq_lens"], max_seq_len=max_len, row_to_batch=d["row_to_batch"],
+                                              group_rows=group_rows)
+    torch.cuda.synchronize()
+    assert sai.device_status() == 0
+    return slots.cpu().numpy(), idx.cpu().numpy(), scores.cpu().numpy()
+
+
+def _kth(s, k):
+    return float(np.sort(s)[::-1][min(s.size, k) - 1]) if s.size else 0.0
+
+
+def _check_dense(got, inp, exact=False, rows=None):
+    rows = list(range(inp.rows)) if rows is None else rows
+    ref = index_scores(inp, rows)
+    for j, i in enumerate(rows):
+        n = int(inp.seq_lens[i])
+        g = got[i, :n].astype(np.float64)
+        r = ref[j].astype(np.float64)
+        if exact:
+            assert np.array_equal(g, r), f"row {i}: first diff at {np.flatnonzero(g != r)[:5]}"
+        else:
+            floor = abs(_kth(ref[j], 512)) if n else 0.0
+            err = np.abs(g - r) / np.maximum(np.maximum(np.abs(r), floor), 1e-30)
+            assert err.max() <= TOL, f"row {i}: max rel err {err.max():.3e} at {int(err.argmax())}"
+
+
+def _check_topk(got, inp, rows=None, k=512):
+    slots, idx, scores = got
+    rows = list(range(inp.rows)) if rows is None else rows
+    ref = index_scores(inp, rows)
+    for j, i in enumerate(rows):
+        n = int(inp.seq_lens[i])
+        kk = min(n, k)
+        gi = idx[i]
+        assert (gi[kk:] == -1).all() and (slots[i][kk:] == -1).all(), f"row {i}: padding"
+        sel = gi[:kk].astype(np.int64)
+        assert (sel >= 0).all() and (sel < n).all(), f"row {i}: index range"
+        assert np.unique(sel).size == kk, f"row {i}: duplicates"
+        s_ora = ref[j].astype(np.float64)
+        s_k = _kth(ref[j], k)
+        tol = TOL * max(abs(s_k), 1e-30)
+        assert (s_ora[sel] >= s_k - tol).all(), f"row {i}: a pick below the k-th score"
+        gs = scores[i][:kk].astype(np.float64)
+        assert (np.abs(gs - s_ora[sel]) <= TOL * np.maximum(np.abs(s_ora[sel]), abs(s_k)) + 1e-30).all(), \
+            f"row {i}: selected score mismatch"
+        assert (gs[:-1] >= gs[1:]).all(), f"row {i}: not score-descending"
+        b = i if inp.row_to_batch is None else int(inp.row_to_batch[i])
+        pages = inp.block_table[b][sel // 128].astype(np.int64)
+        assert np.array_equal(slots[i][:kk], pages * 128 + sel % 128), f"row {i}: slots"
+
+
+def _small(kind="normal", rows=6, lens=(1, 127, 128, 300, 1000, 2500), seed=41):
+    lens = np.asarray(lens[:rows], np.int32)
+    per_row = int(-(-lens.max() // 128))
+    return W.make_fused_inputs(seed, rows, 64, 128, rows * per_row + 3, lens, (rows, per_row), kind=kind)
+
+
+def test_dense_integer_inputs_exact():
+    _check_dense(_dense(_small("int")), _small("int"), exact=True)
+
+
+def test_dense_normal_inputs():
+    inp = _small("normal")
+    _check_dense(_dense(inp), inp)
+
+
+def test_dense_grouped_rows_exact():
+    # 8 rows of two requests (4 each), causal lengths, one block table row per request
+    lens = np.array([997, 998, 999, 1000, 3001, 3002, 3003, 3004], np.int32)
+    inp = W.make_fused_inputs(43, 8, 64, 128, 2 * 24 + 1, lens, (2, 24), row_to_batch=[0, 0, 0, 0, 1, 1, 1, 1],
+                              kind="int")
+    _check_dense(_dense(inp, group_rows=4), inp, exact=True)
+
+
+def test_topk_small():
+    inp = _small("normal")
+    _check_topk(_fused(inp), inp)
+
+
+def test_topk_zero_q_takes_lowest_indices():
+    inp = _small("zero_q")
+    slots, idx, scores = _fused(inp)
+    for i in range(inp.rows):
+        kk = min(int(inp.seq_lens[i]), 512)
+        assert idx[i][:kk].tolist() == list(range(kk))
+
+
+def test_topk_grouped_prefill_like():
+    rows, kv = 64, 6000
+    lens = (kv - rows + 1 + np.arange(rows)).astype(np.int32)
+    blocks = -(-kv // 128)
+    inp = W.make_fused_inputs(44, rows, 64, 128, blocks, lens, (1, blocks), row_to_batch=np.zeros(rows, np.int32))
+    _check_topk(_fused(inp, group_rows=4), inp)
+
+
+def test_topk_decode_many_chunks():
+    inp = W.fused_decode(seed=45, rows=16, min_len=3000, max_len=20000)
+    _check_topk(_fused(inp), inp)
+
+
+def test_fused_decode_full_size():
+    """The fused decode workload at full size (64 rows, 64 heads x 128,
+    seq_lens U[4096, 32768], 16384-block pool), every row checked."""
+    inp = W.fused_decode()
+    _check_topk(_fused(inp), inp)
+
+
+def test_fused_prefill_full_size_sampled():
+    """The fused prefill workload at full size (4096 causal rows on a 32768-
+    token KV, grouped by 4), in the launch configuration the benchmark times;
+    sampled rows against the oracle."""
+    inp = W.fused_prefill()
+    got = _fused(inp, group_rows=4)
+    sample = [0, 1, 2, 3, 1000, 2047, 2048, 3333, 4092, 4093, 4094, 4095]
+    _check_topk(got, inp, rows=sample)
