@@ -1,16 +1,23 @@
 #!/usr/bin/env python
 """Benchmark of the sparse-attention indexer top-k on one GB300.
 
-One step = one pass of the hot path over its synthetic batch:
+One step = one pass of the whole hot path, each part over its synthetic
+batch:
   * topk_transform on the packed-extend prefill chunk (2 requests x 8192
-    rows on a 70000-token KV, scores [16384, 140000] fp32, page_size 1).
+    rows on a 70000-token KV, scores [16384, 140000] fp32, page_size 1);
+  * fused FP8 index score + top-512 for decode (64 rows, 64 heads x 128,
+    seq_lens U[4096, 32768], 128-token blocks);
+  * fused FP8 index score + top-512 for prefill (4096 causal rows on a
+    32768-token KV, grouped by 4).
 
-The JSON line follows the repository's bench contract: `value` is rows/s
-with inputs resident in HBM; `e2e` repeats the step through the C ABI with
-host-resident inputs (pinned host -> device copies and the device -> host
-read of the slots inside the timed region); `roofline` is for the dominant
-kernel; `cpu_baseline` times the CPU oracle on a bounded sample of the same
-workload. `--impl reference` times only the oracle (the reference arm).
+The JSON line follows the repository's bench contract: `value` is query
+rows per second over the whole step with inputs resident in HBM; `e2e`
+repeats the step through the C ABI with host-resident inputs (pinned host ->
+device copies of every input and the device -> host read of every output
+inside the timed region); `roofline` is for the kernel that takes the most
+time, `config.paths` gives every part's own numbers; `cpu_baseline` times
+the CPU oracle on a bounded row sample of each part. `--impl reference`
+times only the oracle (the reference arm).
 """
 
 from __future__ import annotations
@@ -30,10 +37,14 @@ import numpy as np  # noqa: E402
 METRIC = "topk rows/s & HBM GB/s (% peak); fused score+topk keys/s (% roofline)"
 UNIT = "rows/s"
 K = 512
-WORKLOAD = "packed-extend prefill top-k: 2 req x 8192 rows, KV 70000, scores [16384,140000] fp32, k=512, page_size=1"
+WORKLOAD = ("indexer hot path step: packed-extend top-k (16384 rows, KV 70000, fp32 [16384,140000], page_size 1) "
+            "+ fused FP8 score+top-k decode (64 rows, 64x128 heads, U[4096,32768] keys) "
+            "+ fused FP8 score+top-k prefill (4096 causal rows, KV 32768, groups of 4); k=512")
+PATHS = ("topk_packed_extend", "fused_decode", "fused_prefill")
 
 
 def _peaks():
+    """(HBM GB/s, dense bf16 TFLOP/s burst, provenance)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
@@ -41,6 +52,9 @@ def _peaks():
         return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1900.0)), "measured"
     except Exception:
         return 6800.0, 1900.0, "fallback"
+
+
+FP8_OVER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
 
 
 def _dist():
@@ -103,51 +117,158 @@ class ClockSampler:
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+
+
 # --------------------------------------------------------------------------- workload
-def build_inputs(pinned: bool, new_tokens: int = 8192):
+class Part:
+    """One part of the step: host (pinned) inputs, device copies, outputs."""
+
+    def __init__(self, name):
+        self.name = name
+        self.host = {}      # name -> pinned host tensor
+        self.dev = {}       # name -> device tensor
+        self.out = {}       # name -> device output tensor
+        self.rows = 0
+        self.keys = 0.0
+        self.bytes = 0.0    # algorithmic HBM bytes per launch
+        self.flops = 0.0    # algorithmic tensor flops per launch
+        self.launches = 0
+        self.meta = {}
+
+
+def _pin(a):
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    return t.pin_memory()
+
+
+def build_topk_part(dev, new_tokens: int):
     import torch
 
     import workloads as W
 
+    part = Part("topk_packed_extend")
     row_starts, seq_lens, r2b, width = W.packed_extend_meta(new_tokens=new_tokens)
     rows = int(seq_lens.size)
-    host = torch.empty((rows, width), dtype=torch.float32, pin_memory=pinned)
+    host = torch.empty((rows, width), dtype=torch.float32, pin_memory=True)
     hn = host.numpy()
     chunk = 1024
     for r0 in range(0, rows, chunk):
         W.fill_rows(hn[r0:r0 + chunk], r0, 3, row_starts, seq_lens, fill=0.0)
     pt = W.page_table_perm(3, (2, 70000))
-    meta = dict(row_starts=row_starts, seq_lens=seq_lens, row_to_batch=r2b, page_tables=pt, width=width, rows=rows)
-    return host, meta
+    part.host = {"scores": host, "seq_lens": _pin(seq_lens), "row_starts": _pin(row_starts),
+                 "row_to_batch": _pin(r2b), "page_tables": _pin(pt)}
+    part.dev = {k: v.to(dev) for k, v in part.host.items()}
+    part.out = {"slots": torch.empty((rows, K), dtype=torch.int32, device=dev)}
+    part.rows = rows
+    part.keys = float(seq_lens.astype(np.int64).sum())
+    part.bytes = part.keys * 4 + pt.nbytes + rows * (3 * 4 + K * 4)
+    part.launches = 1
+    part.meta = dict(row_starts=row_starts, seq_lens=seq_lens, row_to_batch=r2b, page_tables=pt, width=width)
+    return part
 
 
-def algorithmic_bytes(meta) -> float:
-    keys = float(meta["seq_lens"].astype(np.int64).sum())
-    # scores read once + page-table rows + metadata + slots written
-    return keys * 4 + meta["page_tables"].nbytes + meta["rows"] * (3 * 4 + K * 4)
+def build_fused_part(dev, name: str, inp, group_rows: int):
+    import torch
+
+    part = Part(name)
+    arrays = {"q": inp.q, "w": inp.w, "kcache": inp.kcache, "kscale": inp.kscale,
+              "block_table": inp.block_table, "seq_lens": inp.seq_lens}
+    if inp.row_to_batch is not None:
+        arrays["row_to_batch"] = inp.row_to_batch
+    part.host = {k: _pin(v) for k, v in arrays.items()}
+    part.dev = {k: v.to(dev) for k, v in part.host.items()}
+    rows = inp.rows
+    part.out = {"slots": torch.empty((rows, K), dtype=torch.int32, device=dev),
+                "indices": torch.empty((rows, K), dtype=torch.int32, device=dev),
+                "scores": torch.empty((rows, K), dtype=torch.float32, device=dev)}
+    import sparse_attention_indexer_top_gb300 as sai
+
+    max_len = int(inp.seq_lens.max())
+    ws = sai.index_score_topk_workspace(rows, max_len, group_rows)
+    part.out["workspace"] = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+    part.rows = rows
+    n = inp.seq_lens.astype(np.int64)
+    part.keys = float(n.sum())
+    h, d = inp.heads, inp.dim
+    # each key's fp8 row + its scale, read once per row group; q, w; block ids; outputs
+    groups = -(-rows // group_rows)
+    key_reads = float(sum(int(n[g * group_rows:(g + 1) * group_rows].max()) for g in range(groups)))
+    part.bytes = key_reads * (d + 4) + inp.q.nbytes + inp.w.nbytes + (key_reads / 128) * 4 + rows * K * 12
+    part.flops = part.keys * h * d * 2.0
+    part.launches = 2
+    part.meta = dict(inp=inp, group_rows=group_rows, max_len=max_len)
+    return part
+
+
+def build_parts(dev, args):
+    import workloads as W
+
+    parts = []
+    if "topk_packed_extend" in args.paths:
+        parts.append(build_topk_part(dev, args.new_tokens))
+    if "fused_decode" in args.paths:
+        parts.append(build_fused_part(dev, "fused_decode", W.fused_decode(), 1))
+    if "fused_prefill" in args.paths:
+        parts.append(build_fused_part(dev, "fused_prefill", W.fused_prefill(rows=args.prefill_rows), 4))
+    return parts
+
+
+def launch_part(part, stream):
+    import sparse_attention_indexer_top_gb300 as sai
+
+    d, o = part.dev, part.out
+    if part.name == "topk_packed_extend":
+        sai.topk_transform(d["scores"], d["seq_lens"], d["page_tables"], row_starts=d["row_starts"],
+                           row_to_batch=d["row_to_batch"], out_slots=o["slots"], stream=stream)
+    else:
+        sai.index_score_topk(d["q"], d["w"], d["kcache"], d["kscale"], d["block_table"], d["seq_lens"],
+                             max_seq_len=part.meta["max_len"], row_to_batch=d.get("row_to_batch"),
+                             group_rows=part.meta["group_rows"], out_slots=o["slots"], out_indices=o["indices"],
+                             out_scores=o["scores"], workspace=o["workspace"], stream=stream)
 
 
 # --------------------------------------------------------------------------- oracle
-def oracle_sample(meta, budget_s: float = 15.0, max_rows: int = 4000):
-    """Time the CPU oracle (single-threaded numpy sort) on a row sample."""
+def oracle_part_rate(part_name, meta, budget_s):
+    """Oracle seconds per row of one part, timed on a row sample."""
     import workloads as W
+    from oracle.score import index_score_topk as oracle_fused
     from oracle.topk import topk_transform as oracle_topk
 
-    rows = meta["rows"]
-    sample = np.linspace(0, rows - 1, max_rows).astype(np.int64)
-    done = 0
-    t_total = 0.0
-    for i in sample:
-        n = int(meta["seq_lens"][i])
-        w = W.packed_extend_window(3, int(i), n)
-        b = int(meta["row_to_batch"][i])
-        t0 = time.perf_counter()
-        oracle_topk(w[None, :], np.array([n]), meta["page_tables"][[b]], 1, K)
-        t_total += time.perf_counter() - t0
-        done += 1
-        if t_total > budget_s:
-            break
-    return done / t_total, done, t_total
+    done, spent = 0, 0.0
+    if part_name == "topk_packed_extend":
+        rows = int(meta["seq_lens"].size)
+        for i in np.linspace(0, rows - 1, 4000).astype(np.int64):
+            n = int(meta["seq_lens"][i])
+            w = W.packed_extend_window(3, int(i), n)
+            t0 = time.perf_counter()
+            oracle_topk(w[None, :], np.array([n]), meta["page_tables"][[int(meta["row_to_batch"][i])]], 1, K)
+            spent += time.perf_counter() - t0
+            done += 1
+            if spent > budget_s:
+                break
+    else:
+        inp = meta["inp"]
+        for i in np.linspace(0, inp.rows - 1, 64).astype(np.int64):
+            t0 = time.perf_counter()
+            oracle_fused(inp, rows=[int(i)])
+            spent += time.perf_counter() - t0
+            done += 1
+            if spent > budget_s:
+                break
+    return spent / max(done, 1), done, spent
+
+
+def oracle_step_rate(parts_meta, budget_s):
+    """Rows/s of the oracle over the step's row mix, and a sample summary."""
+    per_step, rows, notes = 0.0, 0, []
+    for name, nrows, meta in parts_meta:
+        sec_per_row, done, spent = oracle_part_rate(name, meta, budget_s / max(len(parts_meta), 1))
+        per_step += sec_per_row * nrows
+        rows += nrows
+        notes.append(f"{name}: {done} rows in {spent:.1f} s")
+    return rows / per_step, "; ".join(notes)
 
 
 def run_reference(args):
@@ -156,22 +277,32 @@ def run_reference(args):
         return
     import workloads as W
 
-    row_starts, seq_lens, r2b, width = W.packed_extend_meta()
-    meta = dict(row_starts=row_starts, seq_lens=seq_lens, row_to_batch=r2b,
-                page_tables=W.page_table_perm(3, (2, 70000)), width=width, rows=int(seq_lens.size))
-    budget = max(2.0, 120.0 / max(1, args.steps + args.warmup))
-    vals = []
+    metas = []
+    if "topk_packed_extend" in args.paths:
+        row_starts, seq_lens, r2b, width = W.packed_extend_meta(new_tokens=args.new_tokens)
+        metas.append(("topk_packed_extend", int(seq_lens.size),
+                      dict(row_starts=row_starts, seq_lens=seq_lens, row_to_batch=r2b,
+                           page_tables=W.page_table_perm(3, (2, 70000)))))
+    if "fused_decode" in args.paths:
+        inp = W.fused_decode()
+        metas.append(("fused_decode", inp.rows, dict(inp=inp)))
+    if "fused_prefill" in args.paths:
+        inp = W.fused_prefill(rows=args.prefill_rows)
+        metas.append(("fused_prefill", inp.rows, dict(inp=inp)))
+    budget = max(3.0, 150.0 / max(1, args.steps + args.warmup))
+    vals, note = [], ""
     for s in range(args.warmup + args.steps):
-        v, n, t = oracle_sample(meta, budget_s=budget, max_rows=400)
+        v, note = oracle_step_rate(metas, budget)
         if s >= args.warmup:
             vals.append(v)
     value = float(np.median(vals))
+    rows = sum(m[1] for m in metas)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 16384 / value * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": rows / value * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "config": {"workload": WORKLOAD},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"rows spread over the 16384-row chunk, about {budget:.0f} s of sorting per step"},
+                             "sample": f"per step, a row sample of each part (about {budget:.0f} s): {note}"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -190,90 +321,110 @@ def run_gpu(args):
     import sparse_attention_indexer_top_gb300 as sai
 
     sai.load()
-    hbm_peak, _, peak_kind = _peaks()
+    hbm_peak, bf16_peak, peak_kind = _peaks()
+    fp8_peak = bf16_peak * FP8_OVER_BF16
 
-    host, meta = build_inputs(pinned=True, new_tokens=args.new_tokens)
-    rows, width = meta["rows"], meta["width"]
-    scores = torch.empty((rows, width), dtype=torch.float32, device=dev)
-    scores.copy_(host, non_blocking=False)
-    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-    seq_lens, row_starts, r2b, pt = t(meta["seq_lens"]), t(meta["row_starts"]), t(meta["row_to_batch"]), t(meta["page_tables"])
-    out_slots = torch.empty((rows, K), dtype=torch.int32, device=dev)
+    parts = build_parts(dev, args)
     stream = torch.cuda.Stream(device=dev)
 
     def step():
-        sai.topk_transform(scores, seq_lens, pt, row_starts=row_starts, row_to_batch=r2b, out_slots=out_slots,
-                           stream=stream)
+        for part in parts:
+            launch_part(part, stream)
 
-    launches_per_step = 1
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             step()
     torch.cuda.synchronize()
-    assert sai.device_status() == 0
+    assert sai.device_status() == 0, "a kernel flagged its inputs"
 
-    # timed region: inputs (4.3 GB of windows) exceed L2, so no flush is needed
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    # timed region: the step's inputs (4.5 GB) are far larger than L2
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in parts]
+          for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         t0 = time.perf_counter()
-        for a, b in evs:
-            a.record(stream)
-            step()
-            b.record(stream)
+        for s in range(args.steps):
+            for j, part in enumerate(parts):
+                ev[s][j][0].record(stream)
+                launch_part(part, stream)
+                ev[s][j][1].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
-    per = [a.elapsed_time(b) for a, b in evs]
-    ms = float(np.mean(per))
+    part_ms = [float(np.mean([ev[s][j][0].elapsed_time(ev[s][j][1]) for s in range(args.steps)]))
+               for j in range(len(parts))]
+    ms = float(np.mean([ev[s][0][0].elapsed_time(ev[s][-1][1]) for s in range(args.steps)]))
     if world > 1:
         tt = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         ms = float(tt.item())
+    rows = sum(p.rows for p in parts)
     value = rows * world / (ms * 1e-3)
-    alg = algorithmic_bytes(meta)
-    achieved = alg / (ms * 1e-3) / 1e9
-    keys = float(meta["seq_lens"].astype(np.int64).sum())
 
-    # end to end: pinned host scores -> device, kernel, slots -> host
-    e2e_steps = 0 if args.no_e2e else max(1, min(3, args.steps))
-    host_out = torch.empty((rows, K), dtype=torch.int32, pin_memory=True)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(e2e_steps):
-            scores.copy_(host, non_blocking=True)
-            step()
-            host_out.copy_(out_slots, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / max(1, e2e_steps)
-    h2d = host.numel() * 4
-    d2h = rows * K * 4
+    paths = {}
+    for part, pm in zip(parts, part_ms):
+        entry = {"ms": pm, "rows_per_s": part.rows / (pm * 1e-3), "keys_per_s": part.keys / (pm * 1e-3),
+                 "hbm_gbs": part.bytes / (pm * 1e-3) / 1e9, "hbm_frac": part.bytes / (pm * 1e-3) / 1e9 / hbm_peak}
+        if part.flops:
+            entry["tflops"] = part.flops / (pm * 1e-3) / 1e12
+            entry["fp8_frac"] = entry["tflops"] / fp8_peak
+        paths[part.name] = entry
+    # the dominant kernel's roofline
+    top = int(np.argmax(part_ms))
+    tp, tm = parts[top], part_ms[top]
+    if tp.name == "fused_prefill":
+        roof = {"bound": "tensor", "achieved": tp.flops / (tm * 1e-3) / 1e12, "peak": fp8_peak, "unit": "TFLOP/s",
+                "peak_kind": f"{peak_kind} bf16 burst x {FP8_OVER_BF16} (nominal fp8/bf16)"}
+    else:
+        roof = {"bound": "hbm", "achieved": tp.bytes / (tm * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                "peak_kind": peak_kind}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = tp.name
+
+    # end to end: every input copied from pinned host memory, every output read back
+    e2e = None
+    if not args.no_e2e:
+        outs_host = {(p.name, k): torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+                     for p in parts for k, v in p.out.items() if k != "workspace"}
+        h2d = sum(t.numel() * t.element_size() for p in parts for t in p.host.values())
+        d2h = sum(t.numel() * t.element_size() for t in outs_host.values())
+        n_e2e = max(1, min(3, args.steps))
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(n_e2e):
+                for p in parts:
+                    for k, t in p.host.items():
+                        p.dev[k].copy_(t, non_blocking=True)
+                step()
+                for p in parts:
+                    for k, v in p.out.items():
+                        if k != "workspace":
+                            outs_host[(p.name, k)].copy_(v, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / n_e2e
+        e2e = {"value": rows / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     cpu = None
     if rank == 0 and not args.no_cpu:
-        v, n, tt = oracle_sample(meta)
-        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{n} rows spread over the chunk ({tt:.1f} s of single-threaded stable sorts)"}
+        v, note = oracle_step_rate([(p.name, p.rows, p.meta) for p in parts], 20.0)
+        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": note}
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "rows": rows, "keys_per_step": keys, "k": K,
-                       "l2": "inputs larger than L2 (4.3 GB of score windows per step)",
-                       "keys_per_s": keys * world / (ms * 1e-3), "hbm_gbs": achieved},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": None, "peak_kind": peak_kind,
-                         "kernel": "topk_stream_kernel"},
-            "e2e": None if args.no_e2e else {"value": rows / (e2e_ms * 1e-3), "unit": UNIT,
-                                             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches_per_step * args.steps,
+            "vs_baseline": None, "dtype": "f32 (top-k), e4m3 x e4m3 -> f32 (fused scores)", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "rows_per_step": rows, "k": K,
+                       "l2": "inputs larger than L2 (4.5 GB per step)", "paths": paths},
+            "roofline": roof,
+            "e2e": e2e,
+            "gpu_launches": sum(p.launches for p in parts) * args.steps,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
             "wall_s_timed": wall,
@@ -291,9 +442,12 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--paths", default=",".join(PATHS), help="comma-separated parts of the step")
     ap.add_argument("--new-tokens", type=int, default=8192,
-                    help="query rows per request (8192 = the full packed-extend chunk; smaller for profiling)")
+                    help="query rows per request of the packed-extend part (8192 = full chunk)")
+    ap.add_argument("--prefill-rows", type=int, default=4096, help="query rows of the fused prefill part")
     args = ap.parse_args()
+    args.paths = [p for p in args.paths.split(",") if p]
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
