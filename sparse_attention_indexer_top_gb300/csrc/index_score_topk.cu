@@ -51,9 +51,7 @@ constexpr int kBlk = 128;     // tokens per KV block = MMA M
 constexpr int kNSf = 4;       // K-tile stages
 constexpr int kFCap = 1024;   // candidate list per row
 constexpr int kFPruneAt = kFCap - kBlk;
-constexpr int kEpi = 128;     // epilogue threads (warps 0-3)
-constexpr int kFThreads = kEpi + 64;
-constexpr int kBarEpi = 1;
+constexpr int kEpiRow = 128;  // epilogue threads per query row (4 warps, one TMEM lane quadrant each)
 
 template <int R>
 struct __align__(1024) FusedSmem {
@@ -62,9 +60,9 @@ struct __align__(1024) FusedSmem {
   float w[R * kH];
   uint32_t ckey[R][kFCap];
   int32_t cidx[R][kFCap];
-  uint32_t aux_key[kTopK];
-  int32_t aux_idx[kTopK];
-  SelectScratch sc;
+  uint32_t aux_key[R][kTopK];
+  int32_t aux_idx[R][kTopK];
+  SelectScratch sc[R];
   uint64_t full[kNSf], empty[kNSf], tfull[2], tempty[2], qfull;
   uint32_t tmem_base;
   int add[R][3];
@@ -122,8 +120,13 @@ __device__ GroupMeta group_meta(const FusedLaunch& p, int g, int c, int (&n)[R],
   return m;
 }
 
+template <int R>
+__host__ __device__ constexpr int fused_threads() {
+  return R * kEpiRow + 64;  // R row groups of 4 epilogue warps, a TMA warp, an MMA warp
+}
+
 template <int R, bool DENSE>
-__global__ void __launch_bounds__(kFThreads, 1)
+__global__ void __launch_bounds__(fused_threads<R>(), 1)
     fused_score_topk_kernel(const __grid_constant__ FusedLaunch p, const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ unsigned char smem_raw[];
@@ -131,6 +134,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
   constexpr int N = R * kH;          // MMA N
   constexpr uint32_t kCols = 2 * N;  // two accumulator buffers
   constexpr uint32_t kIdesc = umma_idesc_e4m3(kBlk, N);
+  constexpr int kEpiWarps = 4 * R;
+  constexpr int kTmaWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x / p.chunks, c = blockIdx.x - g * p.chunks;
   int n[R];
@@ -144,17 +149,17 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S.tfull[i], 1);
-      mbar_init(&S.tempty[i], kEpi / 32);
+      mbar_init(&S.tempty[i], kEpiWarps);
     }
     mbar_init(&S.qfull, 1);
     for (int r = 0; r < R; ++r) S.add[r][0] = S.add[r][1] = S.add[r][2] = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&S.tmem_base, kCols);
     tmem_relinquish();
   }
-  for (int i = tid; i < R * kH; i += kFThreads) {
+  for (int i = tid; i < R * kH; i += fused_threads<R>()) {
     const int r = i / kH;
     S.w[i] = r < m.nrows ? p.w[(long long)(m.row0 + r) * kH + (i - r * kH)] : 0.f;
   }
@@ -164,7 +169,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
   const uint32_t tmem = S.tmem_base;
   bool ok = true;
 
-  if (warp == 4) {
+  if (warp == kTmaWarp) {
     // ---------------- TMA producer
     if (lane == 0 && ntiles > 0) {
       prefetch_tmap(&kmap);
@@ -184,7 +189,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         tma_load_2d(S.kst[s], &kmap, 0, page * kBlk, &S.full[s], keep);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer
     if (lane == 0 && ntiles > 0) {
       bool run = mbar_wait(&S.qfull, 0);
@@ -206,124 +211,115 @@ __global__ void __launch_bounds__(kFThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue: one key (TMEM lane) per thread
+    // ---------------- epilogue: row r = warp / 4 of the group; one key
+    // (TMEM lane quad*32 + lane) per thread
+    const int r = warp >> 2, quad = warp & 3, et = tid - r * kEpiRow;  // et = key within the block
+    const int bar = 1 + r;
+    uint32_t* const ckey = S.ckey[r];
+    int32_t* const cidx = S.cidx[r];
     uint32_t rot = 0;
-    int cnt[R];
-    uint32_t tau[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      cnt[r] = 0;
-      tau[r] = 0;
-    }
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    int cnt = 0;
+    uint32_t tau = 0;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const bool row_live = r < m.nrows;
+    const int nr = n[r];
     for (int i = 0; i < ntiles; ++i) {
       const int blk = m.blk0 + i, buf = i & 1;
-      const int t = blk * kBlk + tid;
+      const int t = blk * kBlk + et;
       const int page = p.block_table[(long long)m.batch * p.bt_stride + blk];
       const bool page_ok = page >= 0 && page < p.num_blocks;
-      const float ks = page_ok ? __ldg(p.kscale + (long long)page * kBlk + tid) : 0.f;
-      if (!page_ok && tid == 0) atomicOr(p.status, kDevBadPage);
+      const float ks = page_ok ? __ldg(p.kscale + (long long)page * kBlk + et) : 0.f;
+      if (!page_ok && et == 0 && r == 0) atomicOr(p.status, kDevBadPage);
       ok = mbar_wait(&S.tfull[buf], (i >> 1) & 1u);
-      float score[R];
+      float score = 0.f;
       if (ok) {
         tc_fence_after();
+        uint32_t a[32], b[32];
+        const uint32_t col = tmem + lane_base + static_cast<uint32_t>(buf * N + r * kH);
+        tmem_ld32(col, a);
+        tmem_ld32(col + 32, b);
+        tmem_ld_wait();
+        const float4* w4 = reinterpret_cast<const float4*>(S.w + r * kH);
+        float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          uint32_t a[32], b[32];
-          const uint32_t col = tmem + lane_base + static_cast<uint32_t>(buf * N + r * kH);
-          tmem_ld32(col, a);
-          tmem_ld32(col + 32, b);
-          tmem_ld_wait();
-          const float4* w4 = reinterpret_cast<const float4*>(S.w + r * kH);
-          float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-          for (int h4 = 0; h4 < 8; ++h4) {
-            const float4 wa = w4[h4], wb = w4[8 + h4];
-            acc0 = fmaf(wa.x, fmaxf(__uint_as_float(a[4 * h4 + 0]), 0.f), acc0);
-            acc1 = fmaf(wa.y, fmaxf(__uint_as_float(a[4 * h4 + 1]), 0.f), acc1);
-            acc0 = fmaf(wa.z, fmaxf(__uint_as_float(a[4 * h4 + 2]), 0.f), acc0);
-            acc1 = fmaf(wa.w, fmaxf(__uint_as_float(a[4 * h4 + 3]), 0.f), acc1);
-            acc0 = fmaf(wb.x, fmaxf(__uint_as_float(b[4 * h4 + 0]), 0.f), acc0);
-            acc1 = fmaf(wb.y, fmaxf(__uint_as_float(b[4 * h4 + 1]), 0.f), acc1);
-            acc0 = fmaf(wb.z, fmaxf(__uint_as_float(b[4 * h4 + 2]), 0.f), acc0);
-            acc1 = fmaf(wb.w, fmaxf(__uint_as_float(b[4 * h4 + 3]), 0.f), acc1);
-          }
-          score[r] = (acc0 + acc1) * ks;
+        for (int h4 = 0; h4 < 8; ++h4) {
+          const float4 wa = w4[h4], wb = w4[8 + h4];
+          acc0 = fmaf(wa.x, fmaxf(__uint_as_float(a[4 * h4 + 0]), 0.f), acc0);
+          acc1 = fmaf(wa.y, fmaxf(__uint_as_float(a[4 * h4 + 1]), 0.f), acc1);
+          acc0 = fmaf(wa.z, fmaxf(__uint_as_float(a[4 * h4 + 2]), 0.f), acc0);
+          acc1 = fmaf(wa.w, fmaxf(__uint_as_float(a[4 * h4 + 3]), 0.f), acc1);
+          acc0 = fmaf(wb.x, fmaxf(__uint_as_float(b[4 * h4 + 0]), 0.f), acc0);
+          acc1 = fmaf(wb.y, fmaxf(__uint_as_float(b[4 * h4 + 1]), 0.f), acc1);
+          acc0 = fmaf(wb.z, fmaxf(__uint_as_float(b[4 * h4 + 2]), 0.f), acc0);
+          acc1 = fmaf(wb.w, fmaxf(__uint_as_float(b[4 * h4 + 3]), 0.f), acc1);
         }
+        score = (acc0 + acc1) * ks;
         tc_fence_before();
       }
       __syncwarp();
       if (lane == 0 && ok) mbar_arrive(&S.tempty[buf]);
-      if (!named_bar_and(kBarEpi, kEpi, ok)) {
-        if (tid == 0) atomicOr(p.status, kDevWaitTimeout);
+      if (!named_bar_and(bar, kEpiRow, ok)) {
+        if (et == 0) atomicOr(p.status, kDevWaitTimeout);
         ok = false;
         break;
       }
+      const bool live = row_live && page_ok && t < nr;
       if constexpr (DENSE) {
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-          if (r < m.nrows && t < n[r] && page_ok) p.dense[(long long)(m.row0 + r) * p.dense_stride + t] = score[r];
+        if (live) p.dense[(long long)(m.row0 + r) * p.dense_stride + t] = score;
       } else {
-        // running top-k filter per row: one ballot and one shared atomic per warp
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const bool pass = page_ok && t < n[r] && score[r] >= tau_float(tau[r]);
-          const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass);
-          if (bal) {
-            int start = 0;
-            if (lane == 0) start = atomicAdd(&S.add[r][rot % 3], __popc(bal));
-            start = __shfl_sync(0xFFFFFFFFu, start, 0);
-            if (pass) {
-              const int q = cnt[r] + start + __popc(bal & ((1u << lane) - 1u));
-              S.ckey[r][q] = order_key(score[r]);
-              S.cidx[r][q] = t;
-            }
+        // running top-k filter of this row: one ballot and one shared atomic per warp
+        const bool pass = live && score >= tau_float(tau);
+        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass);
+        if (bal) {
+          int start = 0;
+          if (lane == 0) start = atomicAdd(&S.add[r][rot % 3], __popc(bal));
+          start = __shfl_sync(0xFFFFFFFFu, start, 0);
+          if (pass) {
+            const int q = cnt + start + __popc(bal & ((1u << lane) - 1u));
+            ckey[q] = order_key(score);
+            cidx[q] = t;
           }
         }
-        named_bar(kBarEpi, kEpi);
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          if (tid == 0) S.add[r][(rot + 2) % 3] = 0;
-          cnt[r] += S.add[r][rot % 3];
-          if (cnt[r] > kFPruneAt) {
-            tau[r] = max(tau[r], select512_to_aux<kEpi, kFCap>(S.ckey[r], S.cidx[r], cnt[r], S.aux_key, S.aux_idx,
-                                                               S.sc, tid, kBarEpi));
-            for (int j = tid; j < kTopK; j += kEpi) {
-              S.ckey[r][j] = S.aux_key[j];
-              S.cidx[r][j] = S.aux_idx[j];
-            }
-            named_bar(kBarEpi, kEpi);
-            cnt[r] = kTopK;
-          }
-        }
+        named_bar(bar, kEpiRow);
+        if (et == 0) S.add[r][(rot + 2) % 3] = 0;  // counter of tile rot+2; last read before this barrier
+        cnt += S.add[r][rot % 3];
         ++rot;
+        if (cnt > kFPruneAt) {
+          tau = max(tau, select512_to_aux<kEpiRow, kFCap>(ckey, cidx, cnt, S.aux_key[r], S.aux_idx[r], S.sc[r], et,
+                                                          bar));
+          for (int j = et; j < kTopK; j += kEpiRow) {
+            ckey[j] = S.aux_key[r][j];
+            cidx[j] = S.aux_idx[r][j];
+          }
+          named_bar(bar, kEpiRow);
+          cnt = kTopK;
+        }
       }
     }
     if constexpr (!DENSE) {
-      // unit end: cut each row's list to 512 and write it as a partial list
-      for (int r = 0; r < m.nrows; ++r) {
+      // unit end: cut this row's list to 512 and write it as a partial list
+      if (row_live) {
         const long long unit = (long long)(m.row0 + r) * p.chunks + c;
-        int cr = ok ? cnt[r] : 0;
-        const uint32_t* src_k = S.ckey[r];
-        const int32_t* src_i = S.cidx[r];
+        int cr = ok ? cnt : 0;
+        const uint32_t* src_k = ckey;
+        const int32_t* src_i = cidx;
         if (cr > kTopK) {
-          select512_to_aux<kEpi, kFCap>(S.ckey[r], S.cidx[r], cr, S.aux_key, S.aux_idx, S.sc, tid, kBarEpi);
+          select512_to_aux<kEpiRow, kFCap>(ckey, cidx, cr, S.aux_key[r], S.aux_idx[r], S.sc[r], et, bar);
           cr = kTopK;
-          src_k = S.aux_key;
-          src_i = S.aux_idx;
+          src_k = S.aux_key[r];
+          src_i = S.aux_idx[r];
         }
-        for (int j = tid; j < cr; j += kEpi) {
+        for (int j = et; j < cr; j += kEpiRow) {
           p.part_key[unit * kTopK + j] = src_k[j];
           p.part_idx[unit * kTopK + j] = src_i[j];
         }
-        if (tid == 0) p.part_cnt[unit] = cr;
-        named_bar(kBarEpi, kEpi);
+        if (et == 0) p.part_cnt[unit] = cr;
       }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kCols);
   }
@@ -376,7 +372,7 @@ cudaError_t launch_fused_t(const FusedLaunch& p, const uint8_t* kcache, cudaStre
     attr_done[dev] = true;
   }
   const int groups = (p.rows + R - 1) / R;
-  fused_score_topk_kernel<R, DENSE><<<groups * p.chunks, kFThreads, smem, stream>>>(p, kmap, qmap);
+  fused_score_topk_kernel<R, DENSE><<<groups * p.chunks, fused_threads<R>(), smem, stream>>>(p, kmap, qmap);
   return cudaGetLastError();
 }
 
