@@ -223,12 +223,21 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const bool row_live = r < m.nrows;
     const int nr = n[r];
+    const int* bt_row = p.block_table + (long long)m.batch * p.bt_stride;
+    // block id and key scale of the next tile are fetched one tile ahead
+    int page_next = ntiles > 0 ? bt_row[m.blk0] : -1;
+    bool ok_next = page_next >= 0 && page_next < p.num_blocks;
+    float ks_next = ok_next ? __ldg(p.kscale + (long long)page_next * kBlk + et) : 0.f;
     for (int i = 0; i < ntiles; ++i) {
       const int blk = m.blk0 + i, buf = i & 1;
       const int t = blk * kBlk + et;
-      const int page = p.block_table[(long long)m.batch * p.bt_stride + blk];
-      const bool page_ok = page >= 0 && page < p.num_blocks;
-      const float ks = page_ok ? __ldg(p.kscale + (long long)page * kBlk + et) : 0.f;
+      const bool page_ok = ok_next;
+      const float ks = ks_next;
+      if (i + 1 < ntiles) {
+        page_next = bt_row[blk + 1];
+        ok_next = page_next >= 0 && page_next < p.num_blocks;
+        ks_next = ok_next ? __ldg(p.kscale + (long long)page_next * kBlk + et) : 0.f;
+      }
       if (!page_ok && et == 0 && r == 0) atomicOr(p.status, kDevBadPage);
       ok = mbar_wait(&S.tfull[buf], (i >> 1) & 1u);
       float score = 0.f;
