@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
         ks_next = ok_next ? __ldg(p.kscale + (long long)page_next * kBlk + et) : 0.f;
       }
       if (!page_ok && et == 0 && r == 0) atomicOr(p.status, kDevBadPage);
-      ok = mbar_wait(&S.tfull[buf], (i >> 1) & 1u);
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(&S.tfull[buf], (i >> 1) & 1u));
       float score = 0.f;
       if (ok) {
         tc_fence_after();
@@ -248,33 +248,34 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
         tmem_ld32(col, a);
         tmem_ld32(col + 32, b);
         tmem_ld_wait();
+        // the accumulator buffer is free as soon as it is in registers
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.tempty[buf]);
         const float4* w4 = reinterpret_cast<const float4*>(S.w + r * kH);
-        float acc0 = 0.f, acc1 = 0.f;
+        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
 #pragma unroll
         for (int h4 = 0; h4 < 8; ++h4) {
           const float4 wa = w4[h4], wb = w4[8 + h4];
           acc0 = fmaf(wa.x, fmaxf(__uint_as_float(a[4 * h4 + 0]), 0.f), acc0);
           acc1 = fmaf(wa.y, fmaxf(__uint_as_float(a[4 * h4 + 1]), 0.f), acc1);
-          acc0 = fmaf(wa.z, fmaxf(__uint_as_float(a[4 * h4 + 2]), 0.f), acc0);
-          acc1 = fmaf(wa.w, fmaxf(__uint_as_float(a[4 * h4 + 3]), 0.f), acc1);
+          acc2 = fmaf(wa.z, fmaxf(__uint_as_float(a[4 * h4 + 2]), 0.f), acc2);
+          acc3 = fmaf(wa.w, fmaxf(__uint_as_float(a[4 * h4 + 3]), 0.f), acc3);
           acc0 = fmaf(wb.x, fmaxf(__uint_as_float(b[4 * h4 + 0]), 0.f), acc0);
           acc1 = fmaf(wb.y, fmaxf(__uint_as_float(b[4 * h4 + 1]), 0.f), acc1);
-          acc0 = fmaf(wb.z, fmaxf(__uint_as_float(b[4 * h4 + 2]), 0.f), acc0);
-          acc1 = fmaf(wb.w, fmaxf(__uint_as_float(b[4 * h4 + 3]), 0.f), acc1);
+          acc2 = fmaf(wb.z, fmaxf(__uint_as_float(b[4 * h4 + 2]), 0.f), acc2);
+          acc3 = fmaf(wb.w, fmaxf(__uint_as_float(b[4 * h4 + 3]), 0.f), acc3);
         }
-        score = (acc0 + acc1) * ks;
-        tc_fence_before();
+        score = ((acc0 + acc1) + (acc2 + acc3)) * ks;
       }
-      __syncwarp();
-      if (lane == 0 && ok) mbar_arrive(&S.tempty[buf]);
-      if (!named_bar_and(bar, kEpiRow, ok)) {
-        if (et == 0) atomicOr(p.status, kDevWaitTimeout);
-        ok = false;
-        break;
-      }
-      const bool live = row_live && page_ok && t < nr;
+      const bool live = ok && row_live && page_ok && t < nr;
       if constexpr (DENSE) {
         if (live) p.dense[(long long)(m.row0 + r) * p.dense_stride + t] = score;
+        if (!named_bar_and(bar, kEpiRow, ok)) {
+          if (et == 0) atomicOr(p.status, kDevWaitTimeout);
+          ok = false;
+          break;
+        }
       } else {
         // running top-k filter of this row: one ballot and one shared atomic per warp
         const bool pass = live && score >= tau_float(tau);
@@ -289,7 +290,11 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
             cidx[q] = t;
           }
         }
-        named_bar(bar, kEpiRow);
+        if (!named_bar_and(bar, kEpiRow, ok)) {
+          if (et == 0) atomicOr(p.status, kDevWaitTimeout);
+          ok = false;
+          break;
+        }
         if (et == 0) S.add[r][(rot + 2) % 3] = 0;  // counter of tile rot+2; last read before this barrier
         cnt += S.add[r][rot % 3];
         ++rot;
