@@ -126,7 +126,7 @@ __host__ __device__ constexpr int fused_threads() {
 }
 
 template <int R, bool DENSE>
-__global__ void __launch_bounds__(fused_threads<R>(), 1)
+__global__ void __maxnreg__(R == 4 ? 112 : 224)
     fused_score_topk_kernel(const __grid_constant__ FusedLaunch p, const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ unsigned char smem_raw[];
@@ -243,28 +243,27 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
       float score = 0.f;
       if (ok) {
         tc_fence_after();
-        uint32_t a[32], b[32];
         const uint32_t col = tmem + lane_base + static_cast<uint32_t>(buf * N + r * kH);
-        tmem_ld32(col, a);
-        tmem_ld32(col + 32, b);
-        tmem_ld_wait();
-        // the accumulator buffer is free as soon as it is in registers
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.tempty[buf]);
         const float4* w4 = reinterpret_cast<const float4*>(S.w + r * kH);
         float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
 #pragma unroll
-        for (int h4 = 0; h4 < 8; ++h4) {
-          const float4 wa = w4[h4], wb = w4[8 + h4];
-          acc0 = fmaf(wa.x, fmaxf(__uint_as_float(a[4 * h4 + 0]), 0.f), acc0);
-          acc1 = fmaf(wa.y, fmaxf(__uint_as_float(a[4 * h4 + 1]), 0.f), acc1);
-          acc2 = fmaf(wa.z, fmaxf(__uint_as_float(a[4 * h4 + 2]), 0.f), acc2);
-          acc3 = fmaf(wa.w, fmaxf(__uint_as_float(a[4 * h4 + 3]), 0.f), acc3);
-          acc0 = fmaf(wb.x, fmaxf(__uint_as_float(b[4 * h4 + 0]), 0.f), acc0);
-          acc1 = fmaf(wb.y, fmaxf(__uint_as_float(b[4 * h4 + 1]), 0.f), acc1);
-          acc2 = fmaf(wb.z, fmaxf(__uint_as_float(b[4 * h4 + 2]), 0.f), acc2);
-          acc3 = fmaf(wb.w, fmaxf(__uint_as_float(b[4 * h4 + 3]), 0.f), acc3);
+        for (int half = 0; half < 2; ++half) {
+          uint32_t a[32];
+          tmem_ld32(col + 32 * half, a);
+          tmem_ld_wait();
+          if (half == 1) {  // the accumulator buffer is free once both halves are in registers
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.tempty[buf]);
+          }
+#pragma unroll
+          for (int h4 = 0; h4 < 8; ++h4) {
+            const float4 wa = w4[8 * half + h4];
+            acc0 = fmaf(wa.x, fmaxf(__uint_as_float(a[4 * h4 + 0]), 0.f), acc0);
+            acc1 = fmaf(wa.y, fmaxf(__uint_as_float(a[4 * h4 + 1]), 0.f), acc1);
+            acc2 = fmaf(wa.z, fmaxf(__uint_as_float(a[4 * h4 + 2]), 0.f), acc2);
+            acc3 = fmaf(wa.w, fmaxf(__uint_as_float(a[4 * h4 + 3]), 0.f), acc3);
+          }
         }
         score = ((acc0 + acc1) + (acc2 + acc3)) * ks;
       }
