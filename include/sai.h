@@ -53,6 +53,12 @@ typedef enum {
 const char* sai_status_string(int status);
 
 /*
+ * Text of the CUDA error behind the calling thread's most recent
+ * SAI_ERR_CUDA ("" if none); valid until that thread's next call.
+ */
+const char* sai_last_error(void);
+
+/*
  * Read (and optionally clear) the device status word of the current device
  * after synchronizing `stream`. *out_bits receives the OR of the bits set by
  * kernels since the last clear: 1 = bad row metadata, 2 = an internal

@@ -17,6 +17,7 @@ _vp = ctypes.c_void_p
 # name -> (restype, argtypes); mirrors include/sai.h
 SIGNATURES = {
     "sai_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "sai_last_error": (ctypes.c_char_p, []),
     "sai_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int), ctypes.c_int, _vp]),
     "sai_topk_transform_workspace": (_c_size, [_c_i64, _c_i64, _c_i32]),
     "sai_topk_transform": (ctypes.c_int, [_vp, _c_i64, _c_i64, _vp, _vp, _vp, _c_i64, _c_i64, _vp, _c_i32, _c_i32,
@@ -36,7 +37,10 @@ _lib = None
 class SaiError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {status_string(status)} (status {status})")
+        detail = ""
+        if status == -5:
+            detail = " [" + load().sai_last_error().decode() + "]"
+        super().__init__(f"{where}: {status_string(status)} (status {status}){detail}")
 
 
 def load() -> ctypes.CDLL:

@@ -39,9 +39,20 @@ bool device_setup(int* dev_out, int** status, int* sms) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+thread_local const char* t_last_error = "";
+
+// Map a CUDA error to a status, remembering its text for sai_last_error.
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return SAI_OK;
+  t_last_error = cudaGetErrorString(e);
+  return SAI_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
+
+const char* sai_last_error(void) { return t_last_error; }
 
 const char* sai_status_string(int status) {
   switch (status) {
@@ -133,8 +144,7 @@ int sai_topk_transform(const float* scores, int64_t rows, int64_t score_stride, 
     p.part_cnt = reinterpret_cast<int*>(w + units * SAI_TOPK * 8);
   }
   p.status = st;
-  cudaError_t e = sai::launch_topk_transform(p, sms, reinterpret_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? SAI_OK : SAI_ERR_CUDA;
+  return cuda_status(sai::launch_topk_transform(p, sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"
@@ -214,7 +224,7 @@ int sai_index_score_topk(const uint8_t* q_fp8, const float* w, const uint8_t* kc
   p.status = st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = sai::launch_fused(p, plan.group, false, kcache_fp8, s);
-  if (e != cudaSuccess) return SAI_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_status(e);
   sai::MergeLaunch m{};
   m.rows = static_cast<int>(rows);
   m.units_per_row = plan.chunks;
@@ -231,8 +241,7 @@ int sai_index_score_topk(const uint8_t* q_fp8, const float* w, const uint8_t* kc
   m.out_idx = out_indices;
   m.out_scores = out_scores;
   m.status = st;
-  e = sai::launch_merge(m, s);
-  return e == cudaSuccess ? SAI_OK : SAI_ERR_CUDA;
+  return cuda_status(sai::launch_merge(m, s));
 }
 
 int sai_index_score(const uint8_t* q_fp8, const float* w, const uint8_t* kcache_fp8, const float* kscale,
@@ -267,8 +276,7 @@ int sai_index_score(const uint8_t* q_fp8, const float* w, const uint8_t* kcache_
   p.dense = out_scores;
   p.dense_stride = out_stride;
   p.status = st;
-  cudaError_t e = sai::launch_fused(p, plan.group, true, kcache_fp8, reinterpret_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? SAI_OK : SAI_ERR_CUDA;
+  return cuda_status(sai::launch_fused(p, plan.group, true, kcache_fp8, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"
