@@ -52,6 +52,7 @@ constexpr int kNSf = 4;       // K-tile stages
 constexpr int kFCap = 1024;   // candidate list per row
 constexpr int kFPruneAt = kFCap - kBlk;
 constexpr int kEpiRow = 128;  // epilogue threads per query row (4 warps, one TMEM lane quadrant each)
+constexpr int kMaxTiles = 256;  // KV blocks per work unit (host plans chunks accordingly)
 
 template <int R>
 struct __align__(1024) FusedSmem {
@@ -63,9 +64,10 @@ struct __align__(1024) FusedSmem {
   uint32_t aux_key[R][kTopK];
   int32_t aux_idx[R][kTopK];
   SelectScratch sc[R];
+  int pages[kMaxTiles];   // the unit's block ids, staged once
   uint64_t full[kNSf], empty[kNSf], tfull[2], tempty[2], qfull;
   uint32_t tmem_base;
-  int add[R][3];
+  int wcnt[R][2][4];      // per-warp pass counts of a tile (double-buffered)
 };
 
 template <int R>
@@ -152,13 +154,14 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
       mbar_init(&S.tempty[i], kEpiWarps);
     }
     mbar_init(&S.qfull, 1);
-    for (int r = 0; r < R; ++r) S.add[r][0] = S.add[r][1] = S.add[r][2] = 0;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
     tmem_alloc(&S.tmem_base, kCols);
     tmem_relinquish();
   }
+  for (int i = tid; i < ntiles; i += fused_threads<R>())
+    S.pages[i] = p.block_table[(long long)m.batch * p.bt_stride + m.blk0 + i];
   for (int i = tid; i < R * kH; i += fused_threads<R>()) {
     const int r = i / kH;
     S.w[i] = r < m.nrows ? p.w[(long long)(m.row0 + r) * kH + (i - r * kH)] : 0.f;
@@ -183,7 +186,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
           atomicOr(p.status, kDevWaitTimeout);
           break;
         }
-        int page = p.block_table[(long long)m.batch * p.bt_stride + m.blk0 + i];
+        int page = S.pages[i];
         if (page < 0 || page >= p.num_blocks) page = 0;  // the epilogue masks this block
         mbar_arrive_expect_tx(&S.full[s], (uint32_t)(kBlk * kD));
         tma_load_2d(S.kst[s], &kmap, 0, page * kBlk, &S.full[s], keep);
@@ -217,24 +220,23 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
     const int bar = 1 + r;
     uint32_t* const ckey = S.ckey[r];
     int32_t* const cidx = S.cidx[r];
-    uint32_t rot = 0;
     int cnt = 0;
     uint32_t tau = 0;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const bool row_live = r < m.nrows;
     const int nr = n[r];
-    const int* bt_row = p.block_table + (long long)m.batch * p.bt_stride;
-    // block id and key scale of the next tile are fetched one tile ahead
-    int page_next = ntiles > 0 ? bt_row[m.blk0] : -1;
+    // the key scale of the next tile is fetched one tile ahead
+    int page_next = ntiles > 0 ? S.pages[0] : -1;
     bool ok_next = page_next >= 0 && page_next < p.num_blocks;
     float ks_next = ok_next ? __ldg(p.kscale + (long long)page_next * kBlk + et) : 0.f;
+    const float2* w2 = reinterpret_cast<const float2*>(S.w + r * kH);
     for (int i = 0; i < ntiles; ++i) {
       const int blk = m.blk0 + i, buf = i & 1;
       const int t = blk * kBlk + et;
       const bool page_ok = ok_next;
       const float ks = ks_next;
       if (i + 1 < ntiles) {
-        page_next = bt_row[blk + 1];
+        page_next = S.pages[i + 1];
         ok_next = page_next >= 0 && page_next < p.num_blocks;
         ks_next = ok_next ? __ldg(p.kscale + (long long)page_next * kBlk + et) : 0.f;
       }
@@ -244,8 +246,8 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
       if (ok) {
         tc_fence_after();
         const uint32_t col = tmem + lane_base + static_cast<uint32_t>(buf * N + r * kH);
-        const float4* w4 = reinterpret_cast<const float4*>(S.w + r * kH);
-        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+        // sum_h w_h relu(s_h): relu per head, then packed (f32x2) FMAs
+        unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t a[32];
@@ -257,15 +259,20 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
             if (lane == 0) mbar_arrive(&S.tempty[buf]);
           }
 #pragma unroll
-          for (int h4 = 0; h4 < 8; ++h4) {
-            const float4 wa = w4[8 * half + h4];
-            acc0 = fmaf(wa.x, fmaxf(__uint_as_float(a[4 * h4 + 0]), 0.f), acc0);
-            acc1 = fmaf(wa.y, fmaxf(__uint_as_float(a[4 * h4 + 1]), 0.f), acc1);
-            acc2 = fmaf(wa.z, fmaxf(__uint_as_float(a[4 * h4 + 2]), 0.f), acc2);
-            acc3 = fmaf(wa.w, fmaxf(__uint_as_float(a[4 * h4 + 3]), 0.f), acc3);
+          for (int h2 = 0; h2 < 16; ++h2) {
+            const float2 wv = w2[16 * half + h2];
+            const float lo = fmaxf(__uint_as_float(a[2 * h2]), 0.f), hi = fmaxf(__uint_as_float(a[2 * h2 + 1]), 0.f);
+            const unsigned long long x = (static_cast<unsigned long long>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+            const unsigned long long wp =
+                (static_cast<unsigned long long>(__float_as_uint(wv.y)) << 32) | __float_as_uint(wv.x);
+            asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc[h2 & 3]) : "l"(x), "l"(wp));
           }
         }
-        score = ((acc0 + acc1) + (acc2 + acc3)) * ks;
+        float sum = 0.f;
+#pragma unroll
+        for (int k2 = 0; k2 < 4; ++k2)
+          sum += __uint_as_float(static_cast<uint32_t>(acc[k2])) + __uint_as_float(static_cast<uint32_t>(acc[k2] >> 32));
+        score = sum * ks;
       }
       const bool live = ok && row_live && page_ok && t < nr;
       if constexpr (DENSE) {
@@ -276,28 +283,31 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
           break;
         }
       } else {
-        // running top-k filter of this row: one ballot and one shared atomic per warp
+        // running top-k filter of this row: per-warp ballot counts are
+        // exchanged through the tile's one barrier, then survivors are placed
         const bool pass = live && score >= tau_float(tau);
         const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass);
-        if (bal) {
-          int start = 0;
-          if (lane == 0) start = atomicAdd(&S.add[r][rot % 3], __popc(bal));
-          start = __shfl_sync(0xFFFFFFFFu, start, 0);
-          if (pass) {
-            const int q = cnt + start + __popc(bal & ((1u << lane) - 1u));
-            ckey[q] = order_key(score);
-            cidx[q] = t;
-          }
-        }
+        if (lane == 0) S.wcnt[r][i & 1][quad] = __popc(bal);
         if (!named_bar_and(bar, kEpiRow, ok)) {
           if (et == 0) atomicOr(p.status, kDevWaitTimeout);
           ok = false;
           break;
         }
-        if (et == 0) S.add[r][(rot + 2) % 3] = 0;  // counter of tile rot+2; last read before this barrier
-        cnt += S.add[r][rot % 3];
-        ++rot;
+        const int* wc = S.wcnt[r][i & 1];
+        int before = 0, total = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          before += q < quad ? wc[q] : 0;
+          total += wc[q];
+        }
+        if (pass) {
+          const int pos = cnt + before + __popc(bal & ((1u << lane) - 1u));
+          ckey[pos] = order_key(score);
+          cidx[pos] = t;
+        }
+        cnt += total;
         if (cnt > kFPruneAt) {
+          named_bar(bar, kEpiRow);  // the list is complete
           tau = max(tau, select512_to_aux<kEpiRow, kFCap>(ckey, cidx, cnt, S.aux_key[r], S.aux_idx[r], S.sc[r], et,
                                                           bar));
           for (int j = et; j < kTopK; j += kEpiRow) {
@@ -311,6 +321,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
     }
     if constexpr (!DENSE) {
       // unit end: cut this row's list to 512 and write it as a partial list
+      named_bar(bar, kEpiRow);  // the last tile's survivors are placed
       if (row_live) {
         const long long unit = (long long)(m.row0 + r) * p.chunks + c;
         int cr = ok ? cnt : 0;
@@ -399,6 +410,7 @@ FusedPlan fused_plan(long long rows, int max_seq_len, int group_rows, int num_sm
   const long long target = 4LL * num_sms;
   long long chunks = groups > 0 ? (target + groups - 1) / groups : 1;
   chunks = std::max<long long>(1, std::min<long long>({chunks, 12LL, max_blocks}));
+  chunks = std::max<long long>(chunks, (max_blocks + kMaxTiles - 1) / kMaxTiles);
   const long long cb = (max_blocks + chunks - 1) / chunks;
   pl.chunk_blocks = static_cast<int>(cb);
   pl.chunks = static_cast<int>((max_blocks + cb - 1) / cb);
