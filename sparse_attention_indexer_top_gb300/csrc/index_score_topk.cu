@@ -49,8 +49,9 @@ constexpr int kH = 64;        // index heads
 constexpr int kD = 128;       // head dim (bytes per fp8 row)
 constexpr int kBlk = 128;     // tokens per KV block = MMA M
 constexpr int kNSf = 4;       // K-tile stages
-constexpr int kFCap = 1024;   // candidate list per row
-constexpr int kFPruneAt = kFCap - kBlk;
+constexpr int kSub = 512;     // candidate sub-list per epilogue warp
+constexpr int kSyncEvery = 4; // tiles between the row group's count exchanges
+constexpr int kSubPruneAt = kSub - kSyncEvery * 32;
 constexpr int kEpiRow = 128;  // epilogue threads per query row (4 warps, one TMEM lane quadrant each)
 constexpr int kMaxTiles = 256;  // KV blocks per work unit (host plans chunks accordingly)
 
@@ -59,15 +60,15 @@ struct __align__(1024) FusedSmem {
   uint8_t kst[kNSf][kBlk * kD];  // 16 KB each, 1024-byte aligned
   uint8_t q[R * kH * kD];
   float w[R * kH];
-  uint32_t ckey[R][kFCap];
-  int32_t cidx[R][kFCap];
+  uint32_t ckey[R][4 * kSub];  // row r: four per-warp sub-lists
+  int32_t cidx[R][4 * kSub];
   uint32_t aux_key[R][kTopK];
   int32_t aux_idx[R][kTopK];
   SelectScratch sc[R];
   int pages[kMaxTiles];   // the unit's block ids, staged once
   uint64_t full[kNSf], empty[kNSf], tfull[2], tempty[2], qfull;
   uint32_t tmem_base;
-  int wcnt[R][2][4];      // per-warp pass counts of a tile (double-buffered)
+  int wcnt[R][2][4];      // per-warp list sizes at a sync point (double-buffered)
 };
 
 template <int R>
@@ -220,11 +221,57 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
     const int bar = 1 + r;
     uint32_t* const ckey = S.ckey[r];
     int32_t* const cidx = S.cidx[r];
-    int cnt = 0;
-    uint32_t tau = 0;
+    int wc = 0;         // entries in this warp's sub-list
+    uint32_t tau = 0;   // keep keys whose order key >= tau (same in the row's 4 warps)
+    int sync_no = 0;
+    uint32_t* const my_key = ckey + quad * kSub;
+    int32_t* const my_idx = cidx + quad * kSub;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const bool row_live = r < m.nrows;
     const int nr = n[r];
+    // Exchange the four sub-list sizes; when one is nearly full (or at the
+    // unit end) cut the row's candidates to the top 512 and rebalance them
+    // (128 per sub-list), or gather them for the partial output.
+    auto exchange = [&](bool final_cut) -> int {
+      if (lane == 0) S.wcnt[r][sync_no & 1][quad] = wc;
+      const bool all_ok = named_bar_and(bar, kEpiRow, ok);
+      int counts[4];
+      int total = 0, maxc = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        counts[q] = S.wcnt[r][sync_no & 1][q];
+        total += counts[q];
+        maxc = max(maxc, counts[q]);
+      }
+      ++sync_no;
+      if (!all_ok) return -1;
+      if (!final_cut && maxc <= kSubPruneAt) return total;
+      int kept = total;
+      if (total > kTopK) {
+        tau = max(tau, select512_sub_to_aux<kEpiRow, 4, kSub>(ckey, cidx, counts, S.aux_key[r], S.aux_idx[r], S.sc[r],
+                                                              et, bar));
+        kept = kTopK;
+      } else {
+        int before = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) before += q < quad ? counts[q] : 0;
+        for (int j = lane; j < wc; j += 32) {
+          S.aux_key[r][before + j] = my_key[j];
+          S.aux_idx[r][before + j] = my_idx[j];
+        }
+        named_bar(bar, kEpiRow);
+      }
+      if (!final_cut) {  // rebalance: sub-list q takes aux[q*128 ...]
+        const int lo = min(kept, quad * (kTopK / 4)), hi = min(kept, (quad + 1) * (kTopK / 4));
+        for (int j = lo + lane; j < hi; j += 32) {
+          my_key[j - lo] = S.aux_key[r][j];
+          my_idx[j - lo] = S.aux_idx[r][j];
+        }
+        wc = hi - lo;
+        named_bar(bar, kEpiRow);
+      }
+      return kept;
+    };
     // the key scale of the next tile is fetched one tile ahead
     int page_next = ntiles > 0 ? S.pages[0] : -1;
     bool ok_next = page_next >= 0 && page_next < p.num_blocks;
@@ -241,13 +288,13 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
         ks_next = ok_next ? __ldg(p.kscale + (long long)page_next * kBlk + et) : 0.f;
       }
       if (!page_ok && et == 0 && r == 0) atomicOr(p.status, kDevBadPage);
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(&S.tfull[buf], (i >> 1) & 1u));
+      ok = ok && __all_sync(0xFFFFFFFFu, mbar_wait(&S.tfull[buf], (i >> 1) & 1u));
       float score = 0.f;
       if (ok) {
         tc_fence_after();
         const uint32_t col = tmem + lane_base + static_cast<uint32_t>(buf * N + r * kH);
-        // sum_h w_h relu(s_h): relu per head, then packed (f32x2) FMAs
-        unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};
+        // sum_h w_h relu(s_h): relu per head, then packed f32x2 FMAs
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t a[32];
@@ -260,82 +307,43 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
           }
 #pragma unroll
           for (int h2 = 0; h2 < 16; ++h2) {
-            const float2 wv = w2[16 * half + h2];
-            const float lo = fmaxf(__uint_as_float(a[2 * h2]), 0.f), hi = fmaxf(__uint_as_float(a[2 * h2 + 1]), 0.f);
-            const unsigned long long x = (static_cast<unsigned long long>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
-            const unsigned long long wp =
-                (static_cast<unsigned long long>(__float_as_uint(wv.y)) << 32) | __float_as_uint(wv.x);
-            asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc[h2 & 3]) : "l"(x), "l"(wp));
+            const float2 x = make_float2(fmaxf(__uint_as_float(a[2 * h2]), 0.f), fmaxf(__uint_as_float(a[2 * h2 + 1]), 0.f));
+            acc[h2 & 3] = __ffma2_rn(x, w2[16 * half + h2], acc[h2 & 3]);
           }
         }
-        float sum = 0.f;
-#pragma unroll
-        for (int k2 = 0; k2 < 4; ++k2)
-          sum += __uint_as_float(static_cast<uint32_t>(acc[k2])) + __uint_as_float(static_cast<uint32_t>(acc[k2] >> 32));
-        score = sum * ks;
+        score = (((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y))) * ks;
       }
       const bool live = ok && row_live && page_ok && t < nr;
       if constexpr (DENSE) {
         if (live) p.dense[(long long)(m.row0 + r) * p.dense_stride + t] = score;
-        if (!named_bar_and(bar, kEpiRow, ok)) {
-          if (et == 0) atomicOr(p.status, kDevWaitTimeout);
-          ok = false;
-          break;
-        }
       } else {
-        // running top-k filter of this row: per-warp ballot counts are
-        // exchanged through the tile's one barrier, then survivors are placed
+        // running top-k filter: append survivors to this warp's sub-list
         const bool pass = live && score >= tau_float(tau);
         const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass);
-        if (lane == 0) S.wcnt[r][i & 1][quad] = __popc(bal);
-        if (!named_bar_and(bar, kEpiRow, ok)) {
-          if (et == 0) atomicOr(p.status, kDevWaitTimeout);
-          ok = false;
-          break;
-        }
-        const int* wc = S.wcnt[r][i & 1];
-        int before = 0, total = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          before += q < quad ? wc[q] : 0;
-          total += wc[q];
-        }
         if (pass) {
-          const int pos = cnt + before + __popc(bal & ((1u << lane) - 1u));
-          ckey[pos] = order_key(score);
-          cidx[pos] = t;
+          const int pos = wc + __popc(bal & ((1u << lane) - 1u));
+          my_key[pos] = order_key(score);
+          my_idx[pos] = t;
         }
-        cnt += total;
-        if (cnt > kFPruneAt) {
-          named_bar(bar, kEpiRow);  // the list is complete
-          tau = max(tau, select512_to_aux<kEpiRow, kFCap>(ckey, cidx, cnt, S.aux_key[r], S.aux_idx[r], S.sc[r], et,
-                                                          bar));
-          for (int j = et; j < kTopK; j += kEpiRow) {
-            ckey[j] = S.aux_key[r][j];
-            cidx[j] = S.aux_idx[r][j];
-          }
-          named_bar(bar, kEpiRow);
-          cnt = kTopK;
+        wc += __popc(bal);
+        // every warp of the row takes part in every exchange, even after a
+        // timeout (it then stops waiting and contributes nothing)
+        if ((i % kSyncEvery) == kSyncEvery - 1 && i != ntiles - 1) {
+          if (exchange(false) < 0) ok = false;
         }
       }
     }
+    if (!ok && et == 0) atomicOr(p.status, kDevWaitTimeout);
     if constexpr (!DENSE) {
-      // unit end: cut this row's list to 512 and write it as a partial list
-      named_bar(bar, kEpiRow);  // the last tile's survivors are placed
+      // unit end: cut the row's list to 512 and write it as a partial list
+      __syncwarp();
+      const int kept = exchange(true);
       if (row_live) {
         const long long unit = (long long)(m.row0 + r) * p.chunks + c;
-        int cr = ok ? cnt : 0;
-        const uint32_t* src_k = ckey;
-        const int32_t* src_i = cidx;
-        if (cr > kTopK) {
-          select512_to_aux<kEpiRow, kFCap>(ckey, cidx, cr, S.aux_key[r], S.aux_idx[r], S.sc[r], et, bar);
-          cr = kTopK;
-          src_k = S.aux_key[r];
-          src_i = S.aux_idx[r];
-        }
+        const int cr = kept < 0 ? 0 : kept;
         for (int j = et; j < cr; j += kEpiRow) {
-          p.part_key[unit * kTopK + j] = src_k[j];
-          p.part_idx[unit * kTopK + j] = src_i[j];
+          p.part_key[unit * kTopK + j] = S.aux_key[r][j];
+          p.part_idx[unit * kTopK + j] = S.aux_idx[r][j];
         }
         if (et == 0) p.part_cnt[unit] = cr;
       }

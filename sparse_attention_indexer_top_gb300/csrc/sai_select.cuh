@@ -585,4 +585,58 @@ __device__ __forceinline__ void rank_sort(const uint32_t* aux_key, const int32_t
   named_bar(bar, NT);
 }
 
+// Exact top-K (K = 512) over W sub-lists (sub-list w holds counts[w] <=
+// sub_cap entries at key/idx[w * sub_cap ...]) into aux_key/aux_idx[0, K)
+// (unordered). Requires the total to exceed K. Returns the lowest key of the
+// final threshold bin (<= the K-th key).
+template <int NT, int W, int SUB>
+__device__ uint32_t select512_sub_to_aux(const uint32_t* key, const int32_t* idx, const int (&counts)[W],
+                                         uint32_t* aux_key, int32_t* aux_idx, SelectScratch& sc, int tid, int bar) {
+  constexpr int K = kTopK;
+  constexpr int n = W * SUB;
+  constexpr int M = (n + NT - 1) / NT;
+  auto valid = [&](int j) { return (j % SUB) < counts[j / SUB]; };
+  const Threshold t = radix_threshold<NT>(n, (uint32_t)K, sc, tid, bar, [&](int j, uint32_t& v) {
+    v = key[j];
+    return valid(j);
+  });
+  Threshold ti{};
+  const bool ties = !t.all_eq;
+  if (ties) {
+    ti = radix_threshold<NT>(n, t.need, sc, tid, bar, [&](int j, uint32_t& v) {
+      v = 0x7FFFFFFFu - static_cast<uint32_t>(idx[j]);
+      return valid(j) && thr_cmp(t, key[j]) == 0;
+    });
+  }
+  uint32_t selm = 0;
+  int c = 0;
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    const int j = tid + NT * m;
+    if (j < n && valid(j)) {
+      const int cc = thr_cmp(t, key[j]);
+      const bool sel = cc > 0 || (cc == 0 && (!ties || thr_cmp(ti, 0x7FFFFFFFu - static_cast<uint32_t>(idx[j])) >= 0));
+      if (sel) {
+        selm |= 1u << m;
+        ++c;
+      }
+    }
+  }
+  int total;
+  int pos = block_exscan<NT>(c, &total, sc.wcnt, tid, bar);
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    if (selm & (1u << m)) {
+      const int j = tid + NT * m;
+      if (pos < K) {
+        aux_key[pos] = key[j];
+        aux_idx[pos] = idx[j];
+      }
+      ++pos;
+    }
+  }
+  named_bar(bar, NT);
+  return t.base + static_cast<uint32_t>(static_cast<uint64_t>(t.prefix) << t.lo);
+}
+
 }  // namespace sai
