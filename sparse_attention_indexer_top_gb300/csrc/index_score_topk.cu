@@ -223,6 +223,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
     int32_t* const cidx = S.cidx[r];
     int wc = 0;         // entries in this warp's sub-list
     uint32_t tau = 0;   // keep keys whose order key >= tau (same in the row's 4 warps)
+    float tf = tau_float(0);
     int sync_no = 0;
     uint32_t* const my_key = ckey + quad * kSub;
     int32_t* const my_idx = cidx + quad * kSub;
@@ -250,6 +251,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
       if (total > kTopK) {
         tau = max(tau, select512_sub_to_aux<kEpiRow, 4, kSub>(ckey, cidx, counts, S.aux_key[r], S.aux_idx[r], S.sc[r],
                                                               et, bar));
+        tf = tau_float(tau);
         kept = kTopK;
       } else {
         int before = 0;
@@ -318,7 +320,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
         if (live) p.dense[(long long)(m.row0 + r) * p.dense_stride + t] = score;
       } else {
         // running top-k filter: append survivors to this warp's sub-list
-        const bool pass = live && score >= tau_float(tau);
+        const bool pass = live && score >= tf;
         const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass);
         if (pass) {
           const int pos = wc + __popc(bal & ((1u << lane) - 1u));

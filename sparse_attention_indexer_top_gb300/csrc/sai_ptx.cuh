@@ -78,8 +78,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   while (true) {
-    for (int i = 0; i < 16; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    // sleeps until the phase completes (or 20 us pass) instead of spinning,
+    // so waiting warps leave the issue slots to working ones
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
