@@ -56,6 +56,12 @@ def _peaks():
 
 FP8_OVER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
 
+# DRAM bytes (read + write) per streamed key, from one ncu capture of the
+# kernel as it stands (profiles/topk_stream_kernel_packed_extend_2048rows.md:
+# 570.3 MB + 4.7 MB for 142.3 M keys); traffic grows with the keys streamed.
+# Set an entry to None whenever its kernel changes until it is re-captured.
+TRAFFIC_BYTES_PER_KEY = {"topk_packed_extend": (570.3e6 + 4.7e6) / 142.3e6}
+
 
 def _dist():
     rank = int(os.environ.get("RANK", "0"))
@@ -380,7 +386,8 @@ def run_gpu(args):
         roof = {"bound": "hbm", "achieved": tp.bytes / (tm * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
                 "peak_kind": peak_kind}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    per_key = TRAFFIC_BYTES_PER_KEY.get(tp.name)
+    roof["traffic"] = None if per_key is None else per_key * tp.keys
     roof["kernel"] = tp.name
 
     # end to end: every input copied from pinned host memory, every output read back
