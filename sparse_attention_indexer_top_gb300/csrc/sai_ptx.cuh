@@ -204,6 +204,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// Two back-to-back 32-column loads (64 consecutive columns) of this thread's
+// TMEM lane; call tmem_ld_wait() before using the values.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
+  uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[32]);
+  tmem_ld32(taddr, lo);
+  tmem_ld32(taddr + 32, hi);
+}
+
 // Shared-memory matrix descriptor for a K-major operand tile stored with the
 // 128-byte swizzle (rows of 128 bytes, 8-row atoms of 1024 bytes), as a TMA
 // tiled load with CU_TENSOR_MAP_SWIZZLE_128B writes it. The tile base must

@@ -639,4 +639,61 @@ __device__ uint32_t select512_sub_to_aux(const uint32_t* key, const int32_t* idx
   return t.base + static_cast<uint32_t>(static_cast<uint64_t>(t.prefix) << t.lo);
 }
 
+// Sort cnt (<= 512) entries of aux_key/aux_idx by (key desc, index asc)
+// with a bitonic network over 128 threads, 4 entries per thread: thread t
+// holds virtual positions 4t .. 4t+3, so strides 1-2 stay in registers,
+// strides 4-64 use warp shuffles and strides 128-256 go through `buf`
+// (512 entries). On return v[j] is the entry of output rank 4t + j
+// (composite key, 0 = padding).
+__device__ __forceinline__ void bitonic_sort512_128(const uint32_t* aux_key, const int32_t* aux_idx, int cnt,
+                                                    unsigned long long* buf, unsigned long long (&v)[4], int tid,
+                                                    int bar) {
+  const int lane = tid & 31;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = tid + 128 * j;  // any placement works: everything gets sorted
+    v[j] = e < cnt ? composite(aux_key[e], aux_idx[e]) : 0ull;
+  }
+#pragma unroll
+  for (int size = 2; size <= 512; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride < 4) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (j & stride) continue;
+          const int j2 = j | stride;
+          const bool asc = ((4 * tid + j) & size) != 0;
+          const unsigned long long x = v[j], y = v[j2];
+          const unsigned long long hi = x > y ? x : y, lo = x > y ? y : x;
+          v[j] = asc ? lo : hi;
+          v[j2] = asc ? hi : lo;
+        }
+      } else if (stride < 128) {
+        const int d = stride >> 2;  // lane distance
+        const bool lower = (lane & d) == 0;
+        const bool asc = ((4 * tid) & size) != 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const unsigned long long p = __shfl_xor_sync(0xFFFFFFFFu, v[j], d);
+          v[j] = (lower != asc) ? (v[j] > p ? v[j] : p) : (v[j] < p ? v[j] : p);
+        }
+      } else {
+        const int d = stride >> 2;  // thread distance
+        const bool lower = (tid & d) == 0;
+        const bool asc = ((4 * tid) & size) != 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) buf[4 * tid + j] = v[j];
+        named_bar(bar, 128);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const unsigned long long p = buf[4 * (tid ^ d) + j];
+          v[j] = (lower != asc) ? (v[j] > p ? v[j] : p) : (v[j] < p ? v[j] : p);
+        }
+        named_bar(bar, 128);
+      }
+    }
+  }
+}
+
 }  // namespace sai

@@ -72,10 +72,7 @@ struct __align__(128) Smem {
       uint32_t key[kCap];
       int32_t idx[kCap];
     } c;
-    struct {
-      uint32_t key[kTopK];
-      int32_t idx[kTopK];
-    } runs;  // final sort (the list is dead by then)
+    unsigned long long sortbuf[kTopK];  // final sort (the list is dead by then)
   } cand;
   uint32_t aux_key[kTopK];
   int32_t aux_idx[kTopK];
@@ -345,14 +342,22 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
         }
         named_bar(kBar, kThreads);
       }
-      uint32_t k[kTopK / kThreads];
-      int32_t ix[kTopK / kThreads];
-      int rk[kTopK / kThreads];
-      rank_sort<kThreads>(S.aux_key, S.aux_idx, cnt, S.cand.runs.key, S.cand.runs.idx, k, ix, rk, tid, kBar);
+      unsigned long long v[4];
+      bitonic_sort512_128(S.aux_key, S.aux_idx, cnt, S.cand.sortbuf, v, tid, kBar);
+      // output rank 4*tid + j
+      uint32_t k[4];
+      int32_t ix[4];
+      int rk[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        k[e] = static_cast<uint32_t>(v[e] >> 32);
+        ix[e] = v[e] ? static_cast<int32_t>(~static_cast<uint32_t>(v[e] & 0xFFFFFFFFull)) : -1;
+        rk[e] = 4 * tid + e;
+      }
       if (tid == 0) S.spec_keys[0] = S.spec_keys[1] = 0;
       named_bar(kBar, kThreads);
 #pragma unroll
-      for (int e = 0; e < kTopK / kThreads; ++e) {
+      for (int e = 0; e < 4; ++e) {
         if (ix[e] >= 0 && rk[e] == kTopK / 2 - 1) S.spec_keys[0] = k[e];
         if (ix[e] >= 0 && rk[e] == kTopK - 1) S.spec_keys[1] = k[e];
       }
@@ -383,13 +388,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
         if (tid == 0) p.part_cnt[unit] = cnt;
       }
       named_bar(kBar, kThreads);
-      // Next unit's starting threshold: extrapolate the tail one octave of
-      // rank down, t = 2*v(512) - v(256), which keeps about twice the
-      // needed count when neighbouring rows look alike.
+      // Next unit's starting threshold: extrapolate the tail half an
+      // octave of rank down, t = v(512) - (v(256) - v(512)) / 2, which keeps
+      // about 1.4x the needed count when neighbouring rows look alike.
       spec = 0;
       if (S.spec_keys[1] != 0) {
         const float v256 = key_to_float(S.spec_keys[0]), v512 = key_to_float(S.spec_keys[1]);
-        const float t = 2.0f * v512 - v256;
+        const float t = v512 - 0.5f * (v256 - v512);
         if (isfinite(t) && isfinite(v256) && isfinite(v512)) spec = order_key(t);
       }
       cnt = 0;
