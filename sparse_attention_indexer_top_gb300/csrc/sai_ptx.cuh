@@ -135,6 +135,20 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bo
   return r != 0;
 }
 
+// Named barrier that also ORs a predicate across the participating threads.
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 // ------------------------------------------------------------------------
 // TMA tiled loads (tensor maps are built on the host with
 // cuTensorMapEncodeTiled and passed as __grid_constant__ parameters).
@@ -203,15 +217,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// Two back-to-back 32-column loads (64 consecutive columns) of this thread's
-// TMEM lane; call tmem_ld_wait() before using the values.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
-  uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
-  uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[32]);
-  tmem_ld32(taddr, lo);
-  tmem_ld32(taddr + 32, hi);
-}
 
 // Shared-memory matrix descriptor for a K-major operand tile stored with the
 // 128-byte swizzle (rows of 128 bytes, 8-row atoms of 1024 bytes), as a TMA

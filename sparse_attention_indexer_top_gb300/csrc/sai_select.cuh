@@ -595,7 +595,13 @@ __device__ uint32_t select512_sub_to_aux(const uint32_t* key, const int32_t* idx
   constexpr int K = kTopK;
   constexpr int n = W * SUB;
   constexpr int M = (n + NT - 1) / NT;
-  auto valid = [&](int j) { return (j % SUB) < counts[j / SUB]; };
+  auto valid = [&](int j) {
+    const int w = j / SUB;
+    int c = counts[0];
+#pragma unroll
+    for (int u = 1; u < W; ++u) c = w == u ? counts[u] : c;  // no dynamic index: keeps counts in registers
+    return (j % SUB) < c;
+  };
   const Threshold t = radix_threshold<NT>(n, (uint32_t)K, sc, tid, bar, [&](int j, uint32_t& v) {
     v = key[j];
     return valid(j);

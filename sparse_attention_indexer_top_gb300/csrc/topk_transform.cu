@@ -21,10 +21,13 @@
 //     folded into every row instead of a separate fallback kernel.
 //   * Each thread compares its 8 scores of a stage against the running
 //     threshold tau (as a float) and appends the survivors (order key,
-//     row-local index) to a shared candidate list. When the list fills up it
-//     is cut to the exact top 512 (radix select in shared memory) and tau
-//     rises to that cut, so the filter stays exact: every dropped element is
-//     beaten by 512 kept ones.
+//     row-local index) to its warp's own candidate sub-list: a ballot prefix
+//     inside the warp, no shared atomics. The one block barrier per stage
+//     (it releases the stage for refill) also ORs "some sub-list is nearly
+//     full"; then all sub-lists are cut together to the exact top 512 (radix
+//     select in shared memory), dealt back 128 per warp, and tau rises to
+//     that cut, so the filter stays exact: every dropped element is beaten
+//     by 512 kept ones.
 //   * At the end of a unit the candidates are cut to 512, sorted by
 //     (score desc, index asc), page-transformed and written (one unit per
 //     row), or written as a partial list for the merge kernel (split rows).
@@ -43,14 +46,17 @@ namespace {
 constexpr int kThreads = 128;                    // 4 warps per CTA
 constexpr int kStage = 1024;                     // floats per stage (4 KB): two float4 per thread
 constexpr int kNStage = 3;                       // 12 KB in flight per CTA
-constexpr int kCap = 2048;                       // candidate capacity
+constexpr int kWarps = kThreads / 32;
+constexpr int kCap = 2048;                       // candidate capacity (all warps)
+constexpr int kSub = kCap / kWarps;              // one candidate sub-list per warp
 constexpr int kMaxExtra = 8;                     // scalar head/tail elements of a window
-constexpr int kPruneAt = kCap - kStage - kMaxExtra;
+constexpr int kWarpStage = kStage / kWarps + kMaxExtra;  // most entries a warp appends per stage
+constexpr int kSubPruneAt = kSub - kWarpStage;   // cut all sub-lists once one holds more
 constexpr int kBar = 1;                          // named barrier id (all 128 threads)
 constexpr int kCtasPerSm = 6;
 
 static_assert(kStage == 8 * kThreads, "two float4 per thread per stage");
-static_assert(kPruneAt > kTopK, "room to keep the top 512 and append one stage");
+static_assert(kSubPruneAt >= kTopK / kWarps, "a dealt-back sub-list must not trigger another cut");
 
 struct StageDesc {
   int unit;          // -1: no more work
@@ -80,7 +86,9 @@ struct __align__(128) Smem {
   uint64_t full[kNStage];
   SelectScratch sc;
   uint32_t spec_keys[2];  // keys at ranks 256 and 512 of the last finished unit
-  int add[3];
+  int wcnt[kWarps];       // sub-list sizes, published before a cut
+  int wapp[kWarps];       // per-warp appends of the unit, published at its end
+  int timeout;            // set by a thread whose stage wait gave up
   struct Cursor {         // thread 0's walk over its work units (issue side)
     int unit;             // current unit (>= units: done)
     int s, nst;           // stage index within the unit, stage count
@@ -174,56 +182,96 @@ __device__ bool issue_stage(const TopkLaunch& p, Smem& S, int slot, uint64_t pol
   return true;
 }
 
-// One block of up to 9 elements per thread: a = elements base+4t..+3,
-// b = elements base+512+4t..+3, x = one scalar element at index xi; bit i
-// of `mask` says element i passes the filter. Survivors are appended to the
-// candidate list (one shared atomic per warp), and the list is cut back to
-// the top 512 when it is nearly full. `rot` rotates the three shared append
-// counters; all 128 threads call this with uniform cnt/tau/rot.
-__device__ __forceinline__ void add_block(Smem& S, const float4& a, const float4& b, float x, int xi, int base,
-                                          uint32_t mask, int& cnt, uint32_t& tau, uint32_t& rot, int& appended,
-                                          int tid) {
+// Append this thread's survivors to its warp's sub-list (key/idx point at
+// the sub-list; it holds wcnt entries). a = elements base+4t..+3, b =
+// elements base+512+4t..+3, x = one scalar element at index xi; bit i of
+// `mask` says element i passes. Survivors are rare (about 1% of a row), so
+// the common case is one survivor on a few lanes: one ballot gives every
+// lane its offset; only when some lane has several does the warp ballot the
+// bits of the per-lane counts (at most 9). Each lane then walks only its set
+// bits. No shared atomics, no block barrier. Returns how many the warp
+// appended (warp-uniform).
+__device__ __forceinline__ int warp_append(uint32_t* key, int32_t* idx, int wcnt, const float4& a, const float4& b,
+                                           float x, int xi, int base, uint32_t mask, int tid) {
   const int lane = tid & 31;
-  const int m = __popc(mask);
-  if (__any_sync(0xFFFFFFFFu, m > 0)) {
-    int incl = m;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-      if (lane >= d) incl += o;
+  const uint32_t any = __ballot_sync(0xFFFFFFFFu, mask != 0);
+  if (any == 0) return 0;
+  const uint32_t lt = (1u << lane) - 1u;
+  const uint32_t multi = __ballot_sync(0xFFFFFFFFu, (mask & (mask - 1u)) != 0);
+  int pos, total;
+  if (multi == 0) {
+    pos = wcnt + __popc(any & lt);
+    total = __popc(any);
+  } else {
+    const uint32_t m = __popc(mask);
+    const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, m & 1u), b1 = __ballot_sync(0xFFFFFFFFu, m & 2u);
+    const uint32_t b2 = __ballot_sync(0xFFFFFFFFu, m & 4u), b3 = __ballot_sync(0xFFFFFFFFu, m & 8u);
+    pos = wcnt + __popc(b0 & lt) + 2 * __popc(b1 & lt) + 4 * __popc(b2 & lt) + 8 * __popc(b3 & lt);
+    total = __popc(b0) + 2 * __popc(b1) + 4 * __popc(b2) + 8 * __popc(b3);
+  }
+  while (mask) {
+    const int i = __ffs(mask) - 1;
+    mask &= mask - 1u;
+    const float4& h = i < 4 ? a : b;
+    const int q = i & 3;
+    float v = q == 0 ? h.x : (q == 1 ? h.y : (q == 2 ? h.z : h.w));
+    int ix = base + 4 * (i < 4 ? tid : kThreads + tid) + q;
+    if (i == 8) {
+      v = x;
+      ix = xi;
     }
-    int start = 0;
-    if (lane == 31) start = atomicAdd(&S.add[rot % 3], incl);
-    int pos = __shfl_sync(0xFFFFFFFFu, start, 31) + cnt + incl - m;
-    if (mask) {
-      const float v[9] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, x};
+    key[pos] = order_key(v);
+    idx[pos] = ix;
+    ++pos;
+  }
+  return total;
+}
+
+// Gather every warp's sub-list into aux: the exact top 512 of their union
+// when it holds more (tau rises to the cut), else all of it. All threads
+// call this with their warp's wcnt; returns the number in aux.
+__device__ int gather_to_aux(Smem& S, int wcnt, uint32_t& tau, int tid) {
+  const int lane = tid & 31, warp = tid >> 5;
+  if (lane == 0) S.wcnt[warp] = wcnt;
+  named_bar(kBar, kThreads);
+  int counts[kWarps];
+  int total = 0, off = 0;
 #pragma unroll
-      for (int i = 0; i < 9; ++i) {
-        if (mask & (1u << i)) {
-          S.cand.c.key[pos] = order_key(v[i]);
-          S.cand.c.idx[pos] = i < 4 ? base + 4 * tid + i : (i < 8 ? base + 4 * (kThreads + tid) + (i - 4) : xi);
-          ++pos;
-        }
-      }
-    }
+  for (int w = 0; w < kWarps; ++w) {
+    counts[w] = S.wcnt[w];
+    off += w < warp ? counts[w] : 0;
+    total += counts[w];
+  }
+  if (total > kTopK) {
+    tau = max(tau, select512_sub_to_aux<kThreads, kWarps, kSub>(S.cand.c.key, S.cand.c.idx, counts, S.aux_key,
+                                                                S.aux_idx, S.sc, tid, kBar));
+    return kTopK;
+  }
+  const uint32_t* key = S.cand.c.key + warp * kSub;
+  const int32_t* idx = S.cand.c.idx + warp * kSub;
+  for (int j = lane; j < wcnt; j += 32) {
+    S.aux_key[off + j] = key[j];
+    S.aux_idx[off + j] = idx[j];
   }
   named_bar(kBar, kThreads);
-  if (tid == 0) S.add[(rot + 2) % 3] = 0;  // counter of block rot+2; last read before this barrier
-  const int added = S.add[rot % 3];
-  ++rot;
-  cnt += added;
-  appended += added;
-  if (cnt > kPruneAt) {
-    uint32_t* const ckey = S.cand.c.key;
-    int32_t* const cidx = S.cand.c.idx;
-    tau = max(tau, select512_to_aux<kThreads, kCap>(ckey, cidx, cnt, S.aux_key, S.aux_idx, S.sc, tid, kBar));
-    for (int j = tid; j < kTopK; j += kThreads) {
-      ckey[j] = S.aux_key[j];
-      cidx[j] = S.aux_idx[j];
-    }
-    named_bar(kBar, kThreads);
-    cnt = kTopK;
+  return total;
+}
+
+// Cut all sub-lists together (gather_to_aux) and deal the kept entries back,
+// 128 per warp. Returns the warp's new sub-list size.
+__device__ __forceinline__ int prune(Smem& S, int wcnt, uint32_t& tau, int tid) {
+  const int lane = tid & 31, warp = tid >> 5;
+  const int total = gather_to_aux(S, wcnt, tau, tid);
+  constexpr int kShare = kTopK / kWarps;
+  const int mine = min(max(total - kShare * warp, 0), kShare);
+  uint32_t* key = S.cand.c.key + warp * kSub;
+  int32_t* idx = S.cand.c.idx + warp * kSub;
+  for (int j = lane; j < mine; j += 32) {
+    key[j] = S.aux_key[kShare * warp + j];
+    idx[j] = S.aux_idx[kShare * warp + j];
   }
+  __syncwarp();
+  return mine;
 }
 
 __device__ __forceinline__ uint32_t pass4(const float4& v, float tf) {
@@ -234,13 +282,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
   extern __shared__ unsigned char smem_raw[];
   Smem& S = smem_ref(smem_raw);
   const int tid = threadIdx.x;
-  uint32_t* const ckey = S.cand.c.key;
-  int32_t* const cidx = S.cand.c.idx;
+  const int lane = tid & 31, warp = tid >> 5;
+  uint32_t* const wkey = S.cand.c.key + warp * kSub;  // this warp's sub-list
+  int32_t* const widx = S.cand.c.idx + warp * kSub;
   uint64_t policy = 0;
   bool issuing = false;
   if (tid == 0) {
     for (int i = 0; i < kNStage; ++i) mbar_init(&S.full[i], 1);
-    S.add[0] = S.add[1] = S.add[2] = 0;
+    S.timeout = 0;
     fence_mbar_init();
     policy = l2_policy_evict_first();
     S.cur.unit = blockIdx.x;
@@ -249,9 +298,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
     for (int i = 0; i < kNStage && issuing; ++i) issuing = issue_stage(p, S, i, policy);
   }
   __syncthreads();
-  uint32_t it = 0, rot = 0;
-  int cnt = 0;        // candidates held (uniform)
-  int appended = 0;   // elements that passed the filter in this unit
+  uint32_t it = 0;
+  int wcnt = 0;       // entries in this warp's sub-list (warp-uniform)
+  int appended = 0;   // elements this warp let through the filter in this unit
   uint32_t tau = 0;   // keep elements whose order key >= tau
   uint32_t spec = 0;  // speculative starting threshold for the next unit (0: none)
   uint32_t spec_used = 0;
@@ -268,32 +317,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
     const int head = ok ? d.head : 0, tail = ok ? d.tail : 0, lo = d.lo, tail_at = d.tail_at, len = d.len;
     const long long woff = d.woff;
     if (flags & 1) {
-      cnt = 0;
+      wcnt = 0;
       appended = 0;
       // Start from the previous unit's threshold estimate; whether it was
       // low enough is checked exactly when the unit ends.
       tau = spec;
       spec_used = spec;
     }
-    const float tf = tau_float(tau);
     float4 va = make_float4(0.f, 0.f, 0.f, 0.f), vb = va;
-    float vx = 0.f;
-    int xi = 0;
-    uint32_t mask = 0;
-    if (4 * tid < nvec) {
-      va = reinterpret_cast<const float4*>(S.stage[slot])[tid];
-      mask = pass4(va, tf);
-    }
-    if (4 * (kThreads + tid) < nvec) {
-      vb = reinterpret_cast<const float4*>(S.stage[slot])[kThreads + tid];
-      mask |= pass4(vb, tf) << 4;
-    }
-    if (tid < head + tail) {  // scalar ends of the window (first stage of a unit)
-      xi = tid < head ? lo + tid : tail_at + (tid - head);
-      vx = __ldg(p.scores + woff + xi);
-      mask |= (vx >= tf ? 1u : 0u) << 8;
-    }
-    if (!named_bar_and(kBar, kThreads, ok)) {
+    if (4 * tid < nvec) va = reinterpret_cast<const float4*>(S.stage[slot])[tid];
+    if (4 * (kThreads + tid) < nvec) vb = reinterpret_cast<const float4*>(S.stage[slot])[kThreads + tid];
+    if (!ok) S.timeout = 1;
+    // Everyone has the stage in registers, so the slot is refilled before any
+    // filtering work (the ring never waits on it). The same barrier tells
+    // whether the last stage's appends left some sub-list too full to take
+    // another stage: then all sub-lists are cut first.
+    const bool any = named_bar_or(kBar, kThreads, !ok || wcnt > kSubPruneAt);
+    if (any && S.timeout) {
       if (tid == 0) {
         atomicOr(p.status, kDevWaitTimeout);
         // let the copies already issued land before the CTA exits (bounded)
@@ -305,13 +345,33 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
       fence_proxy_async_smem();
       issuing = issue_stage(p, S, slot, policy);
     }
-    add_block(S, va, vb, vx, xi, base, mask, cnt, tau, rot, appended, tid);
+    if (any) wcnt = prune(S, wcnt, tau, tid);
+    {
+      const float tf = tau_float(tau);
+      uint32_t mask = 0;
+      if (4 * tid < nvec) mask = pass4(va, tf);
+      if (4 * (kThreads + tid) < nvec) mask |= pass4(vb, tf) << 4;
+      float vx = 0.f;
+      int xi = 0;
+      if (tid < head + tail) {  // scalar ends of the window (first stage of a unit)
+        xi = tid < head ? lo + tid : tail_at + (tid - head);
+        vx = __ldg(p.scores + woff + xi);
+        mask |= (vx >= tf ? 1u : 0u) << 8;
+      }
+      const int added = warp_append(wkey, widx, wcnt, va, vb, vx, xi, base, mask, tid);
+      wcnt += added;
+      appended += added;
+    }
     if (flags & 2) {
-      if (spec_used && appended < min(len, kTopK)) {
+      if (lane == 0) S.wapp[warp] = appended;
+      named_bar(kBar, kThreads);
+      int passed = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) passed += S.wapp[w];
+      if (spec_used && passed < min(len, kTopK)) {
         // The starting threshold was too high for this unit: redo it from
         // global memory with no threshold (exact again, just slower).
-        cnt = 0;
-        appended = 0;
+        wcnt = 0;
         tau = 0;
         for (int b0 = 0; b0 < len; b0 += kStage) {
           const float tf0 = tau_float(tau);
@@ -327,21 +387,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
               rm |= (r[k] >= tf0 ? 1u : 0u) << k;
             }
           }
-          add_block(S, make_float4(r[0], r[1], r[2], r[3]), make_float4(r[4], r[5], r[6], r[7]), 0.f, 0, lo + b0,
-                    rm, cnt, tau, rot, appended, tid);
+          wcnt += warp_append(wkey, widx, wcnt, make_float4(r[0], r[1], r[2], r[3]),
+                              make_float4(r[4], r[5], r[6], r[7]), 0.f, 0, lo + b0, rm, tid);
+          if (named_bar_or(kBar, kThreads, wcnt > kSubPruneAt)) wcnt = prune(S, wcnt, tau, tid);
         }
         spec_used = 0;
       }
-      if (cnt > kTopK) {
-        select512_to_aux<kThreads, kCap>(ckey, cidx, cnt, S.aux_key, S.aux_idx, S.sc, tid, kBar);
-        cnt = kTopK;
-      } else {
-        for (int j = tid; j < cnt; j += kThreads) {
-          S.aux_key[j] = ckey[j];
-          S.aux_idx[j] = cidx[j];
-        }
-        named_bar(kBar, kThreads);
-      }
+      const int cnt = gather_to_aux(S, wcnt, tau, tid);
       unsigned long long v[4];
       bitonic_sort512_128(S.aux_key, S.aux_idx, cnt, S.cand.sortbuf, v, tid, kBar);
       // output rank 4*tid + j
@@ -397,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
         const float t = v512 - 0.5f * (v256 - v512);
         if (isfinite(t) && isfinite(v256) && isfinite(v512)) spec = order_key(t);
       }
-      cnt = 0;
+      wcnt = 0;
     }
     ++it;
   }
