@@ -8,10 +8,12 @@
 // addressing inside the top-k kernel is the "merge build sparse block into
 // topk" step of ROCm/ATOM PR #1282.
 //
-// GB300 design: many small persistent CTAs (4 warps, ~34 KB of shared
-// memory, six per SM), each streaming one work unit (a row, or a chunk of a
+// GB300 design: many small persistent CTAs (4 warps, ~43 KB of shared
+// memory, five per SM), each streaming one work unit (a row, or a chunk of a
 // long row) at a time, so that the serial latency of one CTA's
 // stage -> filter -> barrier chain is hidden by the other CTAs on the SM.
+// The kernel is bound by instruction issue, not by HBM, so each stage is
+// large (8 KB, sixteen scores per thread) to spread the per-stage cost.
 //   * Thread 0 keeps a ring of shared-memory stages filled with 1-D bulk TMA
 //     copies (cp.async.bulk + mbarrier complete_tx, evict-first in L2: every
 //     score is read once). The 16-byte-aligned interior of each window goes
@@ -19,15 +21,15 @@
 //     stride, any row start) are read with scalar loads. This is the scalar
 //     path the pages require for strides that are not a multiple of 4,
 //     folded into every row instead of a separate fallback kernel.
-//   * Each thread compares its 8 scores of a stage against the running
+//   * Each thread compares its 16 scores of a stage against the running
 //     threshold tau (as a float) and appends the survivors (order key,
 //     row-local index) to its warp's own candidate sub-list: a ballot prefix
 //     inside the warp, no shared atomics. The one block barrier per stage
-//     (it releases the stage for refill) also ORs "some sub-list is nearly
-//     full"; then all sub-lists are cut together to the exact top 512 (radix
-//     select in shared memory), dealt back 128 per warp, and tau rises to
-//     that cut, so the filter stays exact: every dropped element is beaten
-//     by 512 kept ones.
+//     (it releases the stage for refill) also ORs "some warp's survivors do
+//     not fit"; then all sub-lists are cut together to the exact top 512
+//     (radix select in shared memory), dealt back 128 per warp, tau rises to
+//     that cut and the stage is appended a quarter at a time. The filter
+//     stays exact: every dropped element is beaten by 512 kept ones.
 //   * At the end of a unit the candidates are cut to 512, sorted by
 //     (score desc, index asc), page-transformed and written (one unit per
 //     row), or written as a partial list for the merge kernel (split rows).
@@ -44,31 +46,39 @@ namespace sai {
 namespace {
 
 constexpr int kThreads = 128;                    // 4 warps per CTA
-constexpr int kStage = 1024;                     // floats per stage (4 KB): two float4 per thread
-constexpr int kNStage = 3;                       // 12 KB in flight per CTA
+constexpr int kVec = 4;                          // float4 loads per thread per stage
+constexpr int kStage = kVec * 4 * kThreads;      // floats per stage (8 KB)
+constexpr int kNStage = 3;                       // 24 KB in flight per CTA
 constexpr int kWarps = kThreads / 32;
-constexpr int kCap = 2048;                       // candidate capacity (all warps)
+constexpr int kCap = 1536;                       // candidate capacity (all warps)
 constexpr int kSub = kCap / kWarps;              // one candidate sub-list per warp
 constexpr int kMaxExtra = 8;                     // scalar head/tail elements of a window
-constexpr int kWarpStage = kStage / kWarps + kMaxExtra;  // most entries a warp appends per stage
-constexpr int kSubPruneAt = kSub - kWarpStage;   // cut all sub-lists once one holds more
+constexpr int kPartWarp = 4 * 32 + kMaxExtra;    // most entries a warp appends from one float4 per lane
+constexpr int kSubCutAt = kSub - kPartWarp;      // slow path: cut before a part that might not fit
 constexpr int kBar = 1;                          // named barrier id (all 128 threads)
-constexpr int kCtasPerSm = 6;
+constexpr int kCtasPerSm = 5;
+constexpr uint32_t kScalarBit = 1u << (4 * kVec);
 
-static_assert(kStage == 8 * kThreads, "two float4 per thread per stage");
-static_assert(kSubPruneAt >= kTopK / kWarps, "a dealt-back sub-list must not trigger another cut");
+static_assert(kSubCutAt >= kTopK / kWarps, "a dealt-back sub-list must take one more part");
 
-struct StageDesc {
-  int unit;          // -1: no more work
+// What a unit's first and last stage need besides the stage itself.
+struct UnitInfo {
   int row;
   int batch;         // page-table row
-  int base;          // row-local index of stage element 0
-  int nvec;          // TMA elements in this stage (multiple of 4)
-  int flags;         // 1: first stage of the unit, 2: last stage of the unit
   int head, tail;    // scalar elements: [lo, lo+head) and [tail_at, tail_at+tail)
   int lo, tail_at;
   int len;           // elements of the unit's window range [lo, lo+len)
+  int pad;
   long long woff;    // element offset of the row's window start in `scores`
+};
+
+// Per-slot descriptor written by the issuing thread: `hot` = {unit (-1: no
+// more work), row-local index of the stage's element 0, TMA elements in the
+// stage (a multiple of 4), flags (1: first stage of the unit, 2: last)} is
+// read every stage; `u` is written and read only when flags != 0.
+struct StageDesc {
+  int4 hot;
+  UnitInfo u;
 };
 
 struct __align__(128) Smem {
@@ -92,9 +102,10 @@ struct __align__(128) Smem {
   struct Cursor {         // thread 0's walk over its work units (issue side)
     int unit;             // current unit (>= units: done)
     int s, nst;           // stage index within the unit, stage count
-    int row, batch;
-    int lo, head, body, tail;
-    long long woff;
+    int base;             // row-local index of the next stage's element 0
+    int body_left;        // TMA elements not issued yet
+    const float* src;     // global address of the next stage
+    UnitInfo u;
   } cur;
 };
 
@@ -125,106 +136,116 @@ __device__ void cursor_load(const TopkLaunch& p, Cursor& c) {
     n = 0;
     b = 0;
   }
-  c.row = row;
-  c.batch = b;
-  c.woff = (long long)row * p.stride + (bad ? 0 : start);
+  const long long woff = (long long)row * p.stride + (bad ? 0 : start);
   int lo = p.chunks > 1 ? ch * p.chunk_len : 0;
   const int hi = p.chunks > 1 ? min(n, lo + p.chunk_len) : n;
   if (lo > hi) lo = hi;
   const int len = hi - lo;
-  int head = (int)(((16u - (reinterpret_cast<uintptr_t>(p.scores + c.woff + lo) & 15u)) & 15u) >> 2);
+  int head = (int)(((16u - (reinterpret_cast<uintptr_t>(p.scores + woff + lo) & 15u)) & 15u) >> 2);
   int body = 0;
   if (len <= kMaxExtra || head > len) {
     head = len;
   } else {
     body = (len - head) & ~3;
   }
-  c.lo = lo;
-  c.head = head;
-  c.body = body;
-  c.tail = len - head - body;
+  c.u.row = row;
+  c.u.batch = b;
+  c.u.head = head;
+  c.u.tail = len - head - body;
+  c.u.lo = lo;
+  c.u.tail_at = lo + head + body;
+  c.u.len = len;
+  c.u.woff = woff;
   c.nst = max(1, (body + kStage - 1) / kStage);
+  c.base = lo + head;
+  c.body_left = body;
+  c.src = p.scores + woff + lo + head;
 }
 
 // Issue the cursor's next stage into `slot` (thread 0 only) and advance.
 // Returns false once the terminal descriptor has been issued.
 __device__ bool issue_stage(const TopkLaunch& p, Smem& S, int slot, uint64_t policy) {
   Cursor& c = S.cur;
-  const int units = p.rows * p.chunks;
   StageDesc& d = S.desc[slot];
-  if (c.unit >= units) {
-    d.unit = -1;
+  if (c.unit >= p.rows * p.chunks) {
+    d.hot = make_int4(-1, 0, 0, 0);
     mbar_arrive(&S.full[slot]);
     return false;
   }
-  d.unit = c.unit;
-  d.row = c.row;
-  d.batch = c.batch;
-  d.flags = (c.s == 0 ? 1 : 0) | (c.s == c.nst - 1 ? 2 : 0);
-  d.base = c.lo + c.head + c.s * kStage;
-  d.nvec = min(kStage, c.body - c.s * kStage);
-  d.head = c.s == 0 ? c.head : 0;
-  d.tail = c.s == 0 ? c.tail : 0;
-  d.lo = c.lo;
-  d.tail_at = c.lo + c.head + c.body;
-  d.len = c.head + c.body + c.tail;
-  d.woff = c.woff;
-  if (d.nvec > 0) {
-    mbar_arrive_expect_tx(&S.full[slot], (uint32_t)d.nvec * 4u);
-    bulk_g2s_stream(S.stage[slot], p.scores + c.woff + d.base, (uint32_t)d.nvec * 4u, &S.full[slot], policy);
+  const int s = c.s, nst = c.nst;
+  const int flags = (s == 0 ? 1 : 0) | (s == nst - 1 ? 2 : 0);
+  const int nvec = min(kStage, c.body_left);
+  d.hot = make_int4(c.unit, c.base, nvec, flags);
+  if (flags) d.u = c.u;
+  if (nvec > 0) {
+    mbar_arrive_expect_tx(&S.full[slot], (uint32_t)nvec * 4u);
+    bulk_g2s_stream(S.stage[slot], c.src, (uint32_t)nvec * 4u, &S.full[slot], policy);
   } else {
     mbar_arrive(&S.full[slot]);
   }
-  if (++c.s >= c.nst) {
+  if (s + 1 >= nst) {
     c.unit += gridDim.x;
     cursor_load(p, c);
+  } else {
+    c.s = s + 1;
+    c.base += kStage;
+    c.body_left -= nvec;
+    c.src += kStage;
   }
   return true;
 }
 
-// Append this thread's survivors to its warp's sub-list (key/idx point at
-// the sub-list; it holds wcnt entries). a = elements base+4t..+3, b =
-// elements base+512+4t..+3, x = one scalar element at index xi; bit i of
-// `mask` says element i passes. Survivors are rare (about 1% of a row), so
-// the common case is one survivor on a few lanes: one ballot gives every
-// lane its offset; only when some lane has several does the warp ballot the
-// bits of the per-lane counts (at most 9). Each lane then walks only its set
-// bits. No shared atomics, no block barrier. Returns how many the warp
-// appended (warp-uniform).
-__device__ __forceinline__ int warp_append(uint32_t* key, int32_t* idx, int wcnt, const float4& a, const float4& b,
-                                           float x, int xi, int base, uint32_t mask, int tid) {
-  const int lane = tid & 31;
+// Offsets of this lane's survivors in its warp's sub-list: bit i of `mask`
+// marks a survivor (at most 4*kVec + 1 per lane). Survivors are rare (about
+// 1% of a row), so the common case is one survivor on a few lanes and one
+// ballot gives every lane its offset; only when some lane has several does
+// the warp ballot the bits of the per-lane counts. Returns the warp total
+// (warp-uniform) and this lane's first offset in *pos.
+__device__ __forceinline__ int warp_offsets(uint32_t mask, int lane, int* pos) {
   const uint32_t any = __ballot_sync(0xFFFFFFFFu, mask != 0);
-  if (any == 0) return 0;
   const uint32_t lt = (1u << lane) - 1u;
+  *pos = 0;
+  if (any == 0) return 0;
   const uint32_t multi = __ballot_sync(0xFFFFFFFFu, (mask & (mask - 1u)) != 0);
-  int pos, total;
   if (multi == 0) {
-    pos = wcnt + __popc(any & lt);
-    total = __popc(any);
-  } else {
-    const uint32_t m = __popc(mask);
-    const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, m & 1u), b1 = __ballot_sync(0xFFFFFFFFu, m & 2u);
-    const uint32_t b2 = __ballot_sync(0xFFFFFFFFu, m & 4u), b3 = __ballot_sync(0xFFFFFFFFu, m & 8u);
-    pos = wcnt + __popc(b0 & lt) + 2 * __popc(b1 & lt) + 4 * __popc(b2 & lt) + 8 * __popc(b3 & lt);
-    total = __popc(b0) + 2 * __popc(b1) + 4 * __popc(b2) + 8 * __popc(b3);
+    *pos = __popc(any & lt);
+    return __popc(any);
   }
-  while (mask) {
-    const int i = __ffs(mask) - 1;
-    mask &= mask - 1u;
-    const float4& h = i < 4 ? a : b;
-    const int q = i & 3;
-    float v = q == 0 ? h.x : (q == 1 ? h.y : (q == 2 ? h.z : h.w));
-    int ix = base + 4 * (i < 4 ? tid : kThreads + tid) + q;
-    if (i == 8) {
-      v = x;
-      ix = xi;
-    }
-    key[pos] = order_key(v);
-    idx[pos] = ix;
-    ++pos;
+  const uint32_t m = __popc(mask);
+  int off = 0, total = 0;
+#pragma unroll
+  for (int k = 0; k < 5; ++k) {
+    const uint32_t bk = __ballot_sync(0xFFFFFFFFu, (m >> k) & 1u);
+    off += __popc(bk & lt) << k;
+    total += __popc(bk) << k;
   }
+  *pos = off;
   return total;
+}
+
+// Write this lane's survivors (order key, row-local index) from position
+// pos of its warp's sub-list on. a[q] holds elements base + 4*(q*kThreads +
+// tid) + 0..3 (mask bits 4q..4q+3); x is one scalar element at index xi
+// (mask bit kScalarBit). Each lane walks only its set bits.
+__device__ __forceinline__ void write_survivors(uint32_t* key, int32_t* idx, int pos, const float4 (&a)[kVec],
+                                                float x, int xi, int base, uint32_t mask, int tid) {
+  if (mask == 0) return;
+#pragma unroll
+  for (int q = 0; q < kVec; ++q) {
+    uint32_t m = (mask >> (4 * q)) & 0xFu;
+    while (m) {
+      const int r = __ffs(m) - 1;
+      m &= m - 1u;
+      const float v = r == 0 ? a[q].x : (r == 1 ? a[q].y : (r == 2 ? a[q].z : a[q].w));
+      key[pos] = order_key(v);
+      idx[pos] = base + 4 * (q * kThreads + tid) + r;
+      ++pos;
+    }
+  }
+  if (mask & kScalarBit) {
+    key[pos] = order_key(x);
+    idx[pos] = xi;
+  }
 }
 
 // Gather every warp's sub-list into aux: the exact top 512 of their union
@@ -278,6 +299,19 @@ __device__ __forceinline__ uint32_t pass4(const float4& v, float tf) {
   return (v.x >= tf ? 1u : 0u) | (v.y >= tf ? 2u : 0u) | (v.z >= tf ? 4u : 0u) | (v.w >= tf ? 8u : 0u);
 }
 
+// Filter mask of a thread's stage data against tf: bits 4q..4q+3 for a[q]
+// (only the float4s that lie inside the stage's nvec elements), plus
+// kScalarBit for the scalar element when it is valid.
+__device__ __forceinline__ uint32_t stage_mask(const float4 (&a)[kVec], int nvec, float x, bool has_x, float tf,
+                                               int tid) {
+  uint32_t mask = 0;
+#pragma unroll
+  for (int q = 0; q < kVec; ++q)
+    if (4 * (q * kThreads + tid) < nvec) mask |= pass4(a[q], tf) << (4 * q);
+  if (has_x && x >= tf) mask |= kScalarBit;
+  return mask;
+}
+
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const __grid_constant__ TopkLaunch p) {
   extern __shared__ unsigned char smem_raw[];
   Smem& S = smem_ref(smem_raw);
@@ -308,14 +342,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
     const int slot = it % kNStage;
     const uint32_t ph = (it / kNStage) & 1u;
     const bool ok = mbar_wait(&S.full[slot], ph);
-    const StageDesc& d = S.desc[slot];
     // after a timeout the descriptor is not trusted: process nothing, then
     // leave together at the barrier below
-    const int unit = ok ? d.unit : 0;
+    const int4 hot = S.desc[slot].hot;
+    const int unit = ok ? hot.x : 0;
     if (unit < 0) break;
-    const int flags = ok ? d.flags : 0, nvec = ok ? d.nvec : 0, base = d.base, row = d.row, batch = d.batch;
-    const int head = ok ? d.head : 0, tail = ok ? d.tail : 0, lo = d.lo, tail_at = d.tail_at, len = d.len;
-    const long long woff = d.woff;
+    const int base = hot.y, nvec = ok ? hot.z : 0, flags = ok ? hot.w : 0;
+    UnitInfo u{};
+    if (flags) u = S.desc[slot].u;  // read before the slot is handed back
+    const int row = u.row, batch = u.batch, lo = u.lo, len = u.len;
+    const long long woff = u.woff;
     if (flags & 1) {
       wcnt = 0;
       appended = 0;
@@ -324,15 +360,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
       tau = spec;
       spec_used = spec;
     }
-    float4 va = make_float4(0.f, 0.f, 0.f, 0.f), vb = va;
-    if (4 * tid < nvec) va = reinterpret_cast<const float4*>(S.stage[slot])[tid];
-    if (4 * (kThreads + tid) < nvec) vb = reinterpret_cast<const float4*>(S.stage[slot])[kThreads + tid];
+    float4 a[kVec];
+#pragma unroll
+    for (int q = 0; q < kVec; ++q) {
+      a[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (4 * (q * kThreads + tid) < nvec) a[q] = reinterpret_cast<const float4*>(S.stage[slot])[q * kThreads + tid];
+    }
+    // scalar ends of the window (first stage of a unit)
+    const bool has_x = (flags & 1) && tid < u.head + u.tail;
+    float x = 0.f;
+    int xi = 0;
+    if (has_x) {
+      xi = tid < u.head ? lo + tid : u.tail_at + (tid - u.head);
+      x = __ldg(p.scores + woff + xi);
+    }
+    const uint32_t mask = stage_mask(a, nvec, x, has_x, tau_float(tau), tid);
+    int pos;
+    const int total = warp_offsets(mask, lane, &pos);
     if (!ok) S.timeout = 1;
-    // Everyone has the stage in registers, so the slot is refilled before any
-    // filtering work (the ring never waits on it). The same barrier tells
-    // whether the last stage's appends left some sub-list too full to take
-    // another stage: then all sub-lists are cut first.
-    const bool any = named_bar_or(kBar, kThreads, !ok || wcnt > kSubPruneAt);
+    // Everyone has the stage in registers, so the slot can be refilled. The
+    // same barrier tells whether some warp's survivors do not fit in its
+    // sub-list: then every warp takes the slow path below.
+    const bool any = named_bar_or(kBar, kThreads, !ok || wcnt + total > kSub);
     if (any && S.timeout) {
       if (tid == 0) {
         atomicOr(p.status, kDevWaitTimeout);
@@ -341,26 +390,33 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
       }
       break;
     }
-    if (tid == 0 && issuing) {  // the slot's data is in registers: refill it now
+    if (tid == 0 && issuing) {
       fence_proxy_async_smem();
       issuing = issue_stage(p, S, slot, policy);
     }
-    if (any) wcnt = prune(S, wcnt, tau, tid);
-    {
-      const float tf = tau_float(tau);
-      uint32_t mask = 0;
-      if (4 * tid < nvec) mask = pass4(va, tf);
-      if (4 * (kThreads + tid) < nvec) mask |= pass4(vb, tf) << 4;
-      float vx = 0.f;
-      int xi = 0;
-      if (tid < head + tail) {  // scalar ends of the window (first stage of a unit)
-        xi = tid < head ? lo + tid : tail_at + (tid - head);
-        vx = __ldg(p.scores + woff + xi);
-        mask |= (vx >= tf ? 1u : 0u) << 8;
+    if (!any) {
+      write_survivors(wkey, widx, wcnt + pos, a, x, xi, base, mask, tid);
+      wcnt += total;
+      appended += total;
+    } else {
+      // The threshold is far below this stage's scores (e.g. the first unit
+      // of a CTA, or a rising row): cut all sub-lists, then append the stage
+      // one float4 per lane at a time, filtered against the raised threshold
+      // and cut again before any part that might not fit.
+      wcnt = prune(S, wcnt, tau, tid);
+#pragma unroll
+      for (int q = 0; q < kVec; ++q) {
+        if (q > 0 && named_bar_or(kBar, kThreads, wcnt > kSubCutAt)) wcnt = prune(S, wcnt, tau, tid);
+        const float tf = tau_float(tau);
+        uint32_t mq = 0;
+        if (4 * (q * kThreads + tid) < nvec) mq = pass4(a[q], tf) << (4 * q);
+        if (q == 0 && has_x && x >= tf) mq |= kScalarBit;
+        int pq;
+        const int tq = warp_offsets(mq, lane, &pq);
+        write_survivors(wkey, widx, wcnt + pq, a, x, xi, base, mq, tid);
+        wcnt += tq;
+        appended += tq;
       }
-      const int added = warp_append(wkey, widx, wcnt, va, vb, vx, xi, base, mask, tid);
-      wcnt += added;
-      appended += added;
     }
     if (flags & 2) {
       if (lane == 0) S.wapp[warp] = appended;
@@ -370,26 +426,31 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
       for (int w = 0; w < kWarps; ++w) passed += S.wapp[w];
       if (spec_used && passed < min(len, kTopK)) {
         // The starting threshold was too high for this unit: redo it from
-        // global memory with no threshold (exact again, just slower).
+        // global memory with no threshold (exact again, just slower), four
+        // elements per lane at a time.
         wcnt = 0;
         tau = 0;
-        for (int b0 = 0; b0 < len; b0 += kStage) {
+        for (int b0 = 0; b0 < len; b0 += 4 * kThreads) {
           const float tf0 = tau_float(tau);
           const float* src = p.scores + woff + lo + b0;
-          float r[8];
+          float4 r[kVec];
+#pragma unroll
+          for (int q = 0; q < kVec; ++q) r[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+          float e[4] = {0.f, 0.f, 0.f, 0.f};
           uint32_t rm = 0;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int j = (k < 4 ? 4 * tid + k : 4 * (kThreads + tid) + (k - 4));
-            r[k] = 0.f;
-            if (b0 + j < len) {
-              r[k] = __ldg(src + j);
-              rm |= (r[k] >= tf0 ? 1u : 0u) << k;
+          for (int k = 0; k < 4; ++k) {
+            if (b0 + 4 * tid + k < len) {
+              e[k] = __ldg(src + 4 * tid + k);
+              rm |= (e[k] >= tf0 ? 1u : 0u) << k;
             }
           }
-          wcnt += warp_append(wkey, widx, wcnt, make_float4(r[0], r[1], r[2], r[3]),
-                              make_float4(r[4], r[5], r[6], r[7]), 0.f, 0, lo + b0, rm, tid);
-          if (named_bar_or(kBar, kThreads, wcnt > kSubPruneAt)) wcnt = prune(S, wcnt, tau, tid);
+          r[0] = make_float4(e[0], e[1], e[2], e[3]);
+          int pr;
+          const int tr = warp_offsets(rm, lane, &pr);
+          write_survivors(wkey, widx, wcnt + pr, r, 0.f, 0, lo + b0, rm, tid);
+          wcnt += tr;
+          if (named_bar_or(kBar, kThreads, wcnt > kSubCutAt)) wcnt = prune(S, wcnt, tau, tid);
         }
         spec_used = 0;
       }
