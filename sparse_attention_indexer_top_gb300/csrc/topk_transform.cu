@@ -248,6 +248,27 @@ __device__ __forceinline__ void write_survivors(uint32_t* key, int32_t* idx, int
   }
 }
 
+// write_survivors for a stage still held in shared memory: the value of
+// mask bit i (a score of this thread's float4 i/4) is re-read from the stage
+// buffer, so a lane's loop is one load and two stores per survivor whichever
+// float4 it sits in.
+__device__ __forceinline__ void write_survivors_smem(uint32_t* key, int32_t* idx, int pos, const float* stage,
+                                                     float x, int xi, int base, uint32_t mask, int tid) {
+  uint32_t m = mask & (kScalarBit - 1u);
+  while (m) {
+    const int i = __ffs(m) - 1;
+    m &= m - 1u;
+    const int off = ((i >> 2) * kThreads + tid) * 4 + (i & 3);
+    key[pos] = order_key(stage[off]);
+    idx[pos] = base + off;
+    ++pos;
+  }
+  if (mask & kScalarBit) {
+    key[pos] = order_key(x);
+    idx[pos] = xi;
+  }
+}
+
 // Gather every warp's sub-list into aux: the exact top 512 of their union
 // when it holds more (tau rises to the cut), else all of it. All threads
 // call this with their warp's wcnt; returns the number in aux.
@@ -377,11 +398,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
     const uint32_t mask = stage_mask(a, nvec, x, has_x, tau_float(tau), tid);
     int pos;
     const int total = warp_offsets(mask, lane, &pos);
+    // A warp whose survivors fit appends them now, while the stage is still
+    // in shared memory; one whose survivors do not fit defers them to the
+    // slow path below (its registers still hold the stage).
+    const bool fits = wcnt + total <= kSub;
+    if (fits) {
+      write_survivors_smem(wkey, widx, wcnt + pos, S.stage[slot], x, xi, base, mask, tid);
+      wcnt += total;
+      appended += total;
+    }
     if (!ok) S.timeout = 1;
-    // Everyone has the stage in registers, so the slot can be refilled. The
-    // same barrier tells whether some warp's survivors do not fit in its
-    // sub-list: then every warp takes the slow path below.
-    const bool any = named_bar_or(kBar, kThreads, !ok || wcnt + total > kSub);
+    // Everyone is done with the stage, so the slot can be refilled. The same
+    // barrier tells whether some warp deferred its survivors.
+    const bool any = named_bar_or(kBar, kThreads, !ok || !fits);
     if (any && S.timeout) {
       if (tid == 0) {
         atomicOr(p.status, kDevWaitTimeout);
@@ -394,23 +423,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
       fence_proxy_async_smem();
       issuing = issue_stage(p, S, slot, policy);
     }
-    if (!any) {
-      write_survivors(wkey, widx, wcnt + pos, a, x, xi, base, mask, tid);
-      wcnt += total;
-      appended += total;
-    } else {
+    if (any) {
       // The threshold is far below this stage's scores (e.g. the first unit
-      // of a CTA, or a rising row): cut all sub-lists, then append the stage
-      // one float4 per lane at a time, filtered against the raised threshold
-      // and cut again before any part that might not fit.
+      // of a CTA, or a rising row) and some warp deferred its survivors: cut
+      // all sub-lists, then the deferred warps append the stage one float4
+      // per lane at a time, filtered against the raised threshold, with a
+      // cut before any part that might not fit.
       wcnt = prune(S, wcnt, tau, tid);
 #pragma unroll
       for (int q = 0; q < kVec; ++q) {
         if (q > 0 && named_bar_or(kBar, kThreads, wcnt > kSubCutAt)) wcnt = prune(S, wcnt, tau, tid);
         const float tf = tau_float(tau);
         uint32_t mq = 0;
-        if (4 * (q * kThreads + tid) < nvec) mq = pass4(a[q], tf) << (4 * q);
-        if (q == 0 && has_x && x >= tf) mq |= kScalarBit;
+        if (!fits && 4 * (q * kThreads + tid) < nvec) mq = pass4(a[q], tf) << (4 * q);
+        if (!fits && q == 0 && has_x && x >= tf) mq |= kScalarBit;
         int pq;
         const int tq = warp_offsets(mq, lane, &pq);
         write_survivors(wkey, widx, wcnt + pq, a, x, xi, base, mq, tid);
