@@ -702,4 +702,126 @@ __device__ __forceinline__ void bitonic_sort512_128(const uint32_t* aux_key, con
   }
 }
 
+// Exact output ranks of the cnt (<= 512) entries of aux_key/aux_idx under
+// (key desc, index asc), without a sorting network. Keys are binned into
+// 1024 bins over [kmin, kmax] (bin 0 holds the highest keys), the bins are
+// counted and prefix-summed, and an entry's rank is its bin's offset plus
+// the number of entries of its own bin that precede it, found by comparing
+// with each of them (a bin holds one or two entries on typical data).
+// Thread tid handles entries j = tid + NT*e: k/ix[e] is the entry (ix = -1:
+// none) and rank[e] its output position. `hist` needs 1024 words and
+// `bucket` 512 halfwords, both free for the call. Returns false, leaving
+// aux untouched, when some bin holds more than 16 entries (heavy ties or a
+// very uneven range); the caller then sorts another way.
+template <int NT>
+__device__ bool bucket_rank512(const uint32_t* aux_key, const int32_t* aux_idx, int cnt, uint32_t* hist,
+                               uint16_t* bucket, SelectScratch& sc, uint32_t (&k)[kTopK / NT],
+                               int32_t (&ix)[kTopK / NT], int (&rank)[kTopK / NT], int tid, int bar) {
+  constexpr int E = kTopK / NT;
+  constexpr int NW = NT / 32;
+  constexpr int kBins = 1024;
+  constexpr int B = kBins / NT;  // bins per thread in the scan
+  constexpr int kMaxBin = 16;
+  static_assert(B % 4 == 0, "bins per thread in whole uint4s");
+  const int lane = tid & 31, warp = tid >> 5;
+  uint32_t lmin = 0xFFFFFFFFu, lmax = 0u;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int j = tid + NT * e;
+    const bool v = j < cnt;
+    k[e] = v ? aux_key[j] : 0u;
+    ix[e] = v ? aux_idx[j] : -1;
+    rank[e] = j;
+    if (v) {
+      lmin = min(lmin, k[e]);
+      lmax = max(lmax, k[e]);
+    }
+  }
+  lmin = __reduce_min_sync(0xFFFFFFFFu, lmin);
+  lmax = __reduce_max_sync(0xFFFFFFFFu, lmax);
+  if (lane == 0) {
+    sc.wmin[warp] = lmin;
+    sc.wmax[warp] = lmax;
+  }
+#pragma unroll
+  for (int i = 0; i < B / 4; ++i) reinterpret_cast<uint4*>(hist)[tid * (B / 4) + i] = make_uint4(0u, 0u, 0u, 0u);
+  named_bar(bar, NT);
+  uint32_t kmin = sc.wmin[0], kmax = sc.wmax[0];
+#pragma unroll
+  for (int w = 1; w < NW; ++w) {
+    kmin = min(kmin, sc.wmin[w]);
+    kmax = max(kmax, sc.wmax[w]);
+  }
+  const uint32_t span = kmax - kmin;
+  const int shift = span >= (uint32_t)kBins ? (32 - __clz(span)) - 10 : 0;
+  int bin[E], slot[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    bin[e] = (int)((kmax - k[e]) >> shift);
+    slot[e] = ix[e] >= 0 ? (int)atomicAdd(&hist[bin[e]], 1u) : 0;
+  }
+  named_bar(bar, NT);
+  // exclusive prefix sum of the bins in place; thread tid owns B bins
+  uint32_t h[B];
+#pragma unroll
+  for (int i = 0; i < B / 4; ++i) {
+    const uint4 q = reinterpret_cast<const uint4*>(hist)[tid * (B / 4) + i];
+    h[4 * i] = q.x;
+    h[4 * i + 1] = q.y;
+    h[4 * i + 2] = q.z;
+    h[4 * i + 3] = q.w;
+  }
+  uint32_t tot = 0;
+#pragma unroll
+  for (int i = 0; i < B; ++i) {
+    const uint32_t c = h[i];
+    h[i] = tot;
+    tot += c;
+  }
+  uint32_t incl = tot;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += o;
+  }
+  if (lane == 31) sc.wcnt[warp] = incl;
+  named_bar(bar, NT);
+  uint32_t off = incl - tot;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) off += w < warp ? sc.wcnt[w] : 0u;
+#pragma unroll
+  for (int i = 0; i < B / 4; ++i)
+    reinterpret_cast<uint4*>(hist)[tid * (B / 4) + i] =
+        make_uint4(h[4 * i] + off, h[4 * i + 1] + off, h[4 * i + 2] + off, h[4 * i + 3] + off);
+  named_bar(bar, NT);
+  int start[E], size[E];
+  bool heavy = false;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    start[e] = 0;
+    size[e] = 0;
+    if (ix[e] >= 0) {
+      start[e] = (int)hist[bin[e]];
+      size[e] = (bin[e] < kBins - 1 ? (int)hist[bin[e] + 1] : cnt) - start[e];
+      bucket[start[e] + slot[e]] = static_cast<uint16_t>(tid + NT * e);
+      heavy = heavy || size[e] > kMaxBin;
+    }
+  }
+  if (named_bar_or(bar, NT, heavy)) return false;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    int r = 0;
+    if (size[e] > 1) {
+      for (int m = 0; m < size[e]; ++m) {
+        const int o = bucket[start[e] + m];
+        const uint32_t ko = aux_key[o];
+        const int32_t io = aux_idx[o];
+        r += (ko > k[e] || (ko == k[e] && io < ix[e])) ? 1 : 0;
+      }
+    }
+    rank[e] = start[e] + r;
+  }
+  return true;
+}
+
 }  // namespace sai

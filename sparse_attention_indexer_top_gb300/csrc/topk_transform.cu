@@ -89,6 +89,10 @@ struct __align__(128) Smem {
       int32_t idx[kCap];
     } c;
     unsigned long long sortbuf[kTopK];  // final sort (the list is dead by then)
+    struct {
+      uint32_t hist[1024];
+      uint16_t bucket[kTopK];
+    } rank;                             // final ranking (likewise)
   } cand;
   uint32_t aux_key[kTopK];
   int32_t aux_idx[kTopK];
@@ -481,17 +485,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
         spec_used = 0;
       }
       const int cnt = gather_to_aux(S, wcnt, tau, tid);
-      unsigned long long v[4];
-      bitonic_sort512_128(S.aux_key, S.aux_idx, cnt, S.cand.sortbuf, v, tid, kBar);
-      // output rank 4*tid + j
+      // entry e of this thread: key k[e], row-local index ix[e] (-1: none),
+      // output rank rk[e]
       uint32_t k[4];
       int32_t ix[4];
       int rk[4];
+      if (!bucket_rank512<kThreads>(S.aux_key, S.aux_idx, cnt, S.cand.rank.hist, S.cand.rank.bucket, S.sc, k, ix, rk,
+                                    tid, kBar)) {
+        unsigned long long v[4];
+        bitonic_sort512_128(S.aux_key, S.aux_idx, cnt, S.cand.sortbuf, v, tid, kBar);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        k[e] = static_cast<uint32_t>(v[e] >> 32);
-        ix[e] = v[e] ? static_cast<int32_t>(~static_cast<uint32_t>(v[e] & 0xFFFFFFFFull)) : -1;
-        rk[e] = 4 * tid + e;
+        for (int e = 0; e < 4; ++e) {
+          k[e] = static_cast<uint32_t>(v[e] >> 32);
+          ix[e] = v[e] ? static_cast<int32_t>(~static_cast<uint32_t>(v[e] & 0xFFFFFFFFull)) : -1;
+          rk[e] = 4 * tid + e;
+        }
       }
       if (tid == 0) S.spec_keys[0] = S.spec_keys[1] = 0;
       named_bar(kBar, kThreads);
