@@ -52,22 +52,20 @@ __device__ __forceinline__ uint32_t shr64(uint32_t o, int lo) {
 }
 
 // Find the threshold bin of the `need` largest values among the active
-// entries j in [0, n) (active/value given by `get(j, v)`). All NT threads of
-// the group call it; `bar` is the group's named barrier id. `need` must not
-// exceed the number of active entries.
-template <int NT, typename Get>
-__device__ Threshold radix_threshold(int n, uint32_t need, SelectScratch& sc, int tid, int bar, Get get) {
+// values of the group. Each thread visits its own share through
+// `each(fn)`, which calls fn(v) once per active value v of the thread. All
+// NT threads of the group call it; `bar` is the group's named barrier id.
+// `need` must not exceed the number of active values.
+template <int NT, typename Each>
+__device__ Threshold radix_threshold_each(uint32_t need, SelectScratch& sc, int tid, int bar, Each each) {
   constexpr int NW = NT / 32;
   const int lane = tid & 31, warp = tid >> 5;
   uint32_t lmin = 0xFFFFFFFFu, lmax = 0u, lcnt = 0u;
-  for (int j = tid; j < n; j += NT) {
-    uint32_t v;
-    if (get(j, v)) {
-      lmin = min(lmin, v);
-      lmax = max(lmax, v);
-      ++lcnt;
-    }
-  }
+  each([&](uint32_t v) {
+    lmin = min(lmin, v);
+    lmax = max(lmax, v);
+    ++lcnt;
+  });
   lmin = __reduce_min_sync(0xFFFFFFFFu, lmin);
   lmax = __reduce_max_sync(0xFFFFFFFFu, lmax);
   lcnt = __reduce_add_sync(0xFFFFFFFFu, lcnt);
@@ -104,15 +102,10 @@ __device__ Threshold radix_threshold(int n, uint32_t need, SelectScratch& sc, in
     const uint32_t dmask = (1u << dbits) - 1u;
     for (int i = tid; i < 256; i += NT) sc.hist[i] = 0;
     named_bar(bar, NT);
-    for (int j0 = 0; j0 < n; j0 += NT) {
-      const int j = j0 + tid;
-      uint32_t v, bin = 0xFFFFFFFFu;
-      if (j < n && get(j, v)) {
-        const uint32_t o = v - t.base;
-        if (shr64(o, t.lo) == t.prefix) bin = (o >> dlo) & dmask;
-      }
-      if (bin != 0xFFFFFFFFu) atomicAdd(&sc.hist[bin], 1u);
-    }
+    each([&](uint32_t v) {
+      const uint32_t o = v - t.base;
+      if (shr64(o, t.lo) == t.prefix) atomicAdd(&sc.hist[(o >> dlo) & dmask], 1u);
+    });
     named_bar(bar, NT);
     if (warp == 0) {
       // Lane l owns bins [8l, 8l+8); scan from the top bin down.
@@ -151,6 +144,18 @@ __device__ Threshold radix_threshold(int n, uint32_t need, SelectScratch& sc, in
     t.lo = dlo;
   }
   return t;
+}
+
+// The same over the entries j in [0, n) of the group, thread tid taking
+// j = tid, tid + NT, ...; entry j is active with value v when get(j, v).
+template <int NT, typename Get>
+__device__ Threshold radix_threshold(int n, uint32_t need, SelectScratch& sc, int tid, int bar, Get get) {
+  return radix_threshold_each<NT>(need, sc, tid, bar, [&](auto fn) {
+    for (int j = tid; j < n; j += NT) {
+      uint32_t v;
+      if (get(j, v)) fn(v);
+    }
+  });
 }
 
 __device__ __forceinline__ int thr_cmp(const Threshold& t, uint32_t v) {
@@ -585,58 +590,59 @@ __device__ __forceinline__ void rank_sort(const uint32_t* aux_key, const int32_t
   named_bar(bar, NT);
 }
 
-// Exact top-K (K = 512) over W sub-lists (sub-list w holds counts[w] <=
-// sub_cap entries at key/idx[w * sub_cap ...]) into aux_key/aux_idx[0, K)
-// (unordered). Requires the total to exceed K. Returns the lowest key of the
-// final threshold bin (<= the K-th key).
+// Exact top-K (K = 512) over W sub-lists, one per warp of the group:
+// sub-list w holds counts[w] <= SUB entries at key/idx[w * SUB ...] and is
+// walked by warp w alone, so every pass touches only filled entries. Writes
+// the top K by (key desc, index asc) to aux_key/aux_idx[0, K) (unordered).
+// Requires the total to exceed K. Returns the lowest key of the final
+// threshold bin (<= the K-th key).
 template <int NT, int W, int SUB>
 __device__ uint32_t select512_sub_to_aux(const uint32_t* key, const int32_t* idx, const int (&counts)[W],
                                          uint32_t* aux_key, int32_t* aux_idx, SelectScratch& sc, int tid, int bar) {
+  static_assert(NT == 32 * W, "one warp per sub-list");
   constexpr int K = kTopK;
-  constexpr int n = W * SUB;
-  constexpr int M = (n + NT - 1) / NT;
-  auto valid = [&](int j) {
-    const int w = j / SUB;
-    int c = counts[0];
+  constexpr int M = SUB / 32;
+  static_assert(SUB % 32 == 0 && M <= 32, "entries per lane fit a 32-bit mask");
+  const int lane = tid & 31, w = tid >> 5;
+  int c = counts[0];
 #pragma unroll
-    for (int u = 1; u < W; ++u) c = w == u ? counts[u] : c;  // no dynamic index: keeps counts in registers
-    return (j % SUB) < c;
-  };
-  const Threshold t = radix_threshold<NT>(n, (uint32_t)K, sc, tid, bar, [&](int j, uint32_t& v) {
-    v = key[j];
-    return valid(j);
+  for (int u = 1; u < W; ++u) c = w == u ? counts[u] : c;  // no dynamic index: keeps counts in registers
+  const uint32_t* const mk = key + w * SUB;
+  const int32_t* const mi = idx + w * SUB;
+  const Threshold t = radix_threshold_each<NT>((uint32_t)K, sc, tid, bar, [&](auto fn) {
+    for (int j = lane; j < c; j += 32) fn(mk[j]);
   });
   Threshold ti{};
   const bool ties = !t.all_eq;
   if (ties) {
-    ti = radix_threshold<NT>(n, t.need, sc, tid, bar, [&](int j, uint32_t& v) {
-      v = 0x7FFFFFFFu - static_cast<uint32_t>(idx[j]);
-      return valid(j) && thr_cmp(t, key[j]) == 0;
+    ti = radix_threshold_each<NT>(t.need, sc, tid, bar, [&](auto fn) {
+      for (int j = lane; j < c; j += 32)
+        if (thr_cmp(t, mk[j]) == 0) fn(0x7FFFFFFFu - static_cast<uint32_t>(mi[j]));
     });
   }
   uint32_t selm = 0;
-  int c = 0;
+  int cs = 0;
 #pragma unroll
   for (int m = 0; m < M; ++m) {
-    const int j = tid + NT * m;
-    if (j < n && valid(j)) {
-      const int cc = thr_cmp(t, key[j]);
-      const bool sel = cc > 0 || (cc == 0 && (!ties || thr_cmp(ti, 0x7FFFFFFFu - static_cast<uint32_t>(idx[j])) >= 0));
+    const int j = lane + 32 * m;
+    if (j < c) {
+      const int cc = thr_cmp(t, mk[j]);
+      const bool sel = cc > 0 || (cc == 0 && (!ties || thr_cmp(ti, 0x7FFFFFFFu - static_cast<uint32_t>(mi[j])) >= 0));
       if (sel) {
         selm |= 1u << m;
-        ++c;
+        ++cs;
       }
     }
   }
   int total;
-  int pos = block_exscan<NT>(c, &total, sc.wcnt, tid, bar);
+  int pos = block_exscan<NT>(cs, &total, sc.wcnt, tid, bar);
 #pragma unroll
   for (int m = 0; m < M; ++m) {
     if (selm & (1u << m)) {
-      const int j = tid + NT * m;
+      const int j = lane + 32 * m;
       if (pos < K) {
-        aux_key[pos] = key[j];
-        aux_idx[pos] = idx[j];
+        aux_key[pos] = mk[j];
+        aux_idx[pos] = mi[j];
       }
       ++pos;
     }
