@@ -274,20 +274,29 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
       }
       return kept;
     };
+    // TMEM is read in the 16x256b shape: a warp loads its 32 keys as two
+    // 16-lane halves, and lane l gets keys l/4 and l/4 + 8 of each half at
+    // heads 8j + 2(l%4) + {0, 1}, j < 8. So a lane needs only those 16 head
+    // weights (kept in registers) and holds partial sums for 4 keys; a
+    // reduce-scatter over the 4 lanes sharing l/4 leaves each lane the full
+    // score of one key, key kl of the block.
+    const int kl = quad * 32 + (lane >> 2) + 8 * ((lane >> 1) & 1) + 16 * (lane & 1);
+    float2 w2[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) w2[j] = *reinterpret_cast<const float2*>(S.w + r * kH + 8 * j + 2 * (lane & 3));
     // the key scale of the next tile is fetched one tile ahead
     int page_next = ntiles > 0 ? S.pages[0] : -1;
     bool ok_next = page_next >= 0 && page_next < p.num_blocks;
-    float ks_next = ok_next ? __ldg(p.kscale + (long long)page_next * kBlk + et) : 0.f;
-    const float2* w2 = reinterpret_cast<const float2*>(S.w + r * kH);
+    float ks_next = ok_next ? __ldg(p.kscale + (long long)page_next * kBlk + kl) : 0.f;
     for (int i = 0; i < ntiles; ++i) {
       const int blk = m.blk0 + i, buf = i & 1;
-      const int t = blk * kBlk + et;
+      const int t = blk * kBlk + kl;
       const bool page_ok = ok_next;
       const float ks = ks_next;
       if (i + 1 < ntiles) {
         page_next = S.pages[i + 1];
         ok_next = page_next >= 0 && page_next < p.num_blocks;
-        ks_next = ok_next ? __ldg(p.kscale + (long long)page_next * kBlk + et) : 0.f;
+        ks_next = ok_next ? __ldg(p.kscale + (long long)page_next * kBlk + kl) : 0.f;
       }
       if (!page_ok && et == 0 && r == 0) atomicOr(p.status, kDevBadPage);
       ok = ok && __all_sync(0xFFFFFFFFu, mbar_wait(&S.tfull[buf], (i >> 1) & 1u));
@@ -295,12 +304,13 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
       if (ok) {
         tc_fence_after();
         const uint32_t col = tmem + lane_base + static_cast<uint32_t>(buf * N + r * kH);
-        // sum_h w_h relu(s_h): relu per head, then packed f32x2 FMAs
+        // sum_h w_h relu(s_h): relu per head, then packed f32x2 FMAs; acc[k]
+        // = this lane's partial for keys l/4, l/4 + 8, 16 + l/4, 24 + l/4
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t a[32];
-          tmem_ld32(col + 32 * half, a);
+          tmem_ld16x256_x8(col + (static_cast<uint32_t>(16 * half) << 16), a);
           tmem_ld_wait();
           if (half == 1) {  // the accumulator buffer is free once both halves are in registers
             tc_fence_before();
@@ -308,12 +318,25 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
             if (lane == 0) mbar_arrive(&S.tempty[buf]);
           }
 #pragma unroll
-          for (int h2 = 0; h2 < 16; ++h2) {
-            const float2 x = make_float2(fmaxf(__uint_as_float(a[2 * h2]), 0.f), fmaxf(__uint_as_float(a[2 * h2 + 1]), 0.f));
-            acc[h2 & 3] = __ffma2_rn(x, w2[16 * half + h2], acc[h2 & 3]);
+          for (int j = 0; j < 8; ++j) {
+            const float2 x0 = make_float2(fmaxf(__uint_as_float(a[4 * j]), 0.f), fmaxf(__uint_as_float(a[4 * j + 1]), 0.f));
+            const float2 x1 =
+                make_float2(fmaxf(__uint_as_float(a[4 * j + 2]), 0.f), fmaxf(__uint_as_float(a[4 * j + 3]), 0.f));
+            acc[2 * half] = __ffma2_rn(x0, w2[j], acc[2 * half]);
+            acc[2 * half + 1] = __ffma2_rn(x1, w2[j], acc[2 * half + 1]);
           }
         }
-        score = (((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y))) * ks;
+        const float p0 = acc[0].x + acc[0].y, p1 = acc[1].x + acc[1].y;
+        const float p2 = acc[2].x + acc[2].y, p3 = acc[3].x + acc[3].y;
+        // reduce-scatter over lanes 4g..4g+3: after the xor-1 step a lane
+        // holds two keys (l/4 and l/4 + 8 if l is even, else 16 + l/4 and
+        // 24 + l/4), after the xor-2 step one (the second of them if l & 2)
+        const bool odd = lane & 1, hi = lane & 2;
+        float k0 = odd ? p2 : p0, k1 = odd ? p3 : p1;
+        k0 += __shfl_xor_sync(0xFFFFFFFFu, odd ? p0 : p2, 1);
+        k1 += __shfl_xor_sync(0xFFFFFFFFu, odd ? p1 : p3, 1);
+        const float keep = hi ? k1 : k0;
+        score = (keep + __shfl_xor_sync(0xFFFFFFFFu, hi ? k0 : k1, 2)) * ks;
       }
       const bool live = ok && row_live && page_ok && t < nr;
       if constexpr (DENSE) {
