@@ -53,20 +53,17 @@ constexpr int kSub = 512;     // candidate sub-list per epilogue warp
 constexpr int kSyncEvery = 4; // tiles between the row group's count exchanges
 constexpr int kSubPruneAt = kSub - kSyncEvery * 32;
 constexpr int kEpiRow = 128;  // epilogue threads per query row (4 warps, one TMEM lane quadrant each)
-constexpr int kMaxTiles = 256;  // KV blocks per work unit (host plans chunks accordingly)
 
 template <int R>
 struct __align__(1024) FusedSmem {
   uint8_t kst[kNSf][kBlk * kD];  // 16 KB each, 1024-byte aligned
-  uint8_t q[R * kH * kD];
-  float w[R * kH];
+  uint8_t q[2][R * kH * kD];     // query tiles of two consecutive units
   uint32_t ckey[R][4 * kSub];  // row r: four per-warp sub-lists
   int32_t cidx[R][4 * kSub];
   uint32_t aux_key[R][kTopK];
   int32_t aux_idx[R][kTopK];
   SelectScratch sc[R];
-  int pages[kMaxTiles];   // the unit's block ids, staged once
-  uint64_t full[kNSf], empty[kNSf], tfull[2], tempty[2], qfull;
+  uint64_t full[kNSf], empty[kNSf], tfull[2], tempty[2], qfull[2], qempty[2];
   uint32_t tmem_base;
   int wcnt[R][2][4];      // per-warp list sizes at a sync point (double-buffered)
 };
@@ -75,6 +72,8 @@ template <int R>
 constexpr size_t fused_smem_bytes() {
   return sizeof(FusedSmem<R>) + 1024;
 }
+
+static_assert(fused_smem_bytes<4>() <= 227 * 1024, "one CTA's shared memory (the opt-in maximum per block)");
 
 template <int R>
 __device__ __forceinline__ FusedSmem<R>& fused_smem(unsigned char* raw) {
@@ -123,6 +122,16 @@ __device__ GroupMeta group_meta(const FusedLaunch& p, int g, int c, int (&n)[R],
   return m;
 }
 
+// relu(s) * 2^-64 for an FP32 dot product s of two 128-element e4m3 rows:
+// s * 2^-64 saturated to [0, 1]. Exact: |s| <= 128 * 448^2 < 2^64, so the
+// clamp at 1 never acts, and s is a multiple of 2^-18, so s * 2^-64 is a
+// normal float (no rounding); negatives and -0 give +0.
+__device__ __forceinline__ float relu_lo(uint32_t s_bits) {
+  float r;
+  asm("mul.rn.sat.f32 %0, %1, 0f1F800000;" : "=f"(r) : "f"(__uint_as_float(s_bits)));
+  return r;
+}
+
 template <int R>
 __host__ __device__ constexpr int fused_threads() {
   return R * kEpiRow + 64;  // R row groups of 4 epilogue warps, a TMA warp, an MMA warp
@@ -140,10 +149,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
   constexpr int kEpiWarps = 4 * R;
   constexpr int kTmaWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = blockIdx.x / p.chunks, c = blockIdx.x - g * p.chunks;
-  int n[R];
-  const GroupMeta m = group_meta<R>(p, g, c, n, tid == 0 && c == 0);
-  const int ntiles = m.blk1 - m.blk0;
+  const int units = ((p.rows + R - 1) / R) * p.chunks;
 
   if (tid == 0) {
     for (int i = 0; i < kNSf; ++i) {
@@ -154,126 +160,98 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
       mbar_init(&S.tfull[i], 1);
       mbar_init(&S.tempty[i], kEpiWarps);
     }
-    mbar_init(&S.qfull, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.qfull[i], 1);
+      mbar_init(&S.qempty[i], 1);
+    }
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
     tmem_alloc(&S.tmem_base, kCols);
     tmem_relinquish();
   }
-  for (int i = tid; i < ntiles; i += fused_threads<R>())
-    S.pages[i] = p.block_table[(long long)m.batch * p.bt_stride + m.blk0 + i];
-  for (int i = tid; i < R * kH; i += fused_threads<R>()) {
-    const int r = i / kH;
-    S.w[i] = r < m.nrows ? p.w[(long long)(m.row0 + r) * kH + (i - r * kH)] : 0.f;
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
-  bool ok = true;
 
+  // Every role walks the same units (u = blockIdx.x, + gridDim.x, ...) and
+  // derives the same tile counts, so the barrier phases below (counted over
+  // all tiles and all units of this CTA) stay in step.
   if (warp == kTmaWarp) {
-    // ---------------- TMA producer
-    if (lane == 0 && ntiles > 0) {
+    // ---------------- TMA producer: the unit's query tile, then its key
+    // blocks through the ring; the block ids come straight from the table
+    if (lane == 0) {
       prefetch_tmap(&kmap);
       prefetch_tmap(&qmap);
-      const uint64_t keep = l2_policy_evict_last();   // q and K are re-read by other CTAs
-      mbar_arrive_expect_tx(&S.qfull, (uint32_t)(N * kD));
-      tma_load_2d(S.q, &qmap, 0, m.row0 * kH, &S.qfull, keep);
-      for (int i = 0; i < ntiles; ++i) {
-        const int s = i % kNSf;
-        if (!mbar_wait(&S.empty[s], ((i / kNSf) & 1u) ^ 1u)) {
-          atomicOr(p.status, kDevWaitTimeout);
-          break;
+      const uint64_t keep = l2_policy_evict_last();  // q and K are re-read by other CTAs
+      uint32_t it = 0, qn = 0;
+      bool run = true;
+      for (int u = blockIdx.x; u < units && run; u += gridDim.x) {
+        int n[R];
+        const GroupMeta m = group_meta<R>(p, u / p.chunks, u % p.chunks, n, false);
+        const int ntiles = m.blk1 - m.blk0;
+        if (ntiles == 0) continue;
+        const int32_t* bt = p.block_table + (long long)m.batch * p.bt_stride + m.blk0;
+        const int qb = qn & 1;
+        run = mbar_wait(&S.qempty[qb], ((qn >> 1) & 1u) ^ 1u);
+        if (!run) break;
+        mbar_arrive_expect_tx(&S.qfull[qb], (uint32_t)(N * kD));
+        tma_load_2d(S.q[qb], &qmap, 0, m.row0 * kH, &S.qfull[qb], keep);
+        ++qn;
+        int page_next = __ldg(bt);
+        for (int i = 0; i < ntiles; ++i, ++it) {
+          int page = page_next;
+          if (i + 1 < ntiles) page_next = __ldg(bt + i + 1);
+          if (page < 0 || page >= p.num_blocks) page = 0;  // the epilogue masks this block
+          const int s = it % kNSf;
+          if (!(run = mbar_wait(&S.empty[s], ((it / kNSf) & 1u) ^ 1u))) break;
+          mbar_arrive_expect_tx(&S.full[s], (uint32_t)(kBlk * kD));
+          tma_load_2d(S.kst[s], &kmap, 0, page * kBlk, &S.full[s], keep);
         }
-        int page = S.pages[i];
-        if (page < 0 || page >= p.num_blocks) page = 0;  // the epilogue masks this block
-        mbar_arrive_expect_tx(&S.full[s], (uint32_t)(kBlk * kD));
-        tma_load_2d(S.kst[s], &kmap, 0, page * kBlk, &S.full[s], keep);
       }
+      if (!run) atomicOr(p.status, kDevWaitTimeout);
     }
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer
-    if (lane == 0 && ntiles > 0) {
-      bool run = mbar_wait(&S.qfull, 0);
-      const uint64_t bdesc = umma_desc_sw128_kmajor(smem_u32(S.q));
-      for (int i = 0; i < ntiles && run; ++i) {
-        const int s = i % kNSf, buf = i & 1;
-        run = mbar_wait(&S.full[s], (i / kNSf) & 1u) && mbar_wait(&S.tempty[buf], ((i >> 1) & 1u) ^ 1u);
-        if (!run) {
-          atomicOr(p.status, kDevWaitTimeout);
-          break;
-        }
-        tc_fence_after();
-        const uint64_t adesc = umma_desc_sw128_kmajor(smem_u32(S.kst[s]));
+    if (lane == 0) {
+      uint32_t it = 0, qn = 0;
+      bool run = true;
+      for (int u = blockIdx.x; u < units && run; u += gridDim.x) {
+        int n[R];
+        const GroupMeta m = group_meta<R>(p, u / p.chunks, u % p.chunks, n, false);
+        const int ntiles = m.blk1 - m.blk0;
+        if (ntiles == 0) continue;
+        const int qb = qn & 1;
+        if (!(run = mbar_wait(&S.qfull[qb], (qn >> 1) & 1u))) break;
+        ++qn;
+        const uint64_t bdesc = umma_desc_sw128_kmajor(smem_u32(S.q[qb]));
+        for (int i = 0; i < ntiles; ++i, ++it) {
+          const int s = it % kNSf, buf = it & 1;
+          run = mbar_wait(&S.full[s], (it / kNSf) & 1u) && mbar_wait(&S.tempty[buf], ((it >> 1) & 1u) ^ 1u);
+          if (!run) break;
+          tc_fence_after();
+          const uint64_t adesc = umma_desc_sw128_kmajor(smem_u32(S.kst[s]));
 #pragma unroll
-        for (int k = 0; k < kD / 32; ++k)
-          umma_f8(tmem + buf * N, adesc + 2 * k, bdesc + 2 * k, kIdesc, k > 0 ? 1u : 0u);
-        umma_commit(&S.empty[s]);
-        umma_commit(&S.tfull[buf]);
+          for (int k = 0; k < kD / 32; ++k)
+            umma_f8(tmem + buf * N, adesc + 2 * k, bdesc + 2 * k, kIdesc, k > 0 ? 1u : 0u);
+          umma_commit(&S.empty[s]);
+          umma_commit(&S.tfull[buf]);
+        }
+        umma_commit(&S.qempty[qb]);  // the query tile is free once this unit's MMAs are done
       }
+      if (!run) atomicOr(p.status, kDevWaitTimeout);
     }
   } else {
-    // ---------------- epilogue: row r = warp / 4 of the group; one key
-    // (TMEM lane quad*32 + lane) per thread
-    const int r = warp >> 2, quad = warp & 3, et = tid - r * kEpiRow;  // et = key within the block
+    // ---------------- epilogue: row r = warp / 4 of the group; TMEM lanes
+    // quad*32 .. quad*32+31 (the warp's quadrant) are its 32 keys
+    const int r = warp >> 2, quad = warp & 3, et = tid - r * kEpiRow;  // et = thread within the row's 128
     const int bar = 1 + r;
     uint32_t* const ckey = S.ckey[r];
     int32_t* const cidx = S.cidx[r];
-    int wc = 0;         // entries in this warp's sub-list
-    uint32_t tau = 0;   // keep keys whose order key >= tau (same in the row's 4 warps)
-    float tf = tau_float(0);
-    int sync_no = 0;
     uint32_t* const my_key = ckey + quad * kSub;
     int32_t* const my_idx = cidx + quad * kSub;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const bool row_live = r < m.nrows;
-    const int nr = n[r];
-    // Exchange the four sub-list sizes; when one is nearly full (or at the
-    // unit end) cut the row's candidates to the top 512 and rebalance them
-    // (128 per sub-list), or gather them for the partial output.
-    auto exchange = [&](bool final_cut) -> int {
-      if (lane == 0) S.wcnt[r][sync_no & 1][quad] = wc;
-      const bool all_ok = named_bar_and(bar, kEpiRow, ok);
-      int counts[4];
-      int total = 0, maxc = 0;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        counts[q] = S.wcnt[r][sync_no & 1][q];
-        total += counts[q];
-        maxc = max(maxc, counts[q]);
-      }
-      ++sync_no;
-      if (!all_ok) return -1;
-      if (!final_cut && maxc <= kSubPruneAt) return total;
-      int kept = total;
-      if (total > kTopK) {
-        tau = max(tau, select512_sub_to_aux<kEpiRow, 4, kSub>(ckey, cidx, counts, S.aux_key[r], S.aux_idx[r], S.sc[r],
-                                                              et, bar));
-        tf = tau_float(tau);
-        kept = kTopK;
-      } else {
-        int before = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) before += q < quad ? counts[q] : 0;
-        for (int j = lane; j < wc; j += 32) {
-          S.aux_key[r][before + j] = my_key[j];
-          S.aux_idx[r][before + j] = my_idx[j];
-        }
-        named_bar(bar, kEpiRow);
-      }
-      if (!final_cut) {  // rebalance: sub-list q takes aux[q*128 ...]
-        const int lo = min(kept, quad * (kTopK / 4)), hi = min(kept, (quad + 1) * (kTopK / 4));
-        for (int j = lo + lane; j < hi; j += 32) {
-          my_key[j - lo] = S.aux_key[r][j];
-          my_idx[j - lo] = S.aux_idx[r][j];
-        }
-        wc = hi - lo;
-        named_bar(bar, kEpiRow);
-      }
-      return kept;
-    };
     // TMEM is read in the 16x256b shape: a warp loads its 32 keys as two
     // 16-lane halves, and lane l gets keys l/4 and l/4 + 8 of each half at
     // heads 8j + 2(l%4) + {0, 1}, j < 8. So a lane needs only those 16 head
@@ -281,98 +259,164 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
     // reduce-scatter over the 4 lanes sharing l/4 leaves each lane the full
     // score of one key, key kl of the block.
     const int kl = quad * 32 + (lane >> 2) + 8 * ((lane >> 1) & 1) + 16 * (lane & 1);
-    float2 w2[8];
+    bool ok = true;     // false after a pipeline wait gave up (then nothing more is waited for)
+    int sync_no = 0;    // exchanges so far (the size slots alternate)
+    uint32_t tt = 0;    // tiles so far (accumulator buffer and phase)
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const int g = u / p.chunks, c = u - g * p.chunks;
+      int n[R];
+      const GroupMeta m = group_meta<R>(p, g, c, n, et == 0 && r == 0 && c == 0);
+      const int ntiles = m.blk1 - m.blk0;
+      const bool row_live = r < m.nrows;
+      const int nr = n[r];
+      const int32_t* bt = p.block_table + (long long)m.batch * p.bt_stride + m.blk0;
+      int wc = 0;         // entries in this warp's sub-list
+      uint32_t tau = 0;   // keep keys whose order key >= tau (same in the row's 4 warps)
+      float tf = tau_float(0);
+      // Exchange the four sub-list sizes; when one is nearly full (or at
+      // the unit end) cut the row's candidates to the top 512 and rebalance
+      // them (128 per sub-list), or gather them for the partial output.
+      auto exchange = [&](bool final_cut) -> int {
+        if (lane == 0) S.wcnt[r][sync_no & 1][quad] = wc;
+        const bool all_ok = named_bar_and(bar, kEpiRow, ok);
+        int counts[4];
+        int total = 0, maxc = 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) w2[j] = *reinterpret_cast<const float2*>(S.w + r * kH + 8 * j + 2 * (lane & 3));
-    // the key scale of the next tile is fetched one tile ahead
-    int page_next = ntiles > 0 ? S.pages[0] : -1;
-    bool ok_next = page_next >= 0 && page_next < p.num_blocks;
-    float ks_next = ok_next ? __ldg(p.kscale + (long long)page_next * kBlk + kl) : 0.f;
-    for (int i = 0; i < ntiles; ++i) {
-      const int blk = m.blk0 + i, buf = i & 1;
-      const int t = blk * kBlk + kl;
-      const bool page_ok = ok_next;
-      const float ks = ks_next;
-      if (i + 1 < ntiles) {
-        page_next = S.pages[i + 1];
-        ok_next = page_next >= 0 && page_next < p.num_blocks;
-        ks_next = ok_next ? __ldg(p.kscale + (long long)page_next * kBlk + kl) : 0.f;
-      }
-      if (!page_ok && et == 0 && r == 0) atomicOr(p.status, kDevBadPage);
-      ok = ok && __all_sync(0xFFFFFFFFu, mbar_wait(&S.tfull[buf], (i >> 1) & 1u));
-      float score = 0.f;
-      if (ok) {
-        tc_fence_after();
-        const uint32_t col = tmem + lane_base + static_cast<uint32_t>(buf * N + r * kH);
-        // sum_h w_h relu(s_h): relu per head, then packed f32x2 FMAs; acc[k]
-        // = this lane's partial for keys l/4, l/4 + 8, 16 + l/4, 24 + l/4
-        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        for (int q = 0; q < 4; ++q) {
+          counts[q] = S.wcnt[r][sync_no & 1][q];
+          total += counts[q];
+          maxc = max(maxc, counts[q]);
+        }
+        ++sync_no;
+        if (!all_ok) return -1;
+        if (!final_cut && maxc <= kSubPruneAt) return total;
+        int kept = total;
+        if (total > kTopK) {
+          tau = max(tau, select512_sub_to_aux<kEpiRow, 4, kSub>(ckey, cidx, counts, S.aux_key[r], S.aux_idx[r],
+                                                                S.sc[r], et, bar));
+          tf = tau_float(tau);
+          kept = kTopK;
+        } else {
+          int before = 0;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t a[32];
-          tmem_ld16x256_x8(col + (static_cast<uint32_t>(16 * half) << 16), a);
-          tmem_ld_wait();
-          if (half == 1) {  // the accumulator buffer is free once both halves are in registers
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.tempty[buf]);
+          for (int q = 0; q < 4; ++q) before += q < quad ? counts[q] : 0;
+          for (int j = lane; j < wc; j += 32) {
+            S.aux_key[r][before + j] = my_key[j];
+            S.aux_idx[r][before + j] = my_idx[j];
           }
+          named_bar(bar, kEpiRow);
+        }
+        if (!final_cut) {  // rebalance: sub-list q takes aux[q*128 ...]
+          const int lo = min(kept, quad * (kTopK / 4)), hi = min(kept, (quad + 1) * (kTopK / 4));
+          for (int j = lo + lane; j < hi; j += 32) {
+            my_key[j - lo] = S.aux_key[r][j];
+            my_idx[j - lo] = S.aux_idx[r][j];
+          }
+          wc = hi - lo;
+          named_bar(bar, kEpiRow);
+        }
+        return kept;
+      };
+      float2 w2[8];
+      const float* wr = p.w + (long long)(row_live ? m.row0 + r : 0) * kH + 2 * (lane & 3);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float2 x0 = make_float2(fmaxf(__uint_as_float(a[4 * j]), 0.f), fmaxf(__uint_as_float(a[4 * j + 1]), 0.f));
-            const float2 x1 =
-                make_float2(fmaxf(__uint_as_float(a[4 * j + 2]), 0.f), fmaxf(__uint_as_float(a[4 * j + 3]), 0.f));
-            acc[2 * half] = __ffma2_rn(x0, w2[j], acc[2 * half]);
-            acc[2 * half + 1] = __ffma2_rn(x1, w2[j], acc[2 * half + 1]);
+      for (int j = 0; j < 8; ++j)  // scaled by 2^64: see relu_lo below
+        w2[j] = row_live ? make_float2(__ldg(wr + 8 * j) * 0x1p64f, __ldg(wr + 8 * j + 1) * 0x1p64f)
+                         : make_float2(0.f, 0.f);
+      // the key scale of the next tile is fetched one tile ahead
+      int page_next = ntiles > 0 ? __ldg(bt) : -1;
+      bool ok_next = page_next >= 0 && page_next < p.num_blocks;
+      float ks_next = ok_next ? __ldg(p.kscale + (long long)page_next * kBlk + kl) : 0.f;
+      for (int i = 0; i < ntiles; ++i, ++tt) {
+        const int blk = m.blk0 + i, buf = tt & 1;
+        const int t = blk * kBlk + kl;
+        const bool page_ok = ok_next;
+        const float ks = ks_next;
+        if (i + 1 < ntiles) {
+          page_next = __ldg(bt + i + 1);
+          ok_next = page_next >= 0 && page_next < p.num_blocks;
+          ks_next = ok_next ? __ldg(p.kscale + (long long)page_next * kBlk + kl) : 0.f;
+        }
+        if (!page_ok && et == 0 && r == 0) atomicOr(p.status, kDevBadPage);
+        ok = ok && __all_sync(0xFFFFFFFFu, mbar_wait(&S.tfull[buf], (tt >> 1) & 1u));
+        float score = 0.f;
+        if (ok) {
+          tc_fence_after();
+          const uint32_t col = tmem + lane_base + static_cast<uint32_t>(buf * N + r * kH);
+          // sum_h w_h relu(s_h) = sum_h (w_h 2^64) relu_lo(s_h): the relu
+          // is one saturating multiply on the FMA pipe (the ALU pipe, where
+          // a max would go, is the busier one), then packed f32x2 FMAs; the
+          // power-of-two scalings are exact, so every product is w_h relu(s_h).
+          // acc[k] = this lane's partial for keys l/4, l/4+8, 16+l/4, 24+l/4
+          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t a[32];
+            tmem_ld16x256_x8(col + (static_cast<uint32_t>(16 * half) << 16), a);
+            tmem_ld_wait();
+            if (half == 1) {  // the accumulator buffer is free once both halves are in registers
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&S.tempty[buf]);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float2 x0 = make_float2(relu_lo(a[4 * j]), relu_lo(a[4 * j + 1]));
+              const float2 x1 = make_float2(relu_lo(a[4 * j + 2]), relu_lo(a[4 * j + 3]));
+              acc[2 * half] = __ffma2_rn(x0, w2[j], acc[2 * half]);
+              acc[2 * half + 1] = __ffma2_rn(x1, w2[j], acc[2 * half + 1]);
+            }
+          }
+          const float p0 = acc[0].x + acc[0].y, p1 = acc[1].x + acc[1].y;
+          const float p2 = acc[2].x + acc[2].y, p3 = acc[3].x + acc[3].y;
+          // reduce-scatter over lanes 4g..4g+3: after the xor-1 step a lane
+          // holds two keys (l/4 and l/4 + 8 if l is even, else 16 + l/4 and
+          // 24 + l/4), after the xor-2 step one (the second of them if l & 2)
+          const bool odd = lane & 1, hi = lane & 2;
+          float k0 = odd ? p2 : p0, k1 = odd ? p3 : p1;
+          k0 += __shfl_xor_sync(0xFFFFFFFFu, odd ? p0 : p2, 1);
+          k1 += __shfl_xor_sync(0xFFFFFFFFu, odd ? p1 : p3, 1);
+          const float keep = hi ? k1 : k0;
+          score = (keep + __shfl_xor_sync(0xFFFFFFFFu, hi ? k0 : k1, 2)) * ks;
+        }
+        const bool live = ok && row_live && page_ok && t < nr;
+        if constexpr (DENSE) {
+          if (live) p.dense[(long long)(m.row0 + r) * p.dense_stride + t] = score;
+        } else {
+          // running top-k filter: append survivors to this warp's sub-list
+          const bool pass = live && score >= tf;
+          const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass);
+          if (pass) {
+            const int pos = wc + __popc(bal & ((1u << lane) - 1u));
+            my_key[pos] = order_key(score);
+            my_idx[pos] = t;
+          }
+          wc += __popc(bal);
+          // every warp of the row takes part in every exchange, even after a
+          // timeout (it then stops waiting and contributes nothing)
+          if ((i % kSyncEvery) == kSyncEvery - 1 && i != ntiles - 1) {
+            if (exchange(false) < 0) ok = false;
           }
         }
-        const float p0 = acc[0].x + acc[0].y, p1 = acc[1].x + acc[1].y;
-        const float p2 = acc[2].x + acc[2].y, p3 = acc[3].x + acc[3].y;
-        // reduce-scatter over lanes 4g..4g+3: after the xor-1 step a lane
-        // holds two keys (l/4 and l/4 + 8 if l is even, else 16 + l/4 and
-        // 24 + l/4), after the xor-2 step one (the second of them if l & 2)
-        const bool odd = lane & 1, hi = lane & 2;
-        float k0 = odd ? p2 : p0, k1 = odd ? p3 : p1;
-        k0 += __shfl_xor_sync(0xFFFFFFFFu, odd ? p0 : p2, 1);
-        k1 += __shfl_xor_sync(0xFFFFFFFFu, odd ? p1 : p3, 1);
-        const float keep = hi ? k1 : k0;
-        score = (keep + __shfl_xor_sync(0xFFFFFFFFu, hi ? k0 : k1, 2)) * ks;
       }
-      const bool live = ok && row_live && page_ok && t < nr;
-      if constexpr (DENSE) {
-        if (live) p.dense[(long long)(m.row0 + r) * p.dense_stride + t] = score;
-      } else {
-        // running top-k filter: append survivors to this warp's sub-list
-        const bool pass = live && score >= tf;
-        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass);
-        if (pass) {
-          const int pos = wc + __popc(bal & ((1u << lane) - 1u));
-          my_key[pos] = order_key(score);
-          my_idx[pos] = t;
+      if constexpr (!DENSE) {
+        // unit end: cut the row's list to 512 and write it as a partial list
+        __syncwarp();
+        const int kept = exchange(true);
+        if (row_live) {
+          const long long pu = (long long)(m.row0 + r) * p.chunks + c;
+          const int cr = kept < 0 ? 0 : kept;
+          for (int j = et; j < cr; j += kEpiRow) {
+            p.part_key[pu * kTopK + j] = S.aux_key[r][j];
+            p.part_idx[pu * kTopK + j] = S.aux_idx[r][j];
+          }
+          if (et == 0) p.part_cnt[pu] = cr;
         }
-        wc += __popc(bal);
-        // every warp of the row takes part in every exchange, even after a
-        // timeout (it then stops waiting and contributes nothing)
-        if ((i % kSyncEvery) == kSyncEvery - 1 && i != ntiles - 1) {
-          if (exchange(false) < 0) ok = false;
-        }
+        // (the next unit's first exchange starts with a barrier of the row,
+        // so aux is read out before anyone writes it again)
       }
     }
     if (!ok && et == 0) atomicOr(p.status, kDevWaitTimeout);
-    if constexpr (!DENSE) {
-      // unit end: cut the row's list to 512 and write it as a partial list
-      __syncwarp();
-      const int kept = exchange(true);
-      if (row_live) {
-        const long long unit = (long long)(m.row0 + r) * p.chunks + c;
-        const int cr = kept < 0 ? 0 : kept;
-        for (int j = et; j < cr; j += kEpiRow) {
-          p.part_key[unit * kTopK + j] = S.aux_key[r][j];
-          p.part_idx[unit * kTopK + j] = S.aux_idx[r][j];
-        }
-        if (et == 0) p.part_cnt[unit] = cr;
-      }
-    }
   }
   tc_fence_before();
   __syncthreads();
@@ -428,8 +472,13 @@ cudaError_t launch_fused_t(const FusedLaunch& p, const uint8_t* kcache, cudaStre
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  const int groups = (p.rows + R - 1) / R;
-  fused_score_topk_kernel<R, DENSE><<<groups * p.chunks, fused_threads<R>(), smem, stream>>>(p, kmap, qmap);
+  // One CTA per unit: decode units differ in length (row lengths vary), and
+  // the hardware's CTA scheduler balances them better than a fixed
+  // assignment of units to resident CTAs (measured); the kernel's unit loop
+  // then runs once per CTA.
+  const long long units = (long long)((p.rows + R - 1) / R) * p.chunks;
+  const int grid = (int)units;
+  fused_score_topk_kernel<R, DENSE><<<grid, fused_threads<R>(), smem, stream>>>(p, kmap, qmap);
   return cudaGetLastError();
 }
 
@@ -443,7 +492,6 @@ FusedPlan fused_plan(long long rows, int max_seq_len, int group_rows, int num_sm
   const long long target = 4LL * num_sms;
   long long chunks = groups > 0 ? (target + groups - 1) / groups : 1;
   chunks = std::max<long long>(1, std::min<long long>({chunks, 12LL, max_blocks}));
-  chunks = std::max<long long>(chunks, (max_blocks + kMaxTiles - 1) / kMaxTiles);
   const long long cb = (max_blocks + chunks - 1) / chunks;
   pl.chunk_blocks = static_cast<int>(cb);
   pl.chunks = static_cast<int>((max_blocks + cb - 1) / cb);
