@@ -147,8 +147,9 @@ size_t sai_index_score_topk_workspace(int64_t rows, int32_t max_seq_len, int32_t
  *             (checked on device; a bad row is emptied and sets bit 1).
  * heads = 64, dim = 128, block_size = 128, k = 512 (else SAI_ERR_UNSUPPORTED).
  * group_rows  1, or 4 when every 4 consecutive rows share one row_to_batch
- *             value (packed prefill): each CTA then scores 4 rows at once.
- *             A group whose rows differ is emptied and sets bit 1.
+ *             value (packed prefill): the kernel then scores the rows in
+ *             pairs, each key block once per pair. A pair whose rows differ
+ *             is emptied and sets bit 1.
  * out_*       any of the three may be NULL, not all.
  * workspace   at least sai_index_score_topk_workspace(...) bytes, 16-byte aligned.
  */

@@ -13,19 +13,22 @@
 // name the fused kernel and its FP8 index cache but print no formula; this
 // is the formula the library adopts (scale outside the relu, no 1/sqrt(d)).
 //
-// GB300 design. One CTA takes a group of R query rows (R = 1 for decode,
-// R = 4 when consecutive rows share one request, as in prefill) and a chunk
-// of that request's KV blocks:
-//   * warp 4 streams each 128-token FP8 key block [128 keys x 128 dims]
-//     through a 4-stage shared-memory ring with 2-D TMA tensor loads (128-byte
+// GB300 design. A work unit is a group of R query rows (R = 1 for decode,
+// R = 2 for packed prefill, where consecutive rows share one request) and a
+// chunk of that request's KV blocks; one CTA per unit (the kernel can also
+// walk several units with its barrier phases carried over). Roles:
+//   * warp 4R streams each 128-token FP8 key block [128 keys x 128 dims]
+//     through a shared-memory ring with 2-D TMA tensor loads (128-byte
 //     swizzle; the paged gather is just the block's row coordinate);
-//   * warp 5 issues tcgen05.mma kind::f8f6f4 with the keys as M = 128 and
+//   * warp 4R+1 issues tcgen05.mma kind::f8f6f4 with the keys as M = 128 and
 //     the group's R x 64 (row, head) query vectors as N, K = 128 dims in four
 //     K = 32 steps, accumulating in FP32 in tensor memory, double-buffered;
-//   * warps 0-3 own TMEM lanes 0-127, i.e. one key each: they load the key's
-//     R x 64 dot products with tcgen05.ld, apply relu, the per-head weights
-//     and the key's scale in FP32, and feed the scores into per-row running
-//     top-k filters (candidate lists cut back to 512 by a radix select in
+//   * warps 4r..4r+3 are row r's epilogue, one TMEM lane quadrant (32 keys)
+//     each: 16x256b tcgen05.ld gives a lane 4 keys x 16 heads, so the lane
+//     keeps its 16 head weights in registers; relu (an exact saturating
+//     multiply), the weighted head sum (f32x2 FMAs), a 4-lane reduce-scatter
+//     to one key per lane, the key's scale, and the row's running top-k
+//     filter (per-warp candidate lists cut back to 512 by a radix select in
 //     shared memory when they fill up).
 // The per-(row, chunk) candidate lists go to a workspace; the merge kernel
 // of topk_transform.cu then selects, sorts and page-transforms each row.
@@ -48,7 +51,16 @@ namespace {
 constexpr int kH = 64;        // index heads
 constexpr int kD = 128;       // head dim (bytes per fp8 row)
 constexpr int kBlk = 128;     // tokens per KV block = MMA M
-constexpr int kNSf = 4;       // K-tile stages
+// K-tile stages and query-tile buffers per CTA: row groups of 2 run two
+// CTAs per SM, so they take a shallower ring and one query buffer.
+template <int R>
+__host__ __device__ constexpr int fused_stages() {
+  return R == 2 ? 3 : 4;
+}
+template <int R>
+__host__ __device__ constexpr int fused_qbufs() {
+  return R == 2 ? 1 : 2;
+}
 constexpr int kSub = 512;     // candidate sub-list per epilogue warp
 constexpr int kSyncEvery = 4; // tiles between the row group's count exchanges
 constexpr int kSubPruneAt = kSub - kSyncEvery * 32;
@@ -56,14 +68,15 @@ constexpr int kEpiRow = 128;  // epilogue threads per query row (4 warps, one TM
 
 template <int R>
 struct __align__(1024) FusedSmem {
-  uint8_t kst[kNSf][kBlk * kD];  // 16 KB each, 1024-byte aligned
-  uint8_t q[2][R * kH * kD];     // query tiles of two consecutive units
+  uint8_t kst[fused_stages<R>()][kBlk * kD];  // 16 KB each, 1024-byte aligned
+  uint8_t q[fused_qbufs<R>()][R * kH * kD];   // query tiles of consecutive units
   uint32_t ckey[R][4 * kSub];  // row r: four per-warp sub-lists
   int32_t cidx[R][4 * kSub];
   uint32_t aux_key[R][kTopK];
   int32_t aux_idx[R][kTopK];
   SelectScratch sc[R];
-  uint64_t full[kNSf], empty[kNSf], tfull[2], tempty[2], qfull[2], qempty[2];
+  uint64_t full[fused_stages<R>()], empty[fused_stages<R>()], tfull[2], tempty[2];
+  uint64_t qfull[fused_qbufs<R>()], qempty[fused_qbufs<R>()];
   uint32_t tmem_base;
   int wcnt[R][2][4];      // per-warp list sizes at a sync point (double-buffered)
 };
@@ -73,7 +86,8 @@ constexpr size_t fused_smem_bytes() {
   return sizeof(FusedSmem<R>) + 1024;
 }
 
-static_assert(fused_smem_bytes<4>() <= 227 * 1024, "one CTA's shared memory (the opt-in maximum per block)");
+static_assert(fused_smem_bytes<1>() <= 227 * 1024, "one CTA's shared memory (the opt-in maximum per block)");
+static_assert(2 * (fused_smem_bytes<2>() + 1024) <= 228 * 1024, "two row-pair CTAs per SM");
 
 template <int R>
 __device__ __forceinline__ FusedSmem<R>& fused_smem(unsigned char* raw) {
@@ -138,7 +152,7 @@ __host__ __device__ constexpr int fused_threads() {
 }
 
 template <int R, bool DENSE>
-__global__ void __launch_bounds__(fused_threads<R>(), 1)
+__global__ void __launch_bounds__(fused_threads<R>(), R == 2 ? 2 : 1)
     fused_score_topk_kernel(const __grid_constant__ FusedLaunch p, const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ unsigned char smem_raw[];
@@ -148,6 +162,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
   constexpr uint32_t kIdesc = umma_idesc_e4m3(kBlk, N);
   constexpr int kEpiWarps = 4 * R;
   constexpr int kTmaWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1;
+  constexpr int kNSf = fused_stages<R>(), kQB = fused_qbufs<R>();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int units = ((p.rows + R - 1) / R) * p.chunks;
 
@@ -160,7 +175,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
       mbar_init(&S.tfull[i], 1);
       mbar_init(&S.tempty[i], kEpiWarps);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kQB; ++i) {
       mbar_init(&S.qfull[i], 1);
       mbar_init(&S.qempty[i], 1);
     }
@@ -193,8 +208,8 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
         const int ntiles = m.blk1 - m.blk0;
         if (ntiles == 0) continue;
         const int32_t* bt = p.block_table + (long long)m.batch * p.bt_stride + m.blk0;
-        const int qb = qn & 1;
-        run = mbar_wait(&S.qempty[qb], ((qn >> 1) & 1u) ^ 1u);
+        const int qb = qn % kQB;
+        run = mbar_wait(&S.qempty[qb], ((qn / kQB) & 1u) ^ 1u);
         if (!run) break;
         mbar_arrive_expect_tx(&S.qfull[qb], (uint32_t)(N * kD));
         tma_load_2d(S.q[qb], &qmap, 0, m.row0 * kH, &S.qfull[qb], keep);
@@ -222,8 +237,8 @@ __global__ void __launch_bounds__(fused_threads<R>(), 1)
         const GroupMeta m = group_meta<R>(p, u / p.chunks, u % p.chunks, n, false);
         const int ntiles = m.blk1 - m.blk0;
         if (ntiles == 0) continue;
-        const int qb = qn & 1;
-        if (!(run = mbar_wait(&S.qfull[qb], (qn >> 1) & 1u))) break;
+        const int qb = qn % kQB;
+        if (!(run = mbar_wait(&S.qfull[qb], (qn / kQB) & 1u))) break;
         ++qn;
         const uint64_t bdesc = umma_desc_sw128_kmajor(smem_u32(S.q[qb]));
         for (int i = 0; i < ntiles; ++i, ++it) {
@@ -486,7 +501,10 @@ cudaError_t launch_fused_t(const FusedLaunch& p, const uint8_t* kcache, cudaStre
 
 FusedPlan fused_plan(long long rows, int max_seq_len, int group_rows, int num_sms) {
   FusedPlan pl{1, 1, 1, 0};
-  pl.group = (group_rows == 4 && rows >= 4) ? 4 : 1;
+  // Packed prefill rows come in groups of 4 sharing a request; the kernel
+  // takes them in pairs (MMA N = 128, two CTAs per SM: measured faster than
+  // groups of 4 with N = 256 and one CTA per SM).
+  pl.group = (group_rows == 4 && rows >= 2) ? 2 : 1;
   const long long max_blocks = std::max<long long>(1, ((long long)max_seq_len + kBlk - 1) / kBlk);
   const long long groups = (rows + pl.group - 1) / pl.group;
   const long long target = 4LL * num_sms;
@@ -500,7 +518,7 @@ FusedPlan fused_plan(long long rows, int max_seq_len, int group_rows, int num_sm
 }
 
 cudaError_t launch_fused(const FusedLaunch& p, int group, bool dense, const uint8_t* kcache, cudaStream_t stream) {
-  if (group == 4) return dense ? launch_fused_t<4, true>(p, kcache, stream) : launch_fused_t<4, false>(p, kcache, stream);
+  if (group == 2) return dense ? launch_fused_t<2, true>(p, kcache, stream) : launch_fused_t<2, false>(p, kcache, stream);
   return dense ? launch_fused_t<1, true>(p, kcache, stream) : launch_fused_t<1, false>(p, kcache, stream);
 }
 
