@@ -13,7 +13,9 @@
 // long row) at a time, so that the serial latency of one CTA's
 // stage -> filter -> barrier chain is hidden by the other CTAs on the SM.
 // The kernel is bound by instruction issue, not by HBM, so each stage is
-// large (8 KB, sixteen scores per thread) to spread the per-stage cost.
+// large (12 KB, 24 scores per thread, two stages per CTA) to spread the
+// per-stage cost (measured against 16 and 32 scores per thread, two and
+// three stages, three to six CTAs per SM).
 //   * Thread 0 keeps a ring of shared-memory stages filled with 1-D bulk TMA
 //     copies (cp.async.bulk + mbarrier complete_tx, evict-first in L2: every
 //     score is read once). The 16-byte-aligned interior of each window goes
@@ -21,7 +23,7 @@
 //     stride, any row start) are read with scalar loads. This is the scalar
 //     path the pages require for strides that are not a multiple of 4,
 //     folded into every row instead of a separate fallback kernel.
-//   * Each thread compares its 16 scores of a stage against the running
+//   * Each thread compares its 24 scores of a stage against the running
 //     threshold tau (as a float) and appends the survivors (order key,
 //     row-local index) to its warp's own candidate sub-list: a ballot prefix
 //     inside the warp, no shared atomics. The one block barrier per stage
@@ -46,9 +48,15 @@ namespace sai {
 namespace {
 
 constexpr int kThreads = 128;                    // 4 warps per CTA
-constexpr int kVec = 4;                          // float4 loads per thread per stage
-constexpr int kStage = kVec * 4 * kThreads;      // floats per stage (8 KB)
-constexpr int kNStage = 3;                       // 24 KB in flight per CTA
+#ifndef SAI_TOPK_VEC
+#define SAI_TOPK_VEC 6
+#endif
+#ifndef SAI_TOPK_CTAS
+#define SAI_TOPK_CTAS 5
+#endif
+constexpr int kVec = SAI_TOPK_VEC;               // float4 loads per thread per stage
+constexpr int kStage = kVec * 4 * kThreads;      // floats per stage (12 KB)
+constexpr int kNStage = 2;                       // 24 KB in flight per CTA
 constexpr int kWarps = kThreads / 32;
 constexpr int kCap = 1536;                       // candidate capacity (all warps)
 constexpr int kSub = kCap / kWarps;              // one candidate sub-list per warp
@@ -56,8 +64,8 @@ constexpr int kMaxExtra = 8;                     // scalar head/tail elements of
 constexpr int kPartWarp = 4 * 32 + kMaxExtra;    // most entries a warp appends from one float4 per lane
 constexpr int kSubCutAt = kSub - kPartWarp;      // slow path: cut before a part that might not fit
 constexpr int kBar = 1;                          // named barrier id (all 128 threads)
-constexpr int kCtasPerSm = 5;
-constexpr uint32_t kScalarBit = 1u << (4 * kVec);
+constexpr int kCtasPerSm = SAI_TOPK_CTAS;
+static_assert(4 * kVec <= 32, "one mask bit per score of a thread's stage");
 
 static_assert(kSubCutAt >= kTopK / kWarps, "a dealt-back sub-list must take one more part");
 
@@ -200,25 +208,26 @@ __device__ bool issue_stage(const TopkLaunch& p, Smem& S, int slot, uint64_t pol
 }
 
 // Offsets of this lane's survivors in its warp's sub-list: bit i of `mask`
-// marks a survivor (at most 4*kVec + 1 per lane). Survivors are rare (about
-// 1% of a row), so the common case is one survivor on a few lanes and one
+// marks a surviving score of the lane's stage data, `xs` a surviving scalar
+// end element (at most 4*kVec + 1 per lane). Survivors are rare (about 1%
+// of a row), so the common case is one survivor on a few lanes and one
 // ballot gives every lane its offset; only when some lane has several does
 // the warp ballot the bits of the per-lane counts. Returns the warp total
 // (warp-uniform) and this lane's first offset in *pos.
-__device__ __forceinline__ int warp_offsets(uint32_t mask, int lane, int* pos) {
-  const uint32_t any = __ballot_sync(0xFFFFFFFFu, mask != 0);
+__device__ __forceinline__ int warp_offsets(uint32_t mask, bool xs, int lane, int* pos) {
+  const uint32_t m = __popc(mask) + (xs ? 1u : 0u);
+  const uint32_t any = __ballot_sync(0xFFFFFFFFu, m != 0);
   const uint32_t lt = (1u << lane) - 1u;
   *pos = 0;
   if (any == 0) return 0;
-  const uint32_t multi = __ballot_sync(0xFFFFFFFFu, (mask & (mask - 1u)) != 0);
+  const uint32_t multi = __ballot_sync(0xFFFFFFFFu, m > 1);
   if (multi == 0) {
     *pos = __popc(any & lt);
     return __popc(any);
   }
-  const uint32_t m = __popc(mask);
   int off = 0, total = 0;
 #pragma unroll
-  for (int k = 0; k < 5; ++k) {
+  for (int k = 0; k < 6; ++k) {
     const uint32_t bk = __ballot_sync(0xFFFFFFFFu, (m >> k) & 1u);
     off += __popc(bk & lt) << k;
     total += __popc(bk) << k;
@@ -230,10 +239,9 @@ __device__ __forceinline__ int warp_offsets(uint32_t mask, int lane, int* pos) {
 // Write this lane's survivors (order key, row-local index) from position
 // pos of its warp's sub-list on. a[q] holds elements base + 4*(q*kThreads +
 // tid) + 0..3 (mask bits 4q..4q+3); x is one scalar element at index xi
-// (mask bit kScalarBit). Each lane walks only its set bits.
+// (kept when xs). Each lane walks only its set bits.
 __device__ __forceinline__ void write_survivors(uint32_t* key, int32_t* idx, int pos, const float4 (&a)[kVec],
-                                                float x, int xi, int base, uint32_t mask, int tid) {
-  if (mask == 0) return;
+                                                float x, int xi, int base, uint32_t mask, bool xs, int tid) {
 #pragma unroll
   for (int q = 0; q < kVec; ++q) {
     uint32_t m = (mask >> (4 * q)) & 0xFu;
@@ -246,7 +254,7 @@ __device__ __forceinline__ void write_survivors(uint32_t* key, int32_t* idx, int
       ++pos;
     }
   }
-  if (mask & kScalarBit) {
+  if (xs) {
     key[pos] = order_key(x);
     idx[pos] = xi;
   }
@@ -257,8 +265,8 @@ __device__ __forceinline__ void write_survivors(uint32_t* key, int32_t* idx, int
 // buffer, so a lane's loop is one load and two stores per survivor whichever
 // float4 it sits in.
 __device__ __forceinline__ void write_survivors_smem(uint32_t* key, int32_t* idx, int pos, const float* stage,
-                                                     float x, int xi, int base, uint32_t mask, int tid) {
-  uint32_t m = mask & (kScalarBit - 1u);
+                                                     float x, int xi, int base, uint32_t mask, bool xs, int tid) {
+  uint32_t m = mask;
   while (m) {
     const int i = __ffs(m) - 1;
     m &= m - 1u;
@@ -267,7 +275,7 @@ __device__ __forceinline__ void write_survivors_smem(uint32_t* key, int32_t* idx
     idx[pos] = base + off;
     ++pos;
   }
-  if (mask & kScalarBit) {
+  if (xs) {
     key[pos] = order_key(x);
     idx[pos] = xi;
   }
@@ -325,15 +333,12 @@ __device__ __forceinline__ uint32_t pass4(const float4& v, float tf) {
 }
 
 // Filter mask of a thread's stage data against tf: bits 4q..4q+3 for a[q]
-// (only the float4s that lie inside the stage's nvec elements), plus
-// kScalarBit for the scalar element when it is valid.
-__device__ __forceinline__ uint32_t stage_mask(const float4 (&a)[kVec], int nvec, float x, bool has_x, float tf,
-                                               int tid) {
+// (only the float4s that lie inside the stage's nvec elements).
+__device__ __forceinline__ uint32_t stage_mask(const float4 (&a)[kVec], int nvec, float tf, int tid) {
   uint32_t mask = 0;
 #pragma unroll
   for (int q = 0; q < kVec; ++q)
     if (4 * (q * kThreads + tid) < nvec) mask |= pass4(a[q], tf) << (4 * q);
-  if (has_x && x >= tf) mask |= kScalarBit;
   return mask;
 }
 
@@ -399,15 +404,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
       xi = tid < u.head ? lo + tid : u.tail_at + (tid - u.head);
       x = __ldg(p.scores + woff + xi);
     }
-    const uint32_t mask = stage_mask(a, nvec, x, has_x, tau_float(tau), tid);
+    const float tf0 = tau_float(tau);
+    const uint32_t mask = stage_mask(a, nvec, tf0, tid);
+    const bool xs = has_x && x >= tf0;
     int pos;
-    const int total = warp_offsets(mask, lane, &pos);
+    const int total = warp_offsets(mask, xs, lane, &pos);
     // A warp whose survivors fit appends them now, while the stage is still
     // in shared memory; one whose survivors do not fit defers them to the
     // slow path below (its registers still hold the stage).
     const bool fits = wcnt + total <= kSub;
     if (fits) {
-      write_survivors_smem(wkey, widx, wcnt + pos, S.stage[slot], x, xi, base, mask, tid);
+      write_survivors_smem(wkey, widx, wcnt + pos, S.stage[slot], x, xi, base, mask, xs, tid);
       wcnt += total;
       appended += total;
     }
@@ -440,10 +447,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
         const float tf = tau_float(tau);
         uint32_t mq = 0;
         if (!fits && 4 * (q * kThreads + tid) < nvec) mq = pass4(a[q], tf) << (4 * q);
-        if (!fits && q == 0 && has_x && x >= tf) mq |= kScalarBit;
+        const bool xq = !fits && q == 0 && has_x && x >= tf;
         int pq;
-        const int tq = warp_offsets(mq, lane, &pq);
-        write_survivors(wkey, widx, wcnt + pq, a, x, xi, base, mq, tid);
+        const int tq = warp_offsets(mq, xq, lane, &pq);
+        write_survivors(wkey, widx, wcnt + pq, a, x, xi, base, mq, xq, tid);
         wcnt += tq;
         appended += tq;
       }
@@ -461,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
         wcnt = 0;
         tau = 0;
         for (int b0 = 0; b0 < len; b0 += 4 * kThreads) {
-          const float tf0 = tau_float(tau);
+          const float tfr = tau_float(tau);
           const float* src = p.scores + woff + lo + b0;
           float4 r[kVec];
 #pragma unroll
@@ -472,13 +479,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
           for (int k = 0; k < 4; ++k) {
             if (b0 + 4 * tid + k < len) {
               e[k] = __ldg(src + 4 * tid + k);
-              rm |= (e[k] >= tf0 ? 1u : 0u) << k;
+              rm |= (e[k] >= tfr ? 1u : 0u) << k;
             }
           }
           r[0] = make_float4(e[0], e[1], e[2], e[3]);
           int pr;
-          const int tr = warp_offsets(rm, lane, &pr);
-          write_survivors(wkey, widx, wcnt + pr, r, 0.f, 0, lo + b0, rm, tid);
+          const int tr = warp_offsets(rm, false, lane, &pr);
+          write_survivors(wkey, widx, wcnt + pr, r, 0.f, 0, lo + b0, rm, false, tid);
           wcnt += tr;
           if (named_bar_or(kBar, kThreads, wcnt > kSubCutAt)) wcnt = prune(S, wcnt, tau, tid);
         }

@@ -59,7 +59,9 @@ def test_decode_bf16_ties(single):
 @pytest.mark.parametrize("kind", ["normal", "bf16", "int", "const", "signed_zero", "inf", "ascending", "descending"])
 @pytest.mark.parametrize("single", [False, True])
 def test_value_kinds(kind, single):
-    lens = [0, 1, 3, 7, 9, 100, 511, 512, 513, 2047, 2048, 2049, 6000, 9001, 20000, 33333]
+    # around k, one and two 1024/2048/3072-score stages, and long rows
+    lens = [0, 1, 3, 7, 9, 100, 511, 512, 513, 2047, 2048, 2049, 3071, 3072, 3073, 6000, 6143, 6145, 9001, 20000,
+            33333]
     inp = W.make_topk_inputs(31, lens, 33340, 128, (len(lens), 261), kind=kind, fill=np.inf)
     _assert_equal(_run(inp, force_single=single), _oracle(inp), kind)
 
