@@ -368,6 +368,29 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
   uint32_t tau = 0;   // keep elements whose order key >= tau
   uint32_t spec = 0;  // speculative starting threshold for the next unit (0: none)
   uint32_t spec_used = 0;
+  // Slow path of a stage (or of a redo step) in which some warp's survivors
+  // did not fit its sub-list: cut all sub-lists, then the warps whose
+  // survivors did not fit (!fits) append their data one float4 per lane at
+  // a time, filtered against the raised threshold, with a cut before any
+  // part that might not fit. Returns how many this warp appended.
+  auto append_parts = [&](const float4(&a)[kVec], int nvec, float x, int xi, bool has_x, int base, bool fits) {
+    int added = 0;
+    wcnt = prune(S, wcnt, tau, tid);
+#pragma unroll
+    for (int q = 0; q < kVec; ++q) {
+      if (q > 0 && named_bar_or(kBar, kThreads, wcnt > kSubCutAt)) wcnt = prune(S, wcnt, tau, tid);
+      const float tf = tau_float(tau);
+      uint32_t mq = 0;
+      if (!fits && 4 * (q * kThreads + tid) < nvec) mq = pass4(a[q], tf) << (4 * q);
+      const bool xq = !fits && q == 0 && has_x && x >= tf;
+      int pq;
+      const int tq = warp_offsets(mq, xq, lane, &pq);
+      write_survivors(wkey, widx, wcnt + pq, a, x, xi, base, mq, xq, tid);
+      wcnt += tq;
+      added += tq;
+    }
+    return added;
+  };
   while (true) {
     const int slot = it % kNStage;
     const uint32_t ph = (it / kNStage) & 1u;
@@ -434,27 +457,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
       fence_proxy_async_smem();
       issuing = issue_stage(p, S, slot, policy);
     }
-    if (any) {
-      // The threshold is far below this stage's scores (e.g. the first unit
-      // of a CTA, or a rising row) and some warp deferred its survivors: cut
-      // all sub-lists, then the deferred warps append the stage one float4
-      // per lane at a time, filtered against the raised threshold, with a
-      // cut before any part that might not fit.
-      wcnt = prune(S, wcnt, tau, tid);
-#pragma unroll
-      for (int q = 0; q < kVec; ++q) {
-        if (q > 0 && named_bar_or(kBar, kThreads, wcnt > kSubCutAt)) wcnt = prune(S, wcnt, tau, tid);
-        const float tf = tau_float(tau);
-        uint32_t mq = 0;
-        if (!fits && 4 * (q * kThreads + tid) < nvec) mq = pass4(a[q], tf) << (4 * q);
-        const bool xq = !fits && q == 0 && has_x && x >= tf;
-        int pq;
-        const int tq = warp_offsets(mq, xq, lane, &pq);
-        write_survivors(wkey, widx, wcnt + pq, a, x, xi, base, mq, xq, tid);
-        wcnt += tq;
-        appended += tq;
-      }
-    }
+    // The threshold is far below this stage's scores (e.g. the first unit of
+    // a CTA, or a rising row) and some warp deferred its survivors.
+    if (any) appended += append_parts(a, nvec, x, xi, has_x, base, fits);
     if (flags & 2) {
       if (lane == 0) S.wapp[warp] = appended;
       named_bar(kBar, kThreads);
@@ -463,31 +468,39 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
       for (int w = 0; w < kWarps; ++w) passed += S.wapp[w];
       if (spec_used && passed < min(len, kTopK)) {
         // The starting threshold was too high for this unit: redo it from
-        // global memory with no threshold (exact again, just slower), four
-        // elements per lane at a time.
+        // global memory with no threshold (exact again): the window's
+        // 16-byte-aligned body in steps of kStage scores (float4 loads), its
+        // scalar ends in the first step, with the stream's fit check and
+        // slow path.
         wcnt = 0;
         tau = 0;
-        for (int b0 = 0; b0 < len; b0 += 4 * kThreads) {
-          const float tfr = tau_float(tau);
-          const float* src = p.scores + woff + lo + b0;
+        const int body = len - u.head - u.tail;
+        const float4* bsrc = reinterpret_cast<const float4*>(p.scores + woff + lo + u.head);
+        for (int b0 = 0; b0 == 0 || b0 < body; b0 += kStage) {
           float4 r[kVec];
 #pragma unroll
-          for (int q = 0; q < kVec; ++q) r[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-          float e[4] = {0.f, 0.f, 0.f, 0.f};
-          uint32_t rm = 0;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            if (b0 + 4 * tid + k < len) {
-              e[k] = __ldg(src + 4 * tid + k);
-              rm |= (e[k] >= tfr ? 1u : 0u) << k;
-            }
+          for (int q = 0; q < kVec; ++q) {
+            const int v4 = q * kThreads + tid;
+            r[q] = 4 * v4 < body - b0 ? __ldg(bsrc + b0 / 4 + v4) : make_float4(0.f, 0.f, 0.f, 0.f);
           }
-          r[0] = make_float4(e[0], e[1], e[2], e[3]);
+          const bool hx = b0 == 0 && tid < u.head + u.tail;
+          float xr = 0.f;
+          int xir = 0;
+          if (hx) {
+            xir = tid < u.head ? lo + tid : u.tail_at + (tid - u.head);
+            xr = __ldg(p.scores + woff + xir);
+          }
+          const float tfr = tau_float(tau);
+          const uint32_t rm = stage_mask(r, body - b0, tfr, tid);
+          const bool rx = hx && xr >= tfr;
           int pr;
-          const int tr = warp_offsets(rm, false, lane, &pr);
-          write_survivors(wkey, widx, wcnt + pr, r, 0.f, 0, lo + b0, rm, false, tid);
-          wcnt += tr;
-          if (named_bar_or(kBar, kThreads, wcnt > kSubCutAt)) wcnt = prune(S, wcnt, tau, tid);
+          const int tr = warp_offsets(rm, rx, lane, &pr);
+          const bool rfits = wcnt + tr <= kSub;
+          if (rfits) {
+            write_survivors(wkey, widx, wcnt + pr, r, xr, xir, lo + u.head + b0, rm, rx, tid);
+            wcnt += tr;
+          }
+          if (named_bar_or(kBar, kThreads, !rfits)) append_parts(r, body - b0, xr, xir, hx, lo + u.head + b0, rfits);
         }
         spec_used = 0;
       }
