@@ -152,7 +152,7 @@ __host__ __device__ constexpr int fused_threads() {
 }
 
 template <int R, bool DENSE>
-__global__ void __launch_bounds__(fused_threads<R>(), R == 2 ? 2 : 1)
+__global__ void __launch_bounds__(fused_threads<R>(), R <= 2 ? 2 : 1)
     fused_score_topk_kernel(const __grid_constant__ FusedLaunch p, const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ unsigned char smem_raw[];
