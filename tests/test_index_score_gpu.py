@@ -164,3 +164,14 @@ def test_fused_prefill_full_size_sampled():
     got = _fused(inp, group_rows=4)
     sample = [0, 1, 2, 3, 1000, 2047, 2048, 3333, 4092, 4093, 4094, 4095]
     _check_topk(got, inp, rows=sample)
+
+
+@pytest.mark.parametrize("kind", ["normal", "int"])
+def test_topk_one_chunk_per_row(kind):
+    """640 single rows give one KV chunk per row, so the fused kernel ranks
+    each row's 512 and writes the outputs itself (no merge pass); integer
+    inputs make many equal scores, which sends the ranking to its fallback."""
+    rows, per_row = 640, 12
+    lens = np.random.default_rng(47).integers(1, per_row * 128 + 1, size=rows).astype(np.int32)
+    inp = W.make_fused_inputs(47, rows, 64, 128, rows * per_row + 1, lens, (rows, per_row), kind=kind)
+    _check_topk(_fused(inp), inp)
