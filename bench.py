@@ -133,6 +133,36 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- workload
+def _bind_host_to_gpu(local: int) -> str:
+    """Run this process on the CPUs next to the GPU, so that the host buffers
+    of the end-to-end timing are allocated (first touch) in that CPU's memory
+    and copied over its own link rather than across sockets. Returns a note
+    for the JSON line."""
+    import torch
+
+    try:
+        bus = torch.cuda.get_device_properties(local).pci_bus_id.lower()
+        bus = bus if bus.count(":") == 2 else "0000:" + bus
+        dom, b, rest = bus.split(":")
+        path = f"/sys/bus/pci/devices/{dom.zfill(4)}:{b}:{rest}/local_cpulist"
+        with open(path) as f:
+            spec = f.read().strip()
+        cpus = set()
+        for part in spec.split(","):
+            if "-" in part:
+                lo, hi = part.split("-")
+                cpus.update(range(int(lo), int(hi) + 1))
+            elif part:
+                cpus.add(int(part))
+        cpus &= os.sched_getaffinity(0)
+        if not cpus:
+            return "host affinity unchanged (no local CPUs listed)"
+        os.sched_setaffinity(0, cpus)
+        return f"host threads on the GPU's {len(cpus)} local CPUs"
+    except Exception as exc:  # no sysfs entry, other platforms
+        return f"host affinity unchanged ({type(exc).__name__})"
+
+
 class Part:
     """One part of the step: host (pinned) inputs, device copies, outputs."""
 
@@ -337,6 +367,7 @@ def run_gpu(args):
     hbm_peak, bf16_peak, peak_kind = _peaks()
     fp8_peak = bf16_peak * FP8_OVER_BF16
 
+    host_note = _bind_host_to_gpu(local)
     parts = build_parts(dev, args)
     stream = torch.cuda.Stream(device=dev)
 
@@ -435,7 +466,7 @@ def run_gpu(args):
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32 (top-k), e4m3 x e4m3 -> f32 (fused scores)", "data": "synthetic",
             "config": {"workload": WORKLOAD, "rows_per_step": rows, "k": K,
-                       "l2": "inputs larger than L2 (4.5 GB per step)", "paths": paths},
+                       "l2": "inputs larger than L2 (4.5 GB per step)", "host": host_note, "paths": paths},
             "roofline": roof,
             "e2e": e2e,
             "gpu_launches": sum(p.launches for p in parts) * args.steps,
