@@ -69,8 +69,9 @@ int sai_device_status(int* out_bits, int clear, sai_stream_t stream);
 
 /*
  * Workspace bytes that sai_topk_transform wants for these sizes on the
- * current device (0 when the one-unit-per-row path is used). Long rows on
- * few rows are split over several CTAs whose partial top-k lists go here.
+ * current device: a 256-byte header (a work counter that lets CTAs take
+ * rows as they finish, zeroed by the call on its stream), plus, when long
+ * rows on few rows are split over several CTAs, their partial top-k lists.
  */
 size_t sai_topk_transform_workspace(int64_t rows, int64_t score_stride, int32_t k);
 
@@ -108,7 +109,9 @@ size_t sai_topk_transform_workspace(int64_t rows, int64_t score_stride, int32_t 
  * workspace    device memory of workspace_bytes (16-byte aligned) or NULL.
  *              If it is smaller than sai_topk_transform_workspace asks for,
  *              every row is processed by a single CTA (correct, slower for
- *              few long rows).
+ *              few long rows); below 256 bytes (or NULL) the CTAs also take
+ *              rows in a fixed order instead of from the work counter.
+ *              Calls that share a workspace must not overlap on the GPU.
  */
 int sai_topk_transform(const float* scores, int64_t rows, int64_t score_stride, const int32_t* row_starts,
                        const int32_t* seq_lens, const int32_t* page_tables, int64_t pt_rows, int64_t pt_stride,

@@ -118,8 +118,8 @@ int sai_topk_transform(const float* scores, int64_t rows, int64_t score_stride, 
   if (!device_setup(&dev, &st, &sms)) return SAI_ERR_CUDA;
 
   sai::TopkPlan plan = sai::topk_plan(rows, score_stride, sms);
-  if (plan.chunks > 1 && (!workspace || workspace_bytes < plan.workspace_bytes || !aligned(workspace, 16)))
-    plan = sai::TopkPlan{1, 0, 0};
+  const bool have_ws = workspace && workspace_bytes >= sai::kTopkWorkHeader && aligned(workspace, 16);
+  if (plan.chunks > 1 && (!have_ws || workspace_bytes < plan.workspace_bytes)) plan = sai::TopkPlan{1, 0, 0};
 
   sai::TopkLaunch p{};
   p.scores = scores;
@@ -136,15 +136,21 @@ int sai_topk_transform(const float* scores, int64_t rows, int64_t score_stride, 
   p.out_idx = out_indices;
   p.chunks = plan.chunks;
   p.chunk_len = plan.chunk_len;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (have_ws) {
+    p.work = static_cast<int*>(workspace);
+    cudaError_t e = cudaMemsetAsync(p.work, 0, sizeof(int), cs);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
   if (plan.chunks > 1) {
     const size_t units = static_cast<size_t>(rows) * plan.chunks;
-    char* w = static_cast<char*>(workspace);
+    char* w = static_cast<char*>(workspace) + sai::kTopkWorkHeader;
     p.part_key = reinterpret_cast<uint32_t*>(w);
     p.part_idx = reinterpret_cast<int32_t*>(w + units * SAI_TOPK * 4);
     p.part_cnt = reinterpret_cast<int*>(w + units * SAI_TOPK * 8);
   }
   p.status = st;
-  return cuda_status(sai::launch_topk_transform(p, sms, reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_status(sai::launch_topk_transform(p, sms, cs));
 }
 
 }  // extern "C"

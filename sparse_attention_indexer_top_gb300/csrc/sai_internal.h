@@ -31,8 +31,12 @@ struct TopkLaunch {
   uint32_t* part_key;  // [rows*chunks, 512] when chunks > 1
   int32_t* part_idx;
   int* part_cnt;       // [rows*chunks]
+  int* work;           // unit counter, zero at launch (null: fixed unit order)
   int* status;
 };
+
+// Bytes at the start of a topk_transform workspace: the unit counter.
+constexpr size_t kTopkWorkHeader = 256;
 
 // How a topk_transform call is split; shared by the workspace query and the
 // launcher so both always agree.

@@ -196,7 +196,9 @@ __device__ bool issue_stage(const TopkLaunch& p, Smem& S, int slot, uint64_t pol
     mbar_arrive(&S.full[slot]);
   }
   if (s + 1 >= nst) {
-    c.unit += gridDim.x;
+    // Units after each CTA's first come from a shared counter when there is
+    // one, so that CTAs that drew short rows (or no redo) take more of them.
+    c.unit = p.work ? static_cast<int>(gridDim.x) + atomicAdd(p.work, 1) : c.unit + static_cast<int>(gridDim.x);
     cursor_load(p, c);
   } else {
     c.s = s + 1;
@@ -649,8 +651,8 @@ bool g_merge_attr_done[64];
 }  // namespace
 
 TopkPlan topk_plan(long long rows, long long max_window, int num_sms) {
-  TopkPlan pl{1, 0, 0};
-  if (rows <= 0 || max_window <= 0) return pl;
+  TopkPlan pl{1, 0, kTopkWorkHeader};
+  if (rows <= 0 || max_window <= 0) return TopkPlan{1, 0, 0};
   const long long slots = 2LL * num_sms;
   constexpr long long kMinChunk = 4096;
   if (rows < slots && max_window > 2 * kMinChunk) {
@@ -662,7 +664,8 @@ TopkPlan topk_plan(long long rows, long long max_window, int num_sms) {
     pl.chunks = static_cast<int>(chunks);
     pl.chunk_len = static_cast<int>(len);
     const long long units = rows * chunks;
-    pl.workspace_bytes = static_cast<size_t>(units) * kTopK * 8 + static_cast<size_t>(units) * 4 + 256;
+    pl.workspace_bytes =
+        kTopkWorkHeader + static_cast<size_t>(units) * kTopK * 8 + static_cast<size_t>(units) * 4 + 256;
   }
   return pl;
 }
