@@ -645,6 +645,74 @@ __global__ void __launch_bounds__(kTopK, 1) merge_kernel(const __grid_constant__
   }
 }
 
+// ---------------------------------------------------------------- rank
+// When every row has a single partial list (the fused path with one KV
+// chunk per row), that list already is the row's exact top 512: only the
+// output order and the page transform remain. Four rows per CTA, 128
+// threads each: load the list, rank it by bucketing (a bitonic network for
+// heavy bins), write indices, slots and scores by rank.
+constexpr int kRankRows = 4;
+
+struct __align__(16) RankRowSmem {
+  uint32_t aux_key[kTopK];
+  int32_t aux_idx[kTopK];
+  union {
+    struct {
+      uint32_t hist[1024];
+      uint16_t bucket[kTopK];
+    } r;
+    unsigned long long sortbuf[kTopK];
+  } s;
+  SelectScratch sc;
+};
+
+__global__ void __launch_bounds__(kRankRows * 128) rank_kernel(const __grid_constant__ MergeLaunch p) {
+  extern __shared__ unsigned char smem_raw[];
+  const int g = threadIdx.x >> 7, t = threadIdx.x & 127;
+  RankRowSmem& S = reinterpret_cast<RankRowSmem*>(smem_raw)[g];
+  const long long row = (long long)blockIdx.x * kRankRows + g;
+  const int bar = 1 + g;
+  const bool live = row < p.rows;
+  const int cnt = live ? min(max(p.part_cnt[row], 0), kTopK) : 0;
+  for (int j = t; j < cnt; j += 128) {
+    S.aux_key[j] = p.part_key[row * kTopK + j];
+    S.aux_idx[j] = p.part_idx[row * kTopK + j];
+  }
+  named_bar(bar, 128);
+  uint32_t k4[4];
+  int32_t i4[4];
+  int rk4[4];
+  if (!bucket_rank512<128>(S.aux_key, S.aux_idx, cnt, S.s.r.hist, S.s.r.bucket, S.sc, k4, i4, rk4, t, bar)) {
+    unsigned long long v[4];
+    bitonic_sort512_128(S.aux_key, S.aux_idx, cnt, S.s.sortbuf, v, t, bar);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      k4[e] = static_cast<uint32_t>(v[e] >> 32);
+      i4[e] = v[e] ? static_cast<int32_t>(~static_cast<uint32_t>(v[e] & 0xFFFFFFFFull)) : -1;
+      rk4[e] = 4 * t + e;
+    }
+  }
+  if (!live) return;
+  const long long o = row * kTopK;
+  const int batch = p.row_to_batch ? p.row_to_batch[row] : (int)row;
+  const int ps = p.page_size;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    if (i4[e] < 0) continue;
+    if (p.out_idx) p.out_idx[o + rk4[e]] = i4[e];
+    if (p.out_scores) p.out_scores[o + rk4[e]] = key_to_float(k4[e]);
+    if (p.out_slots) {
+      const long long page = p.page_tables[(long long)batch * p.pt_stride + (ps == 1 ? i4[e] : i4[e] / ps)];
+      p.out_slots[o + rk4[e]] = static_cast<int>(ps == 1 ? page : page * ps + i4[e] % ps);
+    }
+  }
+  for (int j = cnt + t; j < kTopK; j += 128) {
+    if (p.out_idx) p.out_idx[o + j] = -1;
+    if (p.out_slots) p.out_slots[o + j] = -1;
+    if (p.out_scores) p.out_scores[o + j] = __int_as_float(0x7FC00000);
+  }
+}
+
 bool g_attr_done[64];
 bool g_merge_attr_done[64];
 
@@ -674,6 +742,11 @@ size_t merge_smem_bytes() { return sizeof(MergeSmem); }
 
 cudaError_t launch_merge(const MergeLaunch& p, cudaStream_t stream) {
   if (p.rows <= 0) return cudaSuccess;
+  if (p.units_per_row == 1) {
+    const int grid = (p.rows + kRankRows - 1) / kRankRows;
+    rank_kernel<<<grid, kRankRows * 128, kRankRows * sizeof(RankRowSmem), stream>>>(p);
+    return cudaGetLastError();
+  }
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !g_merge_attr_done[dev]) {
