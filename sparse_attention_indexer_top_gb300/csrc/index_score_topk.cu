@@ -51,15 +51,21 @@ namespace {
 constexpr int kH = 64;        // index heads
 constexpr int kD = 128;       // head dim (bytes per fp8 row)
 constexpr int kBlk = 128;     // tokens per KV block = MMA M
-// K-tile stages and query-tile buffers per CTA: row groups of 2 run two
-// CTAs per SM, so they take a shallower ring and one query buffer.
+// K-tile stages, query-tile buffers and resident CTAs per SM: single rows
+// (decode) run three small CTAs per SM with a 2-stage ring, row pairs
+// (prefill) two with a 3-stage ring; one query buffer each, since every CTA
+// takes one unit (measured against 2-4 stages and 2-3 CTAs per SM).
 template <int R>
 __host__ __device__ constexpr int fused_stages() {
-  return R == 2 ? 3 : 4;
+  return R == 1 ? 2 : (R == 2 ? 3 : 4);
 }
 template <int R>
 __host__ __device__ constexpr int fused_qbufs() {
-  return R == 2 ? 1 : 2;
+  return R <= 2 ? 1 : 2;
+}
+template <int R>
+__host__ __device__ constexpr int fused_ctas_per_sm() {
+  return R == 1 ? 3 : (R == 2 ? 2 : 1);
 }
 constexpr int kSub = 512;     // candidate sub-list per epilogue warp
 constexpr int kSyncEvery = 4; // tiles between the row group's count exchanges
@@ -86,7 +92,7 @@ constexpr size_t fused_smem_bytes() {
   return sizeof(FusedSmem<R>) + 1024;
 }
 
-static_assert(fused_smem_bytes<1>() <= 227 * 1024, "one CTA's shared memory (the opt-in maximum per block)");
+static_assert(3 * (fused_smem_bytes<1>() + 1024) <= 228 * 1024, "three single-row CTAs per SM");
 static_assert(2 * (fused_smem_bytes<2>() + 1024) <= 228 * 1024, "two row-pair CTAs per SM");
 
 template <int R>
@@ -152,7 +158,7 @@ __host__ __device__ constexpr int fused_threads() {
 }
 
 template <int R, bool DENSE>
-__global__ void __launch_bounds__(fused_threads<R>(), R <= 2 ? 2 : 1)
+__global__ void __launch_bounds__(fused_threads<R>(), fused_ctas_per_sm<R>())
     fused_score_topk_kernel(const __grid_constant__ FusedLaunch p, const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ unsigned char smem_raw[];
@@ -507,10 +513,10 @@ FusedPlan fused_plan(long long rows, int max_seq_len, int group_rows, int num_sm
   pl.group = (group_rows == 4 && rows >= 2) ? 2 : 1;
   const long long max_blocks = std::max<long long>(1, ((long long)max_seq_len + kBlk - 1) / kBlk);
   const long long groups = (rows + pl.group - 1) / pl.group;
-  // about two units per SM (one wave of two resident CTAs each): fewer,
-  // longer units cost fewer list cuts and partial lists than finer ones
-  // (measured against 1, 3, 4, 6 and 8 per SM on the decode workload)
-  const long long target = 2LL * num_sms;
+  // about four units per SM (a little over one wave of three resident
+  // single-row CTAs): measured against 2, 3, 5, 6 and 8 per SM on the
+  // decode workload
+  const long long target = 4LL * num_sms;
   long long chunks = groups > 0 ? (target + groups - 1) / groups : 1;
   chunks = std::max<long long>(1, std::min<long long>({chunks, 12LL, max_blocks}));
   const long long cb = (max_blocks + chunks - 1) / chunks;
