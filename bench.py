@@ -77,6 +77,24 @@ def _dist():
     return rank, world, local
 
 
+def _max_over_ranks(x: float, world: int, device) -> float:
+    """The largest x over the ranks: the job's time is its slowest rank's."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_rate(rows_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job rows/s: every rank runs its own replica of the step (weak
+    scaling, no data-path collective), the job takes `ms` per step."""
+    return rows_per_rank * world / (ms * 1e-3)
+
+
 class ClockSampler:
     """Samples SM clocks and throttle reasons with nvidia-smi while running."""
 
@@ -381,7 +399,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     assert sai.device_status() == 0, "a kernel flagged its inputs"
 
-    # timed region: the step's inputs (4.5 GB) are far larger than L2
+    # timed region
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in parts]
           for _ in range(args.steps)]
     if world > 1:
@@ -405,12 +423,9 @@ def run_gpu(args):
     part_ms = [float(np.mean([ev[s][j][0].elapsed_time(ev[s][j][1]) for s in range(args.steps)]))
                for j in range(len(parts))]
     ms = float(np.mean([ev[s][0][0].elapsed_time(ev[s][-1][1]) for s in range(args.steps)]))
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = _max_over_ranks(ms, world, dev)
     rows = sum(p.rows for p in parts)
-    value = rows * world / (ms * 1e-3)
+    value = _job_rate(rows, world, ms)
 
     paths = {}
     for part, pm in zip(parts, part_ms):
