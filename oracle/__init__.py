@@ -13,6 +13,7 @@ Modules
 ``topk``   per-row window top-k (stable sort) and the page-table transform.
 ``score``  the FP8 index score and the fused score + top-k.
 ``brute``  O(n^2) rank-rule selection, used only to pin ``topk``.
+``blocks`` per-row distinct KV blocks of the selected slots.
 
 Every function is pinned by ``tests/test_oracle_*.py`` against closed forms,
 brute force, invariants or library routines; none is "parity unpinned".
@@ -22,3 +23,4 @@ from .fp8 import e4m3fn_decode, e4m3fn_units  # noqa: F401
 from .topk import topk_row, page_transform, topk_transform  # noqa: F401
 from .score import index_scores_row, index_scores, index_score_topk  # noqa: F401
 from .brute import rank_select_bruteforce  # noqa: F401
+from .blocks import sparse_blocks  # noqa: F401

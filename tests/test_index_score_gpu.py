@@ -175,3 +175,31 @@ def test_topk_one_chunk_per_row(kind):
     lens = np.random.default_rng(47).integers(1, per_row * 128 + 1, size=rows).astype(np.int32)
     inp = W.make_fused_inputs(47, rows, 64, 128, rows * per_row + 1, lens, (rows, per_row), kind=kind)
     _check_topk(_fused(inp), inp)
+
+
+def _packed_requests(seed, new_rows, prefixes):
+    """Several requests packed into one call: request b contributes
+    new_rows[b] query rows, causal on a KV of prefixes[b] + new_rows[b]
+    tokens with its own block-table row (row_to_batch = b)."""
+    kv = [p + n for p, n in zip(prefixes, new_rows)]
+    per_row = -(-max(kv) // 128)
+    lens, r2b = [], []
+    for b, (p, n) in enumerate(zip(prefixes, new_rows)):
+        lens += [p + i + 1 for i in range(n)]
+        r2b += [b] * n
+    rows = len(lens)
+    return W.make_fused_inputs(seed, rows, 64, 128, len(kv) * per_row + 5, lens, (len(kv), per_row),
+                               row_to_batch=r2b)
+
+
+def test_topk_packed_requests_grouped():
+    """Three requests with different prefixes, each a multiple of 4 rows, in
+    one call with group_rows=4 (rows scored in pairs of one request)."""
+    inp = _packed_requests(48, [36, 20, 44], [2900, 700, 5100])
+    _check_topk(_fused(inp, group_rows=4), inp)
+
+
+def test_topk_packed_requests_unaligned_single_rows():
+    """Request boundaries that are not multiples of 4: group_rows=1."""
+    inp = _packed_requests(49, [13, 7, 22], [3300, 100, 2000])
+    _check_topk(_fused(inp, group_rows=1), inp)
