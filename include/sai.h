@@ -175,6 +175,29 @@ int sai_index_score(const uint8_t* q_fp8, const float* w, const uint8_t* kcache_
                     int64_t out_stride, sai_stream_t stream);
 
 /*
+ * sai_sparse_blocks -- per-row distinct KV blocks of top-k slots.
+ *
+ * Follows ROCm/ATOM PR #1282 "merge build sparse block into topk" (title and
+ * Motivation): the sparse attention after the indexer reads KV blocks, so
+ * each row's selected physical slots (the out_slots of sai_topk_transform
+ * or sai_index_score_topk) become the list of distinct blocks they fall in.
+ * For each row i:
+ *   B_i = ascending distinct values of slots[i*k + j] / block_size over the
+ *         j in [0, k) with slots[i*k + j] >= 0 (negative slots are padding)
+ *   out_blocks[i*k + t] = B_i[t] for t < |B_i|, -1 for |B_i| <= t < k
+ *   out_counts[i] = |B_i|
+ *
+ * slots       int32 [rows, k], 4-byte aligned; k in [1, 512].
+ * block_size  >= 1 (128: the KV block of the fused path; a slot of the
+ *             page_size=1 top-k is a token slot, so its block is slot / 128).
+ * out_blocks  int32 [rows, k]; out_counts int32 [rows] or NULL.
+ * Errors: NULL pointers, k outside [1, 512] or block_size < 1 are reported
+ * before anything is launched.
+ */
+int sai_sparse_blocks(const int32_t* slots, int64_t rows, int32_t k, int32_t block_size, int32_t* out_blocks,
+                      int32_t* out_counts, sai_stream_t stream);
+
+/*
  * Size of the library-owned device scratch used by
  * sai_topk_transform_noalloc: 8 MiB, held on every GPU that loads the
  * library until the process exits.

@@ -183,3 +183,24 @@ def index_score(q: torch.Tensor, w: torch.Tensor, kcache: torch.Tensor, kscale: 
         int(max_seq_len), int(group_rows), _ptr(out), out.stride(0), _stream(stream))
     check(st, "sai_index_score")
     return out
+
+
+def sparse_blocks(slots: torch.Tensor, block_size: int = 128, *, out_blocks: Optional[torch.Tensor] = None,
+                  out_counts: Optional[torch.Tensor] = None, stream=None):
+    """Per-row distinct KV blocks of top-k slots: ``(blocks [rows, k] int32,
+    ascending, -1 padded; counts [rows] int32)``. Slots < 0 are padding."""
+    dev = slots.device
+    _need(slots, "slots", torch.int32, dev, 2)
+    if not slots.is_contiguous():
+        raise ValueError("slots must be contiguous")
+    rows, k = slots.shape
+    if out_blocks is None:
+        out_blocks = torch.empty((rows, k), dtype=torch.int32, device=dev)
+    if out_counts is None:
+        out_counts = torch.empty((rows,), dtype=torch.int32, device=dev)
+    _need(out_blocks, "out_blocks", torch.int32, dev, 2)
+    _need(out_counts, "out_counts", torch.int32, dev, 1)
+    st = load().sai_sparse_blocks(_ptr(slots), rows, int(k), int(block_size), _ptr(out_blocks), _ptr(out_counts),
+                                  _stream(stream))
+    check(st, "sai_sparse_blocks")
+    return out_blocks, out_counts

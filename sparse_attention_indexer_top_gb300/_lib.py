@@ -29,6 +29,7 @@ SIGNATURES = {
                                        _c_i32, _c_i32, _c_i32, _vp, _c_i64, _vp]),
     "sai_topk_transform_noalloc": (ctypes.c_int, [_vp, _c_i64, _c_i64, _vp, _vp, _vp, _c_i64, _c_i64, _vp, _c_i32,
                                                   _c_i32, _vp, _vp, _vp]),
+    "sai_sparse_blocks": (ctypes.c_int, [_vp, _c_i64, _c_i32, _c_i32, _vp, _vp, _vp]),
 }
 
 _lib = None

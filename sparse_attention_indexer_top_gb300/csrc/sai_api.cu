@@ -286,3 +286,16 @@ int sai_index_score(const uint8_t* q_fp8, const float* w, const uint8_t* kcache_
 }
 
 }  // extern "C"
+
+int sai_sparse_blocks(const int32_t* slots, int64_t rows, int32_t k, int32_t block_size, int32_t* out_blocks,
+                      int32_t* out_counts, sai_stream_t stream) {
+  if (rows < 0 || k < 1 || k > SAI_TOPK || block_size < 1 || rows > INT_MAX / SAI_TOPK) return SAI_ERR_SHAPE;
+  if (rows == 0) return SAI_OK;
+  if (!slots || !out_blocks) return SAI_ERR_NULL;
+  if (!aligned(slots, 4) || !aligned(out_blocks, 4) || (out_counts && !aligned(out_counts, 4))) return SAI_ERR_ALIGN;
+  int dev, sms;
+  int* st;
+  if (!device_setup(&dev, &st, &sms)) return SAI_ERR_CUDA;
+  return cuda_status(sai::launch_sparse_blocks(slots, static_cast<int>(rows), k, block_size, out_blocks, out_counts,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}

@@ -68,6 +68,10 @@ struct MergeLaunch {
 };
 cudaError_t launch_merge(const MergeLaunch& p, cudaStream_t stream);
 
+// Per-row distinct blocks of top-k slots (sparse_blocks.cu).
+cudaError_t launch_sparse_blocks(const int32_t* slots, int rows, int k, int block_size, int32_t* out_blocks,
+                                 int32_t* out_counts, cudaStream_t stream);
+
 struct FusedLaunch {
   const uint8_t* q;        // [rows, 64, 128] e4m3
   const float* w;          // [rows, 64]

@@ -75,3 +75,16 @@ def test_host_validation(lib):
 def test_workspace_query_without_args(lib):
     assert lib.sai_topk_transform_workspace(0, 100, 512) == 0
     assert lib.sai_topk_transform_workspace(10, 100, 256) == 0
+
+
+def test_sparse_blocks_argument_errors(lib):
+    out = ctypes.c_void_p(1 << 20)
+    slots = ctypes.c_void_p(1 << 20)
+    assert lib.sai_sparse_blocks(slots, 4, 0, 128, out, None, None) == -2    # k < 1
+    assert lib.sai_sparse_blocks(slots, 4, 513, 128, out, None, None) == -2  # k > 512
+    assert lib.sai_sparse_blocks(slots, 4, 512, 0, out, None, None) == -2    # block_size < 1
+    assert lib.sai_sparse_blocks(slots, -1, 512, 128, out, None, None) == -2
+    assert lib.sai_sparse_blocks(None, 4, 512, 128, out, None, None) == -1
+    assert lib.sai_sparse_blocks(slots, 4, 512, 128, None, None, None) == -1
+    assert lib.sai_sparse_blocks(ctypes.c_void_p((1 << 20) + 2), 4, 512, 128, out, None, None) == -7
+    assert lib.sai_sparse_blocks(None, 0, 512, 128, None, None, None) == 0  # nothing to do
