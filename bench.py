@@ -263,6 +263,28 @@ def build_fused_part(dev, name: str, inp, group_rows: int):
     return part
 
 
+def build_sparse_blocks_part(dev):
+    """Per-row block lists of a packed-extend-sized top-k output: 16384 rows
+    of 512 token slots of a 140000-slot pool (page_size 1), 128-token blocks.
+    Not part of the default step (a follow-on of the top-k)."""
+    import torch
+
+    rng = np.random.default_rng(6)
+    rows = 16384
+    slots = rng.integers(0, 140000, size=(rows, K)).astype(np.int32)
+    part = Part("sparse_blocks")
+    part.host = {"slots": _pin(slots)}
+    part.dev = {k: v.to(dev) for k, v in part.host.items()}
+    part.out = {"blocks": torch.empty((rows, K), dtype=torch.int32, device=dev),
+                "counts": torch.empty((rows,), dtype=torch.int32, device=dev)}
+    part.rows = rows
+    part.keys = float(rows * K)
+    part.bytes = rows * K * 4 * 2 + rows * 4
+    part.launches = 1
+    part.meta = dict(slots=slots)
+    return part
+
+
 def build_parts(dev, args):
     import workloads as W
 
@@ -273,6 +295,8 @@ def build_parts(dev, args):
         parts.append(build_fused_part(dev, "fused_decode", W.fused_decode(), 1))
     if "fused_prefill" in args.paths:
         parts.append(build_fused_part(dev, "fused_prefill", W.fused_prefill(rows=args.prefill_rows), 4))
+    if "sparse_blocks" in args.paths:
+        parts.append(build_sparse_blocks_part(dev))
     return parts
 
 
@@ -280,7 +304,9 @@ def launch_part(part, stream):
     import sparse_attention_indexer_top_gb300 as sai
 
     d, o = part.dev, part.out
-    if part.name == "topk_packed_extend":
+    if part.name == "sparse_blocks":
+        sai.sparse_blocks(d["slots"], 128, out_blocks=o["blocks"], out_counts=o["counts"], stream=stream)
+    elif part.name == "topk_packed_extend":
         sai.topk_transform(d["scores"], d["seq_lens"], d["page_tables"], row_starts=d["row_starts"],
                            row_to_batch=d["row_to_batch"], out_slots=o["slots"], stream=stream)
     else:
@@ -298,7 +324,18 @@ def oracle_part_rate(part_name, meta, budget_s):
     from oracle.topk import topk_transform as oracle_topk
 
     done, spent = 0, 0.0
-    if part_name == "topk_packed_extend":
+    if part_name == "sparse_blocks":
+        from oracle.blocks import sparse_blocks as oracle_blocks
+
+        slots = meta["slots"]
+        for i in range(0, slots.shape[0], 64):
+            t0 = time.perf_counter()
+            oracle_blocks(slots[i:i + 64], 128)
+            spent += time.perf_counter() - t0
+            done += 64
+            if spent > budget_s:
+                break
+    elif part_name == "topk_packed_extend":
         rows = int(meta["seq_lens"].size)
         for i in np.linspace(0, rows - 1, 4000).astype(np.int64):
             n = int(meta["seq_lens"][i])

@@ -58,3 +58,15 @@ def test_blocks_of_a_topk_output():
                                row_starts=inp.row_starts, row_to_batch=inp.row_to_batch)
     assert np.array_equal(s, ref_slots)
     _check(s, 128)
+
+
+@pytest.mark.parametrize("block_size", [1, 128])
+def test_wide_block_ranges_take_the_sorting_path(block_size):
+    # blocks spread over more than 16384 ids: the bitmap does not apply
+    rng = np.random.default_rng(200 + block_size)
+    rows, k = 21, 512
+    slots = rng.integers(0, 1 << 30, size=(rows, k)).astype(np.int32)
+    slots[2] = slots[2] % 5000 + (1 << 29)  # narrow again: one row on the bitmap path
+    slots[3, 100:] = slots[3, :412]        # duplicates on the sorting path
+    slots[4, ::2] = -1
+    _check(slots, block_size)
