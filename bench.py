@@ -221,7 +221,11 @@ def build_topk_part(dev, new_tokens: int):
     part.host = {"scores": host, "seq_lens": _pin(seq_lens), "row_starts": _pin(row_starts),
                  "row_to_batch": _pin(r2b), "page_tables": _pin(pt)}
     part.dev = {k: v.to(dev) for k, v in part.host.items()}
-    part.out = {"slots": torch.empty((rows, K), dtype=torch.int32, device=dev)}
+    import sparse_attention_indexer_top_gb300 as sai
+
+    ws = sai.topk_transform_workspace(rows, width)
+    part.out = {"slots": torch.empty((rows, K), dtype=torch.int32, device=dev),
+                "workspace": torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)}
     part.rows = rows
     part.keys = float(seq_lens.astype(np.int64).sum())
     part.bytes = part.keys * 4 + pt.nbytes + rows * (3 * 4 + K * 4)
@@ -263,6 +267,33 @@ def build_fused_part(dev, name: str, inp, group_rows: int):
     return part
 
 
+def build_topk_decode_part(dev):
+    """The decode-layout top-k: 128 rows, seq_lens U[8192, 32768], bf16-rounded
+    N(0,1) scores in a [128, 32768] buffer (ties certain), 128-token pages
+    (slot = block*128 + idx%128). Few long rows: split over CTAs + merge.
+    Not part of the default step (it is launch-latency bound)."""
+    import torch
+
+    import workloads as W
+
+    inp = W.decode_topk()
+    part = Part("topk_decode")
+    part.host = {"scores": _pin(inp.scores), "seq_lens": _pin(inp.seq_lens), "page_tables": _pin(inp.page_tables)}
+    part.dev = {k: v.to(dev) for k, v in part.host.items()}
+    import sparse_attention_indexer_top_gb300 as sai
+
+    rows = int(inp.seq_lens.size)
+    ws = sai.topk_transform_workspace(rows, inp.scores.shape[1])
+    part.out = {"slots": torch.empty((rows, K), dtype=torch.int32, device=dev),
+                "workspace": torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)}
+    part.rows = rows
+    part.keys = float(inp.seq_lens.astype(np.int64).sum())
+    part.bytes = part.keys * 4 + rows * (4 + K * 4 + K * 4)  # scores, lens, slots, <= k table reads
+    part.launches = 2
+    part.meta = dict(inp=inp)
+    return part
+
+
 def build_sparse_blocks_part(dev):
     """Per-row block lists of a packed-extend-sized top-k output: 16384 rows
     of 512 token slots of a 140000-slot pool (page_size 1), 128-token blocks.
@@ -297,6 +328,8 @@ def build_parts(dev, args):
         parts.append(build_fused_part(dev, "fused_prefill", W.fused_prefill(rows=args.prefill_rows), 4))
     if "sparse_blocks" in args.paths:
         parts.append(build_sparse_blocks_part(dev))
+    if "topk_decode" in args.paths:
+        parts.append(build_topk_decode_part(dev))
     return parts
 
 
@@ -306,9 +339,13 @@ def launch_part(part, stream):
     d, o = part.dev, part.out
     if part.name == "sparse_blocks":
         sai.sparse_blocks(d["slots"], 128, out_blocks=o["blocks"], out_counts=o["counts"], stream=stream)
+    elif part.name == "topk_decode":
+        sai.topk_transform(d["scores"], d["seq_lens"], d["page_tables"], page_size=128, out_slots=o["slots"],
+                           workspace=o["workspace"], stream=stream)
     elif part.name == "topk_packed_extend":
         sai.topk_transform(d["scores"], d["seq_lens"], d["page_tables"], row_starts=d["row_starts"],
-                           row_to_batch=d["row_to_batch"], out_slots=o["slots"], stream=stream)
+                           row_to_batch=d["row_to_batch"], out_slots=o["slots"], workspace=o["workspace"],
+                           stream=stream)
     else:
         sai.index_score_topk(d["q"], d["w"], d["kcache"], d["kscale"], d["block_table"], d["seq_lens"],
                              max_seq_len=part.meta["max_len"], row_to_batch=d.get("row_to_batch"),
@@ -333,6 +370,16 @@ def oracle_part_rate(part_name, meta, budget_s):
             oracle_blocks(slots[i:i + 64], 128)
             spent += time.perf_counter() - t0
             done += 64
+            if spent > budget_s:
+                break
+    elif part_name == "topk_decode":
+        inp = meta["inp"]
+        for i in range(inp.seq_lens.size):
+            n = int(inp.seq_lens[i])
+            t0 = time.perf_counter()
+            oracle_topk(inp.scores[i:i + 1, :n], np.array([n]), inp.page_tables[i:i + 1], 128, K)
+            spent += time.perf_counter() - t0
+            done += 1
             if spent > budget_s:
                 break
     elif part_name == "topk_packed_extend":
