@@ -10,8 +10,9 @@ it; only the seeded input generators in ``workloads`` serve both.
 Modules
 -------
 ``fp8``    OCP E4M3FN decoding written from the format's bit definition.
+``bf16``   bfloat16 decoding written from the format's bit definition.
 ``topk``   per-row window top-k (stable sort) and the page-table transform.
-``score``  the FP8 index score and the fused score + top-k.
+``score``  the index score (FP8 or bf16 cache) and the fused score + top-k.
 ``brute``  O(n^2) rank-rule selection, used only to pin ``topk``.
 ``blocks`` per-row distinct KV blocks of the selected slots.
 
@@ -20,6 +21,7 @@ brute force, invariants or library routines; none is "parity unpinned".
 """
 
 from .fp8 import e4m3fn_decode, e4m3fn_units  # noqa: F401
+from .bf16 import bf16_decode  # noqa: F401
 from .topk import topk_row, page_transform, topk_transform  # noqa: F401
 from .score import index_scores_row, index_scores, index_score_topk  # noqa: F401
 from .brute import rank_select_bruteforce  # noqa: F401

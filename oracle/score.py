@@ -22,6 +22,13 @@ below 2^53 units. The dot products are therefore formed EXACTLY as float64
 integer matrix products (any summation order is exact); relu, the w-weighted
 head sum and the scale are applied in float64, and the result is rounded once
 to fp32.
+
+bfloat16 index cache (the "auto" cache type, which is the model dtype): q and
+the keys are bfloat16 bit patterns (``inp.dtype == "bf16"``). Each product of
+two bfloat16 values has at most 16 significant bits and is exact in float64;
+the 128-term sums are float64 (rounding error below 2^-46 of the sum of the
+products' magnitudes), then the same relu, head sum and scale follow. A bf16
+cache carries no per-key scale in the pages; ``kscale=None`` means scale 1.
 """
 
 from __future__ import annotations
@@ -30,6 +37,7 @@ from typing import Optional, Sequence
 
 import numpy as np
 
+from .bf16 import bf16_finite
 from .fp8 import e4m3fn_units
 from .topk import page_transform, topk_row
 
@@ -37,30 +45,47 @@ _PROD_UNIT = 2.0 ** -18  # one unit of an e4m3 x e4m3 product
 _MAX_UNITS = 229376  # 448 / 2^-9
 
 
-def _key_units(kcache: np.ndarray, bt_row: np.ndarray, n: int, block_size: int):
+def _units(codes: np.ndarray, dtype: str) -> np.ndarray:
+    """float64 operand values: e4m3 in integer units of 2^-9, bf16 as values."""
+    if dtype == "e4m3":
+        return e4m3fn_units(codes).astype(np.float64)
+    if dtype == "bf16":
+        return bf16_finite(codes)
+    raise ValueError(f"unknown index cache dtype {dtype!r}")
+
+
+def _key_units(kcache: np.ndarray, bt_row: np.ndarray, n: int, block_size: int, dtype: str = "e4m3"):
     t = np.arange(n, dtype=np.int64)
     pages = np.asarray(bt_row, dtype=np.int64)[t // block_size]
-    return e4m3fn_units(kcache[pages, t % block_size, :]).astype(np.float64), pages, t % block_size
+    return _units(kcache[pages, t % block_size, :], dtype), pages, t % block_size
 
 
-def _scores_from_units(qu: np.ndarray, w: np.ndarray, ku: np.ndarray, scale: np.ndarray) -> np.ndarray:
-    """qu [H, D] and ku [n, D] integer-valued float64; returns fp32 [n]."""
-    assert qu.shape[1] * _MAX_UNITS * _MAX_UNITS < 2.0 ** 53
-    s_units = qu @ ku.T  # [H, n], exact integers
-    relu = np.maximum(s_units * _PROD_UNIT, 0.0)  # power-of-two scaling is exact
+def _scale_of(kscale, pages, offs) -> np.ndarray:
+    if kscale is None:
+        return np.ones(pages.shape, np.float64)
+    return kscale[pages, offs]
+
+
+def _scores_from_units(qu: np.ndarray, w: np.ndarray, ku: np.ndarray, scale: np.ndarray,
+                       dtype: str = "e4m3") -> np.ndarray:
+    """qu [H, D] and ku [n, D] float64 operands; returns fp32 [n]."""
+    if dtype == "e4m3":
+        assert qu.shape[1] * _MAX_UNITS * _MAX_UNITS < 2.0 ** 53
+        relu = np.maximum((qu @ ku.T) * _PROD_UNIT, 0.0)  # exact integers; power-of-two scaling
+    else:
+        relu = np.maximum(qu @ ku.T, 0.0)
     acc = np.asarray(w, dtype=np.float64) @ relu  # [n]
     return (acc * np.asarray(scale, dtype=np.float64)).astype(np.float32)
 
 
-def index_scores_row(q_row: np.ndarray, w_row: np.ndarray, kcache: np.ndarray, kscale: np.ndarray,
-                     bt_row: np.ndarray, n: int) -> np.ndarray:
+def index_scores_row(q_row: np.ndarray, w_row: np.ndarray, kcache: np.ndarray, kscale: Optional[np.ndarray],
+                     bt_row: np.ndarray, n: int, dtype: str = "e4m3") -> np.ndarray:
     """Scores of one query row against its first ``n`` keys (fp32 [n])."""
     block_size = kcache.shape[1]
     if n <= 0:
         return np.zeros(0, np.float32)
-    ku, pages, offs = _key_units(kcache, bt_row, n, block_size)
-    qu = e4m3fn_units(q_row).astype(np.float64)
-    return _scores_from_units(qu, w_row, ku, kscale[pages, offs])
+    ku, pages, offs = _key_units(kcache, bt_row, n, block_size, dtype)
+    return _scores_from_units(_units(q_row, dtype), w_row, ku, _scale_of(kscale, pages, offs), dtype)
 
 
 def index_scores(inp, rows: Optional[Sequence[int]] = None) -> list:
@@ -69,6 +94,7 @@ def index_scores(inp, rows: Optional[Sequence[int]] = None) -> list:
     Rows that share a block-table row reuse the gathered keys.
     """
     rows = list(range(inp.rows)) if rows is None else list(rows)
+    dtype = getattr(inp, "dtype", "e4m3")
     out = [None] * len(rows)
     by_batch = {}
     for j, i in enumerate(rows):
@@ -80,13 +106,13 @@ def index_scores(inp, rows: Optional[Sequence[int]] = None) -> list:
             for j in js:
                 out[j] = np.zeros(0, np.float32)
             continue
-        ku, pages, offs = _key_units(inp.kcache, inp.block_table[b], nmax, inp.block_size)
-        scale = inp.kscale[pages, offs]
+        ku, pages, offs = _key_units(inp.kcache, inp.block_table[b], nmax, inp.block_size, dtype)
+        scale = _scale_of(inp.kscale, pages, offs)
         for j in js:
             i = rows[j]
             n = int(inp.seq_lens[i])
-            qu = e4m3fn_units(inp.q[i]).astype(np.float64)
-            out[j] = _scores_from_units(qu, inp.w[i], ku[:n], scale[:n]) if n > 0 else np.zeros(0, np.float32)
+            qu = _units(inp.q[i], dtype)
+            out[j] = _scores_from_units(qu, inp.w[i], ku[:n], scale[:n], dtype) if n > 0 else np.zeros(0, np.float32)
     return out
 
 

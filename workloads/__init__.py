@@ -9,6 +9,7 @@ from .gen import (  # noqa: F401
     TopkInputs,
     FusedInputs,
     e4m3fn_encode,
+    bf16_encode,
     make_topk_inputs,
     make_fused_inputs,
     tiny_decode,

@@ -58,6 +58,14 @@ def e4m3fn_encode(x: np.ndarray) -> np.ndarray:
     return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
 
 
+def bf16_encode(x: np.ndarray) -> np.ndarray:
+    """Round fp32 values to bfloat16 bit patterns (uint16) with torch's RNE cast."""
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+
+
 def _bf16_round(x: np.ndarray) -> np.ndarray:
     import torch
 
@@ -238,9 +246,9 @@ def packed_extend(seed: int = 3, reqs: int = 2, new_tokens: int = 8192, kv_len: 
 class FusedInputs:
     """Inputs of one ``index_score_topk`` call (host arrays)."""
 
-    q: np.ndarray  # [rows, heads, dim] uint8 (e4m3fn codes)
+    q: np.ndarray  # [rows, heads, dim] uint8 e4m3fn codes (or uint16 bf16 bits)
     w: np.ndarray  # [rows, heads] float32
-    kcache: np.ndarray  # [blocks, block_size, dim] uint8 (e4m3fn codes)
+    kcache: np.ndarray  # [blocks, block_size, dim] uint8 e4m3fn codes (or uint16 bf16 bits)
     kscale: np.ndarray  # [blocks, block_size] float32
     block_table: np.ndarray  # [bt_rows, bt_stride] int32
     seq_lens: np.ndarray  # [rows] int32 (causal length per query row)
@@ -248,6 +256,7 @@ class FusedInputs:
     k: int = K_TOP
     name: str = ""
     extra: dict = field(default_factory=dict)
+    dtype: str = "e4m3"  # element type of q and kcache: "e4m3" or "bf16"
 
     @property
     def rows(self) -> int:
@@ -269,23 +278,25 @@ class FusedInputs:
 def make_fused_inputs(seed: int, rows: int, heads: int, dim: int, num_blocks: int,
                       seq_lens, block_table_shape, row_to_batch=None, block_size: int = KV_BLOCK,
                       q_std: float = 0.25, k_std: float = 0.25, k: int = K_TOP,
-                      name: str = "", kind: str = "normal") -> FusedInputs:
-    """q, k ~ e4m3(N(0,1)*std); w ~ U(0,1)/8; kscale ~ U(0.5,2); block table =
-    a permutation of the pool's block ids reshaped to ``block_table_shape``.
+                      name: str = "", kind: str = "normal", dtype: str = "e4m3") -> FusedInputs:
+    """q, k ~ e4m3(N(0,1)*std) (or bf16 with ``dtype="bf16"``); w ~ U(0,1)/8;
+    kscale ~ U(0.5,2); block table = a permutation of the pool's block ids
+    reshaped to ``block_table_shape``.
 
     ``kind="int"`` draws small integer-valued q and k (exact in e4m3) with
     w = 1 and kscale = 1, so every score is an exact integer.
     ``kind="zero_q"`` makes q all zero (every score 0).
     """
     seq_lens = np.asarray(seq_lens, dtype=np.int32)
+    enc = {"e4m3": e4m3fn_encode, "bf16": bf16_encode}[dtype]
     if kind == "int":
-        q = e4m3fn_encode(_rng(seed, 401).integers(-3, 4, size=(rows, heads, dim)).astype(np.float32))
-        kc = e4m3fn_encode(_rng(seed, 402).integers(-3, 4, size=(num_blocks, block_size, dim)).astype(np.float32))
+        q = enc(_rng(seed, 401).integers(-3, 4, size=(rows, heads, dim)).astype(np.float32))
+        kc = enc(_rng(seed, 402).integers(-3, 4, size=(num_blocks, block_size, dim)).astype(np.float32))
         w = np.ones((rows, heads), np.float32)
         ks = np.ones((num_blocks, block_size), np.float32)
     else:
-        q = e4m3fn_encode(_rng(seed, 401).standard_normal((rows, heads, dim), dtype=np.float32) * np.float32(q_std))
-        kc = e4m3fn_encode(_rng(seed, 402).standard_normal((num_blocks, block_size, dim), dtype=np.float32) * np.float32(k_std))
+        q = enc(_rng(seed, 401).standard_normal((rows, heads, dim), dtype=np.float32) * np.float32(q_std))
+        kc = enc(_rng(seed, 402).standard_normal((num_blocks, block_size, dim), dtype=np.float32) * np.float32(k_std))
         w = (_rng(seed, 403).random((rows, heads), dtype=np.float32) / np.float32(8.0)).astype(np.float32)
         ks = (np.float32(0.5) + np.float32(1.5) * _rng(seed, 404).random((num_blocks, block_size), dtype=np.float32)).astype(np.float32)
         if kind == "zero_q":
@@ -297,7 +308,7 @@ def make_fused_inputs(seed: int, rows: int, heads: int, dim: int, num_blocks: in
         raise ValueError("block table larger than the block pool")
     bt = perm[:need].reshape(bt_rows, bt_stride).copy()
     r2b = None if row_to_batch is None else np.asarray(row_to_batch, dtype=np.int32)
-    return FusedInputs(q, w, kc, ks, bt, seq_lens, r2b, k, name)
+    return FusedInputs(q, w, kc, ks, bt, seq_lens, r2b, k, name, dtype=dtype)
 
 
 def fused_decode(seed: int = 4, rows: int = 64, min_len: int = 4096, max_len: int = 32768,
