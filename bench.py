@@ -243,6 +243,9 @@ def build_fused_part(dev, name: str, inp, group_rows: int):
     if inp.row_to_batch is not None:
         arrays["row_to_batch"] = inp.row_to_batch
     part.host = {k: _pin(v) for k, v in arrays.items()}
+    if inp.dtype == "bf16":  # uint16 bit patterns, handed over as torch.bfloat16
+        for k in ("q", "kcache"):
+            part.host[k] = _pin(arrays[k].view(np.int16)).view(torch.bfloat16)
     part.dev = {k: v.to(dev) for k, v in part.host.items()}
     rows = inp.rows
     part.out = {"slots": torch.empty((rows, K), dtype=torch.int32, device=dev),
@@ -257,10 +260,12 @@ def build_fused_part(dev, name: str, inp, group_rows: int):
     n = inp.seq_lens.astype(np.int64)
     part.keys = float(n.sum())
     h, d = inp.heads, inp.dim
-    # each key's fp8 row + its scale, read once per row group; q, w; block ids; outputs
+    # each key's row (fp8 or bf16) + its scale, read once per row group; q, w;
+    # block ids; outputs
     groups = -(-rows // group_rows)
     key_reads = float(sum(int(n[g * group_rows:(g + 1) * group_rows].max()) for g in range(groups)))
-    part.bytes = key_reads * (d + 4) + inp.q.nbytes + inp.w.nbytes + (key_reads / 128) * 4 + rows * K * 12
+    part.bytes = (key_reads * (d * inp.kcache.itemsize + 4) + inp.q.nbytes + inp.w.nbytes + (key_reads / 128) * 4
+                  + rows * K * 12)
     part.flops = part.keys * h * d * 2.0
     part.launches = 2
     part.meta = dict(inp=inp, group_rows=group_rows, max_len=max_len)
@@ -326,6 +331,11 @@ def build_parts(dev, args):
         parts.append(build_fused_part(dev, "fused_decode", W.fused_decode(), 1))
     if "fused_prefill" in args.paths:
         parts.append(build_fused_part(dev, "fused_prefill", W.fused_prefill(rows=args.prefill_rows), 4))
+    if "fused_decode_bf16" in args.paths:
+        parts.append(build_fused_part(dev, "fused_decode_bf16", W.fused_decode(dtype="bf16"), 1))
+    if "fused_prefill_bf16" in args.paths:
+        parts.append(build_fused_part(dev, "fused_prefill_bf16", W.fused_prefill(rows=args.prefill_rows, dtype="bf16"),
+                                      4))
     if "sparse_blocks" in args.paths:
         parts.append(build_sparse_blocks_part(dev))
     if "topk_decode" in args.paths:
@@ -434,6 +444,11 @@ def run_reference(args):
     if "fused_prefill" in args.paths:
         inp = W.fused_prefill(rows=args.prefill_rows)
         metas.append(("fused_prefill", inp.rows, dict(inp=inp)))
+    for dt_name, make in (("fused_decode_bf16", lambda: W.fused_decode(dtype="bf16")),
+                          ("fused_prefill_bf16", lambda: W.fused_prefill(rows=args.prefill_rows, dtype="bf16"))):
+        if dt_name in args.paths:
+            inp = make()
+            metas.append((dt_name, inp.rows, dict(inp=inp)))
     budget = max(3.0, 150.0 / max(1, args.steps + args.warmup))
     vals, note = [], ""
     for s in range(args.warmup + args.steps):
@@ -517,7 +532,10 @@ def run_gpu(args):
                  "hbm_gbs": part.bytes / (pm * 1e-3) / 1e9, "hbm_frac": part.bytes / (pm * 1e-3) / 1e9 / hbm_peak}
         if part.flops:
             entry["tflops"] = part.flops / (pm * 1e-3) / 1e12
-            entry["fp8_frac"] = entry["tflops"] / fp8_peak
+            if part.name.endswith("_bf16"):
+                entry["bf16_frac"] = entry["tflops"] / bf16_peak
+            else:
+                entry["fp8_frac"] = entry["tflops"] / fp8_peak
         paths[part.name] = entry
     # the dominant kernel's roofline
     top = int(np.argmax(part_ms))
@@ -525,6 +543,9 @@ def run_gpu(args):
     if tp.name == "fused_prefill":
         roof = {"bound": "tensor", "achieved": tp.flops / (tm * 1e-3) / 1e12, "peak": fp8_peak, "unit": "TFLOP/s",
                 "peak_kind": f"{peak_kind} bf16 burst x {FP8_OVER_BF16} (nominal fp8/bf16)"}
+    elif tp.name == "fused_prefill_bf16":
+        roof = {"bound": "tensor", "achieved": tp.flops / (tm * 1e-3) / 1e12, "peak": bf16_peak, "unit": "TFLOP/s",
+                "peak_kind": f"{peak_kind} bf16 burst"}
     else:
         roof = {"bound": "hbm", "achieved": tp.bytes / (tm * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
                 "peak_kind": peak_kind}

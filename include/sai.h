@@ -175,6 +175,36 @@ int sai_index_score(const uint8_t* q_fp8, const float* w, const uint8_t* kcache_
                     int64_t out_stride, sai_stream_t stream);
 
 /*
+ * sai_index_score_topk_bf16 / sai_index_score_bf16 -- the same two calls for
+ * a bf16 index cache.
+ *
+ * The index cache may be kept at the model dtype instead of FP8 (ROCm/ATOM PR
+ * #1473: the index-cache type option whose default "auto" is the model dtype,
+ * and its commit "convert auto for bf16 type"; FP8 only when the KV cache
+ * dtype is an fp8 one). Then q and the keys are bfloat16 bit patterns and the
+ * dot products run in bf16 with fp32 accumulation; the score, selection,
+ * outputs, workspace (sai_index_score_topk_workspace) and status bits are those
+ * of the FP8 calls.
+ *
+ * q_bf16       bf16 [rows, heads, dim], 16-byte aligned.
+ * kcache_bf16  bf16 [num_blocks, block_size, dim], 16-byte aligned.
+ * kscale       fp32 [num_blocks, block_size], or NULL: the pages give a bf16
+ *              cache no per-key scale, and NULL means scale 1.
+ * Other arguments as for sai_index_score_topk / sai_index_score.
+ */
+int sai_index_score_topk_bf16(const uint16_t* q_bf16, const float* w, const uint16_t* kcache_bf16,
+                              const float* kscale, int64_t num_blocks, const int32_t* block_table, int64_t bt_rows,
+                              int64_t bt_stride, const int32_t* row_to_batch, const int32_t* seq_lens, int64_t rows,
+                              int32_t heads, int32_t dim, int32_t block_size, int32_t max_seq_len, int32_t group_rows,
+                              int32_t k, int32_t* out_slots, int32_t* out_indices, float* out_scores,
+                              void* workspace, size_t workspace_bytes, sai_stream_t stream);
+int sai_index_score_bf16(const uint16_t* q_bf16, const float* w, const uint16_t* kcache_bf16, const float* kscale,
+                         int64_t num_blocks, const int32_t* block_table, int64_t bt_rows, int64_t bt_stride,
+                         const int32_t* row_to_batch, const int32_t* seq_lens, int64_t rows, int32_t heads,
+                         int32_t dim, int32_t block_size, int32_t max_seq_len, int32_t group_rows, float* out_scores,
+                         int64_t out_stride, sai_stream_t stream);
+
+/*
  * sai_sparse_blocks -- per-row distinct KV blocks of top-k slots.
  *
  * Follows ROCm/ATOM PR #1282 "merge build sparse block into topk" (title and

@@ -117,37 +117,45 @@ def topk_transform_noalloc(scores: torch.Tensor, seq_lens: torch.Tensor, page_ta
 
 
 def _fused_check(q, w, kcache, kscale, block_table, seq_lens, row_to_batch):
+    """Argument checks of the fused calls; returns (device, bf16). The element
+    type follows ``q``: uint8 e4m3 codes (FP8 index cache) or torch.bfloat16
+    (bf16 index cache, where ``kscale`` may be None)."""
     dev = q.device
-    _need(q, "q", torch.uint8, dev, 3)
+    bf16 = q.dtype == torch.bfloat16
+    elem = torch.bfloat16 if bf16 else torch.uint8
+    _need(q, "q", elem, dev, 3)
     _need(w, "w", torch.float32, dev, 2)
-    _need(kcache, "kcache", torch.uint8, dev, 3)
-    _need(kscale, "kscale", torch.float32, dev, 2)
+    _need(kcache, "kcache", elem, dev, 3)
+    if kscale is None and not bf16:
+        raise ValueError("kscale is required for an FP8 index cache")
     _need(block_table, "block_table", torch.int32, dev, 2)
     _need(seq_lens, "seq_lens", torch.int32, dev, 1)
     _need(row_to_batch, "row_to_batch", torch.int32, dev, 1)
+    _need(kscale, "kscale", torch.float32, dev, 2)
     for name, t in (("q", q), ("w", w), ("kcache", kcache), ("kscale", kscale), ("seq_lens", seq_lens)):
-        if not t.is_contiguous():
+        if t is not None and not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
     if block_table.stride(1) != 1:
         raise ValueError("block_table needs unit column stride")
-    return dev
+    return dev, bf16
 
 
 def index_score_topk_workspace(rows: int, max_seq_len: int, group_rows: int = 1, k: int = TOPK) -> int:
     return int(load().sai_index_score_topk_workspace(int(rows), int(max_seq_len), int(group_rows), int(k)))
 
 
-def index_score_topk(q: torch.Tensor, w: torch.Tensor, kcache: torch.Tensor, kscale: torch.Tensor,
+def index_score_topk(q: torch.Tensor, w: torch.Tensor, kcache: torch.Tensor, kscale: Optional[torch.Tensor],
                      block_table: torch.Tensor, seq_lens: torch.Tensor, *, max_seq_len: int,
                      row_to_batch: Optional[torch.Tensor] = None, group_rows: int = 1, k: int = TOPK,
                      out_slots: Optional[torch.Tensor] = None, out_indices: Optional[torch.Tensor] = None,
                      out_scores: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                      stream=None):
-    """Fused FP8 index score + top-k. ``q`` e4m3 codes (uint8) ``[rows, 64,
+    """Fused index score + top-k. ``q`` e4m3 codes (uint8) ``[rows, 64,
     128]``, ``w`` fp32 ``[rows, 64]``, ``kcache`` uint8 ``[blocks, 128, 128]``,
-    ``kscale`` fp32 ``[blocks, 128]``, ``block_table`` int32. Returns
-    ``(slots, indices, scores)``."""
-    dev = _fused_check(q, w, kcache, kscale, block_table, seq_lens, row_to_batch)
+    ``kscale`` fp32 ``[blocks, 128]``, ``block_table`` int32; or ``q`` and
+    ``kcache`` torch.bfloat16 (bf16 index cache, ``kscale`` optional).
+    Returns ``(slots, indices, scores)``."""
+    dev, bf16 = _fused_check(q, w, kcache, kscale, block_table, seq_lens, row_to_batch)
     rows = q.shape[0]
     if out_slots is None:
         out_slots = torch.empty((rows, k), dtype=torch.int32, device=dev)
@@ -158,30 +166,33 @@ def index_score_topk(q: torch.Tensor, w: torch.Tensor, kcache: torch.Tensor, ksc
     ws = index_score_topk_workspace(rows, max_seq_len, group_rows, k) if rows else 0
     if workspace is None and ws:
         workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
-    st = load().sai_index_score_topk(
+    name = "sai_index_score_topk_bf16" if bf16 else "sai_index_score_topk"
+    st = getattr(load(), name)(
         _ptr(q), _ptr(w), _ptr(kcache), _ptr(kscale), kcache.shape[0], _ptr(block_table), block_table.shape[0],
         block_table.stride(0), _ptr(row_to_batch), _ptr(seq_lens), rows, q.shape[1], q.shape[2], kcache.shape[1],
         int(max_seq_len), int(group_rows), int(k), _ptr(out_slots), _ptr(out_indices), _ptr(out_scores),
         _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream(stream))
-    check(st, "sai_index_score_topk")
+    check(st, name)
     return out_slots, out_indices, out_scores
 
 
-def index_score(q: torch.Tensor, w: torch.Tensor, kcache: torch.Tensor, kscale: torch.Tensor,
+def index_score(q: torch.Tensor, w: torch.Tensor, kcache: torch.Tensor, kscale: Optional[torch.Tensor],
                 block_table: torch.Tensor, seq_lens: torch.Tensor, *, max_seq_len: int,
                 row_to_batch: Optional[torch.Tensor] = None, group_rows: int = 1, out: Optional[torch.Tensor] = None,
                 stream=None) -> torch.Tensor:
-    """Dense FP8 index scores ``[rows, max_seq_len]`` (cells past each row's
-    length are left as they were; a new ``out`` starts as NaN)."""
-    dev = _fused_check(q, w, kcache, kscale, block_table, seq_lens, row_to_batch)
+    """Dense index scores ``[rows, max_seq_len]`` (FP8 or bf16 cache, as for
+    ``index_score_topk``; cells past each row's length are left as they were;
+    a new ``out`` starts as NaN)."""
+    dev, bf16 = _fused_check(q, w, kcache, kscale, block_table, seq_lens, row_to_batch)
     rows = q.shape[0]
     if out is None:
         out = torch.full((rows, max(max_seq_len, 1)), float("nan"), dtype=torch.float32, device=dev)
-    st = load().sai_index_score(
+    name = "sai_index_score_bf16" if bf16 else "sai_index_score"
+    st = getattr(load(), name)(
         _ptr(q), _ptr(w), _ptr(kcache), _ptr(kscale), kcache.shape[0], _ptr(block_table), block_table.shape[0],
         block_table.stride(0), _ptr(row_to_batch), _ptr(seq_lens), rows, q.shape[1], q.shape[2], kcache.shape[1],
         int(max_seq_len), int(group_rows), _ptr(out), out.stride(0), _stream(stream))
-    check(st, "sai_index_score")
+    check(st, name)
     return out
 
 

@@ -27,6 +27,11 @@ SIGNATURES = {
                                             _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _vp, _vp, _vp, _vp, _c_size, _vp]),
     "sai_index_score": (ctypes.c_int, [_vp, _vp, _vp, _vp, _c_i64, _vp, _c_i64, _c_i64, _vp, _vp, _c_i64, _c_i32, _c_i32,
                                        _c_i32, _c_i32, _c_i32, _vp, _c_i64, _vp]),
+    "sai_index_score_topk_bf16": (ctypes.c_int, [_vp, _vp, _vp, _vp, _c_i64, _vp, _c_i64, _c_i64, _vp, _vp, _c_i64,
+                                                 _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _vp, _vp, _vp, _vp,
+                                                 _c_size, _vp]),
+    "sai_index_score_bf16": (ctypes.c_int, [_vp, _vp, _vp, _vp, _c_i64, _vp, _c_i64, _c_i64, _vp, _vp, _c_i64, _c_i32,
+                                            _c_i32, _c_i32, _c_i32, _c_i32, _vp, _c_i64, _vp]),
     "sai_topk_transform_noalloc": (ctypes.c_int, [_vp, _c_i64, _c_i64, _vp, _vp, _vp, _c_i64, _c_i64, _vp, _c_i32,
                                                   _c_i32, _vp, _vp, _vp]),
     "sai_sparse_blocks": (ctypes.c_int, [_vp, _c_i64, _c_i32, _c_i32, _vp, _vp, _vp]),

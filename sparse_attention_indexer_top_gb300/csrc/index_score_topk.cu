@@ -32,6 +32,13 @@
 //     shared memory when they fill up).
 // The per-(row, chunk) candidate lists go to a workspace; the merge kernel
 // of topk_transform.cu then selects, sorts and page-transforms each row.
+//
+// bf16 index cache (the "auto" cache type of the same pull request, i.e. the
+// model dtype): q and the keys are bf16, the MMA is kind::f16 (K = 16 per
+// instruction) and a 256-byte key row is staged as two 128-byte-swizzled
+// halves of 64 dims (one TMA box each), so the MMA walks 2 x 4 K-steps; the
+// relu is a plain max (bf16 dot products have no fixed range), and the key
+// scale may be absent (scale 1). Everything else is shared with the FP8 path.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -49,13 +56,15 @@ namespace sai {
 namespace {
 
 constexpr int kH = 64;        // index heads
-constexpr int kD = 128;       // head dim (bytes per fp8 row)
+constexpr int kD = 128;       // head dim (elements per row)
+constexpr int kSwB = 128;     // bytes per row of one 128-byte-swizzled region
 constexpr int kBlk = 128;     // tokens per KV block = MMA M
 // K-tile stages, query-tile buffers and resident CTAs per SM: single rows
 // (decode) run three small CTAs per SM with a 2-stage ring, row pairs
 // (prefill) two with a 3-stage ring; one query buffer each, since every CTA
 // takes one unit (measured against 2-4 stages and 2-3 CTAs per SM).
-template <int R>
+// The bf16 variant has twice the bytes per stage and runs one CTA fewer.
+template <int R, bool BF16 = false>
 __host__ __device__ constexpr int fused_stages() {
   return R == 1 ? 2 : (R == 2 ? 3 : 4);
 }
@@ -63,43 +72,55 @@ template <int R>
 __host__ __device__ constexpr int fused_qbufs() {
   return R <= 2 ? 1 : 2;
 }
-template <int R>
+template <int R, bool BF16 = false>
 __host__ __device__ constexpr int fused_ctas_per_sm() {
-  return R == 1 ? 3 : (R == 2 ? 2 : 1);
+  return BF16 ? (R == 1 ? 2 : 1) : (R == 1 ? 3 : (R == 2 ? 2 : 1));
+}
+template <bool BF16>
+__host__ __device__ constexpr int elem_bytes() {
+  return BF16 ? 2 : 1;
+}
+// 128-byte-swizzled regions per 128-dim row: 1 for FP8, 2 for bf16
+template <bool BF16>
+__host__ __device__ constexpr int sw_regions() {
+  return kD * elem_bytes<BF16>() / kSwB;
 }
 constexpr int kSub = 512;     // candidate sub-list per epilogue warp
 constexpr int kSyncEvery = 4; // tiles between the row group's count exchanges
 constexpr int kSubPruneAt = kSub - kSyncEvery * 32;
 constexpr int kEpiRow = 128;  // epilogue threads per query row (4 warps, one TMEM lane quadrant each)
 
-template <int R>
+template <int R, bool BF16>
 struct __align__(1024) FusedSmem {
-  uint8_t kst[fused_stages<R>()][kBlk * kD];  // 16 KB each, 1024-byte aligned
-  uint8_t q[fused_qbufs<R>()][R * kH * kD];   // query tiles of consecutive units
+  // a key stage / query tile is sw_regions() regions of [rows x 128 bytes]
+  uint8_t kst[fused_stages<R, BF16>()][kBlk * kD * elem_bytes<BF16>()];  // 16 KB (FP8) or 32 KB, 1024-aligned
+  uint8_t q[fused_qbufs<R>()][R * kH * kD * elem_bytes<BF16>()];          // query tiles of consecutive units
   uint32_t ckey[R][4 * kSub];  // row r: four per-warp sub-lists
   int32_t cidx[R][4 * kSub];
   uint32_t aux_key[R][kTopK];
   int32_t aux_idx[R][kTopK];
   SelectScratch sc[R];
-  uint64_t full[fused_stages<R>()], empty[fused_stages<R>()], tfull[2], tempty[2];
+  uint64_t full[fused_stages<R, BF16>()], empty[fused_stages<R, BF16>()], tfull[2], tempty[2];
   uint64_t qfull[fused_qbufs<R>()], qempty[fused_qbufs<R>()];
   uint32_t tmem_base;
   int wcnt[R][2][4];      // per-warp list sizes at a sync point (double-buffered)
 };
 
-template <int R>
+template <int R, bool BF16>
 constexpr size_t fused_smem_bytes() {
-  return sizeof(FusedSmem<R>) + 1024;
+  return sizeof(FusedSmem<R, BF16>) + 1024;
 }
 
-static_assert(3 * (fused_smem_bytes<1>() + 1024) <= 228 * 1024, "three single-row CTAs per SM");
-static_assert(2 * (fused_smem_bytes<2>() + 1024) <= 228 * 1024, "two row-pair CTAs per SM");
+static_assert(3 * (fused_smem_bytes<1, false>() + 1024) <= 228 * 1024, "three single-row CTAs per SM");
+static_assert(2 * (fused_smem_bytes<2, false>() + 1024) <= 228 * 1024, "two row-pair CTAs per SM");
+static_assert(2 * (fused_smem_bytes<1, true>() + 1024) <= 228 * 1024, "two single-row bf16 CTAs per SM");
+static_assert(fused_smem_bytes<2, true>() + 1024 <= 228 * 1024, "one row-pair bf16 CTA per SM");
 
-template <int R>
-__device__ __forceinline__ FusedSmem<R>& fused_smem(unsigned char* raw) {
+template <int R, bool BF16>
+__device__ __forceinline__ FusedSmem<R, BF16>& fused_smem(unsigned char* raw) {
   uintptr_t a = reinterpret_cast<uintptr_t>(raw);
   a = (a + 1023) & ~static_cast<uintptr_t>(1023);
-  return *reinterpret_cast<FusedSmem<R>*>(a);
+  return *reinterpret_cast<FusedSmem<R, BF16>*>(a);
 }
 
 // Row group metadata, recomputed identically by every thread.
@@ -152,23 +173,36 @@ __device__ __forceinline__ float relu_lo(uint32_t s_bits) {
   return r;
 }
 
+// relu of an FP32 accumulator: FP8 keeps it scaled by 2^-64 (exact, see
+// above); bf16 products have no such bound, so there it is a plain max.
+template <bool BF16>
+__device__ __forceinline__ float relu_of(uint32_t s_bits) {
+  if constexpr (BF16)
+    return fmaxf(__uint_as_float(s_bits), 0.f);
+  else
+    return relu_lo(s_bits);
+}
+
 template <int R>
 __host__ __device__ constexpr int fused_threads() {
   return R * kEpiRow + 64;  // R row groups of 4 epilogue warps, a TMA warp, an MMA warp
 }
 
-template <int R, bool DENSE>
-__global__ void __launch_bounds__(fused_threads<R>(), fused_ctas_per_sm<R>())
+template <int R, bool DENSE, bool BF16>
+__global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16>()))
     fused_score_topk_kernel(const __grid_constant__ FusedLaunch p, const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ unsigned char smem_raw[];
-  FusedSmem<R>& S = fused_smem<R>(smem_raw);
+  FusedSmem<R, BF16>& S = fused_smem<R, BF16>(smem_raw);
   constexpr int N = R * kH;          // MMA N
   constexpr uint32_t kCols = 2 * N;  // two accumulator buffers
-  constexpr uint32_t kIdesc = umma_idesc_e4m3(kBlk, N);
+  constexpr uint32_t kIdesc = BF16 ? umma_idesc_bf16(kBlk, N) : umma_idesc_e4m3(kBlk, N);
+  constexpr int kRegions = sw_regions<BF16>();
+  constexpr uint32_t kKeyTileBytes = kBlk * kD * elem_bytes<BF16>();
+  constexpr uint32_t kQTileBytes = N * kD * elem_bytes<BF16>();
   constexpr int kEpiWarps = 4 * R;
   constexpr int kTmaWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1;
-  constexpr int kNSf = fused_stages<R>(), kQB = fused_qbufs<R>();
+  constexpr int kNSf = fused_stages<R, BF16>(), kQB = fused_qbufs<R>();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int units = ((p.rows + R - 1) / R) * p.chunks;
 
@@ -217,8 +251,11 @@ __global__ void __launch_bounds__(fused_threads<R>(), fused_ctas_per_sm<R>())
         const int qb = qn % kQB;
         run = mbar_wait(&S.qempty[qb], ((qn / kQB) & 1u) ^ 1u);
         if (!run) break;
-        mbar_arrive_expect_tx(&S.qfull[qb], (uint32_t)(N * kD));
-        tma_load_2d(S.q[qb], &qmap, 0, m.row0 * kH, &S.qfull[qb], keep);
+        mbar_arrive_expect_tx(&S.qfull[qb], kQTileBytes);
+#pragma unroll
+        for (int h = 0; h < kRegions; ++h)  // region h: dims [64h, 64h + 64) of a bf16 row
+          tma_load_2d(S.q[qb] + h * N * kSwB, &qmap, h * (kSwB / elem_bytes<BF16>()), m.row0 * kH, &S.qfull[qb],
+                      keep);
         ++qn;
         int page_next = __ldg(bt);
         for (int i = 0; i < ntiles; ++i, ++it) {
@@ -227,8 +264,11 @@ __global__ void __launch_bounds__(fused_threads<R>(), fused_ctas_per_sm<R>())
           if (page < 0 || page >= p.num_blocks) page = 0;  // the epilogue masks this block
           const int s = it % kNSf;
           if (!(run = mbar_wait(&S.empty[s], ((it / kNSf) & 1u) ^ 1u))) break;
-          mbar_arrive_expect_tx(&S.full[s], (uint32_t)(kBlk * kD));
-          tma_load_2d(S.kst[s], &kmap, 0, page * kBlk, &S.full[s], keep);
+          mbar_arrive_expect_tx(&S.full[s], kKeyTileBytes);
+#pragma unroll
+          for (int h = 0; h < kRegions; ++h)
+            tma_load_2d(S.kst[s] + h * kBlk * kSwB, &kmap, h * (kSwB / elem_bytes<BF16>()), page * kBlk, &S.full[s],
+                        keep);
         }
       }
       if (!run) atomicOr(p.status, kDevWaitTimeout);
@@ -253,9 +293,21 @@ __global__ void __launch_bounds__(fused_threads<R>(), fused_ctas_per_sm<R>())
           if (!run) break;
           tc_fence_after();
           const uint64_t adesc = umma_desc_sw128_kmajor(smem_u32(S.kst[s]));
+          // each instruction takes 32 bytes of K (32 FP8 or 16 bf16 dims):
+          // four per 128-byte region; the descriptor start field counts 16 B
 #pragma unroll
-          for (int k = 0; k < kD / 32; ++k)
-            umma_f8(tmem + buf * N, adesc + 2 * k, bdesc + 2 * k, kIdesc, k > 0 ? 1u : 0u);
+          for (int h = 0; h < kRegions; ++h) {
+#pragma unroll
+            for (int k = 0; k < kSwB / 32; ++k) {
+              const uint64_t ad = adesc + (uint64_t)(h * kBlk * kSwB / 16 + 2 * k);
+              const uint64_t bd = bdesc + (uint64_t)(h * N * kSwB / 16 + 2 * k);
+              const uint32_t acc = (h > 0 || k > 0) ? 1u : 0u;
+              if constexpr (BF16)
+                umma_bf16(tmem + buf * N, ad, bd, kIdesc, acc);
+              else
+                umma_f8(tmem + buf * N, ad, bd, kIdesc, acc);
+            }
+          }
           umma_commit(&S.empty[s]);
           umma_commit(&S.tfull[buf]);
         }
@@ -280,6 +332,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), fused_ctas_per_sm<R>())
     // reduce-scatter over the 4 lanes sharing l/4 leaves each lane the full
     // score of one key, key kl of the block.
     const int kl = quad * 32 + (lane >> 2) + 8 * ((lane >> 1) & 1) + 16 * (lane & 1);
+    constexpr float kWScale = BF16 ? 1.f : 0x1p64f;
     bool ok = true;     // false after a pipeline wait gave up (then nothing more is waited for)
     int sync_no = 0;    // exchanges so far (the size slots alternate)
     uint32_t tt = 0;    // tiles so far (accumulator buffer and phase)
@@ -341,13 +394,17 @@ __global__ void __launch_bounds__(fused_threads<R>(), fused_ctas_per_sm<R>())
       float2 w2[8];
       const float* wr = p.w + (long long)(row_live ? m.row0 + r : 0) * kH + 2 * (lane & 3);
 #pragma unroll
-      for (int j = 0; j < 8; ++j)  // scaled by 2^64: see relu_lo below
-        w2[j] = row_live ? make_float2(__ldg(wr + 8 * j) * 0x1p64f, __ldg(wr + 8 * j + 1) * 0x1p64f)
+      for (int j = 0; j < 8; ++j)  // FP8: scaled by 2^64, see relu_lo below
+        w2[j] = row_live ? make_float2(__ldg(wr + 8 * j) * kWScale, __ldg(wr + 8 * j + 1) * kWScale)
                          : make_float2(0.f, 0.f);
-      // the key scale of the next tile is fetched one tile ahead
+      // the key scale of the next tile is fetched one tile ahead (1 when the
+      // cache has no scales)
+      auto key_scale = [&](int page) -> float {
+        return p.kscale ? __ldg(p.kscale + (long long)page * kBlk + kl) : 1.f;
+      };
       int page_next = ntiles > 0 ? __ldg(bt) : -1;
       bool ok_next = page_next >= 0 && page_next < p.num_blocks;
-      float ks_next = ok_next ? __ldg(p.kscale + (long long)page_next * kBlk + kl) : 0.f;
+      float ks_next = ok_next ? key_scale(page_next) : 0.f;
       for (int i = 0; i < ntiles; ++i, ++tt) {
         const int blk = m.blk0 + i, buf = tt & 1;
         const int t = blk * kBlk + kl;
@@ -356,7 +413,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), fused_ctas_per_sm<R>())
         if (i + 1 < ntiles) {
           page_next = __ldg(bt + i + 1);
           ok_next = page_next >= 0 && page_next < p.num_blocks;
-          ks_next = ok_next ? __ldg(p.kscale + (long long)page_next * kBlk + kl) : 0.f;
+          ks_next = ok_next ? key_scale(page_next) : 0.f;
         }
         if (!page_ok && et == 0 && r == 0) atomicOr(p.status, kDevBadPage);
         ok = ok && __all_sync(0xFFFFFFFFu, mbar_wait(&S.tfull[buf], (tt >> 1) & 1u));
@@ -382,8 +439,8 @@ __global__ void __launch_bounds__(fused_threads<R>(), fused_ctas_per_sm<R>())
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const float2 x0 = make_float2(relu_lo(a[4 * j]), relu_lo(a[4 * j + 1]));
-              const float2 x1 = make_float2(relu_lo(a[4 * j + 2]), relu_lo(a[4 * j + 3]));
+              const float2 x0 = make_float2(relu_of<BF16>(a[4 * j]), relu_of<BF16>(a[4 * j + 1]));
+              const float2 x1 = make_float2(relu_of<BF16>(a[4 * j + 2]), relu_of<BF16>(a[4 * j + 3]));
               acc[2 * half] = __ffma2_rn(x0, w2[j], acc[2 * half]);
               acc[2 * half + 1] = __ffma2_rn(x1, w2[j], acc[2 * half + 1]);
             }
@@ -465,30 +522,33 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D uint8 map over [rows, 128] with a [box_rows, 128] box, 128-byte swizzle.
-bool make_map(CUtensorMap* map, const void* base, long long rows, int box_rows) {
+// 2-D map over [rows, 128] elements (uint8 FP8 codes or bf16) with a box of
+// box_rows rows x 128 bytes (all 128 FP8 dims, or 64 bf16 dims), 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* base, long long rows, int box_rows, bool bf16) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
+  const int eb = bf16 ? 2 : 1;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD)};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kD), static_cast<cuuint32_t>(box_rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD * eb)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kSwB / eb), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+  return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base),
+            dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int R, bool DENSE>
-cudaError_t launch_fused_t(const FusedLaunch& p, const uint8_t* kcache, cudaStream_t stream) {
+template <int R, bool DENSE, bool BF16>
+cudaError_t launch_fused_t(const FusedLaunch& p, const void* kcache, cudaStream_t stream) {
   CUtensorMap kmap, qmap;
-  if (!make_map(&kmap, kcache, p.num_blocks * kBlk, kBlk)) return cudaErrorInvalidValue;
-  if (!make_map(&qmap, p.q, (long long)p.rows * kH, R * kH)) return cudaErrorInvalidValue;
+  if (!make_map(&kmap, kcache, p.num_blocks * kBlk, kBlk, BF16)) return cudaErrorInvalidValue;
+  if (!make_map(&qmap, p.q, (long long)p.rows * kH, R * kH, BF16)) return cudaErrorInvalidValue;
   static bool attr_done[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  constexpr size_t smem = fused_smem_bytes<R>();
+  constexpr size_t smem = fused_smem_bytes<R, BF16>();
   if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(fused_score_topk_kernel<R, DENSE>,
+    cudaError_t e = cudaFuncSetAttribute(fused_score_topk_kernel<R, DENSE, BF16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
@@ -499,7 +559,7 @@ cudaError_t launch_fused_t(const FusedLaunch& p, const uint8_t* kcache, cudaStre
   // then runs once per CTA.
   const long long units = (long long)((p.rows + R - 1) / R) * p.chunks;
   const int grid = (int)units;
-  fused_score_topk_kernel<R, DENSE><<<grid, fused_threads<R>(), smem, stream>>>(p, kmap, qmap);
+  fused_score_topk_kernel<R, DENSE, BF16><<<grid, fused_threads<R>(), smem, stream>>>(p, kmap, qmap);
   return cudaGetLastError();
 }
 
@@ -526,9 +586,16 @@ FusedPlan fused_plan(long long rows, int max_seq_len, int group_rows, int num_sm
   return pl;
 }
 
-cudaError_t launch_fused(const FusedLaunch& p, int group, bool dense, const uint8_t* kcache, cudaStream_t stream) {
-  if (group == 2) return dense ? launch_fused_t<2, true>(p, kcache, stream) : launch_fused_t<2, false>(p, kcache, stream);
-  return dense ? launch_fused_t<1, true>(p, kcache, stream) : launch_fused_t<1, false>(p, kcache, stream);
+cudaError_t launch_fused(const FusedLaunch& p, int group, bool dense, bool bf16, const void* kcache,
+                         cudaStream_t stream) {
+  if (bf16) {
+    if (group == 2)
+      return dense ? launch_fused_t<2, true, true>(p, kcache, stream) : launch_fused_t<2, false, true>(p, kcache, stream);
+    return dense ? launch_fused_t<1, true, true>(p, kcache, stream) : launch_fused_t<1, false, true>(p, kcache, stream);
+  }
+  if (group == 2)
+    return dense ? launch_fused_t<2, true, false>(p, kcache, stream) : launch_fused_t<2, false, false>(p, kcache, stream);
+  return dense ? launch_fused_t<1, true, false>(p, kcache, stream) : launch_fused_t<1, false, false>(p, kcache, stream);
 }
 
 }  // namespace sai

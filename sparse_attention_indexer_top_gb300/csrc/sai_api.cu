@@ -157,8 +157,9 @@ int sai_topk_transform(const float* scores, int64_t rows, int64_t score_stride, 
 
 namespace {
 
-// Shared argument checks of the two fused-score entry points.
-int check_fused_args(const uint8_t* q, const float* w, const uint8_t* kcache, const float* kscale,
+// Shared argument checks of the fused-score entry points. The FP8 cache needs
+// its per-key scales; a bf16 cache may have none (kscale null = scale 1).
+int check_fused_args(const void* q, const float* w, const void* kcache, const float* kscale, bool bf16,
                      int64_t num_blocks, const int32_t* block_table, int64_t bt_rows, int64_t bt_stride,
                      const int32_t* row_to_batch, const int32_t* seq_lens, int64_t rows, int32_t heads,
                      int32_t dim, int32_t block_size, int32_t max_seq_len, int32_t group_rows) {
@@ -166,52 +167,22 @@ int check_fused_args(const uint8_t* q, const float* w, const uint8_t* kcache, co
   if (heads != 64 || dim != 128 || block_size != 128) return SAI_ERR_UNSUPPORTED;
   if (group_rows != 1 && group_rows != 4) return SAI_ERR_UNSUPPORTED;
   if (rows == 0) return SAI_OK;
-  if (!q || !w || !kcache || !kscale || !block_table || !seq_lens) return SAI_ERR_NULL;
+  if (!q || !w || !kcache || (!kscale && !bf16) || !block_table || !seq_lens) return SAI_ERR_NULL;
   if (num_blocks < 1 || bt_rows < 1 || bt_stride < 1) return SAI_ERR_SHAPE;
   if (num_blocks * 128 > INT_MAX || rows * 64 > INT_MAX || rows > INT_MAX / 16) return SAI_ERR_SHAPE;
   if (!row_to_batch && bt_rows < rows) return SAI_ERR_SHAPE;
-  if (!aligned(q, 16) || !aligned(kcache, 16) || !aligned(w, 16) || !aligned(kscale, 4) ||
+  if (!aligned(q, 16) || !aligned(kcache, 16) || !aligned(w, 16) || (kscale && !aligned(kscale, 4)) ||
       !aligned(block_table, 4) || !aligned(seq_lens, 4) || (row_to_batch && !aligned(row_to_batch, 4)))
     return SAI_ERR_ALIGN;
   return SAI_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-size_t sai_index_score_topk_workspace(int64_t rows, int32_t max_seq_len, int32_t group_rows, int32_t k) {
-  if (rows <= 0 || max_seq_len < 0 || k != SAI_TOPK || (group_rows != 1 && group_rows != 4)) return 0;
-  int dev, sms;
-  int* st;
-  if (!device_setup(&dev, &st, &sms)) return 0;
-  return sai::fused_plan(rows, max_seq_len, group_rows, sms).workspace_bytes;
-}
-
-int sai_index_score_topk(const uint8_t* q_fp8, const float* w, const uint8_t* kcache_fp8, const float* kscale,
-                         int64_t num_blocks, const int32_t* block_table, int64_t bt_rows, int64_t bt_stride,
-                         const int32_t* row_to_batch, const int32_t* seq_lens, int64_t rows, int32_t heads,
-                         int32_t dim, int32_t block_size, int32_t max_seq_len, int32_t group_rows, int32_t k,
-                         int32_t* out_slots, int32_t* out_indices, float* out_scores, void* workspace,
-                         size_t workspace_bytes, sai_stream_t stream) {
-  if (k <= 0) return SAI_ERR_SHAPE;
-  if (k != SAI_TOPK) return SAI_ERR_UNSUPPORTED;
-  if (!out_slots && !out_indices && !out_scores) return SAI_ERR_NULL;
-  int st_arg = check_fused_args(q_fp8, w, kcache_fp8, kscale, num_blocks, block_table, bt_rows, bt_stride,
-                                row_to_batch, seq_lens, rows, heads, dim, block_size, max_seq_len, group_rows);
-  if (st_arg != SAI_OK || rows == 0) return st_arg;
-  if ((out_slots && !aligned(out_slots, 4)) || (out_indices && !aligned(out_indices, 4)) ||
-      (out_scores && !aligned(out_scores, 4)))
-    return SAI_ERR_ALIGN;
-  int dev, sms;
-  int* st;
-  if (!device_setup(&dev, &st, &sms)) return SAI_ERR_CUDA;
-  const sai::FusedPlan plan = sai::fused_plan(rows, max_seq_len, group_rows, sms);
-  if (!workspace || workspace_bytes < plan.workspace_bytes || !aligned(workspace, 16)) return SAI_ERR_WORKSPACE;
-  const size_t units = static_cast<size_t>(rows) * plan.chunks;
-  char* ws = static_cast<char*>(workspace);
+sai::FusedLaunch fused_launch(const void* q, const float* w, const float* kscale, int64_t num_blocks,
+                              const int32_t* block_table, int64_t bt_rows, int64_t bt_stride,
+                              const int32_t* row_to_batch, const int32_t* seq_lens, int64_t rows,
+                              int32_t max_seq_len, const sai::FusedPlan& plan, int* st) {
   sai::FusedLaunch p{};
-  p.q = q_fp8;
+  p.q = q;
   p.w = w;
   p.kscale = kscale;
   p.num_blocks = num_blocks;
@@ -224,12 +195,38 @@ int sai_index_score_topk(const uint8_t* q_fp8, const float* w, const uint8_t* kc
   p.max_len = max_seq_len;
   p.chunks = plan.chunks;
   p.chunk_blocks = plan.chunk_blocks;
+  p.status = st;
+  return p;
+}
+
+int fused_topk(const void* q, const float* w, const void* kcache, const float* kscale, bool bf16, int64_t num_blocks,
+               const int32_t* block_table, int64_t bt_rows, int64_t bt_stride, const int32_t* row_to_batch,
+               const int32_t* seq_lens, int64_t rows, int32_t heads, int32_t dim, int32_t block_size,
+               int32_t max_seq_len, int32_t group_rows, int32_t k, int32_t* out_slots, int32_t* out_indices,
+               float* out_scores, void* workspace, size_t workspace_bytes, sai_stream_t stream) {
+  if (k <= 0) return SAI_ERR_SHAPE;
+  if (k != SAI_TOPK) return SAI_ERR_UNSUPPORTED;
+  if (!out_slots && !out_indices && !out_scores) return SAI_ERR_NULL;
+  int st_arg = check_fused_args(q, w, kcache, kscale, bf16, num_blocks, block_table, bt_rows, bt_stride,
+                                row_to_batch, seq_lens, rows, heads, dim, block_size, max_seq_len, group_rows);
+  if (st_arg != SAI_OK || rows == 0) return st_arg;
+  if ((out_slots && !aligned(out_slots, 4)) || (out_indices && !aligned(out_indices, 4)) ||
+      (out_scores && !aligned(out_scores, 4)))
+    return SAI_ERR_ALIGN;
+  int dev, sms;
+  int* st;
+  if (!device_setup(&dev, &st, &sms)) return SAI_ERR_CUDA;
+  const sai::FusedPlan plan = sai::fused_plan(rows, max_seq_len, group_rows, sms);
+  if (!workspace || workspace_bytes < plan.workspace_bytes || !aligned(workspace, 16)) return SAI_ERR_WORKSPACE;
+  const size_t units = static_cast<size_t>(rows) * plan.chunks;
+  char* ws = static_cast<char*>(workspace);
+  sai::FusedLaunch p = fused_launch(q, w, kscale, num_blocks, block_table, bt_rows, bt_stride, row_to_batch,
+                                    seq_lens, rows, max_seq_len, plan, st);
   p.part_key = reinterpret_cast<uint32_t*>(ws);
   p.part_idx = reinterpret_cast<int32_t*>(ws + units * SAI_TOPK * 4);
   p.part_cnt = reinterpret_cast<int*>(ws + units * SAI_TOPK * 8);
-  p.status = st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = sai::launch_fused(p, plan.group, false, kcache_fp8, s);
+  cudaError_t e = sai::launch_fused(p, plan.group, false, bf16, kcache, s);
   if (e != cudaSuccess) return cuda_status(e);
   sai::MergeLaunch m{};
   m.rows = static_cast<int>(rows);
@@ -250,12 +247,11 @@ int sai_index_score_topk(const uint8_t* q_fp8, const float* w, const uint8_t* kc
   return cuda_status(sai::launch_merge(m, s));
 }
 
-int sai_index_score(const uint8_t* q_fp8, const float* w, const uint8_t* kcache_fp8, const float* kscale,
-                    int64_t num_blocks, const int32_t* block_table, int64_t bt_rows, int64_t bt_stride,
-                    const int32_t* row_to_batch, const int32_t* seq_lens, int64_t rows, int32_t heads, int32_t dim,
-                    int32_t block_size, int32_t max_seq_len, int32_t group_rows, float* out_scores,
-                    int64_t out_stride, sai_stream_t stream) {
-  int st_arg = check_fused_args(q_fp8, w, kcache_fp8, kscale, num_blocks, block_table, bt_rows, bt_stride,
+int fused_dense(const void* q, const float* w, const void* kcache, const float* kscale, bool bf16, int64_t num_blocks,
+                const int32_t* block_table, int64_t bt_rows, int64_t bt_stride, const int32_t* row_to_batch,
+                const int32_t* seq_lens, int64_t rows, int32_t heads, int32_t dim, int32_t block_size,
+                int32_t max_seq_len, int32_t group_rows, float* out_scores, int64_t out_stride, sai_stream_t stream) {
+  int st_arg = check_fused_args(q, w, kcache, kscale, bf16, num_blocks, block_table, bt_rows, bt_stride,
                                 row_to_batch, seq_lens, rows, heads, dim, block_size, max_seq_len, group_rows);
   if (st_arg != SAI_OK || rows == 0) return st_arg;
   if (!out_scores) return SAI_ERR_NULL;
@@ -265,27 +261,64 @@ int sai_index_score(const uint8_t* q_fp8, const float* w, const uint8_t* kcache_
   int* st;
   if (!device_setup(&dev, &st, &sms)) return SAI_ERR_CUDA;
   const sai::FusedPlan plan = sai::fused_plan(rows, max_seq_len, group_rows, sms);
-  sai::FusedLaunch p{};
-  p.q = q_fp8;
-  p.w = w;
-  p.kscale = kscale;
-  p.num_blocks = num_blocks;
-  p.block_table = block_table;
-  p.bt_rows = bt_rows;
-  p.bt_stride = bt_stride;
-  p.row_to_batch = row_to_batch;
-  p.seq_lens = seq_lens;
-  p.rows = static_cast<int>(rows);
-  p.max_len = max_seq_len;
-  p.chunks = plan.chunks;
-  p.chunk_blocks = plan.chunk_blocks;
+  sai::FusedLaunch p = fused_launch(q, w, kscale, num_blocks, block_table, bt_rows, bt_stride, row_to_batch,
+                                    seq_lens, rows, max_seq_len, plan, st);
   p.dense = out_scores;
   p.dense_stride = out_stride;
-  p.status = st;
-  return cuda_status(sai::launch_fused(p, plan.group, true, kcache_fp8, reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_status(sai::launch_fused(p, plan.group, true, bf16, kcache, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-}  // extern "C"
+}  // namespace
+
+extern "C" {
+
+size_t sai_index_score_topk_workspace(int64_t rows, int32_t max_seq_len, int32_t group_rows, int32_t k) {
+  if (rows <= 0 || max_seq_len < 0 || k != SAI_TOPK || (group_rows != 1 && group_rows != 4)) return 0;
+  int dev, sms;
+  int* st;
+  if (!device_setup(&dev, &st, &sms)) return 0;
+  return sai::fused_plan(rows, max_seq_len, group_rows, sms).workspace_bytes;
+}
+
+int sai_index_score_topk(const uint8_t* q_fp8, const float* w, const uint8_t* kcache_fp8, const float* kscale,
+                         int64_t num_blocks, const int32_t* block_table, int64_t bt_rows, int64_t bt_stride,
+                         const int32_t* row_to_batch, const int32_t* seq_lens, int64_t rows, int32_t heads,
+                         int32_t dim, int32_t block_size, int32_t max_seq_len, int32_t group_rows, int32_t k,
+                         int32_t* out_slots, int32_t* out_indices, float* out_scores, void* workspace,
+                         size_t workspace_bytes, sai_stream_t stream) {
+  return fused_topk(q_fp8, w, kcache_fp8, kscale, false, num_blocks, block_table, bt_rows, bt_stride, row_to_batch,
+                    seq_lens, rows, heads, dim, block_size, max_seq_len, group_rows, k, out_slots, out_indices,
+                    out_scores, workspace, workspace_bytes, stream);
+}
+
+int sai_index_score_topk_bf16(const uint16_t* q_bf16, const float* w, const uint16_t* kcache_bf16,
+                              const float* kscale, int64_t num_blocks, const int32_t* block_table, int64_t bt_rows,
+                              int64_t bt_stride, const int32_t* row_to_batch, const int32_t* seq_lens, int64_t rows,
+                              int32_t heads, int32_t dim, int32_t block_size, int32_t max_seq_len, int32_t group_rows,
+                              int32_t k, int32_t* out_slots, int32_t* out_indices, float* out_scores,
+                              void* workspace, size_t workspace_bytes, sai_stream_t stream) {
+  return fused_topk(q_bf16, w, kcache_bf16, kscale, true, num_blocks, block_table, bt_rows, bt_stride, row_to_batch,
+                    seq_lens, rows, heads, dim, block_size, max_seq_len, group_rows, k, out_slots, out_indices,
+                    out_scores, workspace, workspace_bytes, stream);
+}
+
+int sai_index_score(const uint8_t* q_fp8, const float* w, const uint8_t* kcache_fp8, const float* kscale,
+                    int64_t num_blocks, const int32_t* block_table, int64_t bt_rows, int64_t bt_stride,
+                    const int32_t* row_to_batch, const int32_t* seq_lens, int64_t rows, int32_t heads, int32_t dim,
+                    int32_t block_size, int32_t max_seq_len, int32_t group_rows, float* out_scores,
+                    int64_t out_stride, sai_stream_t stream) {
+  return fused_dense(q_fp8, w, kcache_fp8, kscale, false, num_blocks, block_table, bt_rows, bt_stride, row_to_batch,
+                     seq_lens, rows, heads, dim, block_size, max_seq_len, group_rows, out_scores, out_stride, stream);
+}
+
+int sai_index_score_bf16(const uint16_t* q_bf16, const float* w, const uint16_t* kcache_bf16, const float* kscale,
+                         int64_t num_blocks, const int32_t* block_table, int64_t bt_rows, int64_t bt_stride,
+                         const int32_t* row_to_batch, const int32_t* seq_lens, int64_t rows, int32_t heads,
+                         int32_t dim, int32_t block_size, int32_t max_seq_len, int32_t group_rows, float* out_scores,
+                         int64_t out_stride, sai_stream_t stream) {
+  return fused_dense(q_bf16, w, kcache_bf16, kscale, true, num_blocks, block_table, bt_rows, bt_stride, row_to_batch,
+                     seq_lens, rows, heads, dim, block_size, max_seq_len, group_rows, out_scores, out_stride, stream);
+}
 
 int sai_sparse_blocks(const int32_t* slots, int64_t rows, int32_t k, int32_t block_size, int32_t* out_blocks,
                       int32_t* out_counts, sai_stream_t stream) {
@@ -299,3 +332,5 @@ int sai_sparse_blocks(const int32_t* slots, int64_t rows, int32_t k, int32_t blo
   return cuda_status(sai::launch_sparse_blocks(slots, static_cast<int>(rows), k, block_size, out_blocks, out_counts,
                                                reinterpret_cast<cudaStream_t>(stream)));
 }
+
+}  // extern "C"

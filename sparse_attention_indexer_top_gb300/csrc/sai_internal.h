@@ -73,9 +73,9 @@ cudaError_t launch_sparse_blocks(const int32_t* slots, int rows, int k, int bloc
                                  int32_t* out_counts, cudaStream_t stream);
 
 struct FusedLaunch {
-  const uint8_t* q;        // [rows, 64, 128] e4m3
+  const void* q;           // [rows, 64, 128] e4m3 codes or bf16
   const float* w;          // [rows, 64]
-  const float* kscale;     // [num_blocks, 128]
+  const float* kscale;     // [num_blocks, 128], or null (scale 1; bf16 cache only)
   long long num_blocks;
   const int* block_table;  // [bt_rows, bt_stride]
   long long bt_rows, bt_stride;
@@ -99,6 +99,7 @@ struct FusedPlan {
   size_t workspace_bytes;
 };
 FusedPlan fused_plan(long long rows, int max_seq_len, int group_rows, int num_sms);
-cudaError_t launch_fused(const FusedLaunch& p, int group, bool dense, const uint8_t* kcache, cudaStream_t stream);
+cudaError_t launch_fused(const FusedLaunch& p, int group, bool dense, bool bf16, const void* kcache,
+                         cudaStream_t stream);
 
 }  // namespace sai

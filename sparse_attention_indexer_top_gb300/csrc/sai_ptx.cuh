@@ -194,6 +194,18 @@ __device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64
       : "memory");
 }
 
+// D[tmem] (+)= A * B^T for bf16 A (M x 16) and B (N x 16) from shared memory
+// (kind::f16, fp32 accumulation).
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05.mma issued so far by this
 // thread has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -252,6 +264,15 @@ __device__ __forceinline__ uint64_t umma_desc_sw128_kmajor(uint32_t smem_addr) {
 __host__ __device__ constexpr uint32_t umma_idesc_e4m3(int m, int n) {
   return (1u << 4)                               // D format: F32
          | (0u << 7) | (0u << 10)                // A, B format: E4M3
+         | (static_cast<uint32_t>(n >> 3) << 17)  // N / 8
+         | (static_cast<uint32_t>(m >> 4) << 24); // M / 16
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B (K-major) and an
+// FP32 accumulator.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n) {
+  return (1u << 4)                               // D format: F32
+         | (1u << 7) | (1u << 10)                // A, B format: BF16
          | (static_cast<uint32_t>(n >> 3) << 17)  // N / 8
          | (static_cast<uint32_t>(m >> 4) << 24); // M / 16
 }

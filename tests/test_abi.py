@@ -88,3 +88,31 @@ def test_sparse_blocks_argument_errors(lib):
     assert lib.sai_sparse_blocks(slots, 4, 512, 128, None, None, None) == -1
     assert lib.sai_sparse_blocks(ctypes.c_void_p((1 << 20) + 2), 4, 512, 128, out, None, None) == -7
     assert lib.sai_sparse_blocks(None, 0, 512, 128, None, None, None) == 0  # nothing to do
+
+
+def test_fused_argument_errors(lib):
+    # (q, w, kcache, kscale, num_blocks, bt, bt_rows, bt_stride, r2b, seq_lens, rows, heads, dim, bs, max_len, group)
+    p = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 2)
+
+    def args(q=p, kscale=p, heads=64, group=1, rows=4):
+        return (q, p, p, kscale, 8, p, 4, 8, None, p, rows, heads, 128, 128, 1024, group)
+
+    for name in ("sai_index_score_topk", "sai_index_score_topk_bf16"):
+        f = getattr(lib, name)
+        tail = (512, p, p, p, p, 1 << 20, None)
+        assert f(*args(heads=32), *tail) == -3
+        assert f(*args(group=2), *tail) == -3
+        assert f(*args(rows=-1), *tail) == -2
+        assert f(*args(q=None), *tail) == -1
+        assert f(*args(rows=0), *tail) == 0
+    for name in ("sai_index_score", "sai_index_score_bf16"):
+        f = getattr(lib, name)
+        assert f(*args(heads=32), p, 1024, None) == -3
+        assert f(*args(q=None), p, 1024, None) == -1
+    # a missing key scale is an error for the FP8 cache only: the bf16 calls
+    # get past the null check and stop at the misaligned q
+    assert lib.sai_index_score_topk(*args(q=odd, kscale=None), 512, p, p, p, p, 1 << 20, None) == -1
+    assert lib.sai_index_score_topk_bf16(*args(q=odd, kscale=None), 512, p, p, p, p, 1 << 20, None) == -7
+    assert lib.sai_index_score(*args(q=odd, kscale=None), p, 1024, None) == -1
+    assert lib.sai_index_score_bf16(*args(q=odd, kscale=None), p, 1024, None) == -7

@@ -1,4 +1,5 @@
-"""GPU parity of the fused FP8 index score (+ top-k) against the CPU oracle.
+"""GPU parity of the fused index score (+ top-k) against the CPU oracle, for
+the FP8 index cache and the bf16 one.
 
 Scores: the oracle forms the FP8 dot products exactly, the kernel in FP32 on
 the tensor cores; they must agree within 1e-3 relative (floored at the row's
@@ -27,7 +28,12 @@ def _t(a):
 
 
 def _dev_inputs(inp):
-    return dict(q=_t(inp.q), w=_t(inp.w), kcache=_t(inp.kcache), kscale=_t(inp.kscale),
+    if inp.dtype == "bf16":  # uint16 bit patterns -> torch.bfloat16
+        def elem(a):
+            return _t(a.view(np.int16)).view(torch.bfloat16)
+    else:
+        elem = _t
+    return dict(q=elem(inp.q), w=_t(inp.w), kcache=elem(inp.kcache), kscale=_t(inp.kscale),
                 block_table=_t(inp.block_table), seq_lens=_t(inp.seq_lens), row_to_batch=_t(inp.row_to_batch))
 
 
@@ -100,10 +106,11 @@ def _check_topk(got, inp, rows=None, k=512):
         assert np.array_equal(slots[i][:kk], pages * 128 + sel % 128), f"row {i}: slots"
 
 
-def _small(kind="normal", rows=6, lens=(1, 127, 128, 300, 1000, 2500), seed=41):
+def _small(kind="normal", rows=6, lens=(1, 127, 128, 300, 1000, 2500), seed=41, dtype="e4m3"):
     lens = np.asarray(lens[:rows], np.int32)
     per_row = int(-(-lens.max() // 128))
-    return W.make_fused_inputs(seed, rows, 64, 128, rows * per_row + 3, lens, (rows, per_row), kind=kind)
+    return W.make_fused_inputs(seed, rows, 64, 128, rows * per_row + 3, lens, (rows, per_row), kind=kind,
+                               dtype=dtype)
 
 
 def test_dense_integer_inputs_exact():
@@ -177,7 +184,7 @@ def test_topk_one_chunk_per_row(kind):
     _check_topk(_fused(inp), inp)
 
 
-def _packed_requests(seed, new_rows, prefixes):
+def _packed_requests(seed, new_rows, prefixes, dtype="e4m3"):
     """Several requests packed into one call: request b contributes
     new_rows[b] query rows, causal on a KV of prefixes[b] + new_rows[b]
     tokens with its own block-table row (row_to_batch = b)."""
@@ -189,7 +196,7 @@ def _packed_requests(seed, new_rows, prefixes):
         r2b += [b] * n
     rows = len(lens)
     return W.make_fused_inputs(seed, rows, 64, 128, len(kv) * per_row + 5, lens, (len(kv), per_row),
-                               row_to_batch=r2b)
+                               row_to_batch=r2b, dtype=dtype)
 
 
 def test_topk_packed_requests_grouped():
@@ -203,3 +210,76 @@ def test_topk_packed_requests_unaligned_single_rows():
     """Request boundaries that are not multiples of 4: group_rows=1."""
     inp = _packed_requests(49, [13, 7, 22], [3300, 100, 2000])
     _check_topk(_fused(inp, group_rows=1), inp)
+
+
+# ---------------------------------------------------------------- bf16 index cache
+# Same checks with q and the keys in bf16 (tcgen05 kind::f16, two 64-dim
+# halves per key row); integer inputs pin the operand layout bit-exactly, and
+# a cache without per-key scales (kscale = None) means scale 1.
+
+
+def test_bf16_dense_integer_inputs_exact():
+    inp = _small("int", dtype="bf16")
+    _check_dense(_dense(inp), inp, exact=True)
+
+
+@pytest.mark.parametrize("no_scale", [False, True])
+def test_bf16_dense_normal_inputs(no_scale):
+    inp = _small("normal", dtype="bf16", seed=51)
+    if no_scale:
+        inp.kscale = None
+    _check_dense(_dense(inp), inp)
+
+
+def test_bf16_dense_grouped_rows_exact():
+    lens = np.array([997, 998, 999, 1000, 3001, 3002, 3003, 3004], np.int32)
+    inp = W.make_fused_inputs(52, 8, 64, 128, 2 * 24 + 1, lens, (2, 24), row_to_batch=[0, 0, 0, 0, 1, 1, 1, 1],
+                              kind="int", dtype="bf16")
+    _check_dense(_dense(inp, group_rows=4), inp, exact=True)
+
+
+def test_bf16_topk_small_and_zero_q():
+    inp = _small("normal", dtype="bf16", seed=53)
+    _check_topk(_fused(inp), inp)
+    inp = _small("zero_q", dtype="bf16")
+    slots, idx, scores = _fused(inp)
+    for i in range(inp.rows):
+        kk = min(int(inp.seq_lens[i]), 512)
+        assert idx[i][:kk].tolist() == list(range(kk))
+
+
+def test_bf16_topk_grouped_prefill_like_no_scale():
+    rows, kv = 64, 6000
+    lens = (kv - rows + 1 + np.arange(rows)).astype(np.int32)
+    blocks = -(-kv // 128)
+    inp = W.make_fused_inputs(54, rows, 64, 128, blocks, lens, (1, blocks), row_to_batch=np.zeros(rows, np.int32),
+                              dtype="bf16")
+    inp.kscale = None
+    _check_topk(_fused(inp, group_rows=4), inp)
+
+
+def test_bf16_topk_packed_requests():
+    inp = _packed_requests(55, [36, 20, 44], [2900, 700, 5100], dtype="bf16")
+    _check_topk(_fused(inp, group_rows=4), inp)
+    inp = _packed_requests(56, [13, 7, 22], [3300, 100, 2000], dtype="bf16")
+    _check_topk(_fused(inp, group_rows=1), inp)
+
+
+def test_bf16_topk_one_chunk_per_row():
+    rows, per_row = 640, 12
+    lens = np.random.default_rng(57).integers(1, per_row * 128 + 1, size=rows).astype(np.int32)
+    inp = W.make_fused_inputs(57, rows, 64, 128, rows * per_row + 1, lens, (rows, per_row), dtype="bf16")
+    _check_topk(_fused(inp), inp)
+
+
+def test_bf16_fused_decode_full_size():
+    """The decode workload's shapes with a bf16 cache: 64 rows, seq_lens
+    U[4096, 32768], a 16384-block pool; every row checked."""
+    inp = W.fused_decode(dtype="bf16")
+    _check_topk(_fused(inp), inp)
+
+
+def test_bf16_fused_prefill_full_size_sampled():
+    inp = W.fused_prefill(dtype="bf16")
+    got = _fused(inp, group_rows=4)
+    _check_topk(got, inp, rows=[0, 1, 2, 3, 2047, 2048, 4093, 4094, 4095])

@@ -312,20 +312,20 @@ def make_fused_inputs(seed: int, rows: int, heads: int, dim: int, num_blocks: in
 
 
 def fused_decode(seed: int = 4, rows: int = 64, min_len: int = 4096, max_len: int = 32768,
-                 heads: int = IDX_HEADS, dim: int = HEAD_DIM) -> FusedInputs:
+                 heads: int = IDX_HEADS, dim: int = HEAD_DIM, dtype: str = "e4m3") -> FusedInputs:
     """Decode: one query row per request, each with its own block-table row."""
     lens = _rng(seed, 303).integers(min_len, max_len + 1, size=rows).astype(np.int32)
     per_row = -(-max_len // KV_BLOCK)
     return make_fused_inputs(seed, rows, heads, dim, rows * per_row, lens, (rows, per_row),
-                             name="fused_decode")
+                             name="fused_decode", dtype=dtype)
 
 
 def fused_prefill(seed: int = 5, rows: int = 4096, kv_len: int = 32768,
-                  heads: int = IDX_HEADS, dim: int = HEAD_DIM) -> FusedInputs:
+                  heads: int = IDX_HEADS, dim: int = HEAD_DIM, dtype: str = "e4m3") -> FusedInputs:
     """Prefill of one request: the query rows are the last ``rows`` positions
     of a ``kv_len``-token KV, so row r sees ``kv_len - rows + r + 1`` keys."""
     blocks = -(-kv_len // KV_BLOCK)
     lens = (kv_len - rows + 1 + np.arange(rows)).astype(np.int32)
     r2b = np.zeros(rows, np.int32)
     return make_fused_inputs(seed, rows, heads, dim, blocks, lens, (1, blocks), row_to_batch=r2b,
-                             name="fused_prefill")
+                             name="fused_prefill", dtype=dtype)
