@@ -62,7 +62,8 @@ constexpr int kBlk = 128;     // tokens per KV block = MMA M
 // K-tile stages, query-tile buffers and resident CTAs per SM: single rows
 // (decode) run three small CTAs per SM with a 2-stage ring, row pairs
 // (prefill) two with a 3-stage ring; one query buffer each, since every CTA
-// takes one unit (measured against 2-4 stages and 2-3 CTAs per SM).
+// takes one unit (measured against 2-4 stages and 2-3 CTAs per SM; a 3-stage
+// ring at three CTAs per SM, with 384-entry sub-lists to fit, was slower).
 // The bf16 variant has twice the bytes per stage and runs one CTA fewer.
 template <int R, bool BF16 = false>
 __host__ __device__ constexpr int fused_stages() {
@@ -85,9 +86,14 @@ template <bool BF16>
 __host__ __device__ constexpr int sw_regions() {
   return kD * elem_bytes<BF16>() / kSwB;
 }
-constexpr int kSub = 512;     // candidate sub-list per epilogue warp
 constexpr int kSyncEvery = 4; // tiles between the row group's count exchanges
-constexpr int kSubPruneAt = kSub - kSyncEvery * 32;
+// Candidate sub-list per epilogue warp. A list is cut back once it holds
+// more than fused_sub() - 4 tiles x 32 entries, and a warp appends at most
+// 32 per tile, so it never overflows; the cut leaves 128 per list.
+template <int R, bool BF16>
+__host__ __device__ constexpr int fused_sub() {
+  return 512;
+}
 constexpr int kEpiRow = 128;  // epilogue threads per query row (4 warps, one TMEM lane quadrant each)
 
 template <int R, bool BF16>
@@ -95,8 +101,8 @@ struct __align__(1024) FusedSmem {
   // a key stage / query tile is sw_regions() regions of [rows x 128 bytes]
   uint8_t kst[fused_stages<R, BF16>()][kBlk * kD * elem_bytes<BF16>()];  // 16 KB (FP8) or 32 KB, 1024-aligned
   uint8_t q[fused_qbufs<R>()][R * kH * kD * elem_bytes<BF16>()];          // query tiles of consecutive units
-  uint32_t ckey[R][4 * kSub];  // row r: four per-warp sub-lists
-  int32_t cidx[R][4 * kSub];
+  uint32_t ckey[R][4 * fused_sub<R, BF16>()];  // row r: four per-warp sub-lists
+  int32_t cidx[R][4 * fused_sub<R, BF16>()];
   uint32_t aux_key[R][kTopK];
   int32_t aux_idx[R][kTopK];
   SelectScratch sc[R];
@@ -229,6 +235,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
+  if constexpr (!DENSE) pdl_trigger();  // the merge may be scheduled now; it waits for this grid to finish
 
   // Every role walks the same units (u = blockIdx.x, + gridDim.x, ...) and
   // derives the same tile counts, so the barrier phases below (counted over
@@ -322,6 +329,9 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
     const int bar = 1 + r;
     uint32_t* const ckey = S.ckey[r];
     int32_t* const cidx = S.cidx[r];
+    constexpr int kSub = fused_sub<R, BF16>();
+    constexpr int kSubPruneAt = kSub - kSyncEvery * 32;
+    static_assert(kSubPruneAt >= kTopK / 4 && 4 * kSub > kTopK, "sub-list sizes");
     uint32_t* const my_key = ckey + quad * kSub;
     int32_t* const my_idx = cidx + quad * kSub;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;

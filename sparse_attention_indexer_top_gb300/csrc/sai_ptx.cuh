@@ -268,6 +268,14 @@ __host__ __device__ constexpr uint32_t umma_idesc_e4m3(int m, int n) {
          | (static_cast<uint32_t>(m >> 4) << 24); // M / 16
 }
 
+// Programmatic dependent launch. A grid launched after this one on the same
+// stream with the programmatic-serialization attribute may be scheduled once
+// every CTA of this grid has executed pdl_trigger() or exited; before it reads
+// anything this grid writes it calls pdl_wait(), which returns when this grid
+// has completed and its memory operations are visible.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Instruction descriptor of kind::f16 with bf16 A and B (K-major) and an
 // FP32 accumulator.
 __host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n) {

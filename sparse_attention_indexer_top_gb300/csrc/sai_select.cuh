@@ -374,14 +374,19 @@ __device__ __forceinline__ int compact_ge(uint32_t* ckey, int32_t* cidx, int n, 
 }
 
 // Exact top-K (K = 512) of ckey/cidx[0, n), n > K, by (key desc, index asc),
-// written to aux_key/aux_idx[0, K). `hist` (4096 words) is scratch and is
-// left zeroed. CAPT bounds n.
+// written to aux_key/aux_idx[0, K). Keys are counted in 4096 bins,
+// bin = (key - kmin) >> shift, which must be < 4096 for every key (kmin <=
+// every key); bins fitted to the keys' range leave few keys in the bin that
+// holds the K-th. `hist` (4096 words) is scratch and is left zeroed. CAPT
+// bounds n.
 template <int CAPT>
-__device__ void fast_select512(const uint32_t* ckey, const int32_t* cidx, int n, uint32_t* hist, uint32_t* aux_key,
-                               int32_t* aux_idx, SelectScratch& sc, uint32_t* bcast, int tid, int bar) {
+__device__ void fast_select512(const uint32_t* ckey, const int32_t* cidx, int n, uint32_t kmin, int shift,
+                               uint32_t* hist, uint32_t* aux_key, int32_t* aux_idx, SelectScratch& sc,
+                               uint32_t* bcast, int tid, int bar) {
   constexpr int K = kTopK;
   constexpr int M = (CAPT + 511) / 512;
-  for (int j = tid; j < n; j += 512) atomicAdd(&hist[ckey[j] >> 20], 1u);
+  auto bin_of = [&](uint32_t key) { return (key - kmin) >> shift; };
+  for (int j = tid; j < n; j += 512) atomicAdd(&hist[bin_of(ckey[j])], 1u);
   named_bar(bar, 512);
   const BinCut cut = hist_cut4096(hist, K, sc.wmin, bcast, tid, bar);
   const uint32_t B = (uint32_t)cut.bin;
@@ -393,13 +398,13 @@ __device__ void fast_select512(const uint32_t* ckey, const int32_t* cidx, int n,
   if (!t.all_eq) {
     t = radix_threshold<512>(n, cut.need_in_bin, sc, tid, bar, [&](int j, uint32_t& v) {
       v = ckey[j];
-      return (v >> 20) == B;
+      return bin_of(v) == B;
     });
     ties = !t.all_eq;
     if (ties) {
       ti = radix_threshold<512>(n, t.need, sc, tid, bar, [&](int j, uint32_t& v) {
         v = 0x7FFFFFFFu - static_cast<uint32_t>(cidx[j]);
-        return (ckey[j] >> 20) == B && thr_cmp(t, ckey[j]) == 0;
+        return bin_of(ckey[j]) == B && thr_cmp(t, ckey[j]) == 0;
       });
     }
   }
@@ -413,7 +418,7 @@ __device__ void fast_select512(const uint32_t* ckey, const int32_t* cidx, int n,
     const int j = tid + 512 * m;
     if (j < n) {
       const uint32_t key = ckey[j];
-      const uint32_t hb = key >> 20;
+      const uint32_t hb = bin_of(key);
       bool sel = hb > B;
       if (hb == B) {
         if (cut.bin_count == cut.need_in_bin) {

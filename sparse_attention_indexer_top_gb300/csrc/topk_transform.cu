@@ -349,6 +349,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
   Smem& S = smem_ref(smem_raw);
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
+  pdl_trigger();  // the merge may be scheduled now; it waits for this grid to finish
   uint32_t* const wkey = S.cand.c.key + warp * kSub;  // this warp's sub-list
   int32_t* const widx = S.cand.c.idx + warp * kSub;
   uint64_t policy = 0;
@@ -592,29 +593,92 @@ struct __align__(16) MergeSmem {
   int32_t aux_idx[kTopK];
   SelectScratch sc;
   uint32_t bcast[4];
+  uint32_t umin[kMergeUnits];  // lowest key of each full partial list
+  uint32_t kmin, kmax;         // range of the kept candidates
 };
 
 __global__ void __launch_bounds__(kTopK, 1) merge_kernel(const __grid_constant__ MergeLaunch p) {
   extern __shared__ unsigned char smem_raw[];
   MergeSmem& S = *reinterpret_cast<MergeSmem*>(smem_raw);
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
   const long long row = blockIdx.x;
+  const int U = p.units_per_row;  // <= kMergeUnits
   reinterpret_cast<uint4*>(S.hist)[2 * tid] = make_uint4(0, 0, 0, 0);
   reinterpret_cast<uint4*>(S.hist)[2 * tid + 1] = make_uint4(0, 0, 0, 0);
-  int total = 0;
-  for (int c = 0; c < p.units_per_row; ++c) {
-    const long long unit = row * p.units_per_row + c;
-    const int n = min(p.part_cnt[unit], kTopK);
-    if (tid < n) {
-      S.cand.c.key[total + tid] = p.part_key[unit * kTopK + tid];
-      S.cand.c.idx[total + tid] = p.part_idx[unit * kTopK + tid];
+  if (tid < kMergeUnits) S.umin[tid] = 0xFFFFFFFFu;
+  if (tid == 0) {
+    S.kmin = 0xFFFFFFFFu;
+    S.kmax = 0u;
+  }
+  pdl_wait();  // the partial lists come from the grid launched just before
+  // entry tid of every partial list of the row, all loads in flight at once
+  const long long base = row * U;
+  int n[kMergeUnits];
+  uint32_t kv[kMergeUnits];
+  int32_t iv[kMergeUnits];
+#pragma unroll
+  for (int c = 0; c < kMergeUnits; ++c) n[c] = c < U ? min(max(p.part_cnt[base + c], 0), kTopK) : 0;
+#pragma unroll
+  for (int c = 0; c < kMergeUnits; ++c) {
+    kv[c] = 0;
+    iv[c] = -1;
+    if (tid < n[c]) {
+      kv[c] = p.part_key[(base + c) * kTopK + tid];
+      iv[c] = p.part_idx[(base + c) * kTopK + tid];
     }
-    total += n;
+  }
+  __syncthreads();
+  // A full list holds the exact top 512 of its range, so its lowest key is
+  // at most the row's 512th key: entries below the largest such bound cannot
+  // be selected, and at least 512 entries reach it.
+#pragma unroll
+  for (int c = 0; c < kMergeUnits; ++c) {
+    if (n[c] == kTopK) {  // the same for the whole block
+      const uint32_t m = __reduce_min_sync(0xFFFFFFFFu, kv[c]);
+      if (lane == 0) atomicMin(&S.umin[c], m);
+    }
+  }
+  __syncthreads();
+  uint32_t bound = 0;
+#pragma unroll
+  for (int c = 0; c < kMergeUnits; ++c)
+    if (n[c] == kTopK) bound = max(bound, S.umin[c]);
+  uint32_t selm = 0;
+  int mine = 0;
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+#pragma unroll
+  for (int c = 0; c < kMergeUnits; ++c) {
+    if (tid < n[c] && kv[c] >= bound) {
+      selm |= 1u << c;
+      ++mine;
+      lo = min(lo, kv[c]);
+      hi = max(hi, kv[c]);
+    }
+  }
+  lo = __reduce_min_sync(0xFFFFFFFFu, lo);
+  hi = __reduce_max_sync(0xFFFFFFFFu, hi);
+  if (lane == 0) {
+    atomicMin(&S.kmin, lo);
+    atomicMax(&S.kmax, hi);
+  }
+  int total;
+  int pos = block_exscan512(mine, &total, S.sc.wcnt, tid, 1);
+#pragma unroll
+  for (int c = 0; c < kMergeUnits; ++c) {
+    if (selm & (1u << c)) {
+      S.cand.c.key[pos] = kv[c];
+      S.cand.c.idx[pos] = iv[c];
+      ++pos;
+    }
   }
   __syncthreads();
   int cnt = total;
   if (cnt > kTopK) {
-    fast_select512<kMergeCap>(S.cand.c.key, S.cand.c.idx, cnt, S.hist, S.aux_key, S.aux_idx, S.sc, S.bcast, tid, 1);
+    // 4096 bins over the candidates' key range
+    const uint32_t span = S.kmax - S.kmin;
+    const int shift = span >= 4096u ? (32 - __clz(span)) - 12 : 0;
+    fast_select512<kMergeCap>(S.cand.c.key, S.cand.c.idx, cnt, S.kmin, shift, S.hist, S.aux_key, S.aux_idx, S.sc,
+                              S.bcast, tid, 1);
     cnt = kTopK;
   } else {
     if (tid < cnt) {
@@ -623,20 +687,40 @@ __global__ void __launch_bounds__(kTopK, 1) merge_kernel(const __grid_constant__
     }
     __syncthreads();
   }
-  uint32_t k[1];
-  int32_t ix[1];
-  int rk[1];
-  rank_sort<kTopK>(S.aux_key, S.aux_idx, cnt, S.cand.runs.key, S.cand.runs.idx, k, ix, rk, tid, 1);
+  // output order: rank the 512 by bucketing (half the threads, two entries
+  // each), or with the sorting ranks when a bucket is too full
   const long long o = row * kTopK;
-  if (ix[0] >= 0) {
-    if (p.out_idx) p.out_idx[o + rk[0]] = ix[0];
-    if (p.out_scores) p.out_scores[o + rk[0]] = key_to_float(k[0]);
+  const int batch = p.row_to_batch ? p.row_to_batch[row] : (int)row;
+  auto emit = [&](uint32_t key, int32_t ix, int rk) {
+    if (p.out_idx) p.out_idx[o + rk] = ix;
+    if (p.out_scores) p.out_scores[o + rk] = key_to_float(key);
     if (p.out_slots) {
-      const int batch = p.row_to_batch ? p.row_to_batch[row] : (int)row;
       const int ps = p.page_size;
-      const long long page = p.page_tables[(long long)batch * p.pt_stride + (ps == 1 ? ix[0] : ix[0] / ps)];
-      p.out_slots[o + rk[0]] = static_cast<int>(ps == 1 ? page : page * ps + ix[0] % ps);
+      const long long page = p.page_tables[(long long)batch * p.pt_stride + (ps == 1 ? ix : ix / ps)];
+      p.out_slots[o + rk] = static_cast<int>(ps == 1 ? page : page * ps + ix % ps);
     }
+  };
+  uint32_t k2[2];
+  int32_t i2[2];
+  int r2[2];
+  if (tid < kTopK / 2) {
+    const bool ok = bucket_rank512<kTopK / 2>(S.aux_key, S.aux_idx, cnt, S.hist,
+                                              reinterpret_cast<uint16_t*>(S.hist + 1024), S.sc, k2, i2, r2, tid, 2);
+    if (tid == 0) S.bcast[0] = ok ? 1u : 0u;
+  }
+  __syncthreads();
+  if (S.bcast[0]) {
+    if (tid < kTopK / 2) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        if (i2[e] >= 0) emit(k2[e], i2[e], r2[e]);
+    }
+  } else {
+    uint32_t k[1];
+    int32_t ix[1];
+    int rk[1];
+    rank_sort<kTopK>(S.aux_key, S.aux_idx, cnt, S.cand.runs.key, S.cand.runs.idx, k, ix, rk, tid, 1);
+    if (ix[0] >= 0) emit(k[0], ix[0], rk[0]);
   }
   if (tid >= cnt) {
     if (p.out_idx) p.out_idx[o + tid] = -1;
@@ -673,6 +757,7 @@ __global__ void __launch_bounds__(kRankRows * 128) rank_kernel(const __grid_cons
   const long long row = (long long)blockIdx.x * kRankRows + g;
   const int bar = 1 + g;
   const bool live = row < p.rows;
+  pdl_wait();  // the lists come from the grid launched just before
   const int cnt = live ? min(max(p.part_cnt[row], 0), kTopK) : 0;
   for (int j = t; j < cnt; j += 128) {
     S.aux_key[j] = p.part_key[row * kTopK + j];
@@ -740,12 +825,30 @@ TopkPlan topk_plan(long long rows, long long max_window, int num_sms) {
 
 size_t merge_smem_bytes() { return sizeof(MergeSmem); }
 
+// Launch a kernel that starts with pdl_wait() so that it may be scheduled
+// while the grid before it on the stream finishes.
+template <typename Kernel>
+cudaError_t launch_dependent(Kernel kernel, int grid, int block, size_t smem, cudaStream_t stream,
+                             const MergeLaunch& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 cudaError_t launch_merge(const MergeLaunch& p, cudaStream_t stream) {
   if (p.rows <= 0) return cudaSuccess;
+  if (p.units_per_row < 1 || p.units_per_row > kMergeUnits) return cudaErrorInvalidValue;
   if (p.units_per_row == 1) {
     const int grid = (p.rows + kRankRows - 1) / kRankRows;
-    rank_kernel<<<grid, kRankRows * 128, kRankRows * sizeof(RankRowSmem), stream>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(rank_kernel, grid, kRankRows * 128, kRankRows * sizeof(RankRowSmem), stream, p);
   }
   int dev = 0;
   cudaGetDevice(&dev);
@@ -755,8 +858,7 @@ cudaError_t launch_merge(const MergeLaunch& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     g_merge_attr_done[dev] = true;
   }
-  merge_kernel<<<p.rows, kTopK, sizeof(MergeSmem), stream>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(merge_kernel, p.rows, kTopK, sizeof(MergeSmem), stream, p);
 }
 
 cudaError_t launch_topk_transform(const TopkLaunch& p, int num_sms, cudaStream_t stream) {
