@@ -57,6 +57,9 @@ __device__ __forceinline__ uint32_t shr64(uint32_t o, int lo) {
 // NT threads of the group call it; `bar` is the group's named barrier id.
 // `need` must not exceed the number of active values.
 template <int NT, typename Each>
+__device__ Threshold radix_refine(Threshold t, SelectScratch& sc, int tid, int bar, Each each);
+
+template <int NT, typename Each>
 __device__ Threshold radix_threshold_each(uint32_t need, SelectScratch& sc, int tid, int bar, Each each) {
   constexpr int NW = NT / 32;
   const int lane = tid & 31, warp = tid >> 5;
@@ -96,6 +99,14 @@ __device__ Threshold radix_threshold_each(uint32_t need, SelectScratch& sc, int 
   t.prefix = 0;
   t.need = need;
   t.all_eq = (sc.nact == need);
+  return radix_refine<NT>(t, sc, tid, bar, each);
+}
+
+// Narrow a threshold 8 bits at a time: among the values whose bits above t.lo
+// (relative to t.base) equal t.prefix, find the t.need-th largest.
+template <int NT, typename Each>
+__device__ Threshold radix_refine(Threshold t, SelectScratch& sc, int tid, int bar, Each each) {
+  const int lane = tid & 31, warp = tid >> 5;
   while (t.lo > 0 && !t.all_eq) {
     const int dlo = t.lo > 8 ? t.lo - 8 : 0;
     const int dbits = t.lo - dlo;
@@ -143,6 +154,121 @@ __device__ Threshold radix_threshold_each(uint32_t need, SelectScratch& sc, int 
     t.all_eq = (sc.bin_count == t.need);
     t.lo = dlo;
   }
+  return t;
+}
+
+// radix_threshold_each with a wider first step: the values are counted in
+// up to 512 bins fitted to [vmin, vmax] (`bins`: 512 words of scratch), and
+// when the bin that holds the need-th largest value then holds at most 32
+// values, one warp ranks them directly, so no further pass over the values
+// is made; otherwise the 8-bit passes continue inside that bin.
+template <int NT, typename Each>
+__device__ Threshold radix_threshold_fast(uint32_t need, SelectScratch& sc, uint32_t* bins, int tid, int bar,
+                                          Each each) {
+  constexpr int NW = NT / 32;
+  constexpr int kBins = 512;
+  constexpr int BPT = kBins / NT;  // bins per thread in the scan
+  static_assert(kBins % NT == 0, "whole bins per thread");
+  const int lane = tid & 31, warp = tid >> 5;
+  uint32_t lmin = 0xFFFFFFFFu, lmax = 0u, lcnt = 0u;
+  each([&](uint32_t v) {
+    lmin = min(lmin, v);
+    lmax = max(lmax, v);
+    ++lcnt;
+  });
+  lmin = __reduce_min_sync(0xFFFFFFFFu, lmin);
+  lmax = __reduce_max_sync(0xFFFFFFFFu, lmax);
+  lcnt = __reduce_add_sync(0xFFFFFFFFu, lcnt);
+  if (lane == 0) {
+    sc.wmin[warp] = lmin;
+    sc.wmax[warp] = lmax;
+    sc.wcnt[warp] = lcnt;
+  }
+#pragma unroll
+  for (int i = 0; i < BPT; ++i) bins[BPT * tid + i] = 0u;
+  if (tid == 0) sc.out_cnt = 0;
+  named_bar(bar, NT);
+  uint32_t vmin = sc.wmin[0], vmax = sc.wmax[0], nact = sc.wcnt[0];
+#pragma unroll
+  for (int w = 1; w < NW; ++w) {
+    vmin = min(vmin, sc.wmin[w]);
+    vmax = max(vmax, sc.wmax[w]);
+    nact += sc.wcnt[w];
+  }
+  Threshold t;
+  t.base = vmin;
+  const uint32_t span = vmax - vmin;
+  t.lo = span ? 32 - __clz(span) : 0;
+  t.prefix = 0;
+  t.need = need;
+  t.all_eq = (nact == need);
+  if (t.lo == 0 || t.all_eq) return t;  // (uniform: every thread read the same partials)
+  const int dlo = t.lo > 9 ? t.lo - 9 : 0;
+  each([&](uint32_t v) { atomicAdd(&bins[(v - t.base) >> dlo], 1u); });
+  named_bar(bar, NT);  // also: every thread has read the pass-0 partials
+  // bin holding the need-th largest value; thread tid owns bins [BPT*tid, BPT*tid + BPT)
+  uint32_t h[BPT];
+  uint32_t tot = 0;
+#pragma unroll
+  for (int i = 0; i < BPT; ++i) {
+    h[i] = bins[BPT * tid + i];
+    tot += h[i];
+  }
+  uint32_t suf = tot;  // inclusive suffix sum over lanes (higher lanes own higher bins)
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t o = __shfl_down_sync(0xFFFFFFFFu, suf, d);
+    if (lane + d < 32) suf += o;
+  }
+  if (lane == 0) sc.wcnt[warp] = suf;  // warp total
+  named_bar(bar, NT);
+  uint32_t above = suf - tot;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) above += w > warp ? sc.wcnt[w] : 0u;
+  if (above < need && need <= above + tot) {
+#pragma unroll
+    for (int i = BPT - 1; i >= 0; --i) {
+      if (above < need && need <= above + h[i]) {
+        sc.bin = BPT * tid + i;
+        sc.need_after = need - above;
+        sc.bin_count = h[i];
+      }
+      above += h[i];
+    }
+  }
+  named_bar(bar, NT);
+  const uint32_t B = sc.bin, nb = sc.need_after, cb = sc.bin_count;
+  t.prefix = B;
+  t.need = nb;
+  t.all_eq = (cb == nb);
+  t.lo = dlo;
+  if (t.all_eq || dlo == 0) return t;
+  if (cb > 32) return radix_refine<NT>(t, sc, tid, bar, each);
+  // few values in the bin: collect them (sc.wmin holds 32) and rank them in one warp
+  each([&](uint32_t v) {
+    if (((v - t.base) >> dlo) == B) sc.wmin[atomicAdd(&sc.out_cnt, 1)] = v;
+  });
+  named_bar(bar, NT);
+  if (warp == 0) {
+    const uint32_t x = lane < (int)cb ? sc.wmin[lane] : 0u;
+    uint32_t gt = 0, eq = 0;
+    for (uint32_t j = 0; j < cb; ++j) {
+      const uint32_t y = sc.wmin[j];
+      gt += y > x ? 1u : 0u;
+      eq += y == x ? 1u : 0u;
+    }
+    // the nb-th largest of the bin (lanes holding the same value write the same)
+    if (lane < (int)cb && gt < nb && nb <= gt + eq) {
+      sc.tau = x;
+      sc.need_after = nb - gt;
+      sc.bin_count = eq;
+    }
+  }
+  named_bar(bar, NT);
+  t.prefix = sc.tau - t.base;
+  t.lo = 0;
+  t.need = sc.need_after;
+  t.all_eq = (sc.bin_count == t.need);
   return t;
 }
 
@@ -614,7 +740,8 @@ __device__ uint32_t select512_sub_to_aux(const uint32_t* key, const int32_t* idx
   for (int u = 1; u < W; ++u) c = w == u ? counts[u] : c;  // no dynamic index: keeps counts in registers
   const uint32_t* const mk = key + w * SUB;
   const int32_t* const mi = idx + w * SUB;
-  const Threshold t = radix_threshold_each<NT>((uint32_t)K, sc, tid, bar, [&](auto fn) {
+  // aux_key is this call's output and free until the end: it serves as bins
+  const Threshold t = radix_threshold_fast<NT>((uint32_t)K, sc, aux_key, tid, bar, [&](auto fn) {
     for (int j = lane; j < c; j += 32) fn(mk[j]);
   });
   Threshold ti{};
