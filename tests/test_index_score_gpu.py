@@ -283,3 +283,32 @@ def test_bf16_fused_prefill_full_size_sampled():
     inp = W.fused_prefill(dtype="bf16")
     got = _fused(inp, group_rows=4)
     _check_topk(got, inp, rows=[0, 1, 2, 3, 2047, 2048, 4093, 4094, 4095])
+
+
+@pytest.mark.parametrize("dtype", ["e4m3", "bf16"])
+def test_chunked_prefix_calls_match_one_call(dtype):
+    """A long extend processed as several calls, each holding one chunk of the
+    query rows (causal over prefix + chunk, the same block table): every
+    row's slots, indices and scores equal those of one call over all rows,
+    bit for bit (a row's scores and selection do not depend on the other
+    rows of the call or on how the keys are split into units)."""
+    import sparse_attention_indexer_top_gb300 as sai
+
+    rows, kv = 96, 9000
+    lens = (kv - rows + 1 + np.arange(rows)).astype(np.int32)
+    blocks = -(-kv // 128)
+    inp = W.make_fused_inputs(58, rows, 64, 128, blocks + 3, lens, (1, blocks), row_to_batch=np.zeros(rows, np.int32),
+                              dtype=dtype)
+    whole = _fused(inp, group_rows=4)
+    _check_topk(whole, inp, rows=[0, 1, 47, 94, 95])
+    d = _dev_inputs(inp)
+    for lo, hi in ((0, 32), (32, 40), (40, 96)):
+        n = d["seq_lens"][lo:hi]
+        s, i, sc = sai.index_score_topk(d["q"][lo:hi], d["w"][lo:hi], d["kcache"], d["kscale"], d["block_table"], n,
+                                        max_seq_len=int(lens[hi - 1]), row_to_batch=d["row_to_batch"][lo:hi],
+                                        group_rows=4)
+        torch.cuda.synchronize()
+        assert sai.device_status() == 0
+        assert np.array_equal(s.cpu().numpy(), whole[0][lo:hi])
+        assert np.array_equal(i.cpu().numpy(), whole[1][lo:hi])
+        assert np.array_equal(sc.cpu().numpy().view(np.uint32), whole[2][lo:hi].view(np.uint32))

@@ -169,3 +169,23 @@ def test_packed_extend_full_size_sampled():
         rs, ri = oracle_topk(w[None, :], np.array([n]), pt[[r2b[i]]], 1, 512)
         assert np.array_equal(gi[i], ri[0]), i
         assert np.array_equal(gs[i], rs[0]), i
+
+
+def test_chunked_prefix_calls_match_one_call():
+    """Chunked-prefix-cache extend: the packed plan (row_starts, seq_lens,
+    row_to_batch) covers the whole forward, but each call holds one chunk of
+    the score rows and that chunk's slice of the plan. Each chunk's outputs
+    equal the rows of one call over everything, and the oracle."""
+    import sparse_attention_indexer_top_gb300 as sai
+
+    inp = W.packed_extend(seed=16, reqs=2, new_tokens=150, kv_len=6000, fill=np.inf)
+    whole = _run(inp)
+    _assert_equal(whole, _oracle(inp), "one call vs oracle")
+    pt = _t(inp.page_tables)
+    for lo, hi in ((0, 70), (70, 151), (151, 300)):
+        slots, idx = sai.topk_transform(_t(inp.scores[lo:hi]), _t(inp.seq_lens[lo:hi]), pt, page_size=inp.page_size,
+                                        row_starts=_t(inp.row_starts[lo:hi]), row_to_batch=_t(inp.row_to_batch[lo:hi]),
+                                        want_indices=True)
+        torch.cuda.synchronize()
+        assert sai.device_status() == 0
+        _assert_equal((slots.cpu().numpy(), idx.cpu().numpy()), (whole[0][lo:hi], whole[1][lo:hi]), f"chunk {lo}:{hi}")
