@@ -136,3 +136,55 @@ def index_score_topk(inp, rows: Optional[Sequence[int]] = None):
         tops[j, : sel.size] = scores[j][sel]
         slots[j, : sel.size] = page_transform(sel, inp.block_table[b], inp.block_size)
     return slots, idxs, tops, scores
+
+
+def index_scores_per_head(inp, rows: Optional[Sequence[int]] = None) -> list:
+    """Per-index-head scores: one float32 array [H, n] per listed row with
+    ``score_h(t) = kscale[p, o] * w[i, h] * relu(q[i, h] . k[p, o])``.
+
+    The fused decode kernel of ROCm/ATOM PR #1473 is launched over
+    ``(total_q, num_idx_heads, num_topk_chunks)`` (review diff of
+    ``index_topk.py``), one program per index head, which admits a selection
+    per head; a head's score is then its summand of the head-summed score.
+    The dot products are exact (integer e4m3 units) or float64 (bf16), the
+    product ``kscale * w * relu`` is formed in float64 and rounded once.
+    """
+    rows = list(range(inp.rows)) if rows is None else list(rows)
+    dtype = getattr(inp, "dtype", "e4m3")
+    out = []
+    for i in rows:
+        b = i if inp.row_to_batch is None else int(inp.row_to_batch[i])
+        n = int(inp.seq_lens[i])
+        heads = inp.q.shape[1]
+        if n <= 0:
+            out.append(np.zeros((heads, 0), np.float32))
+            continue
+        ku, pages, offs = _key_units(inp.kcache, inp.block_table[b], n, inp.block_size, dtype)
+        scale = _scale_of(inp.kscale, pages, offs).astype(np.float64)
+        dots = _units(inp.q[i], dtype) @ ku.T  # [H, n]
+        if dtype == "e4m3":
+            dots = dots * _PROD_UNIT
+        relu = np.maximum(dots, 0.0)
+        w = np.asarray(inp.w[i], dtype=np.float64)[:, None]
+        out.append((relu * w * scale[None, :]).astype(np.float32))
+    return out
+
+
+def index_score_topk_per_head(inp, rows: Optional[Sequence[int]] = None):
+    """Top-k per (row, index head): ``(slots, indices, scores)`` with slots and
+    indices int32 ``[R, H, k]`` (-1 padded) selected by (score desc, index
+    asc) from each head's scores, and the per-row [H, n] score arrays."""
+    rows = list(range(inp.rows)) if rows is None else list(rows)
+    k = inp.k
+    heads = inp.q.shape[1]
+    scores = index_scores_per_head(inp, rows)
+    slots = np.full((len(rows), heads, k), -1, np.int32)
+    idxs = np.full((len(rows), heads, k), -1, np.int32)
+    for j, i in enumerate(rows):
+        b = i if inp.row_to_batch is None else int(inp.row_to_batch[i])
+        for h in range(heads):
+            sel = topk_row(scores[j][h], k)
+            idxs[j, h, : sel.size] = sel
+            slots[j, h, : sel.size] = page_transform(sel, inp.block_table[b], inp.block_size)
+    return slots, idxs, scores
+
