@@ -205,6 +205,61 @@ int sai_index_score_bf16(const uint16_t* q_bf16, const float* w, const uint16_t*
                          int64_t out_stride, sai_stream_t stream);
 
 /*
+ * Per-index-head top-k: one selection per (query row, index head).
+ *
+ * The fused decode kernel of ROCm/ATOM PR #1473 is launched over (query,
+ * index head, key chunk) (review diff of index_topk.py), which admits a
+ * selection per index head. Head h's score is its summand of the
+ * head-summed score:
+ *   score_h(t) = kscale[p*128 + o] * w[i*64 + h] * relu(sum_d q[i,h,d] k[p,o,d])
+ * (p, o, n, b as for sai_index_score_topk), and each (i, h) takes its top-k
+ * keys by (score desc, index asc).
+ *
+ * sai_index_score_per_head[_bf16] writes the scores densely:
+ *   out_scores[(i*64 + h)*out_stride + t] = score_h(t) for t < seq_lens[i]
+ * (other cells untouched; a key on a block id outside [0, num_blocks) gets
+ * -inf and sets status bit 4). out_stride >= max_seq_len.
+ *
+ * sai_index_score_topk_per_head[_bf16] computes those scores into its
+ * workspace and selects with the top-k kernel:
+ *   out_indices[(i*64 + h)*512 + j] = t_j, out_slots[...] = p_j*128 + o_j
+ * (-1 padded; either output may be NULL, not both). The workspace holds
+ * rows*64 score rows of max_seq_len floats (rounded up to 4) plus metadata:
+ * sai_index_score_topk_per_head_workspace(...) bytes, 256-byte aligned
+ * (about 17 MB per decode row of 32768 keys).
+ *
+ * Arguments as for sai_index_score_topk (FP8) / sai_index_score_topk_bf16
+ * (bf16, kscale may be NULL), without group_rows (rows are scored one per
+ * unit). Same host errors; bad rows are emptied and flagged as there.
+ */
+size_t sai_index_score_topk_per_head_workspace(int64_t rows, int32_t max_seq_len, int32_t k);
+int sai_index_score_per_head(const uint8_t* q_fp8, const float* w, const uint8_t* kcache_fp8, const float* kscale,
+                             int64_t num_blocks, const int32_t* block_table, int64_t bt_rows, int64_t bt_stride,
+                             const int32_t* row_to_batch, const int32_t* seq_lens, int64_t rows, int32_t heads,
+                             int32_t dim, int32_t block_size, int32_t max_seq_len, float* out_scores,
+                             int64_t out_stride, sai_stream_t stream);
+int sai_index_score_per_head_bf16(const uint16_t* q_bf16, const float* w, const uint16_t* kcache_bf16,
+                                  const float* kscale, int64_t num_blocks, const int32_t* block_table,
+                                  int64_t bt_rows, int64_t bt_stride, const int32_t* row_to_batch,
+                                  const int32_t* seq_lens, int64_t rows, int32_t heads, int32_t dim,
+                                  int32_t block_size, int32_t max_seq_len, float* out_scores, int64_t out_stride,
+                                  sai_stream_t stream);
+int sai_index_score_topk_per_head(const uint8_t* q_fp8, const float* w, const uint8_t* kcache_fp8,
+                                  const float* kscale, int64_t num_blocks, const int32_t* block_table,
+                                  int64_t bt_rows, int64_t bt_stride, const int32_t* row_to_batch,
+                                  const int32_t* seq_lens, int64_t rows, int32_t heads, int32_t dim,
+                                  int32_t block_size, int32_t max_seq_len, int32_t k, int32_t* out_slots,
+                                  int32_t* out_indices, void* workspace, size_t workspace_bytes,
+                                  sai_stream_t stream);
+int sai_index_score_topk_per_head_bf16(const uint16_t* q_bf16, const float* w, const uint16_t* kcache_bf16,
+                                       const float* kscale, int64_t num_blocks, const int32_t* block_table,
+                                       int64_t bt_rows, int64_t bt_stride, const int32_t* row_to_batch,
+                                       const int32_t* seq_lens, int64_t rows, int32_t heads, int32_t dim,
+                                       int32_t block_size, int32_t max_seq_len, int32_t k, int32_t* out_slots,
+                                       int32_t* out_indices, void* workspace, size_t workspace_bytes,
+                                       sai_stream_t stream);
+
+/*
  * sai_sparse_blocks -- per-row distinct KV blocks of top-k slots.
  *
  * Follows ROCm/ATOM PR #1282 "merge build sparse block into topk" (title and

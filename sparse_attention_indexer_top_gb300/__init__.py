@@ -196,6 +196,58 @@ def index_score(q: torch.Tensor, w: torch.Tensor, kcache: torch.Tensor, kscale: 
     return out
 
 
+def index_score_per_head(q: torch.Tensor, w: torch.Tensor, kcache: torch.Tensor, kscale: Optional[torch.Tensor],
+                         block_table: torch.Tensor, seq_lens: torch.Tensor, *, max_seq_len: int,
+                         row_to_batch: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                         stream=None) -> torch.Tensor:
+    """Dense per-index-head scores ``[rows, 64, max_seq_len]``: head h's
+    summand ``kscale * w_h * relu(q_h . k)`` of the index score (FP8 or bf16
+    cache, as for ``index_score_topk``; a new ``out`` starts as NaN)."""
+    dev, bf16 = _fused_check(q, w, kcache, kscale, block_table, seq_lens, row_to_batch)
+    rows, heads = q.shape[0], q.shape[1]
+    if out is None:
+        out = torch.full((rows, heads, max(max_seq_len, 1)), float("nan"), dtype=torch.float32, device=dev)
+    if out.dim() != 3 or out.stride(2) != 1 or out.stride(0) != heads * out.stride(1):
+        raise ValueError("out must be [rows, 64, stride] with rows of 64 contiguous head rows")
+    name = "sai_index_score_per_head_bf16" if bf16 else "sai_index_score_per_head"
+    st = getattr(load(), name)(
+        _ptr(q), _ptr(w), _ptr(kcache), _ptr(kscale), kcache.shape[0], _ptr(block_table), block_table.shape[0],
+        block_table.stride(0), _ptr(row_to_batch), _ptr(seq_lens), rows, heads, q.shape[2], kcache.shape[1],
+        int(max_seq_len), _ptr(out), out.stride(1), _stream(stream))
+    check(st, name)
+    return out
+
+
+def index_score_topk_per_head_workspace(rows: int, max_seq_len: int, k: int = TOPK) -> int:
+    return int(load().sai_index_score_topk_per_head_workspace(int(rows), int(max_seq_len), int(k)))
+
+
+def index_score_topk_per_head(q: torch.Tensor, w: torch.Tensor, kcache: torch.Tensor, kscale: Optional[torch.Tensor],
+                              block_table: torch.Tensor, seq_lens: torch.Tensor, *, max_seq_len: int,
+                              row_to_batch: Optional[torch.Tensor] = None, k: int = TOPK,
+                              out_slots: Optional[torch.Tensor] = None, out_indices: Optional[torch.Tensor] = None,
+                              workspace: Optional[torch.Tensor] = None, stream=None):
+    """Top-k per (row, index head) of the per-head scores: ``(slots,
+    indices)``, int32 ``[rows, 64, k]`` (-1 padded)."""
+    dev, bf16 = _fused_check(q, w, kcache, kscale, block_table, seq_lens, row_to_batch)
+    rows, heads = q.shape[0], q.shape[1]
+    if out_slots is None:
+        out_slots = torch.empty((rows, heads, k), dtype=torch.int32, device=dev)
+    if out_indices is None:
+        out_indices = torch.empty((rows, heads, k), dtype=torch.int32, device=dev)
+    ws = index_score_topk_per_head_workspace(rows, max_seq_len, k) if rows else 0
+    if workspace is None and ws:
+        workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+    name = "sai_index_score_topk_per_head_bf16" if bf16 else "sai_index_score_topk_per_head"
+    st = getattr(load(), name)(
+        _ptr(q), _ptr(w), _ptr(kcache), _ptr(kscale), kcache.shape[0], _ptr(block_table), block_table.shape[0],
+        block_table.stride(0), _ptr(row_to_batch), _ptr(seq_lens), rows, heads, q.shape[2], kcache.shape[1],
+        int(max_seq_len), int(k), _ptr(out_slots), _ptr(out_indices), _ptr(workspace),
+        0 if workspace is None else workspace.numel(), _stream(stream))
+    check(st, name)
+    return out_slots, out_indices
+
+
 def sparse_blocks(slots: torch.Tensor, block_size: int = 128, *, out_blocks: Optional[torch.Tensor] = None,
                   out_counts: Optional[torch.Tensor] = None, stream=None):
     """Per-row distinct KV blocks of top-k slots: ``(blocks [rows, k] int32,

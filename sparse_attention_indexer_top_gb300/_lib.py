@@ -32,6 +32,17 @@ SIGNATURES = {
                                                  _c_size, _vp]),
     "sai_index_score_bf16": (ctypes.c_int, [_vp, _vp, _vp, _vp, _c_i64, _vp, _c_i64, _c_i64, _vp, _vp, _c_i64, _c_i32,
                                             _c_i32, _c_i32, _c_i32, _c_i32, _vp, _c_i64, _vp]),
+    "sai_index_score_topk_per_head_workspace": (_c_size, [_c_i64, _c_i32, _c_i32]),
+    "sai_index_score_per_head": (ctypes.c_int, [_vp, _vp, _vp, _vp, _c_i64, _vp, _c_i64, _c_i64, _vp, _vp, _c_i64,
+                                                _c_i32, _c_i32, _c_i32, _c_i32, _vp, _c_i64, _vp]),
+    "sai_index_score_per_head_bf16": (ctypes.c_int, [_vp, _vp, _vp, _vp, _c_i64, _vp, _c_i64, _c_i64, _vp, _vp,
+                                                     _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _vp, _c_i64, _vp]),
+    "sai_index_score_topk_per_head": (ctypes.c_int, [_vp, _vp, _vp, _vp, _c_i64, _vp, _c_i64, _c_i64, _vp, _vp,
+                                                     _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _vp, _vp, _vp,
+                                                     _c_size, _vp]),
+    "sai_index_score_topk_per_head_bf16": (ctypes.c_int, [_vp, _vp, _vp, _vp, _c_i64, _vp, _c_i64, _c_i64, _vp, _vp,
+                                                          _c_i64, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _vp, _vp,
+                                                          _vp, _c_size, _vp]),
     "sai_topk_transform_noalloc": (ctypes.c_int, [_vp, _c_i64, _c_i64, _vp, _vp, _vp, _c_i64, _c_i64, _vp, _c_i32,
                                                   _c_i32, _vp, _vp, _vp]),
     "sai_sparse_blocks": (ctypes.c_int, [_vp, _c_i64, _c_i32, _c_i32, _vp, _vp, _vp]),

@@ -194,7 +194,11 @@ __host__ __device__ constexpr int fused_threads() {
   return R * kEpiRow + 64;  // R row groups of 4 epilogue warps, a TMA warp, an MMA warp
 }
 
-template <int R, bool DENSE, bool BF16>
+// What the epilogue produces: the running top-k (partial lists), the dense
+// head-summed scores, or the dense per-head scores (each head's summand).
+constexpr int kModeTopk = 0, kModeDense = 1, kModePerHead = 2;
+
+template <int R, int MODE, bool BF16>
 __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16>()))
     fused_score_topk_kernel(const __grid_constant__ FusedLaunch p, const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap qmap) {
@@ -235,7 +239,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
-  if constexpr (!DENSE) pdl_trigger();  // the merge may be scheduled now; it waits for this grid to finish
+  if constexpr (MODE == kModeTopk) pdl_trigger();  // the merge may be scheduled now; it waits for this grid to finish
 
   // Every role walks the same units (u = blockIdx.x, + gridDim.x, ...) and
   // derives the same tile counts, so the barrier phases below (counted over
@@ -420,6 +424,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
         const int t = blk * kBlk + kl;
         const bool page_ok = ok_next;
         const float ks = ks_next;
+        const int page = page_next;
         if (i + 1 < ntiles) {
           page_next = __ldg(bt + i + 1);
           ok_next = page_next >= 0 && page_next < p.num_blocks;
@@ -437,6 +442,18 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
           // power-of-two scalings are exact, so every product is w_h relu(s_h).
           // acc[k] = this lane's partial for keys l/4, l/4+8, 16+l/4, 24+l/4
           float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+          // per-head mode: the scales of this lane's 4 keys, and its row's
+          // [64, dense_stride] block of the output
+          float ksq[4] = {0.f, 0.f, 0.f, 0.f};
+          float* const ph_out = p.dense + (long long)(m.row0 + (row_live ? r : 0)) * kH * p.dense_stride;
+          if constexpr (MODE == kModePerHead) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int key = quad * 32 + (lane >> 2) + 8 * (e & 1) + 16 * (e >> 1);
+              ksq[e] = page_ok ? (p.kscale ? __ldg(p.kscale + (long long)page * kBlk + key) : 1.f)
+                               : __int_as_float(0xFF800000);  // a key on a bad block scores -inf
+            }
+          }
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             uint32_t a[32];
@@ -451,8 +468,27 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
             for (int j = 0; j < 8; ++j) {
               const float2 x0 = make_float2(relu_of<BF16>(a[4 * j]), relu_of<BF16>(a[4 * j + 1]));
               const float2 x1 = make_float2(relu_of<BF16>(a[4 * j + 2]), relu_of<BF16>(a[4 * j + 3]));
-              acc[2 * half] = __ffma2_rn(x0, w2[j], acc[2 * half]);
-              acc[2 * half + 1] = __ffma2_rn(x1, w2[j], acc[2 * half + 1]);
+              if constexpr (MODE == kModePerHead) {
+                // heads h0, h0 + 1 of keys key0 and key0 + 8: w_h relu(s_h) x scale
+                const int h0 = 8 * j + 2 * (lane & 3);
+                const int key0 = quad * 32 + 16 * half + (lane >> 2);
+                const int t0 = blk * kBlk + key0, t1 = t0 + 8;
+                float* const o0 = ph_out + (long long)h0 * p.dense_stride;
+                float* const o1 = o0 + p.dense_stride;
+                if (row_live && t0 < nr) {
+                  const float sc = ksq[2 * half];
+                  o0[t0] = page_ok ? x0.x * w2[j].x * sc : sc;
+                  o1[t0] = page_ok ? x0.y * w2[j].y * sc : sc;
+                }
+                if (row_live && t1 < nr) {
+                  const float sc = ksq[2 * half + 1];
+                  o0[t1] = page_ok ? x1.x * w2[j].x * sc : sc;
+                  o1[t1] = page_ok ? x1.y * w2[j].y * sc : sc;
+                }
+              } else {
+                acc[2 * half] = __ffma2_rn(x0, w2[j], acc[2 * half]);
+                acc[2 * half + 1] = __ffma2_rn(x1, w2[j], acc[2 * half + 1]);
+              }
             }
           }
           const float p0 = acc[0].x + acc[0].y, p1 = acc[1].x + acc[1].y;
@@ -468,9 +504,9 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
           score = (keep + __shfl_xor_sync(0xFFFFFFFFu, hi ? k0 : k1, 2)) * ks;
         }
         const bool live = ok && row_live && page_ok && t < nr;
-        if constexpr (DENSE) {
+        if constexpr (MODE == kModeDense) {
           if (live) p.dense[(long long)(m.row0 + r) * p.dense_stride + t] = score;
-        } else {
+        } else if constexpr (MODE == kModeTopk) {
           // running top-k filter: append survivors to this warp's sub-list
           const bool pass = live && score >= tf;
           const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass);
@@ -487,7 +523,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
           }
         }
       }
-      if constexpr (!DENSE) {
+      if constexpr (MODE == kModeTopk) {
         // unit end: cut the row's list to 512 and write it as a partial list
         __syncwarp();
         const int kept = exchange(true);
@@ -548,7 +584,7 @@ bool make_map(CUtensorMap* map, const void* base, long long rows, int box_rows, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int R, bool DENSE, bool BF16>
+template <int R, int MODE, bool BF16>
 cudaError_t launch_fused_t(const FusedLaunch& p, const void* kcache, cudaStream_t stream) {
   CUtensorMap kmap, qmap;
   if (!make_map(&kmap, kcache, p.num_blocks * kBlk, kBlk, BF16)) return cudaErrorInvalidValue;
@@ -558,7 +594,7 @@ cudaError_t launch_fused_t(const FusedLaunch& p, const void* kcache, cudaStream_
   cudaGetDevice(&dev);
   constexpr size_t smem = fused_smem_bytes<R, BF16>();
   if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(fused_score_topk_kernel<R, DENSE, BF16>,
+    cudaError_t e = cudaFuncSetAttribute(fused_score_topk_kernel<R, MODE, BF16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
@@ -569,7 +605,7 @@ cudaError_t launch_fused_t(const FusedLaunch& p, const void* kcache, cudaStream_
   // then runs once per CTA.
   const long long units = (long long)((p.rows + R - 1) / R) * p.chunks;
   const int grid = (int)units;
-  fused_score_topk_kernel<R, DENSE, BF16><<<grid, fused_threads<R>(), smem, stream>>>(p, kmap, qmap);
+  fused_score_topk_kernel<R, MODE, BF16><<<grid, fused_threads<R>(), smem, stream>>>(p, kmap, qmap);
   return cudaGetLastError();
 }
 
@@ -596,16 +632,21 @@ FusedPlan fused_plan(long long rows, int max_seq_len, int group_rows, int num_sm
   return pl;
 }
 
-cudaError_t launch_fused(const FusedLaunch& p, int group, bool dense, bool bf16, const void* kcache,
+template <int MODE>
+cudaError_t launch_fused_m(const FusedLaunch& p, int group, bool bf16, const void* kcache, cudaStream_t stream) {
+  if (bf16)
+    return group == 2 ? launch_fused_t<2, MODE, true>(p, kcache, stream) : launch_fused_t<1, MODE, true>(p, kcache, stream);
+  return group == 2 ? launch_fused_t<2, MODE, false>(p, kcache, stream) : launch_fused_t<1, MODE, false>(p, kcache, stream);
+}
+
+cudaError_t launch_fused(const FusedLaunch& p, int group, FusedOut out, bool bf16, const void* kcache,
                          cudaStream_t stream) {
-  if (bf16) {
-    if (group == 2)
-      return dense ? launch_fused_t<2, true, true>(p, kcache, stream) : launch_fused_t<2, false, true>(p, kcache, stream);
-    return dense ? launch_fused_t<1, true, true>(p, kcache, stream) : launch_fused_t<1, false, true>(p, kcache, stream);
+  switch (out) {
+    case FusedOut::kTopk: return launch_fused_m<kModeTopk>(p, group, bf16, kcache, stream);
+    case FusedOut::kDense: return launch_fused_m<kModeDense>(p, group, bf16, kcache, stream);
+    case FusedOut::kPerHead: return launch_fused_m<kModePerHead>(p, group, bf16, kcache, stream);
   }
-  if (group == 2)
-    return dense ? launch_fused_t<2, true, false>(p, kcache, stream) : launch_fused_t<2, false, false>(p, kcache, stream);
-  return dense ? launch_fused_t<1, true, false>(p, kcache, stream) : launch_fused_t<1, false, false>(p, kcache, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace sai

@@ -2,6 +2,7 @@
 // status word, launch on the caller's stream. See include/sai.h.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cstdint>
 #include <mutex>
@@ -226,7 +227,7 @@ int fused_topk(const void* q, const float* w, const void* kcache, const float* k
   p.part_idx = reinterpret_cast<int32_t*>(ws + units * SAI_TOPK * 4);
   p.part_cnt = reinterpret_cast<int*>(ws + units * SAI_TOPK * 8);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = sai::launch_fused(p, plan.group, false, bf16, kcache, s);
+  cudaError_t e = sai::launch_fused(p, plan.group, sai::FusedOut::kTopk, bf16, kcache, s);
   if (e != cudaSuccess) return cuda_status(e);
   sai::MergeLaunch m{};
   m.rows = static_cast<int>(rows);
@@ -265,7 +266,89 @@ int fused_dense(const void* q, const float* w, const void* kcache, const float* 
                                     seq_lens, rows, max_seq_len, plan, st);
   p.dense = out_scores;
   p.dense_stride = out_stride;
-  return cuda_status(sai::launch_fused(p, plan.group, true, bf16, kcache, reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_status(
+      sai::launch_fused(p, plan.group, sai::FusedOut::kDense, bf16, kcache, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// Per-head top-k workspace: dense per-head scores [rows * 64, stride], the
+// per-(row, head) lengths and block-table rows, then the top-k workspace.
+struct PerHeadLayout {
+  long long stride;
+  size_t lens_off, batch_off, topk_off, topk_bytes, total;
+};
+
+bool per_head_layout(int64_t rows, int32_t max_seq_len, int sms, PerHeadLayout* L) {
+  if (rows <= 0 || max_seq_len < 0 || rows > INT_MAX / (16 * 64)) return false;
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const long long hr = rows * 64;
+  L->stride = std::max<long long>(4, (static_cast<long long>(max_seq_len) + 3) / 4 * 4);
+  const size_t dense = static_cast<size_t>(hr) * L->stride * sizeof(float);
+  L->lens_off = up(dense);
+  L->batch_off = L->lens_off + up(static_cast<size_t>(hr) * 4);
+  L->topk_off = L->batch_off + up(static_cast<size_t>(hr) * 4);
+  L->topk_bytes = sai::topk_plan(hr, L->stride, sms).workspace_bytes;
+  L->total = L->topk_off + up(std::max<size_t>(L->topk_bytes, 256));
+  return true;
+}
+
+int fused_per_head_dense(const void* q, const float* w, const void* kcache, const float* kscale, bool bf16,
+                         int64_t num_blocks, const int32_t* block_table, int64_t bt_rows, int64_t bt_stride,
+                         const int32_t* row_to_batch, const int32_t* seq_lens, int64_t rows, int32_t heads,
+                         int32_t dim, int32_t block_size, int32_t max_seq_len, float* out_scores, int64_t out_stride,
+                         sai_stream_t stream) {
+  int st_arg = check_fused_args(q, w, kcache, kscale, bf16, num_blocks, block_table, bt_rows, bt_stride,
+                                row_to_batch, seq_lens, rows, heads, dim, block_size, max_seq_len, 1);
+  if (st_arg != SAI_OK || rows == 0) return st_arg;
+  if (!out_scores) return SAI_ERR_NULL;
+  if (out_stride < max_seq_len) return SAI_ERR_SHAPE;
+  if (!aligned(out_scores, 4)) return SAI_ERR_ALIGN;
+  int dev, sms;
+  int* st;
+  if (!device_setup(&dev, &st, &sms)) return SAI_ERR_CUDA;
+  const sai::FusedPlan plan = sai::fused_plan(rows, max_seq_len, 1, sms);
+  sai::FusedLaunch p = fused_launch(q, w, kscale, num_blocks, block_table, bt_rows, bt_stride, row_to_batch,
+                                    seq_lens, rows, max_seq_len, plan, st);
+  p.dense = out_scores;
+  p.dense_stride = out_stride;
+  return cuda_status(
+      sai::launch_fused(p, plan.group, sai::FusedOut::kPerHead, bf16, kcache, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fused_per_head_topk(const void* q, const float* w, const void* kcache, const float* kscale, bool bf16,
+                        int64_t num_blocks, const int32_t* block_table, int64_t bt_rows, int64_t bt_stride,
+                        const int32_t* row_to_batch, const int32_t* seq_lens, int64_t rows, int32_t heads,
+                        int32_t dim, int32_t block_size, int32_t max_seq_len, int32_t k, int32_t* out_slots,
+                        int32_t* out_indices, void* workspace, size_t workspace_bytes, sai_stream_t stream) {
+  if (k <= 0) return SAI_ERR_SHAPE;
+  if (k != SAI_TOPK) return SAI_ERR_UNSUPPORTED;
+  if (!out_slots && !out_indices) return SAI_ERR_NULL;
+  int st_arg = check_fused_args(q, w, kcache, kscale, bf16, num_blocks, block_table, bt_rows, bt_stride,
+                                row_to_batch, seq_lens, rows, heads, dim, block_size, max_seq_len, 1);
+  if (st_arg != SAI_OK || rows == 0) return st_arg;
+  if ((out_slots && !aligned(out_slots, 4)) || (out_indices && !aligned(out_indices, 4))) return SAI_ERR_ALIGN;
+  int dev, sms;
+  int* st;
+  if (!device_setup(&dev, &st, &sms)) return SAI_ERR_CUDA;
+  PerHeadLayout L;
+  if (!per_head_layout(rows, max_seq_len, sms, &L)) return SAI_ERR_SHAPE;
+  if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256)) return SAI_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  float* dense = reinterpret_cast<float*>(ws);
+  int* lens = reinterpret_cast<int*>(ws + L.lens_off);
+  int* batch = reinterpret_cast<int*>(ws + L.batch_off);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = sai::launch_per_head_expand(seq_lens, row_to_batch, static_cast<int>(rows), max_seq_len, bt_rows,
+                                              bt_stride, lens, batch, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  const sai::FusedPlan plan = sai::fused_plan(rows, max_seq_len, 1, sms);
+  sai::FusedLaunch p = fused_launch(q, w, kscale, num_blocks, block_table, bt_rows, bt_stride, row_to_batch,
+                                    seq_lens, rows, max_seq_len, plan, st);
+  p.dense = dense;
+  p.dense_stride = L.stride;
+  e = sai::launch_fused(p, plan.group, sai::FusedOut::kPerHead, bf16, kcache, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  return sai_topk_transform(dense, rows * 64, L.stride, nullptr, lens, block_table, bt_rows, bt_stride, batch, 128,
+                            SAI_TOPK, out_slots, out_indices, ws + L.topk_off, L.topk_bytes, stream);
 }
 
 }  // namespace
@@ -318,6 +401,60 @@ int sai_index_score_bf16(const uint16_t* q_bf16, const float* w, const uint16_t*
                          int64_t out_stride, sai_stream_t stream) {
   return fused_dense(q_bf16, w, kcache_bf16, kscale, true, num_blocks, block_table, bt_rows, bt_stride, row_to_batch,
                      seq_lens, rows, heads, dim, block_size, max_seq_len, group_rows, out_scores, out_stride, stream);
+}
+
+size_t sai_index_score_topk_per_head_workspace(int64_t rows, int32_t max_seq_len, int32_t k) {
+  if (k != SAI_TOPK || rows <= 0 || max_seq_len < 0) return 0;
+  int dev, sms;
+  int* st;
+  if (!device_setup(&dev, &st, &sms)) return 0;
+  PerHeadLayout L;
+  return per_head_layout(rows, max_seq_len, sms, &L) ? L.total : 0;
+}
+
+int sai_index_score_per_head(const uint8_t* q_fp8, const float* w, const uint8_t* kcache_fp8, const float* kscale,
+                             int64_t num_blocks, const int32_t* block_table, int64_t bt_rows, int64_t bt_stride,
+                             const int32_t* row_to_batch, const int32_t* seq_lens, int64_t rows, int32_t heads,
+                             int32_t dim, int32_t block_size, int32_t max_seq_len, float* out_scores,
+                             int64_t out_stride, sai_stream_t stream) {
+  return fused_per_head_dense(q_fp8, w, kcache_fp8, kscale, false, num_blocks, block_table, bt_rows, bt_stride,
+                              row_to_batch, seq_lens, rows, heads, dim, block_size, max_seq_len, out_scores,
+                              out_stride, stream);
+}
+
+int sai_index_score_per_head_bf16(const uint16_t* q_bf16, const float* w, const uint16_t* kcache_bf16,
+                                  const float* kscale, int64_t num_blocks, const int32_t* block_table,
+                                  int64_t bt_rows, int64_t bt_stride, const int32_t* row_to_batch,
+                                  const int32_t* seq_lens, int64_t rows, int32_t heads, int32_t dim,
+                                  int32_t block_size, int32_t max_seq_len, float* out_scores, int64_t out_stride,
+                                  sai_stream_t stream) {
+  return fused_per_head_dense(q_bf16, w, kcache_bf16, kscale, true, num_blocks, block_table, bt_rows, bt_stride,
+                              row_to_batch, seq_lens, rows, heads, dim, block_size, max_seq_len, out_scores,
+                              out_stride, stream);
+}
+
+int sai_index_score_topk_per_head(const uint8_t* q_fp8, const float* w, const uint8_t* kcache_fp8,
+                                  const float* kscale, int64_t num_blocks, const int32_t* block_table,
+                                  int64_t bt_rows, int64_t bt_stride, const int32_t* row_to_batch,
+                                  const int32_t* seq_lens, int64_t rows, int32_t heads, int32_t dim,
+                                  int32_t block_size, int32_t max_seq_len, int32_t k, int32_t* out_slots,
+                                  int32_t* out_indices, void* workspace, size_t workspace_bytes,
+                                  sai_stream_t stream) {
+  return fused_per_head_topk(q_fp8, w, kcache_fp8, kscale, false, num_blocks, block_table, bt_rows, bt_stride,
+                             row_to_batch, seq_lens, rows, heads, dim, block_size, max_seq_len, k, out_slots,
+                             out_indices, workspace, workspace_bytes, stream);
+}
+
+int sai_index_score_topk_per_head_bf16(const uint16_t* q_bf16, const float* w, const uint16_t* kcache_bf16,
+                                       const float* kscale, int64_t num_blocks, const int32_t* block_table,
+                                       int64_t bt_rows, int64_t bt_stride, const int32_t* row_to_batch,
+                                       const int32_t* seq_lens, int64_t rows, int32_t heads, int32_t dim,
+                                       int32_t block_size, int32_t max_seq_len, int32_t k, int32_t* out_slots,
+                                       int32_t* out_indices, void* workspace, size_t workspace_bytes,
+                                       sai_stream_t stream) {
+  return fused_per_head_topk(q_bf16, w, kcache_bf16, kscale, true, num_blocks, block_table, bt_rows, bt_stride,
+                             row_to_batch, seq_lens, rows, heads, dim, block_size, max_seq_len, k, out_slots,
+                             out_indices, workspace, workspace_bytes, stream);
 }
 
 int sai_sparse_blocks(const int32_t* slots, int64_t rows, int32_t k, int32_t block_size, int32_t* out_blocks,

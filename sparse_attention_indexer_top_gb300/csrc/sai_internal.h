@@ -88,7 +88,7 @@ struct FusedLaunch {
   uint32_t* part_key;
   int32_t* part_idx;
   int* part_cnt;     // [rows * chunks]
-  float* dense;      // scores-only mode: [rows, dense_stride]
+  float* dense;      // dense modes: [rows, dense_stride] or [rows, 64, dense_stride]
   long long dense_stride;
   int* status;
 };
@@ -99,7 +99,17 @@ struct FusedPlan {
   size_t workspace_bytes;
 };
 FusedPlan fused_plan(long long rows, int max_seq_len, int group_rows, int num_sms);
-cudaError_t launch_fused(const FusedLaunch& p, int group, bool dense, bool bf16, const void* kcache,
+// What a fused launch writes: per-(row, chunk) partial top-k lists, dense
+// head-summed scores [rows, dense_stride], or dense per-head scores
+// [rows, 64, dense_stride].
+enum class FusedOut { kTopk, kDense, kPerHead };
+cudaError_t launch_fused(const FusedLaunch& p, int group, FusedOut out, bool bf16, const void* kcache,
                          cudaStream_t stream);
+// Per-(row, head) lengths and block-table rows of the per-head top-k:
+// n = seq_lens[row] (0 for a row the fused kernel would reject), batch =
+// row_to_batch ? row_to_batch[row] : row.
+cudaError_t launch_per_head_expand(const int* seq_lens, const int* row_to_batch, int rows, int max_len,
+                                   long long bt_rows, long long bt_stride, int* out_lens, int* out_batch,
+                                   cudaStream_t stream);
 
 }  // namespace sai

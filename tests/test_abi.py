@@ -116,3 +116,28 @@ def test_fused_argument_errors(lib):
     assert lib.sai_index_score_topk_bf16(*args(q=odd, kscale=None), 512, p, p, p, p, 1 << 20, None) == -7
     assert lib.sai_index_score(*args(q=odd, kscale=None), p, 1024, None) == -1
     assert lib.sai_index_score_bf16(*args(q=odd, kscale=None), p, 1024, None) == -7
+
+
+def test_per_head_argument_errors(lib):
+    p = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 2)
+
+    def args(q=p, kscale=p, heads=64, rows=4):
+        return (q, p, p, kscale, 8, p, 4, 8, None, p, rows, heads, 128, 128, 1024)
+
+    for name in ("sai_index_score_topk_per_head", "sai_index_score_topk_per_head_bf16"):
+        f = getattr(lib, name)
+        tail = (512, p, p, p, 1 << 30, None)
+        assert f(*args(heads=32), *tail) == -3
+        assert f(*args(rows=-1), *tail) == -2
+        assert f(*args(q=None), *tail) == -1
+        assert f(*args(rows=0), *tail) == 0
+        assert f(*args(), 256, p, p, p, 1 << 30, None) == -3  # k must be 512
+        assert f(*args(), 512, None, None, p, 1 << 30, None) == -1  # no output
+    for name in ("sai_index_score_per_head", "sai_index_score_per_head_bf16"):
+        f = getattr(lib, name)
+        assert f(*args(heads=32), p, 1024, None) == -3
+        assert f(*args(), p, 1000, None) == -2  # out_stride < max_seq_len
+    assert lib.sai_index_score_topk_per_head(*args(q=odd, kscale=None), 512, p, p, p, 1 << 30, None) == -1
+    assert lib.sai_index_score_topk_per_head_bf16(*args(q=odd, kscale=None), 512, p, p, p, 1 << 30, None) == -7
+    assert lib.sai_index_score_topk_per_head_workspace(0, 100, 512) == 0
