@@ -302,6 +302,32 @@ def build_topk_decode_part(dev):
     return part
 
 
+def build_per_head_part(dev):
+    """Per-index-head top-k on the fused decode workload (64 rows, 64 heads x
+    128 e4m3, U[4096, 32768] keys): 4096 (row, head) selections. Not part of
+    the default step (a variant). Bytes: the key stream and the outputs (a
+    single-pass kernel's traffic); the library's two-stage design also writes
+    and reads a [4096, 32768] fp32 score buffer."""
+    import torch
+
+    import workloads as W
+
+    inp = W.fused_decode()
+    part = build_fused_part(dev, "per_head_decode", inp, 1)
+    rows = inp.rows
+    import sparse_attention_indexer_top_gb300 as sai
+
+    max_len = int(inp.seq_lens.max())
+    part.out = {"slots": torch.empty((rows, 64, K), dtype=torch.int32, device=dev),
+                "indices": torch.empty((rows, 64, K), dtype=torch.int32, device=dev)}
+    ws = sai.index_score_topk_per_head_workspace(rows, max_len)
+    part.out["workspace"] = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
+    n = inp.seq_lens.astype(np.int64)
+    part.bytes = float(n.sum()) * (inp.dim + 4) + inp.q.nbytes + inp.w.nbytes + rows * 64 * K * 8
+    part.launches = 3
+    return part
+
+
 def build_sparse_blocks_part(dev):
     """Per-row block lists of a packed-extend-sized top-k output: 16384 rows
     of 512 token slots of a 140000-slot pool (page_size 1), 128-token blocks.
@@ -341,6 +367,8 @@ def build_parts(dev, args):
                                       4))
     if "sparse_blocks" in args.paths:
         parts.append(build_sparse_blocks_part(dev))
+    if "per_head_decode" in args.paths:
+        parts.append(build_per_head_part(dev))
     if "topk_decode" in args.paths:
         parts.append(build_topk_decode_part(dev))
     return parts
@@ -352,6 +380,11 @@ def launch_part(part, stream):
     d, o = part.dev, part.out
     if part.name == "sparse_blocks":
         sai.sparse_blocks(d["slots"], 128, out_blocks=o["blocks"], out_counts=o["counts"], stream=stream)
+    elif part.name == "per_head_decode":
+        sai.index_score_topk_per_head(d["q"], d["w"], d["kcache"], d["kscale"], d["block_table"], d["seq_lens"],
+                                      max_seq_len=part.meta["max_len"], row_to_batch=d.get("row_to_batch"),
+                                      out_slots=o["slots"], out_indices=o["indices"], workspace=o["workspace"],
+                                      stream=stream)
     elif part.name == "topk_decode":
         sai.topk_transform(d["scores"], d["seq_lens"], d["page_tables"], page_size=128, out_slots=o["slots"],
                            workspace=o["workspace"], stream=stream)
@@ -383,6 +416,17 @@ def oracle_part_rate(part_name, meta, budget_s):
             oracle_blocks(slots[i:i + 64], 128)
             spent += time.perf_counter() - t0
             done += 64
+            if spent > budget_s:
+                break
+    elif part_name == "per_head_decode":
+        from oracle.score import index_score_topk_per_head
+
+        inp = meta["inp"]
+        for i in np.linspace(0, inp.rows - 1, 16).astype(np.int64):
+            t0 = time.perf_counter()
+            index_score_topk_per_head(inp, rows=[int(i)])
+            spent += time.perf_counter() - t0
+            done += 1
             if spent > budget_s:
                 break
     elif part_name == "topk_decode":

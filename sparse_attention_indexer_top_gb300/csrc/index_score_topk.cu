@@ -408,9 +408,14 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
       float2 w2[8];
       const float* wr = p.w + (long long)(row_live ? m.row0 + r : 0) * kH + 2 * (lane & 3);
 #pragma unroll
-      for (int j = 0; j < 8; ++j)  // FP8: scaled by 2^64, see relu_lo below
-        w2[j] = row_live ? make_float2(__ldg(wr + 8 * j) * kWScale, __ldg(wr + 8 * j + 1) * kWScale)
-                         : make_float2(0.f, 0.f);
+      for (int j = 0; j < 8; ++j) {  // FP8: scaled by 2^64, see relu_lo below
+        float wa = row_live ? __ldg(wr + 8 * j) : 0.f, wb = row_live ? __ldg(wr + 8 * j + 1) : 0.f;
+        if (MODE == kModePerHead && p.sign_w) {
+          wa = static_cast<float>((wa > 0.f) - (wa < 0.f));
+          wb = static_cast<float>((wb > 0.f) - (wb < 0.f));
+        }
+        w2[j] = make_float2(wa * kWScale, wb * kWScale);
+      }
       // the key scale of the next tile is fetched one tile ahead (1 when the
       // cache has no scales)
       auto key_scale = [&](int page) -> float {

@@ -345,6 +345,10 @@ int fused_per_head_topk(const void* q, const float* w, const void* kcache, const
                                     seq_lens, rows, max_seq_len, plan, st);
   p.dense = dense;
   p.dense_stride = L.stride;
+  // a positive factor per (row, head) does not change that row's selection;
+  // without |w_h| the score rows have comparable scales, which the top-k
+  // kernel's threshold carried from row to row relies on
+  p.sign_w = 1;
   e = sai::launch_fused(p, plan.group, sai::FusedOut::kPerHead, bf16, kcache, s);
   if (e != cudaSuccess) return cuda_status(e);
   return sai_topk_transform(dense, rows * 64, L.stride, nullptr, lens, block_table, bt_rows, bt_stride, batch, 128,

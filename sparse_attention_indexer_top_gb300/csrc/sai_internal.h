@@ -89,6 +89,7 @@ struct FusedLaunch {
   int32_t* part_idx;
   int* part_cnt;     // [rows * chunks]
   float* dense;      // dense modes: [rows, dense_stride] or [rows, 64, dense_stride]
+  int sign_w;        // per-head mode: use sign(w_h) for w_h (same order per (row, head), comparable scales)
   long long dense_stride;
   int* status;
 };
