@@ -283,6 +283,33 @@ __device__ __forceinline__ void write_survivors_smem(uint32_t* key, int32_t* idx
   }
 }
 
+// Starting threshold for a unit that has no estimate carried from the CTA's
+// previous unit (a CTA's first unit): the m-th largest of 1024 scores
+// sampled evenly over the window, m = twice the expected number of samples
+// above the window's 512th score plus 8, so that it lies below the 512th
+// score except with negligible probability (the unit end checks this
+// exactly and redoes the unit otherwise); about 1024 + len/128 scores then
+// pass. 0 (no threshold) for windows under 4096. Out of line: it runs once
+// per CTA or so, and stays out of the stream loop's registers.
+__device__ __noinline__ uint32_t sample_tau(const float* win, int len, Smem& S, int tid) {
+  constexpr int kSamples = 1024, kPer = kSamples / kThreads;
+  if (len < 4096) return 0u;
+  const uint32_t expect = static_cast<uint32_t>(((long long)kSamples * kTopK + len - 1) / len);
+  const uint32_t m = 2u * expect + 8u;
+  if (m >= static_cast<uint32_t>(kSamples)) return 0u;
+  uint32_t v[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    const long long j = tid + kThreads * e;
+    v[e] = order_key(__ldg(win + ((2 * j + 1) * len) / (2 * kSamples)));
+  }
+  const Threshold t = radix_threshold_each<kThreads>(m, S.sc, tid, kBar, [&](auto fn) {
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) fn(v[e]);
+  });
+  return t.base + static_cast<uint32_t>(static_cast<uint64_t>(t.prefix) << t.lo);
+}
+
 // Gather every warp's sub-list into aux: the exact top 512 of their union
 // when it holds more (tau rises to the cut), else all of it. All threads
 // call this with their warp's wcnt; returns the number in aux.
@@ -369,7 +396,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
   int wcnt = 0;       // entries in this warp's sub-list (warp-uniform)
   int appended = 0;   // elements this warp let through the filter in this unit
   uint32_t tau = 0;   // keep elements whose order key >= tau
-  uint32_t spec = 0;  // speculative starting threshold for the next unit (0: none)
+  // the previous unit's 512th score, its gap to the 256th, and its length
+  // (spec_len 0: no estimate), from which the next unit's start is taken
+  float spec_v512 = 0.f, spec_gap = 0.f;
+  int spec_len = 0;
   uint32_t spec_used = 0;
   // Slow path of a stage (or of a redo step) in which some warp's survivors
   // did not fit its sub-list: cut all sub-lists, then the warps whose
@@ -411,10 +441,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
     if (flags & 1) {
       wcnt = 0;
       appended = 0;
-      // Start from the previous unit's threshold estimate; whether it was
-      // low enough is checked exactly when the unit ends.
-      tau = spec;
-      spec_used = spec;
+      // Start from a threshold extrapolated from the previous unit (or a
+      // sampled one); whether it was low enough is checked exactly when the
+      // unit ends. The previous unit's 256th and 512th scores are two points
+      // of the score tail at quantiles 256/n' and 512/n'; the start is put
+      // at quantile 1.4 * 512 / n on the line through them in log-quantile
+      // (t = v512 - (v256 - v512) * log2(1.4 n' / n)), which keeps about
+      // 1.4x the needed count when rows look alike, whatever their lengths.
+      uint32_t est = 0;
+      if (spec_len > 0 && len > 0) {
+        const float t = spec_v512 - spec_gap * log2f(1.4f * static_cast<float>(spec_len) / static_cast<float>(len));
+        if (isfinite(t)) est = order_key(t);
+      }
+      tau = est ? est : sample_tau(p.scores + woff + lo, len, S, tid);
+      spec_used = tau;
     }
     float4 a[kVec];
 #pragma unroll
@@ -558,14 +598,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
         if (tid == 0) p.part_cnt[unit] = cnt;
       }
       named_bar(kBar, kThreads);
-      // Next unit's starting threshold: extrapolate the tail half an
-      // octave of rank down, t = v(512) - (v(256) - v(512)) / 2, which keeps
-      // about 1.4x the needed count when neighbouring rows look alike.
-      spec = 0;
+      // The tail points the next unit's starting threshold comes from.
+      spec_len = 0;
       if (S.spec_keys[1] != 0) {
         const float v256 = key_to_float(S.spec_keys[0]), v512 = key_to_float(S.spec_keys[1]);
-        const float t = v512 - 0.5f * (v256 - v512);
-        if (isfinite(t) && isfinite(v256) && isfinite(v512)) spec = order_key(t);
+        if (isfinite(v256) && isfinite(v512)) {
+          spec_v512 = v512;
+          spec_gap = v256 - v512;
+          spec_len = len;
+        }
       }
       wcnt = 0;
     }

@@ -189,3 +189,36 @@ def test_chunked_prefix_calls_match_one_call():
         torch.cuda.synchronize()
         assert sai.device_status() == 0
         _assert_equal((slots.cpu().numpy(), idx.cpu().numpy()), (whole[0][lo:hi], whole[1][lo:hi]), f"chunk {lo}:{hi}")
+
+
+@pytest.mark.parametrize("single", [True, False])
+def test_sampled_start_threshold_too_high_is_redone(single):
+    """A unit with no threshold carried from its CTA's previous unit starts
+    from one estimated on 1024 evenly spaced samples of its window. Here the
+    largest scores sit exactly at those positions, so the estimate lies above
+    the 512th score and fewer than 512 scores pass: the unit must be redone
+    exactly. (White-box: the positions are the kernel's sample positions,
+    (2j + 1) * n / 2048, for a window of n scores.)"""
+    rows, n = 6, 65536
+    rng = np.random.default_rng(71)
+    scores = rng.standard_normal((rows, n)).astype(np.float32)
+    pos = ((2 * np.arange(1024, dtype=np.int64) + 1) * n) // 2048
+    scores[:, pos] = (100.0 + rng.permutation(1024)).astype(np.float32)
+    pt = rng.permutation(rows * n).astype(np.int32).reshape(rows, n)
+    inp = W.TopkInputs(scores, np.full(rows, n, np.int32), pt, 1)
+    _assert_equal(_run(inp, force_single=single), _oracle(inp), "sampled threshold redo")
+
+
+def test_sampled_start_threshold_short_and_mixed_rows():
+    """First units of many CTAs with windows of 4096..70000 scores, including
+    heavy ties (bf16-rounded values) and a constant row."""
+    rng = np.random.default_rng(72)
+    lens = np.array([4096, 4097, 9000, 30000, 70000, 65536, 5000, 12000], np.int32)
+    width = int(lens.max())
+    scores = rng.standard_normal((lens.size, width)).astype(np.float32)
+    scores[1] = torch.from_numpy(scores[1]).to(torch.bfloat16).float().numpy()
+    scores[5] = 3.0
+    pt = rng.permutation(lens.size * width).astype(np.int32).reshape(lens.size, width)
+    inp = W.TopkInputs(scores, lens, pt, 1)
+    _assert_equal(_run(inp, force_single=True), _oracle(inp), "mixed rows")
+    _assert_equal(_run(inp), _oracle(inp), "mixed rows, split path")
