@@ -64,10 +64,12 @@ constexpr int kBlk = 128;     // tokens per KV block = MMA M
 // (prefill) two with a 3-stage ring; one query buffer each, since every CTA
 // takes one unit (measured against 2-4 stages and 2-3 CTAs per SM; a 3-stage
 // ring at three CTAs per SM, with 384-entry sub-lists to fit, was slower).
-// The bf16 variant has twice the bytes per stage and runs one CTA fewer.
+// The ring holds 16 KB slots, one 128-byte-swizzled region of a key tile
+// each: an FP8 tile is one region, a bf16 tile two (dims 0-63, 64-127), so
+// the bf16 variant keeps a tile in flight with the same CTAs per SM.
 template <int R, bool BF16 = false>
 __host__ __device__ constexpr int fused_stages() {
-  return R == 1 ? 2 : (R == 2 ? 3 : 4);
+  return BF16 ? 2 : (R == 1 ? 2 : (R == 2 ? 3 : 4));
 }
 template <int R>
 __host__ __device__ constexpr int fused_qbufs() {
@@ -75,7 +77,7 @@ __host__ __device__ constexpr int fused_qbufs() {
 }
 template <int R, bool BF16 = false>
 __host__ __device__ constexpr int fused_ctas_per_sm() {
-  return BF16 ? (R == 1 ? 2 : 1) : (R == 1 ? 3 : (R == 2 ? 2 : 1));
+  return R == 1 ? 3 : (R == 2 ? 2 : 1);
 }
 template <bool BF16>
 __host__ __device__ constexpr int elem_bytes() {
@@ -98,8 +100,9 @@ constexpr int kEpiRow = 128;  // epilogue threads per query row (4 warps, one TM
 
 template <int R, bool BF16>
 struct __align__(1024) FusedSmem {
-  // a key stage / query tile is sw_regions() regions of [rows x 128 bytes]
-  uint8_t kst[fused_stages<R, BF16>()][kBlk * kD * elem_bytes<BF16>()];  // 16 KB (FP8) or 32 KB, 1024-aligned
+  // a ring slot is one region of a key tile, [128 keys x 128 bytes]; a query
+  // tile is sw_regions() regions of [R*64 rows x 128 bytes]
+  uint8_t kst[fused_stages<R, BF16>()][kBlk * kSwB];  // 16 KB each, 1024-aligned
   uint8_t q[fused_qbufs<R>()][R * kH * kD * elem_bytes<BF16>()];          // query tiles of consecutive units
   uint32_t ckey[R][4 * fused_sub<R, BF16>()];  // row r: four per-warp sub-lists
   int32_t cidx[R][4 * fused_sub<R, BF16>()];
@@ -119,8 +122,8 @@ constexpr size_t fused_smem_bytes() {
 
 static_assert(3 * (fused_smem_bytes<1, false>() + 1024) <= 228 * 1024, "three single-row CTAs per SM");
 static_assert(2 * (fused_smem_bytes<2, false>() + 1024) <= 228 * 1024, "two row-pair CTAs per SM");
-static_assert(2 * (fused_smem_bytes<1, true>() + 1024) <= 228 * 1024, "two single-row bf16 CTAs per SM");
-static_assert(fused_smem_bytes<2, true>() + 1024 <= 228 * 1024, "one row-pair bf16 CTA per SM");
+static_assert(3 * (fused_smem_bytes<1, true>() + 1024) <= 228 * 1024, "three single-row bf16 CTAs per SM");
+static_assert(2 * (fused_smem_bytes<2, true>() + 1024) <= 228 * 1024, "two row-pair bf16 CTAs per SM");
 
 template <int R, bool BF16>
 __device__ __forceinline__ FusedSmem<R, BF16>& fused_smem(unsigned char* raw) {
@@ -208,7 +211,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
   constexpr uint32_t kCols = 2 * N;  // two accumulator buffers
   constexpr uint32_t kIdesc = BF16 ? umma_idesc_bf16(kBlk, N) : umma_idesc_e4m3(kBlk, N);
   constexpr int kRegions = sw_regions<BF16>();
-  constexpr uint32_t kKeyTileBytes = kBlk * kD * elem_bytes<BF16>();
+  constexpr uint32_t kSlotBytes = kBlk * kSwB;  // one region of a key tile
   constexpr uint32_t kQTileBytes = N * kD * elem_bytes<BF16>();
   constexpr int kEpiWarps = 4 * R;
   constexpr int kTmaWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1;
@@ -269,17 +272,17 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
                       keep);
         ++qn;
         int page_next = __ldg(bt);
-        for (int i = 0; i < ntiles; ++i, ++it) {
+        for (int i = 0; i < ntiles && run; ++i) {
           int page = page_next;
           if (i + 1 < ntiles) page_next = __ldg(bt + i + 1);
           if (page < 0 || page >= p.num_blocks) page = 0;  // the epilogue masks this block
-          const int s = it % kNSf;
-          if (!(run = mbar_wait(&S.empty[s], ((it / kNSf) & 1u) ^ 1u))) break;
-          mbar_arrive_expect_tx(&S.full[s], kKeyTileBytes);
 #pragma unroll
-          for (int h = 0; h < kRegions; ++h)
-            tma_load_2d(S.kst[s] + h * kBlk * kSwB, &kmap, h * (kSwB / elem_bytes<BF16>()), page * kBlk, &S.full[s],
-                        keep);
+          for (int h = 0; h < kRegions; ++h, ++it) {  // region h: dims [64h, 64h + 64) of a bf16 key
+            const int s = it % kNSf;
+            if (!(run = mbar_wait(&S.empty[s], ((it / kNSf) & 1u) ^ 1u))) break;
+            mbar_arrive_expect_tx(&S.full[s], kSlotBytes);
+            tma_load_2d(S.kst[s], &kmap, h * (kSwB / elem_bytes<BF16>()), page * kBlk, &S.full[s], keep);
+          }
         }
       }
       if (!run) atomicOr(p.status, kDevWaitTimeout);
@@ -287,7 +290,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer
     if (lane == 0) {
-      uint32_t it = 0, qn = 0;
+      uint32_t it = 0, rs = 0, qn = 0;  // tiles (accumulator buffers) and ring slots consumed
       bool run = true;
       for (int u = blockIdx.x; u < units && run; u += gridDim.x) {
         int n[R];
@@ -298,19 +301,20 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
         if (!(run = mbar_wait(&S.qfull[qb], (qn / kQB) & 1u))) break;
         ++qn;
         const uint64_t bdesc = umma_desc_sw128_kmajor(smem_u32(S.q[qb]));
-        for (int i = 0; i < ntiles; ++i, ++it) {
-          const int s = it % kNSf, buf = it & 1;
-          run = mbar_wait(&S.full[s], (it / kNSf) & 1u) && mbar_wait(&S.tempty[buf], ((it >> 1) & 1u) ^ 1u);
-          if (!run) break;
-          tc_fence_after();
-          const uint64_t adesc = umma_desc_sw128_kmajor(smem_u32(S.kst[s]));
+        for (int i = 0; i < ntiles && run; ++i, ++it) {
+          const int buf = it & 1;
+          if (!(run = mbar_wait(&S.tempty[buf], ((it >> 1) & 1u) ^ 1u))) break;
           // each instruction takes 32 bytes of K (32 FP8 or 16 bf16 dims):
-          // four per 128-byte region; the descriptor start field counts 16 B
+          // four per region (ring slot); the descriptor start field counts 16 B
 #pragma unroll
-          for (int h = 0; h < kRegions; ++h) {
+          for (int h = 0; h < kRegions; ++h, ++rs) {
+            const int s = rs % kNSf;
+            if (!(run = mbar_wait(&S.full[s], (rs / kNSf) & 1u))) break;
+            tc_fence_after();
+            const uint64_t adesc = umma_desc_sw128_kmajor(smem_u32(S.kst[s]));
 #pragma unroll
             for (int k = 0; k < kSwB / 32; ++k) {
-              const uint64_t ad = adesc + (uint64_t)(h * kBlk * kSwB / 16 + 2 * k);
+              const uint64_t ad = adesc + (uint64_t)(2 * k);
               const uint64_t bd = bdesc + (uint64_t)(h * N * kSwB / 16 + 2 * k);
               const uint32_t acc = (h > 0 || k > 0) ? 1u : 0u;
               if constexpr (BF16)
@@ -318,8 +322,9 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
               else
                 umma_f8(tmem + buf * N, ad, bd, kIdesc, acc);
             }
+            umma_commit(&S.empty[s]);
           }
-          umma_commit(&S.empty[s]);
+          if (!run) break;
           umma_commit(&S.tfull[buf]);
         }
         umma_commit(&S.qempty[qb]);  // the query tile is free once this unit's MMAs are done
