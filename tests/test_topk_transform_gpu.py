@@ -210,10 +210,10 @@ def test_sampled_start_threshold_too_high_is_redone(single):
 
 
 def test_sampled_start_threshold_short_and_mixed_rows():
-    """First units of many CTAs with windows of 4096..70000 scores, including
+    """First units of many CTAs with windows of 1535..70000 scores, including
     heavy ties (bf16-rounded values) and a constant row."""
     rng = np.random.default_rng(72)
-    lens = np.array([4096, 4097, 9000, 30000, 70000, 65536, 5000, 12000], np.int32)
+    lens = np.array([4096, 4097, 9000, 30000, 70000, 65536, 5000, 12000, 1535, 1536, 2048, 3000], np.int32)
     width = int(lens.max())
     scores = rng.standard_normal((lens.size, width)).astype(np.float32)
     scores[1] = torch.from_numpy(scores[1]).to(torch.bfloat16).float().numpy()
