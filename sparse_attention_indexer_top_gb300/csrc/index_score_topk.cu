@@ -90,12 +90,11 @@ __host__ __device__ constexpr int sw_regions() {
 }
 constexpr int kSyncEvery = 4; // tiles between the row group's count exchanges
 // Candidate sub-list per epilogue warp. A list is cut back once it holds
-// more than fused_sub() - 4 tiles x 32 entries, and a warp appends at most
-// 32 per tile, so it never overflows; the cut leaves 128 per list.
-template <int R, bool BF16>
-__host__ __device__ constexpr int fused_sub() {
-  return 512;
-}
+// more than kSub - 4 tiles x 32 entries, and a warp appends at most 32 per
+// tile, so it never overflows; the cut leaves 128 per list.
+constexpr int kSub = 512;
+constexpr int kSubPruneAt = kSub - kSyncEvery * 32;
+static_assert(kSubPruneAt >= kTopK / 4 && 4 * kSub > kTopK, "sub-list sizes");
 constexpr int kEpiRow = 128;  // epilogue threads per query row (4 warps, one TMEM lane quadrant each)
 
 template <int R, bool BF16>
@@ -104,8 +103,8 @@ struct __align__(1024) FusedSmem {
   // tile is sw_regions() regions of [R*64 rows x 128 bytes]
   uint8_t kst[fused_stages<R, BF16>()][kBlk * kSwB];  // 16 KB each, 1024-aligned
   uint8_t q[fused_qbufs<R>()][R * kH * kD * elem_bytes<BF16>()];          // query tiles of consecutive units
-  uint32_t ckey[R][4 * fused_sub<R, BF16>()];  // row r: four per-warp sub-lists
-  int32_t cidx[R][4 * fused_sub<R, BF16>()];
+  uint32_t ckey[R][4 * kSub];  // row r: four per-warp sub-lists
+  int32_t cidx[R][4 * kSub];
   uint32_t aux_key[R][kTopK];
   int32_t aux_idx[R][kTopK];
   SelectScratch sc[R];
@@ -338,9 +337,6 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
     const int bar = 1 + r;
     uint32_t* const ckey = S.ckey[r];
     int32_t* const cidx = S.cidx[r];
-    constexpr int kSub = fused_sub<R, BF16>();
-    constexpr int kSubPruneAt = kSub - kSyncEvery * 32;
-    static_assert(kSubPruneAt >= kTopK / 4 && 4 * kSub > kTopK, "sub-list sizes");
     uint32_t* const my_key = ckey + quad * kSub;
     int32_t* const my_idx = cidx + quad * kSub;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;

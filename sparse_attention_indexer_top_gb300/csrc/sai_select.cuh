@@ -349,33 +349,6 @@ __device__ uint32_t select_topk(uint32_t* ckey, int32_t* cidx, int n, int K, uin
   return tau;
 }
 
-// Append the entries of keys/idxs whose bit is set in `mask` at positions
-// base + (running count in *counter); one shared atomic per warp.
-template <int M>
-__device__ __forceinline__ void append_masked(uint32_t* ckey, int32_t* cidx, int base, int* counter,
-                                              const uint32_t (&keys)[M], const int32_t (&idxs)[M], uint32_t mask,
-                                              int lane) {
-  const int m = __popc(mask);
-  if (!__any_sync(0xFFFFFFFFu, m > 0)) return;
-  int incl = m;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-    if (lane >= d) incl += o;
-  }
-  int start = 0;
-  if (lane == 31) start = atomicAdd(counter, incl);
-  int pos = __shfl_sync(0xFFFFFFFFu, start, 31) + base + incl - m;
-#pragma unroll
-  for (int i = 0; i < M; ++i) {
-    if (mask & (1u << i)) {
-      ckey[pos] = keys[i];
-      cidx[pos] = idxs[i];
-      ++pos;
-    }
-  }
-}
-
 // Composite sort key: key in the high word, bit-inverted index in the low
 // word, so a larger composite means higher score, then lower index. Padding
 // entries use 0, which sorts after every real entry.
@@ -459,44 +432,6 @@ __device__ __forceinline__ BinCut hist_cut4096(const uint32_t* hist, uint32_t ne
   c.need_in_bin = bcast[1];
   c.bin_count = bcast[2];
   return c;
-}
-
-// Keep the entries of ckey/cidx[0, n) with key >= tau, compacted to the
-// front (order not kept). Returns the new count. CAPT bounds n.
-template <int CAPT>
-__device__ __forceinline__ int compact_ge(uint32_t* ckey, int32_t* cidx, int n, uint32_t tau, uint32_t* wsum,
-                                          int tid, int bar) {
-  constexpr int M = (CAPT + 511) / 512;
-  uint32_t k[M];
-  int32_t ix[M];
-  uint32_t keep = 0;
-  int c = 0;
-#pragma unroll
-  for (int m = 0; m < M; ++m) {
-    const int j = tid + 512 * m;
-    k[m] = 0;
-    ix[m] = 0;
-    if (j < n) {
-      k[m] = ckey[j];
-      ix[m] = cidx[j];
-      if (k[m] >= tau) {
-        keep |= 1u << m;
-        ++c;
-      }
-    }
-  }
-  int total;
-  int pos = block_exscan512(c, &total, wsum, tid, bar);  // its barrier orders all reads before the writes
-#pragma unroll
-  for (int m = 0; m < M; ++m) {
-    if (keep & (1u << m)) {
-      ckey[pos] = k[m];
-      cidx[pos] = ix[m];
-      ++pos;
-    }
-  }
-  named_bar(bar, 512);
-  return total;
 }
 
 // Exact top-K (K = 512) of ckey/cidx[0, n), n > K, by (key desc, index asc),
@@ -607,59 +542,6 @@ __device__ __forceinline__ int block_exscan(int c, int* total, uint32_t* wsum, i
   }
   *total = tot;
   return off + incl - c;
-}
-
-// Exact top-K (K = 512) of ckey/cidx[0, n), n > K, by (key desc, index
-// asc) into aux_key/aux_idx[0, K) (unordered; ckey/cidx are left intact).
-// Returns the lowest key of the final threshold bin, a value <= the K-th
-// key (so "key >= returned value" is a valid filter for later elements).
-template <int NT, int CAPT>
-__device__ uint32_t select512_to_aux(const uint32_t* ckey, const int32_t* cidx, int n, uint32_t* aux_key,
-                                     int32_t* aux_idx, SelectScratch& sc, int tid, int bar) {
-  constexpr int K = kTopK;
-  constexpr int M = (CAPT + NT - 1) / NT;
-  const Threshold t = radix_threshold<NT>(n, (uint32_t)K, sc, tid, bar, [&](int j, uint32_t& v) {
-    v = ckey[j];
-    return true;
-  });
-  Threshold ti{};
-  const bool ties = !t.all_eq;
-  if (ties) {
-    ti = radix_threshold<NT>(n, t.need, sc, tid, bar, [&](int j, uint32_t& v) {
-      v = 0x7FFFFFFFu - static_cast<uint32_t>(cidx[j]);
-      return thr_cmp(t, ckey[j]) == 0;
-    });
-  }
-  uint32_t selm = 0;
-  int c = 0;
-#pragma unroll
-  for (int m = 0; m < M; ++m) {
-    const int j = tid + NT * m;
-    if (j < n) {
-      const int cc = thr_cmp(t, ckey[j]);
-      const bool sel =
-          cc > 0 || (cc == 0 && (!ties || thr_cmp(ti, 0x7FFFFFFFu - static_cast<uint32_t>(cidx[j])) >= 0));
-      if (sel) {
-        selm |= 1u << m;
-        ++c;
-      }
-    }
-  }
-  int total;
-  int pos = block_exscan<NT>(c, &total, sc.wcnt, tid, bar);
-#pragma unroll
-  for (int m = 0; m < M; ++m) {
-    if (selm & (1u << m)) {
-      const int j = tid + NT * m;
-      if (pos < K) {
-        aux_key[pos] = ckey[j];
-        aux_idx[pos] = cidx[j];
-      }
-      ++pos;
-    }
-  }
-  named_bar(bar, NT);
-  return t.base + static_cast<uint32_t>(static_cast<uint64_t>(t.prefix) << t.lo);
 }
 
 // Sort the `cnt` (<= 512) entries of aux_key/aux_idx by (key desc, index
