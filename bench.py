@@ -58,18 +58,18 @@ FP8_OVER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s
 
 # DRAM bytes (read + write) per key, from one ncu capture of each kernel as
 # it stands (summaries under profiles/, by kernel and workload): top-k stream
-# on 2048 packed-extend rows, 584.76 MB + 3.29 MB for 142.3 M keys; fused
-# prefill on 4096 rows, 39.06 MB + 0.008 MB for 125.8 M keys; fused decode on
-# 64 rows, 158.42 MB + 3.44 MB for 1.19 M keys; the bf16-cache variants of
-# the same two workloads, 77.17 MB + 1.12 MB and 312.09 MB + 0.42 MB. Traffic
+# on 2048 packed-extend rows, 584.77 MB + 2.96 MB for 142.3 M keys; fused
+# prefill on 4096 rows, 39.14 MB + 0.0003 MB for 125.8 M keys; fused decode
+# on 64 rows, 158.42 MB + 3.42 MB for 1.19 M keys; the bf16-cache variants of
+# the same two workloads, 76.90 MB + 1.03 MB and 312.09 MB + 0.43 MB. Traffic
 # grows with the keys streamed. Set an entry to None whenever its kernel
 # changes until it is re-captured.
 TRAFFIC_BYTES_PER_KEY = {
-    "topk_packed_extend": (584.757248e6 + 3.287296e6) / 142312448,
-    "fused_prefill": (39.05792e6 + 0.008192e6) / 125831168,
-    "fused_decode": (158.42304e6 + 3.437568e6) / 1190814,
-    "fused_prefill_bf16": (77.169152e6 + 1.118976e6) / 125831168,
-    "fused_decode_bf16": (312.088832e6 + 0.424704e6) / 1190814,
+    "topk_packed_extend": (584.774144e6 + 2.956544e6) / 142312448,
+    "fused_prefill": (39.135488e6 + 0.000256e6) / 125831168,
+    "fused_decode": (158.424064e6 + 3.421696e6) / 1190814,
+    "fused_prefill_bf16": (76.904704e6 + 1.028608e6) / 125831168,
+    "fused_decode_bf16": (312.089088e6 + 0.429824e6) / 1190814,
 }
 
 
