@@ -34,6 +34,29 @@ def test_decode_all_patterns():
     assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
 
 
+def test_decode_golden_values():
+    """tests/golden/bf16_format_values.txt: patterns whose values follow from
+    the format definition (min normal 2^-126, min subnormal 2^-133, largest
+    finite (2 - 2^-7) 2^127, infinities, NaNs)."""
+    import os
+
+    path = os.path.join(os.path.dirname(__file__), "golden", "bf16_format_values.txt")
+    bits, vals = [], []
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        b, v = line.split()
+        bits.append(int(b, 16))
+        vals.append(float(v))
+    got = bf16_decode(np.array(bits, np.uint16))
+    for b, g, v in zip(bits, got, vals):
+        if np.isnan(v):
+            assert np.isnan(g), hex(b)
+        else:
+            assert g == v and np.signbit(g) == np.signbit(v), (hex(b), g, v)
+
+
 def test_decode_fields():
     assert bf16_decode(np.array([0x3F80, 0xC000, 0x0001, 0x7F7F, 0x8000], np.uint16)).tolist() == \
         [1.0, -2.0, 2.0**-133, (2 - 2**-7) * 2.0**127, -0.0]
