@@ -181,14 +181,18 @@ __device__ __forceinline__ float relu_lo(uint32_t s_bits) {
   return r;
 }
 
-// relu of an FP32 accumulator: FP8 keeps it scaled by 2^-64 (exact, see
-// above); bf16 products have no such bound, so there it is a plain max.
+// relu of an FP32 accumulator, on the FMA pipe (the ALU pipe is the busier
+// one): FP8 keeps it scaled by 2^-64 (exact, see above); bf16 products have
+// no such bound, so there it is s + |s| = 2 relu(s), exact for |s| < 2^127,
+// with the 1/2 folded into the weights.
 template <bool BF16>
 __device__ __forceinline__ float relu_of(uint32_t s_bits) {
-  if constexpr (BF16)
-    return fmaxf(__uint_as_float(s_bits), 0.f);
-  else
+  if constexpr (BF16) {
+    const float s = __uint_as_float(s_bits);
+    return __fadd_rn(s, fabsf(s));
+  } else {
     return relu_lo(s_bits);
+  }
 }
 
 template <int R>
@@ -347,7 +351,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
     // reduce-scatter over the 4 lanes sharing l/4 leaves each lane the full
     // score of one key, key kl of the block.
     const int kl = quad * 32 + (lane >> 2) + 8 * ((lane >> 1) & 1) + 16 * (lane & 1);
-    constexpr float kWScale = BF16 ? 1.f : 0x1p64f;
+    constexpr float kWScale = BF16 ? 0.5f : 0x1p64f;  // undoes relu_of's scaling
     bool ok = true;     // false after a pipeline wait gave up (then nothing more is waited for)
     int sync_no = 0;    // exchanges so far (the size slots alternate)
     uint32_t tt = 0;    // tiles so far (accumulator buffer and phase)
