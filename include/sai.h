@@ -298,18 +298,23 @@ int sai_sparse_blocks(const int32_t* slots, int64_t rows, int32_t k, int32_t blo
  * counterpart: this entry point exists only for such callers.
  *
  * Arguments, outputs, ordering and errors are those of sai_topk_transform.
- * Instead of a caller workspace, the split path for few long rows uses a
- * fixed library-owned device array of SAI_NOALLOC_SCRATCH_BYTES. Calls
- * whose sizes need more scratch than that (as reported by
- * sai_topk_transform_workspace) are rejected with SAI_ERR_WORKSPACE before
- * anything is launched. Nothing is allocated: no cudaMalloc, no cudaFree.
+ * Instead of a caller workspace, every call uses a fixed library-owned
+ * device array of SAI_NOALLOC_SCRATCH_BYTES: its first 256 bytes hold the
+ * work counter from which the CTAs take rows (reset to zero by each call on
+ * its stream), and the split path for few long rows also keeps its partial
+ * top-k lists there. Calls whose sizes need more scratch than that (as
+ * reported by sai_topk_transform_workspace) are rejected with
+ * SAI_ERR_WORKSPACE before anything is launched. Nothing is allocated: no
+ * cudaMalloc, no cudaFree.
  *
  * The first call on a device looks up the array's device address with that
  * device current; make that first call before any stream capture. All calls
  * on a device share the one array and it keeps the previous call's contents
- * (nothing in it needs to start at zero). Calls that can overlap on the GPU
- * (different streams without ordering between them) race on the array and
- * must be serialized by the caller.
+ * (the counter is the only part that must start at zero, and each call
+ * clears it). Any two calls that can overlap on the GPU (different streams
+ * without ordering between them), short rows or long, race on the work
+ * counter and, when split, on the partial lists: rows can be skipped and
+ * outputs left unwritten. The caller must serialize them.
  */
 int sai_topk_transform_noalloc(const float* scores, int64_t rows, int64_t score_stride, const int32_t* row_starts,
                                const int32_t* seq_lens, const int32_t* page_tables, int64_t pt_rows,

@@ -48,8 +48,10 @@ extern "C" int sai_topk_transform_noalloc(const float* scores, int64_t rows, int
                                           const int32_t* page_tables, int64_t pt_rows, int64_t pt_stride,
                                           const int32_t* row_to_batch, int32_t page_size, int32_t k,
                                           int32_t* out_slots, int32_t* out_indices, sai_stream_t stream) {
-  // Scratch the split path wants for these sizes (0 when one CTA per row is
-  // used, or when the arguments are invalid: the call below reports those).
+  // Scratch these sizes want: the 256-byte header with the row work counter
+  // for every valid call (also when each row is one CTA's unit), plus the
+  // partial lists when long rows are split; 0 only for invalid arguments,
+  // which the call below reports.
   const size_t need = sai_topk_transform_workspace(rows, score_stride, k);
   if (need > SAI_NOALLOC_SCRATCH_BYTES) return SAI_ERR_WORKSPACE;
   void* scratch = nullptr;
@@ -57,7 +59,8 @@ extern "C" int sai_topk_transform_noalloc(const float* scores, int64_t rows, int
     scratch = scratch_on_current_device();
     if (!scratch) return SAI_ERR_CUDA;
   }
-  // Nothing in the scratch has to start at zero: every work unit writes its
+  // Only the work counter has to start at zero, and sai_topk_transform
+  // clears it on the stream before its launch; every work unit writes its
   // candidate count and entries before the merge kernel reads them.
   return sai_topk_transform(scores, rows, score_stride, row_starts, seq_lens, page_tables, pt_rows, pt_stride,
                             row_to_batch, page_size, k, out_slots, out_indices, scratch,
