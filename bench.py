@@ -54,7 +54,41 @@ def _peaks():
         return 6800.0, 1900.0, "fallback"
 
 
-FP8_OVER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
+FP8_OVER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s), used only if the GEMM fails
+
+
+def measure_fp8_peak(dev, n: int = 8192, reps: int = 10):
+    """Dense e4m3 x e4m3 -> bf16 GEMM throughput (TFLOP/s) of this GPU: a
+    cuBLASLt GEMM through torch._scaled_mm on n^3 (2 n^3 flops), best of
+    `reps` launches timed with CUDA events after 3 warm-ups. Returns
+    (TFLOP/s, note) or (None, why) when the GEMM is unavailable."""
+    import torch
+
+    try:
+        g = torch.Generator(device=dev).manual_seed(7)
+        a = torch.randn((n, n), device=dev, generator=g).to(torch.float8_e4m3fn)
+        b = torch.randn((n, n), device=dev, generator=g).to(torch.float8_e4m3fn)
+        one = torch.ones((), device=dev, dtype=torch.float32)
+
+        def run():
+            return torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+
+        for _ in range(3):
+            run()
+        torch.cuda.synchronize(dev)
+        best = float("inf")
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            run()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            best = min(best, e0.elapsed_time(e1))
+        del a, b
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12, f"torch._scaled_mm e4m3 {n}^3, best of {reps} ({best:.3f} ms)"
+    except Exception as exc:  # no fp8 GEMM in this torch build
+        return None, f"fp8 GEMM unavailable ({type(exc).__name__}: {exc})"
 
 # DRAM bytes (read + write) per key, from one ncu capture of each kernel as
 # it stands (summaries under profiles/, by kernel and workload): top-k stream
@@ -195,7 +229,8 @@ class Part:
         self.out = {}       # name -> device output tensor
         self.rows = 0
         self.keys = 0.0
-        self.bytes = 0.0    # algorithmic HBM bytes per launch
+        self.bytes = 0.0    # algorithmic HBM bytes per launch (each input byte once)
+        self.l2_bytes = 0.0  # bytes the kernels stream, re-reads served by L2 included
         self.flops = 0.0    # algorithmic tensor flops per launch
         self.launches = 0
         self.meta = {}
@@ -267,9 +302,16 @@ def build_fused_part(dev, name: str, inp, group_rows: int):
     # each key's row (fp8 or bf16) + its scale, read once per row group; q, w;
     # block ids; outputs
     groups = -(-rows // group_rows)
+    key_bytes = d * inp.kcache.itemsize + 4  # a key row and its scale
+    # keys streamed by the kernel: once per row group (L2 serves the re-reads
+    # of a request's keys by its other groups)
     key_reads = float(sum(int(n[g * group_rows:(g + 1) * group_rows].max()) for g in range(groups)))
-    part.bytes = (key_reads * (d * inp.kcache.itemsize + 4) + inp.q.nbytes + inp.w.nbytes + (key_reads / 128) * 4
-                  + rows * K * 12)
+    # distinct keys, read once from HBM: per block-table row, its longest row
+    batch = np.arange(rows) if inp.row_to_batch is None else inp.row_to_batch
+    key_unique = float(sum(int(n[batch == b].max()) for b in np.unique(batch)))
+    fixed = inp.q.nbytes + inp.w.nbytes + rows * K * 12
+    part.bytes = key_unique * (key_bytes + 4 / 128) + fixed
+    part.l2_bytes = key_reads * (key_bytes + 4 / 128) + fixed
     part.flops = part.keys * h * d * 2.0
     part.launches = 2
     part.meta = dict(inp=inp, group_rows=group_rows, max_len=max_len)
@@ -401,83 +443,155 @@ def launch_part(part, stream):
 
 
 # --------------------------------------------------------------------------- oracle
-def oracle_part_rate(part_name, meta, budget_s):
-    """Oracle seconds per row of one part, timed on a row sample."""
+# The CPU oracle, timed on the host cores: a pool of worker processes (spawn,
+# one per core), each running the oracle on its share of a part's rows until
+# its time budget is spent. Only the oracle calls are timed; loading the
+# inputs (memory-mapped .npy files written by the parent) and regenerating a
+# top-k window from its seed are not. A part's rate is the rows all workers
+# finished divided by the longest worker's oracle time (they run at once).
+_ORACLE_INPUTS = {}
+
+
+def _oracle_warm(_):
+    import oracle.blocks  # noqa: F401
+    import oracle.score  # noqa: F401
+    import oracle.topk  # noqa: F401
+    import workloads  # noqa: F401
+
+    return os.getpid()
+
+
+def _oracle_inputs(spec):
+    key = spec.get("folder") or spec["kind"]
+    if key not in _ORACLE_INPUTS:
+        import workloads as W
+
+        arr = {}
+        if "folder" in spec:
+            for f in os.listdir(spec["folder"]):
+                arr[f[:-4]] = np.load(os.path.join(spec["folder"], f), mmap_mode="r")
+        if spec["kind"] == "fused":
+            r2b = arr.get("row_to_batch")
+            arr = W.FusedInputs(arr["q"], arr["w"], arr["kcache"], arr.get("kscale"), arr["block_table"],
+                                np.asarray(arr["seq_lens"]), None if r2b is None else np.asarray(r2b),
+                                dtype=spec["dtype"])
+        _ORACLE_INPUTS[key] = arr
+    return _ORACLE_INPUTS[key]
+
+
+def _oracle_rows(task):
+    """Worker: the oracle on `rows` of one part until `budget` seconds of
+    oracle time are spent. Returns (rows done, oracle seconds)."""
     import workloads as W
+    from oracle.blocks import sparse_blocks as oracle_blocks
     from oracle.score import index_score_topk as oracle_fused
+    from oracle.score import index_score_topk_per_head
     from oracle.topk import topk_transform as oracle_topk
 
+    name, spec, rows, budget = task
+    data = _oracle_inputs(spec)
     done, spent = 0, 0.0
-    if part_name == "sparse_blocks":
-        from oracle.blocks import sparse_blocks as oracle_blocks
-
-        slots = meta["slots"]
-        for i in range(0, slots.shape[0], 64):
+    for i in rows:
+        i = int(i)
+        if name == "topk_packed_extend":
+            n = int(spec["seq_lens"][i])
+            w = W.packed_extend_window(3, i, n)
             t0 = time.perf_counter()
-            oracle_blocks(slots[i:i + 64], 128)
-            spent += time.perf_counter() - t0
-            done += 64
-            if spent > budget_s:
-                break
-    elif part_name == "per_head_decode":
-        from oracle.score import index_score_topk_per_head
-
-        inp = meta["inp"]
-        for i in np.linspace(0, inp.rows - 1, 16).astype(np.int64):
+            oracle_topk(w[None, :], np.array([n]), spec["page_tables"][[int(spec["row_to_batch"][i])]], 1, K)
+        elif name == "topk_decode":
+            n = int(data["seq_lens"][i])
             t0 = time.perf_counter()
-            index_score_topk_per_head(inp, rows=[int(i)])
-            spent += time.perf_counter() - t0
-            done += 1
-            if spent > budget_s:
-                break
-    elif part_name == "topk_decode":
-        inp = meta["inp"]
-        for i in range(inp.seq_lens.size):
-            n = int(inp.seq_lens[i])
+            oracle_topk(np.asarray(data["scores"][i:i + 1, :n]), np.array([n]), data["page_tables"][i:i + 1], 128, K)
+        elif name == "sparse_blocks":  # 64 rows per item
             t0 = time.perf_counter()
-            oracle_topk(inp.scores[i:i + 1, :n], np.array([n]), inp.page_tables[i:i + 1], 128, K)
-            spent += time.perf_counter() - t0
-            done += 1
-            if spent > budget_s:
-                break
-    elif part_name == "topk_packed_extend":
-        rows = int(meta["seq_lens"].size)
-        for i in np.linspace(0, rows - 1, 4000).astype(np.int64):
-            n = int(meta["seq_lens"][i])
-            w = W.packed_extend_window(3, int(i), n)
+            oracle_blocks(np.asarray(data["slots"][64 * i:64 * i + 64]), 128)
+        elif name == "per_head_decode":
             t0 = time.perf_counter()
-            oracle_topk(w[None, :], np.array([n]), meta["page_tables"][[int(meta["row_to_batch"][i])]], 1, K)
-            spent += time.perf_counter() - t0
-            done += 1
-            if spent > budget_s:
-                break
-    else:
-        inp = meta["inp"]
-        for i in np.linspace(0, inp.rows - 1, 64).astype(np.int64):
+            index_score_topk_per_head(data, rows=[i])
+        else:
             t0 = time.perf_counter()
-            oracle_fused(inp, rows=[int(i)])
-            spent += time.perf_counter() - t0
-            done += 1
-            if spent > budget_s:
-                break
-    return spent / max(done, 1), done, spent
+            oracle_fused(data, rows=[i])
+        spent += time.perf_counter() - t0
+        done += 64 if name == "sparse_blocks" else 1
+        if spent > budget:
+            break
+    return done, spent
 
 
-def oracle_step_rate(parts_meta, budget_s):
-    """Rows/s of the oracle over the step's row mix, and a sample summary."""
-    per_step, rows, notes = 0.0, 0, []
+def _oracle_specs(parts_meta, folder):
+    """Per part: (name, rows of the step, worker input spec, item order)."""
+    specs = []
     for name, nrows, meta in parts_meta:
-        sec_per_row, done, spent = oracle_part_rate(name, meta, budget_s / max(len(parts_meta), 1))
-        per_step += sec_per_row * nrows
-        rows += nrows
-        notes.append(f"{name}: {done} rows in {spent:.1f} s")
-    return rows / per_step, "; ".join(notes)
+        if name == "topk_packed_extend":
+            spec = dict(kind="packed", seq_lens=meta["seq_lens"], row_to_batch=meta["row_to_batch"],
+                        page_tables=meta["page_tables"])
+            items = np.arange(nrows)
+        else:
+            sub = os.path.join(folder, name)
+            os.makedirs(sub)
+            if name == "sparse_blocks":
+                arrays, spec = {"slots": meta["slots"]}, dict(kind="blocks")
+                items = np.arange(nrows // 64)
+            elif name == "topk_decode":
+                inp = meta["inp"]
+                arrays = {"scores": inp.scores, "seq_lens": inp.seq_lens, "page_tables": inp.page_tables}
+                spec, items = dict(kind="topk"), np.arange(nrows)
+            else:
+                inp = meta["inp"]
+                arrays = {f: getattr(inp, f) for f in ("q", "w", "kcache", "kscale", "block_table", "seq_lens",
+                                                       "row_to_batch")}
+                spec, items = dict(kind="fused", dtype=inp.dtype), np.arange(nrows)
+            for f, a in arrays.items():
+                if a is not None:
+                    np.save(os.path.join(sub, f + ".npy"), np.ascontiguousarray(a))
+            spec["folder"] = sub
+        # spread each worker's items over the whole part (row lengths vary along it)
+        rng = np.random.default_rng(11)
+        specs.append((name, nrows, spec, rng.permutation(items)))
+    return specs
 
 
-def run_reference(args):
-    rank, world, _ = _dist()
-    if rank != 0:
-        return
+class OraclePool:
+    """The oracle's worker pool over the host cores (spawn start method: a
+    process forked after CUDA was used can hang)."""
+
+    def __init__(self, parts_meta, workers=None):
+        import multiprocessing as mp
+        import tempfile
+
+        for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[v] = "1"  # one BLAS thread per worker process
+        self.workers = workers or len(os.sched_getaffinity(0))
+        self._tmp = tempfile.TemporaryDirectory()
+        self.specs = _oracle_specs(parts_meta, self._tmp.name)
+        self.pool = mp.get_context("spawn").Pool(self.workers)
+        self.pool.map(_oracle_warm, range(self.workers))
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+        self._tmp.cleanup()
+
+    def step_rate(self, budget_s):
+        """Rows/s of the oracle over the step's row mix (all workers), the
+        same for one core, and a note on the sample."""
+        per_step, per_step_1, rows, notes = 0.0, 0.0, 0, []
+        budget = budget_s / max(len(self.specs), 1)
+        for name, nrows, spec, items in self.specs:
+            tasks = [(name, spec, items[w::self.workers], budget) for w in range(self.workers)]
+            res = self.pool.map(_oracle_rows, tasks)
+            done = sum(r[0] for r in res)
+            longest = max(r[1] for r in res)
+            total = sum(r[1] for r in res)
+            per_step += nrows * longest / max(done, 1)
+            per_step_1 += nrows * total / max(done, 1)
+            rows += nrows
+            notes.append(f"{name}: {done} of {nrows} rows in {longest:.1f} s on {self.workers} processes "
+                         f"({total:.1f} s of oracle time)")
+        return rows / per_step, rows / per_step_1, "; ".join(notes)
+
+
+def _parts_meta_for_reference(args):
     import workloads as W
 
     metas = []
@@ -497,20 +611,34 @@ def run_reference(args):
         if dt_name in args.paths:
             inp = make()
             metas.append((dt_name, inp.rows, dict(inp=inp)))
+    return metas
+
+
+def run_reference(args):
+    rank, world, _ = _dist()
+    if rank != 0:
+        return
+    pool = OraclePool(_parts_meta_for_reference(args))
     budget = max(3.0, 150.0 / max(1, args.steps + args.warmup))
-    vals, note = [], ""
-    for s in range(args.warmup + args.steps):
-        v, note = oracle_step_rate(metas, budget)
-        if s >= args.warmup:
-            vals.append(v)
+    vals, note, one = [], "", 0.0
+    try:
+        for s in range(args.warmup + args.steps):
+            v, one, note = pool.step_rate(budget)
+            if s >= args.warmup:
+                vals.append(v)
+    finally:
+        pool.close()
     value = float(np.median(vals))
-    rows = sum(m[1] for m in metas)
+    rows = sum(m[1] for m in pool.specs)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": rows / value * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "config": {"workload": WORKLOAD},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"per step, a row sample of each part (about {budget:.0f} s): {note}"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": pool.workers, "kind": "oracle",
+                             "one_core_value": one,
+                             "sample": (f"per step, a bounded row sample of each part (about {budget:.0f} s of wall "
+                                        f"time over {pool.workers} worker processes); ms_per_step is extrapolated "
+                                        f"from the sample's rate to the whole step; last step: {note}")},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -530,7 +658,12 @@ def run_gpu(args):
 
     sai.load()
     hbm_peak, bf16_peak, peak_kind = _peaks()
-    fp8_peak = bf16_peak * FP8_OVER_BF16
+    fp8_peak, fp8_note = measure_fp8_peak(dev)
+    if fp8_peak is not None:
+        fp8_kind = f"measured fp8 burst on this GPU: {fp8_note}"
+    else:
+        fp8_peak = bf16_peak * FP8_OVER_BF16
+        fp8_kind = f"{peak_kind} bf16 burst x {FP8_OVER_BF16} (nominal fp8/bf16; {fp8_note})"
 
     host_note = _bind_host_to_gpu(local)
     parts = build_parts(dev, args)
@@ -567,9 +700,10 @@ def run_gpu(args):
                 ev[s][j][1].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
-    part_ms = [float(np.mean([ev[s][j][0].elapsed_time(ev[s][j][1]) for s in range(args.steps)]))
+    # medians over the timed steps
+    part_ms = [float(np.median([ev[s][j][0].elapsed_time(ev[s][j][1]) for s in range(args.steps)]))
                for j in range(len(parts))]
-    ms = float(np.mean([ev[s][0][0].elapsed_time(ev[s][-1][1]) for s in range(args.steps)]))
+    ms = float(np.median([ev[s][0][0].elapsed_time(ev[s][-1][1]) for s in range(args.steps)]))
     ms = _max_over_ranks(ms, world, dev)
     rows = sum(p.rows for p in parts)
     value = _job_rate(rows, world, ms)
@@ -578,6 +712,8 @@ def run_gpu(args):
     for part, pm in zip(parts, part_ms):
         entry = {"ms": pm, "rows_per_s": part.rows / (pm * 1e-3), "keys_per_s": part.keys / (pm * 1e-3),
                  "hbm_gbs": part.bytes / (pm * 1e-3) / 1e9, "hbm_frac": part.bytes / (pm * 1e-3) / 1e9 / hbm_peak}
+        if part.l2_bytes > part.bytes:  # re-reads of a request's keys, served by L2
+            entry["l2_gbs"] = part.l2_bytes / (pm * 1e-3) / 1e9
         if part.flops:
             entry["tflops"] = part.flops / (pm * 1e-3) / 1e12
             if part.name.endswith("_bf16"):
@@ -590,7 +726,7 @@ def run_gpu(args):
     tp, tm = parts[top], part_ms[top]
     if tp.name == "fused_prefill":
         roof = {"bound": "tensor", "achieved": tp.flops / (tm * 1e-3) / 1e12, "peak": fp8_peak, "unit": "TFLOP/s",
-                "peak_kind": f"{peak_kind} bf16 burst x {FP8_OVER_BF16} (nominal fp8/bf16)"}
+                "peak_kind": fp8_kind}
     elif tp.name == "fused_prefill_bf16":
         roof = {"bound": "tensor", "achieved": tp.flops / (tm * 1e-3) / 1e12, "peak": bf16_peak, "unit": "TFLOP/s",
                 "peak_kind": f"{peak_kind} bf16 burst"}
@@ -631,8 +767,14 @@ def run_gpu(args):
 
     cpu = None
     if rank == 0 and not args.no_cpu:
-        v, note = oracle_step_rate([(p.name, p.rows, p.meta) for p in parts], 20.0)
-        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": note}
+        pool = OraclePool([(p.name, p.rows, p.meta) for p in parts])
+        try:
+            v, one, note = pool.step_rate(20.0)
+        finally:
+            pool.close()
+        cpu = {"value": v, "unit": UNIT, "cores": pool.workers, "kind": "oracle", "one_core_value": one,
+               "sample": f"a bounded row sample of each part (about 20 s of wall time), rate extrapolated to the "
+                         f"step's rows: {note}"}
 
     if rank == 0:
         line = {

@@ -6,8 +6,11 @@ the tensor cores; they must agree within 1e-3 relative (floored at the row's
 k-th score). Integer-valued inputs make every score an exact integer on both
 sides, so there the comparison is bit-exact and pins the MMA operand layout.
 Selection: a GPU pick is accepted when its oracle score is at least the
-oracle's k-th score minus that tolerance; the count, distinctness, order and
-the slot transform of the GPU's own indices are checked exactly.
+oracle's k-th score minus that tolerance; the count, distinctness, order
+(score descending, equal GPU scores by ascending index) and the slot
+transform of the GPU's own indices are checked exactly. The full-size
+workloads are checked on every row, in a pool of processes over the host
+cores (tests/parity_pool.py).
 """
 
 import numpy as np
@@ -16,11 +19,11 @@ import torch
 
 import workloads as W
 from oracle.score import index_scores
+from parity_pool import TOL, check_fused_all_rows, check_fused_rows, kth
 
 pytestmark = pytest.mark.gpu
 
 DEV = torch.device("cuda:0")
-TOL = 1e-3
 
 
 def _t(a):
@@ -62,48 +65,18 @@ def _fused(inp, group_rows=1):
     return slots.cpu().numpy(), idx.cpu().numpy(), scores.cpu().numpy()
 
 
-def _kth(s, k):
-    return float(np.sort(s)[::-1][min(s.size, k) - 1]) if s.size else 0.0
-
-
-def _check_dense(got, inp, exact=False, rows=None):
-    rows = list(range(inp.rows)) if rows is None else rows
-    ref = index_scores(inp, rows)
-    for j, i in enumerate(rows):
-        n = int(inp.seq_lens[i])
-        g = got[i, :n].astype(np.float64)
-        r = ref[j].astype(np.float64)
-        if exact:
-            assert np.array_equal(g, r), f"row {i}: first diff at {np.flatnonzero(g != r)[:5]}"
-        else:
-            floor = abs(_kth(ref[j], 512)) if n else 0.0
-            err = np.abs(g - r) / np.maximum(np.maximum(np.abs(r), floor), 1e-30)
-            assert err.max() <= TOL, f"row {i}: max rel err {err.max():.3e} at {int(err.argmax())}"
-
-
 def _check_topk(got, inp, rows=None, k=512):
     slots, idx, scores = got
     rows = list(range(inp.rows)) if rows is None else rows
-    ref = index_scores(inp, rows)
-    for j, i in enumerate(rows):
-        n = int(inp.seq_lens[i])
-        kk = min(n, k)
-        gi = idx[i]
-        assert (gi[kk:] == -1).all() and (slots[i][kk:] == -1).all(), f"row {i}: padding"
-        sel = gi[:kk].astype(np.int64)
-        assert (sel >= 0).all() and (sel < n).all(), f"row {i}: index range"
-        assert np.unique(sel).size == kk, f"row {i}: duplicates"
-        s_ora = ref[j].astype(np.float64)
-        s_k = _kth(ref[j], k)
-        tol = TOL * max(abs(s_k), 1e-30)
-        assert (s_ora[sel] >= s_k - tol).all(), f"row {i}: a pick below the k-th score"
-        gs = scores[i][:kk].astype(np.float64)
-        assert (np.abs(gs - s_ora[sel]) <= TOL * np.maximum(np.abs(s_ora[sel]), abs(s_k)) + 1e-30).all(), \
-            f"row {i}: selected score mismatch"
-        assert (gs[:-1] >= gs[1:]).all(), f"row {i}: not score-descending"
-        b = i if inp.row_to_batch is None else int(inp.row_to_batch[i])
-        pages = inp.block_table[b][sel // 128].astype(np.int64)
-        assert np.array_equal(slots[i][:kk], pages * 128 + sel % 128), f"row {i}: slots"
+    bad = check_fused_rows(inp, rows, index_scores(inp, rows), slots, idx, scores, k)
+    assert not bad, f"{len(bad)} rows fail: {bad[:5]}"
+
+
+def _check_all_rows_in_pool(got, inp):
+    """Every row against the oracle, the rows spread over the host cores."""
+    slots, idx, scores = got
+    bad = check_fused_all_rows(inp, slots, idx, scores)
+    assert not bad, f"{len(bad)} rows fail: {bad[:5]}"
 
 
 def _small(kind="normal", rows=6, lens=(1, 127, 128, 300, 1000, 2500), seed=41, dtype="e4m3"):
@@ -163,14 +136,12 @@ def test_fused_decode_full_size():
     _check_topk(_fused(inp), inp)
 
 
-def test_fused_prefill_full_size_sampled():
+def test_fused_prefill_full_size():
     """The fused prefill workload at full size (4096 causal rows on a 32768-
     token KV, grouped by 4), in the launch configuration the benchmark times;
-    sampled rows against the oracle."""
+    every row against the oracle."""
     inp = W.fused_prefill()
-    got = _fused(inp, group_rows=4)
-    sample = [0, 1, 2, 3, 1000, 2047, 2048, 3333, 4092, 4093, 4094, 4095]
-    _check_topk(got, inp, rows=sample)
+    _check_all_rows_in_pool(_fused(inp, group_rows=4), inp)
 
 
 @pytest.mark.parametrize("kind", ["normal", "int"])
@@ -279,10 +250,10 @@ def test_bf16_fused_decode_full_size():
     _check_topk(_fused(inp), inp)
 
 
-def test_bf16_fused_prefill_full_size_sampled():
+def test_bf16_fused_prefill_full_size():
+    """The prefill workload's shapes with a bf16 cache; every row checked."""
     inp = W.fused_prefill(dtype="bf16")
-    got = _fused(inp, group_rows=4)
-    _check_topk(got, inp, rows=[0, 1, 2, 3, 2047, 2048, 4093, 4094, 4095])
+    _check_all_rows_in_pool(_fused(inp, group_rows=4), inp)
 
 
 @pytest.mark.parametrize("dtype", ["e4m3", "bf16"])

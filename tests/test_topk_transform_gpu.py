@@ -10,6 +10,7 @@ import torch
 
 import workloads as W
 from oracle.topk import topk_transform as oracle_topk
+from parity_pool import check_packed_extend_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -135,11 +136,12 @@ def test_bad_row_metadata_is_flagged_and_emptied():
     assert sai.device_status() == 0
 
 
-def test_packed_extend_full_size_sampled():
+def test_packed_extend_full_size():
     """The packed-extend prefill workload at full size ([16384, 140000]
     scores, two requests on a 70000-token KV, +inf outside the windows), in
-    the launch configuration the benchmark times; sampled rows are checked
-    against the oracle, every row against the output invariants."""
+    the launch configuration the benchmark times; every row against the
+    oracle, element by element (the oracle runs in a pool of processes over
+    the host cores, each regenerating its rows' windows from the seed)."""
     import sparse_attention_indexer_top_gb300 as sai
 
     row_starts, seq_lens, r2b, width = W.packed_extend_meta()
@@ -156,19 +158,8 @@ def test_packed_extend_full_size_sampled():
                                     row_to_batch=_t(r2b), want_indices=True)
     torch.cuda.synchronize()
     assert sai.device_status() == 0
-    gi = idx.cpu().numpy()
-    gs = slots.cpu().numpy()
-    # every row: 512 distinct in-window indices, slots = transform of them
-    assert (gi >= 0).all() and (gi < seq_lens[:, None]).all()
-    srt = np.sort(gi, axis=1)
-    assert (srt[:, 1:] != srt[:, :-1]).all()
-    assert np.array_equal(gs, pt[r2b[:, None], gi])
-    for i in list(range(0, rows, 331)) + [8191, 8192, rows - 1]:
-        n = int(seq_lens[i])
-        w = W.packed_extend_window(3, i, n)
-        rs, ri = oracle_topk(w[None, :], np.array([n]), pt[[r2b[i]]], 1, 512)
-        assert np.array_equal(gi[i], ri[0]), i
-        assert np.array_equal(gs[i], rs[0]), i
+    bad = check_packed_extend_rows(3, seq_lens, r2b, pt, 1, 512, slots.cpu().numpy(), idx.cpu().numpy())
+    assert not bad, f"{len(bad)} rows differ: {bad[:5]}"
 
 
 def test_chunked_prefix_calls_match_one_call():
