@@ -65,6 +65,21 @@ def _fused(inp, group_rows=1):
     return slots.cpu().numpy(), idx.cpu().numpy(), scores.cpu().numpy()
 
 
+def _check_dense(got, inp, exact=False, rows=None):
+    rows = list(range(inp.rows)) if rows is None else rows
+    ref = index_scores(inp, rows)
+    for j, i in enumerate(rows):
+        n = int(inp.seq_lens[i])
+        g = got[i, :n].astype(np.float64)
+        r = ref[j].astype(np.float64)
+        if exact:
+            assert np.array_equal(g, r), f"row {i}: first diff at {np.flatnonzero(g != r)[:5]}"
+        else:
+            floor = abs(kth(ref[j], 512)) if n else 0.0
+            err = np.abs(g - r) / np.maximum(np.maximum(np.abs(r), floor), 1e-30)
+            assert err.max() <= TOL, f"row {i}: max rel err {err.max():.3e} at {int(err.argmax())}"
+
+
 def _check_topk(got, inp, rows=None, k=512):
     slots, idx, scores = got
     rows = list(range(inp.rows)) if rows is None else rows
