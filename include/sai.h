@@ -99,13 +99,24 @@ size_t sai_topk_transform_workspace(int64_t rows, int64_t score_stride, int32_t 
  * row_starts   int32 [rows] or NULL. The caller guarantees
  *              start + n <= score_stride (checked on device).
  * seq_lens     int32 [rows], >= 0.
- * page_tables  int32 [pt_rows, pt_stride]; required when out_slots != NULL.
+ * page_tables  int32 [pt_rows, pt_stride]; required when out_slots or
+ *              out_blocks is given.
  *              Without row_to_batch, pt_rows >= rows is checked here; with
  *              it, 0 <= row_to_batch[i] < pt_rows is checked on device.
  * page_size    >= 1 (1 = one slot per token, the "wide" table).
  * k            must be 512 (SAI_ERR_UNSUPPORTED otherwise).
  * out_slots    int32 [rows, 512] or NULL; out_indices int32 [rows, 512] or
- *              NULL (row-local positions); at least one must be given.
+ *              NULL (row-local positions).
+ * out_blocks   int32 [rows, 512] or NULL: the row's selected slots as the
+ *              ascending distinct blocks slot / block_size, -1 padded, built
+ *              by the same call from the slots it picks (ROCm/ATOM PR #1282
+ *              "merge build sparse block into topk": the block list comes out
+ *              of the top-k, not out of a second pass over the slots); needs
+ *              page_tables. block_size >= 1 when out_blocks is given (128:
+ *              a 128-token KV block; ignored otherwise). out_counts int32
+ *              [rows] or NULL: each row's number of blocks (only with
+ *              out_blocks). At least one of out_slots, out_indices and
+ *              out_blocks must be given.
  * workspace    device memory of workspace_bytes (16-byte aligned) or NULL.
  *              If it is smaller than sai_topk_transform_workspace asks for,
  *              every row is processed by a single CTA (correct, slower for
@@ -116,7 +127,8 @@ size_t sai_topk_transform_workspace(int64_t rows, int64_t score_stride, int32_t 
 int sai_topk_transform(const float* scores, int64_t rows, int64_t score_stride, const int32_t* row_starts,
                        const int32_t* seq_lens, const int32_t* page_tables, int64_t pt_rows, int64_t pt_stride,
                        const int32_t* row_to_batch, int32_t page_size, int32_t k, int32_t* out_slots,
-                       int32_t* out_indices, void* workspace, size_t workspace_bytes, sai_stream_t stream);
+                       int32_t* out_indices, int32_t block_size, int32_t* out_blocks, int32_t* out_counts,
+                       void* workspace, size_t workspace_bytes, sai_stream_t stream);
 
 /*
  * Workspace bytes that sai_index_score_topk needs for these sizes on the
@@ -138,7 +150,10 @@ size_t sai_index_score_topk_workspace(int64_t rows, int32_t max_seq_len, int32_t
  *   for t < n, p = block_table[b*bt_stride + t/128], o = t % 128;
  * then the top-k keys by (score desc, index asc):
  *   out_indices[i*512 + j] = t_j, out_slots[...] = p_j*128 + o_j,
- *   out_scores[...] = score(t_j) (fp32), padded with -1 / NaN.
+ *   out_scores[...] = score(t_j) (fp32), padded with -1 / NaN;
+ *   optionally out_blocks[i*512 + j] = the row's ascending distinct
+ *   out_slots / list_block_size (-1 padded) and out_counts[i] their number,
+ *   as for sai_topk_transform (list_block_size 128 gives the block ids p_j).
  *
  * q_fp8       e4m3fn [rows, heads, dim], 16-byte aligned.
  * w           fp32 [rows, heads].
@@ -153,15 +168,18 @@ size_t sai_index_score_topk_workspace(int64_t rows, int32_t max_seq_len, int32_t
  *             value (packed prefill): the kernel then scores the rows in
  *             pairs, each key block once per pair. A pair whose rows differ
  *             is emptied and sets bit 1.
- * out_*       any of the three may be NULL, not all.
+ * out_*       any of out_slots, out_indices, out_scores, out_blocks may be
+ *             NULL, not all; out_counts only with out_blocks, which needs
+ *             list_block_size >= 1.
  * workspace   at least sai_index_score_topk_workspace(...) bytes, 16-byte aligned.
  */
 int sai_index_score_topk(const uint8_t* q_fp8, const float* w, const uint8_t* kcache_fp8, const float* kscale,
                          int64_t num_blocks, const int32_t* block_table, int64_t bt_rows, int64_t bt_stride,
                          const int32_t* row_to_batch, const int32_t* seq_lens, int64_t rows, int32_t heads,
                          int32_t dim, int32_t block_size, int32_t max_seq_len, int32_t group_rows, int32_t k,
-                         int32_t* out_slots, int32_t* out_indices, float* out_scores, void* workspace,
-                         size_t workspace_bytes, sai_stream_t stream);
+                         int32_t* out_slots, int32_t* out_indices, float* out_scores, int32_t list_block_size,
+                         int32_t* out_blocks, int32_t* out_counts, void* workspace, size_t workspace_bytes,
+                         sai_stream_t stream);
 
 /*
  * sai_index_score -- the same FP8 index scores written densely (for tests):
@@ -197,7 +215,8 @@ int sai_index_score_topk_bf16(const uint16_t* q_bf16, const float* w, const uint
                               int64_t bt_stride, const int32_t* row_to_batch, const int32_t* seq_lens, int64_t rows,
                               int32_t heads, int32_t dim, int32_t block_size, int32_t max_seq_len, int32_t group_rows,
                               int32_t k, int32_t* out_slots, int32_t* out_indices, float* out_scores,
-                              void* workspace, size_t workspace_bytes, sai_stream_t stream);
+                              int32_t list_block_size, int32_t* out_blocks, int32_t* out_counts, void* workspace,
+                              size_t workspace_bytes, sai_stream_t stream);
 int sai_index_score_bf16(const uint16_t* q_bf16, const float* w, const uint16_t* kcache_bf16, const float* kscale,
                          int64_t num_blocks, const int32_t* block_table, int64_t bt_rows, int64_t bt_stride,
                          const int32_t* row_to_batch, const int32_t* seq_lens, int64_t rows, int32_t heads,
@@ -262,6 +281,8 @@ int sai_index_score_topk_per_head_bf16(const uint16_t* q_bf16, const float* w, c
 /*
  * sai_sparse_blocks -- per-row distinct KV blocks of top-k slots.
  *
+ * For callers that already hold slots; the top-k entry points above build
+ * the same lists in their last stage when given out_blocks.
  * Follows ROCm/ATOM PR #1282 "merge build sparse block into topk" (title and
  * Motivation): the sparse attention after the indexer reads KV blocks, so
  * each row's selected physical slots (the out_slots of sai_topk_transform
@@ -297,8 +318,9 @@ int sai_sparse_blocks(const int32_t* slots, int64_t rows, int32_t k, int32_t blo
  * allocator beyond its fixed input and output buffers). The paper has no
  * counterpart: this entry point exists only for such callers.
  *
- * Arguments, outputs, ordering and errors are those of sai_topk_transform.
- * Instead of a caller workspace, every call uses a fixed library-owned
+ * Arguments, outputs, ordering and errors are those of sai_topk_transform
+ * without the block-list outputs. Instead of a caller workspace, every call
+ * uses a fixed library-owned
  * device array of SAI_NOALLOC_SCRATCH_BYTES: its first 256 bytes hold the
  * work counter from which the CTAs take rows (reset to zero by each call on
  * its stream), and the split path for few long rows also keeps its partial

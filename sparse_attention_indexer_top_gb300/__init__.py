@@ -51,18 +51,33 @@ def topk_transform_workspace(rows: int, score_stride: int, k: int = TOPK) -> int
     return int(load().sai_topk_transform_workspace(int(rows), int(score_stride), int(k)))
 
 
+def _block_outputs(rows, k, dev, want_blocks, out_blocks, out_counts):
+    if want_blocks or out_blocks is not None:
+        if out_blocks is None:
+            out_blocks = torch.empty((rows, k), dtype=torch.int32, device=dev)
+        if out_counts is None:
+            out_counts = torch.empty((rows,), dtype=torch.int32, device=dev)
+        _need(out_blocks, "out_blocks", torch.int32, dev, 2)
+        _need(out_counts, "out_counts", torch.int32, dev, 1)
+    return out_blocks, out_counts
+
+
 def topk_transform(scores: torch.Tensor, seq_lens: torch.Tensor, page_tables: Optional[torch.Tensor] = None, *,
                    page_size: int = 1, k: int = TOPK, row_starts: Optional[torch.Tensor] = None,
                    row_to_batch: Optional[torch.Tensor] = None, out_slots: Optional[torch.Tensor] = None,
                    out_indices: Optional[torch.Tensor] = None, want_indices: bool = False,
-                   workspace: Optional[torch.Tensor] = None, stream=None):
+                   block_size: int = 128, want_blocks: bool = False, out_blocks: Optional[torch.Tensor] = None,
+                   out_counts: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, stream=None):
     """Top-k of each row's score window mapped through its page-table row.
 
     ``scores`` is fp32 ``[rows, stride]`` with unit column stride (any row
     stride); ``seq_lens``, ``row_starts``, ``row_to_batch`` are int32
     ``[rows]``; ``page_tables`` int32 ``[pt_rows, pt_stride]`` with unit
     column stride. Returns ``out_slots`` (int32 ``[rows, k]``), or
-    ``(out_slots, out_indices)`` when indices are requested.
+    ``(out_slots, out_indices)`` when indices are requested. With
+    ``want_blocks`` (or ``out_blocks``) the same call also builds each row's
+    ascending distinct blocks ``slot // block_size`` (int32 ``[rows, k]``, -1
+    padded) and their counts (int32 ``[rows]``), appended to the result.
     """
     dev = scores.device
     _need(scores, "scores", torch.float32, dev, 2)
@@ -85,14 +100,19 @@ def topk_transform(scores: torch.Tensor, seq_lens: torch.Tensor, page_tables: Op
     if workspace is None and ws_bytes:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     pt_rows, pt_stride = (page_tables.shape[0], page_tables.stride(0)) if page_tables is not None else (0, 0)
+    out_blocks, out_counts = _block_outputs(rows, k, dev, want_blocks, out_blocks, out_counts)
     st = load().sai_topk_transform(
         _ptr(scores), rows, stride, _ptr(row_starts), _ptr(seq_lens), _ptr(page_tables), pt_rows, pt_stride,
-        _ptr(row_to_batch), int(page_size), int(k), _ptr(out_slots), _ptr(out_indices), _ptr(workspace),
+        _ptr(row_to_batch), int(page_size), int(k), _ptr(out_slots), _ptr(out_indices), int(block_size),
+        _ptr(out_blocks), _ptr(out_counts), _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream))
     check(st, "sai_topk_transform")
+    blocks = () if out_blocks is None else (out_blocks, out_counts)
     if out_slots is None:
-        return out_indices
-    return (out_slots, out_indices) if (want_indices or out_indices is not None) else out_slots
+        return (out_indices, *blocks) if blocks else out_indices
+    if want_indices or out_indices is not None:
+        return (out_slots, out_indices, *blocks)
+    return (out_slots, *blocks) if blocks else out_slots
 
 
 def topk_transform_noalloc(scores: torch.Tensor, seq_lens: torch.Tensor, page_tables: torch.Tensor, *,
@@ -148,13 +168,16 @@ def index_score_topk(q: torch.Tensor, w: torch.Tensor, kcache: torch.Tensor, ksc
                      block_table: torch.Tensor, seq_lens: torch.Tensor, *, max_seq_len: int,
                      row_to_batch: Optional[torch.Tensor] = None, group_rows: int = 1, k: int = TOPK,
                      out_slots: Optional[torch.Tensor] = None, out_indices: Optional[torch.Tensor] = None,
-                     out_scores: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                     stream=None):
+                     out_scores: Optional[torch.Tensor] = None, block_size: int = 128, want_blocks: bool = False,
+                     out_blocks: Optional[torch.Tensor] = None, out_counts: Optional[torch.Tensor] = None,
+                     workspace: Optional[torch.Tensor] = None, stream=None):
     """Fused index score + top-k. ``q`` e4m3 codes (uint8) ``[rows, 64,
     128]``, ``w`` fp32 ``[rows, 64]``, ``kcache`` uint8 ``[blocks, 128, 128]``,
     ``kscale`` fp32 ``[blocks, 128]``, ``block_table`` int32; or ``q`` and
     ``kcache`` torch.bfloat16 (bf16 index cache, ``kscale`` optional).
-    Returns ``(slots, indices, scores)``."""
+    Returns ``(slots, indices, scores)``, plus ``(blocks, counts)`` (each
+    row's ascending distinct ``slot // block_size``, -1 padded) with
+    ``want_blocks`` or ``out_blocks``."""
     dev, bf16 = _fused_check(q, w, kcache, kscale, block_table, seq_lens, row_to_batch)
     rows = q.shape[0]
     if out_slots is None:
@@ -166,13 +189,17 @@ def index_score_topk(q: torch.Tensor, w: torch.Tensor, kcache: torch.Tensor, ksc
     ws = index_score_topk_workspace(rows, max_seq_len, group_rows, k) if rows else 0
     if workspace is None and ws:
         workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+    out_blocks, out_counts = _block_outputs(rows, k, dev, want_blocks, out_blocks, out_counts)
     name = "sai_index_score_topk_bf16" if bf16 else "sai_index_score_topk"
     st = getattr(load(), name)(
         _ptr(q), _ptr(w), _ptr(kcache), _ptr(kscale), kcache.shape[0], _ptr(block_table), block_table.shape[0],
         block_table.stride(0), _ptr(row_to_batch), _ptr(seq_lens), rows, q.shape[1], q.shape[2], kcache.shape[1],
         int(max_seq_len), int(group_rows), int(k), _ptr(out_slots), _ptr(out_indices), _ptr(out_scores),
-        _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream(stream))
+        int(block_size), _ptr(out_blocks), _ptr(out_counts), _ptr(workspace),
+        0 if workspace is None else workspace.numel(), _stream(stream))
     check(st, name)
+    if out_blocks is not None:
+        return out_slots, out_indices, out_scores, out_blocks, out_counts
     return out_slots, out_indices, out_scores
 
 

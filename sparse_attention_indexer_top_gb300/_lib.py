@@ -21,15 +21,16 @@ SIGNATURES = {
     "sai_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int), ctypes.c_int, _vp]),
     "sai_topk_transform_workspace": (_c_size, [_c_i64, _c_i64, _c_i32]),
     "sai_topk_transform": (ctypes.c_int, [_vp, _c_i64, _c_i64, _vp, _vp, _vp, _c_i64, _c_i64, _vp, _c_i32, _c_i32,
-                                          _vp, _vp, _vp, _c_size, _vp]),
+                                          _vp, _vp, _c_i32, _vp, _vp, _vp, _c_size, _vp]),
     "sai_index_score_topk_workspace": (_c_size, [_c_i64, _c_i32, _c_i32, _c_i32]),
     "sai_index_score_topk": (ctypes.c_int, [_vp, _vp, _vp, _vp, _c_i64, _vp, _c_i64, _c_i64, _vp, _vp, _c_i64, _c_i32,
-                                            _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _vp, _vp, _vp, _vp, _c_size, _vp]),
+                                            _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _vp, _vp, _vp, _c_i32, _vp, _vp,
+                                            _vp, _c_size, _vp]),
     "sai_index_score": (ctypes.c_int, [_vp, _vp, _vp, _vp, _c_i64, _vp, _c_i64, _c_i64, _vp, _vp, _c_i64, _c_i32, _c_i32,
                                        _c_i32, _c_i32, _c_i32, _vp, _c_i64, _vp]),
     "sai_index_score_topk_bf16": (ctypes.c_int, [_vp, _vp, _vp, _vp, _c_i64, _vp, _c_i64, _c_i64, _vp, _vp, _c_i64,
-                                                 _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _vp, _vp, _vp, _vp,
-                                                 _c_size, _vp]),
+                                                 _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _vp, _vp, _vp,
+                                                 _c_i32, _vp, _vp, _vp, _c_size, _vp]),
     "sai_index_score_bf16": (ctypes.c_int, [_vp, _vp, _vp, _vp, _c_i64, _vp, _c_i64, _c_i64, _vp, _vp, _c_i64, _c_i32,
                                             _c_i32, _c_i32, _c_i32, _c_i32, _vp, _c_i64, _vp]),
     "sai_index_score_topk_per_head_workspace": (_c_size, [_c_i64, _c_i32, _c_i32]),

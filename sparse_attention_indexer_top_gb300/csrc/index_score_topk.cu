@@ -14,10 +14,11 @@
 // is the formula the library adopts (scale outside the relu, no 1/sqrt(d)).
 //
 // GB300 design. A work unit is a group of R query rows (R = 1 for decode,
-// R = 2 for packed prefill, where consecutive rows share one request) and a
-// chunk of that request's KV blocks; one CTA per unit (the kernel can also
-// walk several units with its barrier phases carried over). Roles:
-//   * warp 4R streams each 128-token FP8 key block [128 keys x 128 dims]
+// R = 4 for packed prefill, whose rows come in groups of 4 sharing one
+// request) and a chunk of that request's KV blocks; one CTA per unit (the
+// kernel can also walk several units with its barrier phases carried over).
+// Roles:
+//   * warp 4R streams each 128-token key block [128 keys x 128 dims]
 //     through a shared-memory ring with 2-D TMA tensor loads (128-byte
 //     swizzle; the paged gather is just the block's row coordinate);
 //   * warp 4R+1 issues tcgen05.mma kind::f8f6f4 with the keys as M = 128 and
@@ -28,8 +29,24 @@
 //     keeps its 16 head weights in registers; relu (an exact saturating
 //     multiply), the weighted head sum (f32x2 FMAs), a 4-lane reduce-scatter
 //     to one key per lane, the key's scale, and the row's running top-k
-//     filter (per-warp candidate lists cut back to 512 by a radix select in
-//     shared memory when they fill up).
+//     filter.
+//
+// Running top-k. Each epilogue warp keeps its own candidate list and never
+// waits for the row's other warps while the unit streams: when its list is
+// about to overflow it cuts it, alone, to its own exact top 512 (every
+// dropped key is beaten by 512 keys of the same warp). The row's warps meet
+// twice per unit. (1) The unit's tiles are streamed starting from its middle
+// tile (then wrapping around); after the first kSampleTiles tiles every
+// key of those tiles is a candidate, and the row sets a start threshold at
+// the m-th largest of those sampled scores, m chosen so that about
+// kSpecMargin x 512 keys of the whole unit are expected to pass. (2) At the
+// unit end the row's candidates are cut to its top 512. The start threshold
+// is a guess: if fewer than 512 candidates reached it, keys above the true
+// 512th may have been dropped, so the unit is streamed again (TMA, MMA and
+// epilogue all replay it) without a start threshold. With at least 512
+// candidates at or above the threshold, the 512th key is at or above it and
+// nothing that belongs to the top 512 was dropped.
+//
 // The per-(row, chunk) candidate lists go to a workspace; the merge kernel
 // of topk_transform.cu then selects, sorts and page-transforms each row.
 //
@@ -37,7 +54,7 @@
 // model dtype): q and the keys are bf16, the MMA is kind::f16 (K = 16 per
 // instruction) and a 256-byte key row is staged as two 128-byte-swizzled
 // halves of 64 dims (one TMA box each), so the MMA walks 2 x 4 K-steps; the
-// relu is a plain max (bf16 dot products have no fixed range), and the key
+// relu is s + |s| (bf16 dot products have no fixed range), and the key
 // scale may be absent (scale 1). Everything else is shared with the FP8 path.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -59,25 +76,19 @@ constexpr int kH = 64;        // index heads
 constexpr int kD = 128;       // head dim (elements per row)
 constexpr int kSwB = 128;     // bytes per row of one 128-byte-swizzled region
 constexpr int kBlk = 128;     // tokens per KV block = MMA M
-// K-tile stages, query-tile buffers and resident CTAs per SM: single rows
-// (decode) run three small CTAs per SM with a 2-stage ring, row pairs
-// (prefill) two with a 3-stage ring; one query buffer each, since every CTA
-// takes one unit (measured against 2-4 stages and 2-3 CTAs per SM; a 3-stage
-// ring at three CTAs per SM, with 384-entry sub-lists to fit, was slower).
-// The ring holds 16 KB slots, one 128-byte-swizzled region of a key tile
-// each: an FP8 tile is one region, a bf16 tile two (dims 0-63, 64-127), so
-// the bf16 variant keeps a tile in flight with the same CTAs per SM.
+// K-tile ring slots and resident CTAs per SM: single rows (decode) run three
+// small CTAs per SM with a 2-slot ring; groups of four rows (prefill, MMA
+// N = 256, both accumulator buffers filling the SM's 512 TMEM columns) run
+// one CTA per SM with a 4-slot ring (3 for bf16, whose query tile is twice
+// as large). A ring slot is one 16 KB 128-byte-swizzled region of a key
+// tile: an FP8 tile is one region, a bf16 tile two (dims 0-63, 64-127).
 template <int R, bool BF16 = false>
 __host__ __device__ constexpr int fused_stages() {
-  return BF16 ? 2 : (R == 1 ? 2 : (R == 2 ? 3 : 4));
-}
-template <int R>
-__host__ __device__ constexpr int fused_qbufs() {
-  return R <= 2 ? 1 : 2;
+  return R == 1 ? 2 : (BF16 ? 3 : 4);
 }
 template <int R, bool BF16 = false>
 __host__ __device__ constexpr int fused_ctas_per_sm() {
-  return R == 1 ? 3 : (R == 2 ? 2 : 1);
+  return R == 1 ? 3 : 1;
 }
 template <bool BF16>
 __host__ __device__ constexpr int elem_bytes() {
@@ -88,30 +99,34 @@ template <bool BF16>
 __host__ __device__ constexpr int sw_regions() {
   return kD * elem_bytes<BF16>() / kSwB;
 }
-constexpr int kSyncEvery = 4; // tiles between the row group's count exchanges
-// Candidate sub-list per epilogue warp. A list is cut back once it holds
-// more than kSub - 4 tiles x 32 entries, and a warp appends at most 32 per
-// tile, so it never overflows; the cut leaves 128 per list.
-constexpr int kSub = 512;
-constexpr int kSubPruneAt = kSub - kSyncEvery * 32;
-static_assert(kSubPruneAt >= kTopK / 4 && 4 * kSub > kTopK, "sub-list sizes");
-constexpr int kEpiRow = 128;  // epilogue threads per query row (4 warps, one TMEM lane quadrant each)
+// Candidate list per epilogue warp: a warp appends at most 32 per tile, and
+// cuts its list to 512 when the next tile might not fit.
+constexpr int kSub = 640;
+static_assert(kSub >= kTopK + 32 && kSub % 32 == 0 && kSub / 32 <= 32, "sub-list size");
+constexpr int kEpiRow = 128;       // epilogue threads per query row (4 warps, one TMEM lane quadrant each)
+constexpr int kSampleTiles = 8;    // tiles sampled, spread over the unit, before the start threshold
+constexpr int kSpecMinKeys = 2048; // a row's unit needs this many keys to start from a sampled threshold
+constexpr int kSpecMargin = 2;     // about kSpecMargin x 512 of the unit's keys are expected to pass it
 
 template <int R, bool BF16>
 struct __align__(1024) FusedSmem {
-  // a ring slot is one region of a key tile, [128 keys x 128 bytes]; a query
-  // tile is sw_regions() regions of [R*64 rows x 128 bytes]
+  // a ring slot is one region of a key tile, [128 keys x 128 bytes]; the
+  // query tile is sw_regions() regions of [R*64 rows x 128 bytes]
   uint8_t kst[fused_stages<R, BF16>()][kBlk * kSwB];  // 16 KB each, 1024-aligned
-  uint8_t q[fused_qbufs<R>()][R * kH * kD * elem_bytes<BF16>()];          // query tiles of consecutive units
-  uint32_t ckey[R][4 * kSub];  // row r: four per-warp sub-lists
+  uint8_t q[R * kH * kD * elem_bytes<BF16>()];
+  uint32_t ckey[R][4 * kSub];  // row r: four per-warp candidate lists
   int32_t cidx[R][4 * kSub];
+  // the row's cut output; between the row's two meetings, each warp's 1 KB
+  // quarter of it is that warp's histogram for cutting its own list
   uint32_t aux_key[R][kTopK];
   int32_t aux_idx[R][kTopK];
   SelectScratch sc[R];
   uint64_t full[fused_stages<R, BF16>()], empty[fused_stages<R, BF16>()], tfull[2], tempty[2];
-  uint64_t qfull[fused_qbufs<R>()], qempty[fused_qbufs<R>()];
+  uint64_t qfull, qempty, verdict;
   uint32_t tmem_base;
-  int wcnt[R][2][4];      // per-warp list sizes at a sync point (double-buffered)
+  int wcnt[R][4];       // per-warp list sizes at a meeting of the row
+  int row_fail[2][R];   // rows whose start threshold was too high, by pass parity
+  int replay;           // the verdict of the last pass: 1 = stream the unit again
 };
 
 template <int R, bool BF16>
@@ -120,9 +135,9 @@ constexpr size_t fused_smem_bytes() {
 }
 
 static_assert(3 * (fused_smem_bytes<1, false>() + 1024) <= 228 * 1024, "three single-row CTAs per SM");
-static_assert(2 * (fused_smem_bytes<2, false>() + 1024) <= 228 * 1024, "two row-pair CTAs per SM");
 static_assert(3 * (fused_smem_bytes<1, true>() + 1024) <= 228 * 1024, "three single-row bf16 CTAs per SM");
-static_assert(2 * (fused_smem_bytes<2, true>() + 1024) <= 228 * 1024, "two row-pair bf16 CTAs per SM");
+static_assert(fused_smem_bytes<4, false>() <= 227 * 1024, "one four-row CTA per SM");
+static_assert(fused_smem_bytes<4, true>() <= 227 * 1024, "one four-row bf16 CTA per SM");
 
 template <int R, bool BF16>
 __device__ __forceinline__ FusedSmem<R, BF16>& fused_smem(unsigned char* raw) {
@@ -171,6 +186,18 @@ __device__ GroupMeta group_meta(const FusedLaunch& p, int g, int c, int (&n)[R],
   return m;
 }
 
+// The order in which a unit's T tiles are streamed (every role walks the
+// same one): position i holds tile (i + T/2) mod T when the unit has at
+// least 2 x kSampleTiles tiles, so the kSampleTiles tiles sampled for the
+// start threshold come from the middle of the unit (not its first tokens,
+// which can score high for every query, nor its most recent ones); shorter
+// units stream in ascending order.
+__device__ __forceinline__ int tile_at(int i, int T) {
+  if (T < 2 * kSampleTiles) return i;
+  const int t = i + (T >> 1);
+  return t < T ? t : t - T;
+}
+
 // relu(s) * 2^-64 for an FP32 dot product s of two 128-element e4m3 rows:
 // s * 2^-64 saturated to [0, 1]. Exact: |s| <= 128 * 448^2 < 2^64, so the
 // clamp at 1 never acts, and s is a multiple of 2^-18, so s * 2^-64 is a
@@ -193,6 +220,150 @@ __device__ __forceinline__ float relu_of(uint32_t s_bits) {
   } else {
     return relu_lo(s_bits);
   }
+}
+
+// ---- one warp's candidate list
+
+// Keep, in place and in order, the entries of key/idx[0, n) for which
+// keep(key, idx) holds; returns how many.
+template <typename Keep>
+__device__ __forceinline__ int warp_compact(uint32_t* key, int32_t* idx, int n, int lane, Keep keep) {
+  int out = 0;
+  for (int j0 = 0; j0 < n; j0 += 32) {
+    const int j = j0 + lane;
+    uint32_t k = 0;
+    int32_t x = 0;
+    bool kp = false;
+    if (j < n) {
+      k = key[j];
+      x = idx[j];
+      kp = keep(k, x);
+    }
+    const uint32_t b = __ballot_sync(0xFFFFFFFFu, kp);
+    __syncwarp();  // every lane has read its entry before any is overwritten (writes go to positions <= j)
+    if (kp) {
+      const int o = out + __popc(b & ((1u << lane) - 1u));
+      key[o] = k;
+      idx[o] = x;
+    }
+    out += __popc(b);
+  }
+  __syncwarp();
+  return out;
+}
+
+// The need-th largest of the values v(j) (j < n, taken where get(j, v)
+// holds) by four 8-bit radix passes over a 256-word histogram: on return
+// `value` is that value and `need` how many of the entries equal to it are
+// among the need largest (>= 1). Requires need <= the number of entries.
+template <typename Get>
+__device__ void warp_radix_select(int n, uint32_t& value, uint32_t& need, uint32_t* hist, int lane, Get get) {
+  uint32_t prefix = 0, mask = 0;
+#pragma unroll 1
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int b = lane; b < 256; b += 32) hist[b] = 0u;
+    __syncwarp();
+    for (int j = lane; j < n; j += 32) {
+      uint32_t v;
+      if (get(j, v) && (v & mask) == prefix) atomicAdd(&hist[(v >> shift) & 255u], 1u);
+    }
+    __syncwarp();
+    uint32_t h[8], tot = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      h[i] = hist[8 * lane + i];
+      tot += h[i];
+    }
+    uint32_t suf = tot;  // inclusive suffix sum over lanes (lane l holds bins 8l .. 8l+7)
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint32_t o = __shfl_down_sync(0xFFFFFFFFu, suf, d);
+      if (lane + d < 32) suf += o;
+    }
+    uint32_t above = suf - tot;
+    int pick = -1;
+    uint32_t pick_above = 0;
+    if (above < need && need <= suf) {
+#pragma unroll
+      for (int i = 7; i >= 0; --i) {
+        if (pick < 0 && above < need && need <= above + h[i]) {
+          pick = 8 * lane + i;
+          pick_above = above;
+        }
+        above += h[i];
+      }
+    }
+    const int src = __ffs(__ballot_sync(0xFFFFFFFFu, pick >= 0)) - 1;
+    pick = __shfl_sync(0xFFFFFFFFu, pick, src);
+    pick_above = __shfl_sync(0xFFFFFFFFu, pick_above, src);
+    prefix |= static_cast<uint32_t>(pick) << shift;
+    mask |= 0xFFu << shift;
+    need -= pick_above;
+    __syncwarp();  // the histogram is read before the next pass clears it
+  }
+  value = prefix;
+}
+
+// Cut one warp's list key/idx[0, n), n > 512, in place to its top 512 by
+// (key desc, index asc). Returns the 512th key: every dropped entry is below
+// it or equal to it with a larger index.
+__device__ __noinline__ uint32_t warp_cut512(uint32_t* key, int32_t* idx, int n, uint32_t* hist, int lane) {
+  uint32_t kv, need = kTopK;
+  warp_radix_select(n, kv, need, hist, lane, [&](int j, uint32_t& v) {
+    v = key[j];
+    return true;
+  });
+  uint32_t eq = 0;
+  for (int j = lane; j < n; j += 32) eq += key[j] == kv ? 1u : 0u;
+  eq = __reduce_add_sync(0xFFFFFFFFu, eq);
+  // among the entries equal to kv, the `need` lowest indices stay
+  uint32_t iv = 0;
+  if (eq > need) {
+    uint32_t need_i = need;
+    warp_radix_select(n, iv, need_i, hist, lane, [&](int j, uint32_t& v) {
+      v = 0x7FFFFFFFu - static_cast<uint32_t>(idx[j]);
+      return key[j] == kv;
+    });
+  }
+  const int kept = warp_compact(key, idx, n, lane, [&](uint32_t k, int32_t x) {
+    return k > kv || (k == kv && 0x7FFFFFFFu - static_cast<uint32_t>(x) >= iv);
+  });
+  (void)kept;  // == 512
+  return kv;
+}
+
+// The row's start threshold after its sample tiles (all 128 threads of the
+// row, named barrier `bar`): the m-th largest of the row's sampled scores,
+// m = kSpecMargin x 512 x sampled / n_unit, as the lowest key of the radix
+// bin that holds it (at least m sampled keys reach it); each warp then keeps
+// only its list's entries at or above it. Returns {threshold (0: none set),
+// this warp's new list size}. `bins` (512 words) is the row's aux array.
+__device__ __forceinline__ uint2 spec_threshold(int* wcnt, SelectScratch& sc, uint32_t* bins, uint32_t* my_key,
+                                             int32_t* my_idx, int wc, int n_unit, int quad, int et, int lane,
+                                             int bar) {
+  __syncwarp();
+  if (lane == 0) wcnt[quad] = wc;
+  named_bar(bar, kEpiRow);
+  int counts[4];
+  int sampled = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    counts[q] = wcnt[q];
+    sampled += counts[q];
+  }
+  uint32_t ts = 0;
+  const long long mm = ((long long)kSpecMargin * kTopK * sampled + n_unit - 1) / n_unit;
+  if (mm >= 1 && mm < sampled) {
+    const int cq = counts[quad];
+    const Threshold th = radix_threshold_fast<kEpiRow>((uint32_t)mm, sc, bins, et, bar, [&](auto fn) {
+      for (int j = lane; j < cq; j += 32) fn(my_key[j]);
+    });
+    ts = th.base + static_cast<uint32_t>(static_cast<uint64_t>(th.prefix) << th.lo);
+    wc = warp_compact(my_key, my_idx, wc, lane, [&](uint32_t k, int32_t) { return k >= ts; });
+    ts = max(ts, 1u);  // (a key of 0 would pass everything anyway)
+  }
+  named_bar(bar, kEpiRow);  // everyone has read the counts; aux is free again
+  return make_uint2(ts, static_cast<uint32_t>(wc));
 }
 
 template <int R>
@@ -218,7 +389,10 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
   constexpr uint32_t kQTileBytes = N * kD * elem_bytes<BF16>();
   constexpr int kEpiWarps = 4 * R;
   constexpr int kTmaWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1;
-  constexpr int kNSf = fused_stages<R, BF16>(), kQB = fused_qbufs<R>();
+  constexpr int kNSf = fused_stages<R, BF16>();
+  constexpr int kEpiBar = 1 + R;  // named barrier of all epilogue threads (rows use 1 .. R)
+  // only the top-k mode can replay a unit (the dense modes set no start threshold)
+  constexpr bool kTopkMode = MODE == kModeTopk;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int units = ((p.rows + R - 1) / R) * p.chunks;
 
@@ -231,10 +405,9 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
       mbar_init(&S.tfull[i], 1);
       mbar_init(&S.tempty[i], kEpiWarps);
     }
-    for (int i = 0; i < kQB; ++i) {
-      mbar_init(&S.qfull[i], 1);
-      mbar_init(&S.qempty[i], 1);
-    }
+    mbar_init(&S.qfull, 1);
+    mbar_init(&S.qempty, 1);
+    mbar_init(&S.verdict, 1);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -248,8 +421,9 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
   if constexpr (MODE == kModeTopk) pdl_trigger();  // the merge may be scheduled now; it waits for this grid to finish
 
   // Every role walks the same units (u = blockIdx.x, + gridDim.x, ...) and
-  // derives the same tile counts, so the barrier phases below (counted over
-  // all tiles and all units of this CTA) stay in step.
+  // passes (a unit is streamed again when the epilogue's verdict says so)
+  // and derives the same tile counts, so the barrier phases below (counted
+  // over all tiles, passes and units of this CTA) stay in step.
   if (warp == kTmaWarp) {
     // ---------------- TMA producer: the unit's query tile, then its key
     // blocks through the ring; the block ids come straight from the table
@@ -257,7 +431,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
       prefetch_tmap(&kmap);
       prefetch_tmap(&qmap);
       const uint64_t keep = l2_policy_evict_last();  // q and K are re-read by other CTAs
-      uint32_t it = 0, qn = 0;
+      uint32_t it = 0, qn = 0, vn = 0;
       bool run = true;
       for (int u = blockIdx.x; u < units && run; u += gridDim.x) {
         int n[R];
@@ -265,26 +439,33 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
         const int ntiles = m.blk1 - m.blk0;
         if (ntiles == 0) continue;
         const int32_t* bt = p.block_table + (long long)m.batch * p.bt_stride + m.blk0;
-        const int qb = qn % kQB;
-        run = mbar_wait(&S.qempty[qb], ((qn / kQB) & 1u) ^ 1u);
+        run = mbar_wait(&S.qempty, (qn & 1u) ^ 1u);
         if (!run) break;
-        mbar_arrive_expect_tx(&S.qfull[qb], kQTileBytes);
+        mbar_arrive_expect_tx(&S.qfull, kQTileBytes);
 #pragma unroll
         for (int h = 0; h < kRegions; ++h)  // region h: dims [64h, 64h + 64) of a bf16 row
-          tma_load_2d(S.q[qb] + h * N * kSwB, &qmap, h * (kSwB / elem_bytes<BF16>()), m.row0 * kH, &S.qfull[qb],
-                      keep);
+          tma_load_2d(S.q + h * N * kSwB, &qmap, h * (kSwB / elem_bytes<BF16>()), m.row0 * kH, &S.qfull, keep);
         ++qn;
-        int page_next = __ldg(bt);
-        for (int i = 0; i < ntiles && run; ++i) {
-          int page = page_next;
-          if (i + 1 < ntiles) page_next = __ldg(bt + i + 1);
-          if (page < 0 || page >= p.num_blocks) page = 0;  // the epilogue masks this block
+        bool again = true;
+        while (again && run) {
+          int page_next = __ldg(bt + tile_at(0, ntiles));
+          for (int i = 0; i < ntiles && run; ++i) {
+            int page = page_next;
+            if (i + 1 < ntiles) page_next = __ldg(bt + tile_at(i + 1, ntiles));
+            if (page < 0 || page >= p.num_blocks) page = 0;  // the epilogue masks this block
 #pragma unroll
-          for (int h = 0; h < kRegions; ++h, ++it) {  // region h: dims [64h, 64h + 64) of a bf16 key
-            const int s = it % kNSf;
-            if (!(run = mbar_wait(&S.empty[s], ((it / kNSf) & 1u) ^ 1u))) break;
-            mbar_arrive_expect_tx(&S.full[s], kSlotBytes);
-            tma_load_2d(S.kst[s], &kmap, h * (kSwB / elem_bytes<BF16>()), page * kBlk, &S.full[s], keep);
+            for (int h = 0; h < kRegions; ++h, ++it) {  // region h: dims [64h, 64h + 64) of a bf16 key
+              const int s = it % kNSf;
+              if (!(run = mbar_wait(&S.empty[s], ((it / kNSf) & 1u) ^ 1u))) break;
+              mbar_arrive_expect_tx(&S.full[s], kSlotBytes);
+              tma_load_2d(S.kst[s], &kmap, h * (kSwB / elem_bytes<BF16>()), page * kBlk, &S.full[s], keep);
+            }
+          }
+          again = false;
+          if (kTopkMode && run) {  // the epilogue's verdict on this pass
+            if (!(run = mbar_wait(&S.verdict, vn & 1u))) break;
+            ++vn;
+            again = *reinterpret_cast<volatile int*>(&S.replay) != 0;
           }
         }
       }
@@ -293,44 +474,52 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer
     if (lane == 0) {
-      uint32_t it = 0, rs = 0, qn = 0;  // tiles (accumulator buffers) and ring slots consumed
+      uint32_t it = 0, rs = 0, qn = 0, vn = 0;  // tiles (accumulator buffers), ring slots, query tiles, verdicts
       bool run = true;
       for (int u = blockIdx.x; u < units && run; u += gridDim.x) {
         int n[R];
         const GroupMeta m = group_meta<R>(p, u / p.chunks, u % p.chunks, n, false);
         const int ntiles = m.blk1 - m.blk0;
         if (ntiles == 0) continue;
-        const int qb = qn % kQB;
-        if (!(run = mbar_wait(&S.qfull[qb], (qn / kQB) & 1u))) break;
+        if (!(run = mbar_wait(&S.qfull, qn & 1u))) break;
         ++qn;
-        const uint64_t bdesc = umma_desc_sw128_kmajor(smem_u32(S.q[qb]));
-        for (int i = 0; i < ntiles && run; ++i, ++it) {
-          const int buf = it & 1;
-          if (!(run = mbar_wait(&S.tempty[buf], ((it >> 1) & 1u) ^ 1u))) break;
-          // each instruction takes 32 bytes of K (32 FP8 or 16 bf16 dims):
-          // four per region (ring slot); the descriptor start field counts 16 B
+        const uint64_t bdesc = umma_desc_sw128_kmajor(smem_u32(S.q));
+        bool again = true;
+        while (again && run) {
+          for (int i = 0; i < ntiles && run; ++i, ++it) {
+            const int buf = it & 1;
+            if (!(run = mbar_wait(&S.tempty[buf], ((it >> 1) & 1u) ^ 1u))) break;
+            // each instruction takes 32 bytes of K (32 FP8 or 16 bf16 dims):
+            // four per region (ring slot); the descriptor start field counts 16 B
 #pragma unroll
-          for (int h = 0; h < kRegions; ++h, ++rs) {
-            const int s = rs % kNSf;
-            if (!(run = mbar_wait(&S.full[s], (rs / kNSf) & 1u))) break;
-            tc_fence_after();
-            const uint64_t adesc = umma_desc_sw128_kmajor(smem_u32(S.kst[s]));
+            for (int h = 0; h < kRegions; ++h, ++rs) {
+              const int s = rs % kNSf;
+              if (!(run = mbar_wait(&S.full[s], (rs / kNSf) & 1u))) break;
+              tc_fence_after();
+              const uint64_t adesc = umma_desc_sw128_kmajor(smem_u32(S.kst[s]));
 #pragma unroll
-            for (int k = 0; k < kSwB / 32; ++k) {
-              const uint64_t ad = adesc + (uint64_t)(2 * k);
-              const uint64_t bd = bdesc + (uint64_t)(h * N * kSwB / 16 + 2 * k);
-              const uint32_t acc = (h > 0 || k > 0) ? 1u : 0u;
-              if constexpr (BF16)
-                umma_bf16(tmem + buf * N, ad, bd, kIdesc, acc);
-              else
-                umma_f8(tmem + buf * N, ad, bd, kIdesc, acc);
+              for (int k = 0; k < kSwB / 32; ++k) {
+                const uint64_t ad = adesc + (uint64_t)(2 * k);
+                const uint64_t bd = bdesc + (uint64_t)(h * N * kSwB / 16 + 2 * k);
+                const uint32_t acc = (h > 0 || k > 0) ? 1u : 0u;
+                if constexpr (BF16)
+                  umma_bf16(tmem + buf * N, ad, bd, kIdesc, acc);
+                else
+                  umma_f8(tmem + buf * N, ad, bd, kIdesc, acc);
+              }
+              umma_commit(&S.empty[s]);
             }
-            umma_commit(&S.empty[s]);
+            if (!run) break;
+            umma_commit(&S.tfull[buf]);
           }
-          if (!run) break;
-          umma_commit(&S.tfull[buf]);
+          again = false;
+          if (kTopkMode && run) {
+            if (!(run = mbar_wait(&S.verdict, vn & 1u))) break;
+            ++vn;
+            again = *reinterpret_cast<volatile int*>(&S.replay) != 0;
+          }
         }
-        umma_commit(&S.qempty[qb]);  // the query tile is free once this unit's MMAs are done
+        umma_commit(&S.qempty);  // the query tile is free once this unit's MMAs are done
       }
       if (!run) atomicOr(p.status, kDevWaitTimeout);
     }
@@ -343,6 +532,8 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
     int32_t* const cidx = S.cidx[r];
     uint32_t* const my_key = ckey + quad * kSub;
     int32_t* const my_idx = cidx + quad * kSub;
+    // this warp's histogram for cutting its own list: its quarter of aux
+    uint32_t* const whist = quad < 2 ? S.aux_key[r] + 256 * quad : reinterpret_cast<uint32_t*>(S.aux_idx[r]) + 256 * (quad - 2);
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     // TMEM is read in the 16x256b shape: a warp loads its 32 keys as two
     // 16-lane halves, and lane l gets keys l/4 and l/4 + 8 of each half at
@@ -353,63 +544,23 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
     const int kl = quad * 32 + (lane >> 2) + 8 * ((lane >> 1) & 1) + 16 * (lane & 1);
     constexpr float kWScale = BF16 ? 0.5f : 0x1p64f;  // undoes relu_of's scaling
     bool ok = true;     // false after a pipeline wait gave up (then nothing more is waited for)
-    int sync_no = 0;    // exchanges so far (the size slots alternate)
     uint32_t tt = 0;    // tiles so far (accumulator buffer and phase)
+    uint32_t vn = 0;    // verdicts so far (passes over units)
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const int g = u / p.chunks, c = u - g * p.chunks;
       int n[R];
       const GroupMeta m = group_meta<R>(p, g, c, n, et == 0 && r == 0 && c == 0);
       const int ntiles = m.blk1 - m.blk0;
+      if (ntiles == 0) {
+        // nothing streamed: an empty partial list per row
+        if (kTopkMode && r < m.nrows && et == 0) p.part_cnt[(long long)(m.row0 + r) * p.chunks + c] = 0;
+        continue;
+      }
       const bool row_live = r < m.nrows;
       const int nr = n[r];
       const int32_t* bt = p.block_table + (long long)m.batch * p.bt_stride + m.blk0;
-      int wc = 0;         // entries in this warp's sub-list
-      uint32_t tau = 0;   // keep keys whose order key >= tau (same in the row's 4 warps)
-      float tf = tau_float(0);
-      // Exchange the four sub-list sizes; when one is nearly full (or at
-      // the unit end) cut the row's candidates to the top 512 and rebalance
-      // them (128 per sub-list), or gather them for the partial output.
-      auto exchange = [&](bool final_cut) -> int {
-        if (lane == 0) S.wcnt[r][sync_no & 1][quad] = wc;
-        const bool all_ok = named_bar_and(bar, kEpiRow, ok);
-        int counts[4];
-        int total = 0, maxc = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          counts[q] = S.wcnt[r][sync_no & 1][q];
-          total += counts[q];
-          maxc = max(maxc, counts[q]);
-        }
-        ++sync_no;
-        if (!all_ok) return -1;
-        if (!final_cut && maxc <= kSubPruneAt) return total;
-        int kept = total;
-        if (total > kTopK) {
-          tau = max(tau, select512_sub_to_aux<kEpiRow, 4, kSub>(ckey, cidx, counts, S.aux_key[r], S.aux_idx[r],
-                                                                S.sc[r], et, bar));
-          tf = tau_float(tau);
-          kept = kTopK;
-        } else {
-          int before = 0;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) before += q < quad ? counts[q] : 0;
-          for (int j = lane; j < wc; j += 32) {
-            S.aux_key[r][before + j] = my_key[j];
-            S.aux_idx[r][before + j] = my_idx[j];
-          }
-          named_bar(bar, kEpiRow);
-        }
-        if (!final_cut) {  // rebalance: sub-list q takes aux[q*128 ...]
-          const int lo = min(kept, quad * (kTopK / 4)), hi = min(kept, (quad + 1) * (kTopK / 4));
-          for (int j = lo + lane; j < hi; j += 32) {
-            my_key[j - lo] = S.aux_key[r][j];
-            my_idx[j - lo] = S.aux_idx[r][j];
-          }
-          wc = hi - lo;
-          named_bar(bar, kEpiRow);
-        }
-        return kept;
-      };
+      // keys of this row in this unit
+      const int n_unit = row_live ? max(0, min(nr - m.blk0 * kBlk, ntiles * kBlk)) : 0;
       float2 w2[8];
       const float* wr = p.w + (long long)(row_live ? m.row0 + r : 0) * kH + 2 * (lane & 3);
 #pragma unroll
@@ -426,128 +577,203 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
       auto key_scale = [&](int page) -> float {
         return p.kscale ? __ldg(p.kscale + (long long)page * kBlk + kl) : 1.f;
       };
-      int page_next = ntiles > 0 ? __ldg(bt) : -1;
-      bool ok_next = page_next >= 0 && page_next < p.num_blocks;
-      float ks_next = ok_next ? key_scale(page_next) : 0.f;
-      for (int i = 0; i < ntiles; ++i, ++tt) {
-        const int blk = m.blk0 + i, buf = tt & 1;
-        const int t = blk * kBlk + kl;
-        const bool page_ok = ok_next;
-        const float ks = ks_next;
-        const int page = page_next;
-        if (i + 1 < ntiles) {
-          page_next = __ldg(bt + i + 1);
-          ok_next = page_next >= 0 && page_next < p.num_blocks;
-          ks_next = ok_next ? key_scale(page_next) : 0.f;
-        }
-        if (!page_ok && et == 0 && r == 0) atomicOr(p.status, kDevBadPage);
-        ok = ok && __all_sync(0xFFFFFFFFu, mbar_wait(&S.tfull[buf], (tt >> 1) & 1u));
-        float score = 0.f;
-        if (ok) {
-          tc_fence_after();
-          const uint32_t col = tmem + lane_base + static_cast<uint32_t>(buf * N + r * kH);
-          // sum_h w_h relu(s_h) = sum_h (w_h 2^64) relu_lo(s_h): the relu
-          // is one saturating multiply on the FMA pipe (the ALU pipe, where
-          // a max would go, is the busier one), then packed f32x2 FMAs; the
-          // power-of-two scalings are exact, so every product is w_h relu(s_h).
-          // acc[k] = this lane's partial for keys l/4, l/4+8, 16+l/4, 24+l/4
-          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-          // per-head mode: the scales of this lane's 4 keys, and its row's
-          // [64, dense_stride] block of the output
-          float ksq[4] = {0.f, 0.f, 0.f, 0.f};
-          float* const ph_out = p.dense + (long long)(m.row0 + (row_live ? r : 0)) * kH * p.dense_stride;
-          if constexpr (MODE == kModePerHead) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int key = quad * 32 + (lane >> 2) + 8 * (e & 1) + 16 * (e >> 1);
-              ksq[e] = page_ok ? (p.kscale ? __ldg(p.kscale + (long long)page * kBlk + key) : 1.f)
-                               : __int_as_float(0xFF800000);  // a key on a bad block scores -inf
-            }
+      bool row_done = !row_live || !kTopkMode;  // this row's partial list is written
+      for (int pass = 0;; ++pass) {
+        // a row streams its keys on the first pass, and again on a replay
+        // if its start threshold failed; a done row only drains the tiles
+        const bool active = !row_done || !kTopkMode;
+        // the start threshold is sampled on the first pass only
+        const bool spec = kTopkMode && active && pass == 0 && ntiles >= 2 * kSampleTiles && n_unit >= kSpecMinKeys;
+        int wc = 0;         // entries in this warp's list
+        uint32_t tau = 0;   // keep keys whose order key >= tau
+        float tf = tau_float(0);
+        bool spec_used = false;
+        int page_next = __ldg(bt + tile_at(0, ntiles));
+        bool ok_next = page_next >= 0 && page_next < p.num_blocks;
+        float ks_next = (ok_next && active) ? key_scale(page_next) : 0.f;
+        for (int i = 0; i < ntiles; ++i, ++tt) {
+          const int blk = m.blk0 + tile_at(i, ntiles), buf = tt & 1;
+          const int t = blk * kBlk + kl;
+          const bool page_ok = ok_next;
+          const float ks = ks_next;
+          const int page = page_next;
+          if (i + 1 < ntiles) {
+            page_next = __ldg(bt + tile_at(i + 1, ntiles));
+            ok_next = page_next >= 0 && page_next < p.num_blocks;
+            ks_next = (ok_next && active) ? key_scale(page_next) : 0.f;
           }
+          if (!page_ok && et == 0 && r == 0 && pass == 0) atomicOr(p.status, kDevBadPage);
+          ok = ok && __all_sync(0xFFFFFFFFu, mbar_wait(&S.tfull[buf], (tt >> 1) & 1u));
+          if (!active) {  // drain: free the accumulator buffer
+            if (ok) tc_fence_after();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0 && ok) mbar_arrive(&S.tempty[buf]);
+            continue;
+          }
+          float score = 0.f;
+          if (ok) {
+            tc_fence_after();
+            const uint32_t col = tmem + lane_base + static_cast<uint32_t>(buf * N + r * kH);
+            // sum_h w_h relu(s_h) = sum_h (w_h 2^64) relu_lo(s_h): the relu
+            // is one saturating multiply on the FMA pipe (the ALU pipe, where
+            // a max would go, is the busier one), then packed f32x2 FMAs; the
+            // power-of-two scalings are exact, so every product is w_h relu(s_h).
+            // acc[k] = this lane's partial for keys l/4, l/4+8, 16+l/4, 24+l/4
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            // per-head mode: the scales of this lane's 4 keys, and its row's
+            // [64, dense_stride] block of the output
+            float ksq[4] = {0.f, 0.f, 0.f, 0.f};
+            float* const ph_out = p.dense + (long long)(m.row0 + (row_live ? r : 0)) * kH * p.dense_stride;
+            if constexpr (MODE == kModePerHead) {
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t a[32];
-            tmem_ld16x256_x8(col + (static_cast<uint32_t>(16 * half) << 16), a);
-            tmem_ld_wait();
-            if (half == 1) {  // the accumulator buffer is free once both halves are in registers
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&S.tempty[buf]);
+              for (int e = 0; e < 4; ++e) {
+                const int key = quad * 32 + (lane >> 2) + 8 * (e & 1) + 16 * (e >> 1);
+                ksq[e] = page_ok ? (p.kscale ? __ldg(p.kscale + (long long)page * kBlk + key) : 1.f)
+                                 : __int_as_float(0xFF800000);  // a key on a bad block scores -inf
+              }
             }
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float2 x0 = make_float2(relu_of<BF16>(a[4 * j]), relu_of<BF16>(a[4 * j + 1]));
-              const float2 x1 = make_float2(relu_of<BF16>(a[4 * j + 2]), relu_of<BF16>(a[4 * j + 3]));
-              if constexpr (MODE == kModePerHead) {
-                // heads h0, h0 + 1 of keys key0 and key0 + 8: w_h relu(s_h) x scale
-                const int h0 = 8 * j + 2 * (lane & 3);
-                const int key0 = quad * 32 + 16 * half + (lane >> 2);
-                const int t0 = blk * kBlk + key0, t1 = t0 + 8;
-                float* const o0 = ph_out + (long long)h0 * p.dense_stride;
-                float* const o1 = o0 + p.dense_stride;
-                if (row_live && t0 < nr) {
-                  const float sc = ksq[2 * half];
-                  o0[t0] = page_ok ? x0.x * w2[j].x * sc : sc;
-                  o1[t0] = page_ok ? x0.y * w2[j].y * sc : sc;
+            for (int half = 0; half < 2; ++half) {
+              uint32_t a[32];
+              tmem_ld16x256_x8(col + (static_cast<uint32_t>(16 * half) << 16), a);
+              tmem_ld_wait();
+              if (half == 1) {  // the accumulator buffer is free once both halves are in registers
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.tempty[buf]);
+              }
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float2 x0 = make_float2(relu_of<BF16>(a[4 * j]), relu_of<BF16>(a[4 * j + 1]));
+                const float2 x1 = make_float2(relu_of<BF16>(a[4 * j + 2]), relu_of<BF16>(a[4 * j + 3]));
+                if constexpr (MODE == kModePerHead) {
+                  // heads h0, h0 + 1 of keys key0 and key0 + 8: w_h relu(s_h) x scale
+                  const int h0 = 8 * j + 2 * (lane & 3);
+                  const int key0 = quad * 32 + 16 * half + (lane >> 2);
+                  const int t0 = blk * kBlk + key0, t1 = t0 + 8;
+                  float* const o0 = ph_out + (long long)h0 * p.dense_stride;
+                  float* const o1 = o0 + p.dense_stride;
+                  if (row_live && t0 < nr) {
+                    const float sc = ksq[2 * half];
+                    o0[t0] = page_ok ? x0.x * w2[j].x * sc : sc;
+                    o1[t0] = page_ok ? x0.y * w2[j].y * sc : sc;
+                  }
+                  if (row_live && t1 < nr) {
+                    const float sc = ksq[2 * half + 1];
+                    o0[t1] = page_ok ? x1.x * w2[j].x * sc : sc;
+                    o1[t1] = page_ok ? x1.y * w2[j].y * sc : sc;
+                  }
+                } else {
+                  acc[2 * half] = __ffma2_rn(x0, w2[j], acc[2 * half]);
+                  acc[2 * half + 1] = __ffma2_rn(x1, w2[j], acc[2 * half + 1]);
                 }
-                if (row_live && t1 < nr) {
-                  const float sc = ksq[2 * half + 1];
-                  o0[t1] = page_ok ? x1.x * w2[j].x * sc : sc;
-                  o1[t1] = page_ok ? x1.y * w2[j].y * sc : sc;
-                }
-              } else {
-                acc[2 * half] = __ffma2_rn(x0, w2[j], acc[2 * half]);
-                acc[2 * half + 1] = __ffma2_rn(x1, w2[j], acc[2 * half + 1]);
+              }
+            }
+            const float p0 = acc[0].x + acc[0].y, p1 = acc[1].x + acc[1].y;
+            const float p2 = acc[2].x + acc[2].y, p3 = acc[3].x + acc[3].y;
+            // reduce-scatter over lanes 4g..4g+3: after the xor-1 step a lane
+            // holds two keys (l/4 and l/4 + 8 if l is even, else 16 + l/4 and
+            // 24 + l/4), after the xor-2 step one (the second of them if l & 2)
+            const bool odd = lane & 1, hi = lane & 2;
+            float k0 = odd ? p2 : p0, k1 = odd ? p3 : p1;
+            k0 += __shfl_xor_sync(0xFFFFFFFFu, odd ? p0 : p2, 1);
+            k1 += __shfl_xor_sync(0xFFFFFFFFu, odd ? p1 : p3, 1);
+            const float keep = hi ? k1 : k0;
+            score = (keep + __shfl_xor_sync(0xFFFFFFFFu, hi ? k0 : k1, 2)) * ks;
+          }
+          const bool live = ok && row_live && page_ok && t < nr;
+          if constexpr (MODE == kModeDense) {
+            if (live) p.dense[(long long)(m.row0 + r) * p.dense_stride + t] = score;
+          } else if constexpr (MODE == kModeTopk) {
+            // running top-k filter: cut this warp's list if the tile's
+            // survivors might not fit, then append them
+            if (wc > kSub - 32) {
+              tau = max(tau, warp_cut512(my_key, my_idx, wc, whist, lane));
+              tf = tau_float(tau);
+              wc = kTopK;
+            }
+            const bool pass_ = live && score >= tf;
+            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass_);
+            if (pass_) {
+              const int pos = wc + __popc(bal & ((1u << lane) - 1u));
+              my_key[pos] = order_key(score);
+              my_idx[pos] = t;
+            }
+            wc += __popc(bal);
+            if (spec && i == kSampleTiles - 1) {
+              // the sample tiles are in: the row's start threshold
+              const uint2 sw = spec_threshold(S.wcnt[r], S.sc[r], S.aux_key[r], my_key, my_idx, wc, n_unit, quad, et,
+                                              lane, bar);
+              wc = static_cast<int>(sw.y);
+              if (sw.x != 0u) {
+                tau = max(tau, sw.x);
+                tf = tau_float(tau);
+                spec_used = true;
               }
             }
           }
-          const float p0 = acc[0].x + acc[0].y, p1 = acc[1].x + acc[1].y;
-          const float p2 = acc[2].x + acc[2].y, p3 = acc[3].x + acc[3].y;
-          // reduce-scatter over lanes 4g..4g+3: after the xor-1 step a lane
-          // holds two keys (l/4 and l/4 + 8 if l is even, else 16 + l/4 and
-          // 24 + l/4), after the xor-2 step one (the second of them if l & 2)
-          const bool odd = lane & 1, hi = lane & 2;
-          float k0 = odd ? p2 : p0, k1 = odd ? p3 : p1;
-          k0 += __shfl_xor_sync(0xFFFFFFFFu, odd ? p0 : p2, 1);
-          k1 += __shfl_xor_sync(0xFFFFFFFFu, odd ? p1 : p3, 1);
-          const float keep = hi ? k1 : k0;
-          score = (keep + __shfl_xor_sync(0xFFFFFFFFu, hi ? k0 : k1, 2)) * ks;
         }
-        const bool live = ok && row_live && page_ok && t < nr;
-        if constexpr (MODE == kModeDense) {
-          if (live) p.dense[(long long)(m.row0 + r) * p.dense_stride + t] = score;
-        } else if constexpr (MODE == kModeTopk) {
-          // running top-k filter: append survivors to this warp's sub-list
-          const bool pass = live && score >= tf;
-          const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass);
-          if (pass) {
-            const int pos = wc + __popc(bal & ((1u << lane) - 1u));
-            my_key[pos] = order_key(score);
-            my_idx[pos] = t;
+        bool row_failed = false;
+        if constexpr (MODE == kModeTopk) {
+          if (active) {
+            // unit end: cut the row's candidates to 512
+            __syncwarp();
+            if (lane == 0) S.wcnt[r][quad] = wc;
+            const bool all_ok = named_bar_and(bar, kEpiRow, ok);
+            int counts[4];
+            int total = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              counts[q] = S.wcnt[r][q];
+              total += counts[q];
+            }
+            int kept = 0;  // after a timeout the lists are not trusted: an empty list
+            if (all_ok && total > kTopK) {
+              select512_sub_to_aux<kEpiRow, 4, kSub>(ckey, cidx, counts, S.aux_key[r], S.aux_idx[r], S.sc[r], et,
+                                                     bar);
+              kept = kTopK;
+            } else if (all_ok) {
+              kept = total;
+              int before = 0;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) before += q < quad ? counts[q] : 0;
+              for (int j = lane; j < wc; j += 32) {
+                S.aux_key[r][before + j] = my_key[j];
+                S.aux_idx[r][before + j] = my_idx[j];
+              }
+              named_bar(bar, kEpiRow);
+            }
+            // too high a start threshold: fewer than 512 keys reached it
+            row_failed = all_ok && spec_used && total < kTopK;
+            if (!row_failed && row_live) {
+              const long long pu = (long long)(m.row0 + r) * p.chunks + c;
+              const int cr = kept;
+              for (int j = et; j < cr; j += kEpiRow) {
+                p.part_key[pu * kTopK + j] = S.aux_key[r][j];
+                p.part_idx[pu * kTopK + j] = S.aux_idx[r][j];
+              }
+              if (et == 0) p.part_cnt[pu] = cr;
+            }
           }
-          wc += __popc(bal);
-          // every warp of the row takes part in every exchange, even after a
-          // timeout (it then stops waiting and contributes nothing)
-          if ((i % kSyncEvery) == kSyncEvery - 1 && i != ntiles - 1) {
-            if (exchange(false) < 0) ok = false;
+          // the verdict of this pass: stream the unit again if a row failed
+          if (et == 0) S.row_fail[vn & 1][r] = row_failed ? 1 : 0;
+          named_bar(kEpiBar, R * kEpiRow);
+          bool any = false;
+#pragma unroll
+          for (int q = 0; q < R; ++q) any = any || S.row_fail[vn & 1][q] != 0;
+          if (tid == 0) {
+            S.replay = any ? 1 : 0;
+            mbar_arrive(&S.verdict);  // releases the replay flag to the TMA and MMA threads
           }
+          ++vn;
+          if (active && !row_failed) row_done = true;
+          if (!any) break;
+          // (aux and the lists are rewritten only after the row's next
+          // barrier, which every thread of the row reaches after reading them)
+        } else {
+          break;
         }
-      }
-      if constexpr (MODE == kModeTopk) {
-        // unit end: cut the row's list to 512 and write it as a partial list
-        __syncwarp();
-        const int kept = exchange(true);
-        if (row_live) {
-          const long long pu = (long long)(m.row0 + r) * p.chunks + c;
-          const int cr = kept < 0 ? 0 : kept;
-          for (int j = et; j < cr; j += kEpiRow) {
-            p.part_key[pu * kTopK + j] = S.aux_key[r][j];
-            p.part_idx[pu * kTopK + j] = S.aux_idx[r][j];
-          }
-          if (et == 0) p.part_cnt[pu] = cr;
-        }
-        // (the next unit's first exchange starts with a barrier of the row,
-        // so aux is read out before anyone writes it again)
       }
     }
     if (!ok && et == 0) atomicOr(p.status, kDevWaitTimeout);
@@ -624,9 +850,10 @@ cudaError_t launch_fused_t(const FusedLaunch& p, const void* kcache, cudaStream_
 FusedPlan fused_plan(long long rows, int max_seq_len, int group_rows, int num_sms) {
   FusedPlan pl{1, 1, 1, 0};
   // Packed prefill rows come in groups of 4 sharing a request; the kernel
-  // takes them in pairs (MMA N = 128, two CTAs per SM: measured faster than
-  // groups of 4 with N = 256 and one CTA per SM).
-  pl.group = (group_rows == 4 && rows >= 2) ? 2 : 1;
+  // takes each group in one CTA (MMA N = 256, one CTA per SM: each key tile
+  // is staged once for four rows; measured faster than pairs of rows with
+  // N = 128 and two CTAs per SM).
+  pl.group = group_rows == 4 ? 4 : 1;
   const long long max_blocks = std::max<long long>(1, ((long long)max_seq_len + kBlk - 1) / kBlk);
   const long long groups = (rows + pl.group - 1) / pl.group;
   // about four units per SM (a little over one wave of three resident
@@ -645,8 +872,8 @@ FusedPlan fused_plan(long long rows, int max_seq_len, int group_rows, int num_sm
 template <int MODE>
 cudaError_t launch_fused_m(const FusedLaunch& p, int group, bool bf16, const void* kcache, cudaStream_t stream) {
   if (bf16)
-    return group == 2 ? launch_fused_t<2, MODE, true>(p, kcache, stream) : launch_fused_t<1, MODE, true>(p, kcache, stream);
-  return group == 2 ? launch_fused_t<2, MODE, false>(p, kcache, stream) : launch_fused_t<1, MODE, false>(p, kcache, stream);
+    return group == 4 ? launch_fused_t<4, MODE, true>(p, kcache, stream) : launch_fused_t<1, MODE, true>(p, kcache, stream);
+  return group == 4 ? launch_fused_t<4, MODE, false>(p, kcache, stream) : launch_fused_t<1, MODE, false>(p, kcache, stream);
 }
 
 cudaError_t launch_fused(const FusedLaunch& p, int group, FusedOut out, bool bf16, const void* kcache,

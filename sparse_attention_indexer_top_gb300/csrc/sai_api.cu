@@ -97,22 +97,26 @@ size_t sai_topk_transform_workspace(int64_t rows, int64_t score_stride, int32_t 
 int sai_topk_transform(const float* scores, int64_t rows, int64_t score_stride, const int32_t* row_starts,
                        const int32_t* seq_lens, const int32_t* page_tables, int64_t pt_rows, int64_t pt_stride,
                        const int32_t* row_to_batch, int32_t page_size, int32_t k, int32_t* out_slots,
-                       int32_t* out_indices, void* workspace, size_t workspace_bytes, sai_stream_t stream) {
+                       int32_t* out_indices, int32_t block_size, int32_t* out_blocks, int32_t* out_counts,
+                       void* workspace, size_t workspace_bytes, sai_stream_t stream) {
   if (k <= 0 || rows < 0) return SAI_ERR_SHAPE;
   if (k != SAI_TOPK) return SAI_ERR_UNSUPPORTED;
   if (rows > INT_MAX / 16) return SAI_ERR_SHAPE;
-  if (!out_slots && !out_indices) return SAI_ERR_NULL;
+  if (!out_slots && !out_indices && !out_blocks) return SAI_ERR_NULL;
+  if (out_counts && !out_blocks) return SAI_ERR_NULL;
+  if (out_blocks && block_size < 1) return SAI_ERR_SHAPE;
   if (rows == 0) return SAI_OK;
   if (!scores || !seq_lens) return SAI_ERR_NULL;
   if (score_stride < 1) return SAI_ERR_SHAPE;
-  if (out_slots && !page_tables) return SAI_ERR_NULL;
+  if ((out_slots || out_blocks) && !page_tables) return SAI_ERR_NULL;
   if (page_tables) {
     if (page_size < 1 || pt_rows < 1 || pt_stride < 1) return SAI_ERR_SHAPE;
     if (!row_to_batch && pt_rows < rows) return SAI_ERR_SHAPE;
   }
   if (!aligned(scores, 4) || !aligned(seq_lens, 4) || (row_starts && !aligned(row_starts, 4)) ||
       (page_tables && !aligned(page_tables, 4)) || (row_to_batch && !aligned(row_to_batch, 4)) ||
-      (out_slots && !aligned(out_slots, 4)) || (out_indices && !aligned(out_indices, 4)))
+      (out_slots && !aligned(out_slots, 4)) || (out_indices && !aligned(out_indices, 4)) ||
+      (out_blocks && !aligned(out_blocks, 4)) || (out_counts && !aligned(out_counts, 4)))
     return SAI_ERR_ALIGN;
   int dev, sms;
   int* st;
@@ -135,6 +139,9 @@ int sai_topk_transform(const float* scores, int64_t rows, int64_t score_stride, 
   p.page_size = page_tables ? page_size : 1;
   p.out_slots = out_slots;
   p.out_idx = out_indices;
+  p.block_size = out_blocks ? block_size : 1;
+  p.out_blocks = out_blocks;
+  p.out_counts = out_counts;
   p.chunks = plan.chunks;
   p.chunk_len = plan.chunk_len;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
@@ -204,15 +211,19 @@ int fused_topk(const void* q, const float* w, const void* kcache, const float* k
                const int32_t* block_table, int64_t bt_rows, int64_t bt_stride, const int32_t* row_to_batch,
                const int32_t* seq_lens, int64_t rows, int32_t heads, int32_t dim, int32_t block_size,
                int32_t max_seq_len, int32_t group_rows, int32_t k, int32_t* out_slots, int32_t* out_indices,
-               float* out_scores, void* workspace, size_t workspace_bytes, sai_stream_t stream) {
+               float* out_scores, int32_t list_block_size, int32_t* out_blocks, int32_t* out_counts,
+               void* workspace, size_t workspace_bytes, sai_stream_t stream) {
   if (k <= 0) return SAI_ERR_SHAPE;
   if (k != SAI_TOPK) return SAI_ERR_UNSUPPORTED;
-  if (!out_slots && !out_indices && !out_scores) return SAI_ERR_NULL;
+  if (!out_slots && !out_indices && !out_scores && !out_blocks) return SAI_ERR_NULL;
+  if (out_counts && !out_blocks) return SAI_ERR_NULL;
+  if (out_blocks && list_block_size < 1) return SAI_ERR_SHAPE;
   int st_arg = check_fused_args(q, w, kcache, kscale, bf16, num_blocks, block_table, bt_rows, bt_stride,
                                 row_to_batch, seq_lens, rows, heads, dim, block_size, max_seq_len, group_rows);
   if (st_arg != SAI_OK || rows == 0) return st_arg;
   if ((out_slots && !aligned(out_slots, 4)) || (out_indices && !aligned(out_indices, 4)) ||
-      (out_scores && !aligned(out_scores, 4)))
+      (out_scores && !aligned(out_scores, 4)) || (out_blocks && !aligned(out_blocks, 4)) ||
+      (out_counts && !aligned(out_counts, 4)))
     return SAI_ERR_ALIGN;
   int dev, sms;
   int* st;
@@ -245,6 +256,9 @@ int fused_topk(const void* q, const float* w, const void* kcache, const float* k
   m.out_idx = out_indices;
   m.out_scores = out_scores;
   m.status = st;
+  m.block_size = out_blocks ? list_block_size : 1;
+  m.out_blocks = out_blocks;
+  m.out_counts = out_counts;
   return cuda_status(sai::launch_merge(m, s));
 }
 
@@ -352,7 +366,8 @@ int fused_per_head_topk(const void* q, const float* w, const void* kcache, const
   e = sai::launch_fused(p, plan.group, sai::FusedOut::kPerHead, bf16, kcache, s);
   if (e != cudaSuccess) return cuda_status(e);
   return sai_topk_transform(dense, rows * 64, L.stride, nullptr, lens, block_table, bt_rows, bt_stride, batch, 128,
-                            SAI_TOPK, out_slots, out_indices, ws + L.topk_off, L.topk_bytes, stream);
+                            SAI_TOPK, out_slots, out_indices, 0, nullptr, nullptr, ws + L.topk_off, L.topk_bytes,
+                            stream);
 }
 
 }  // namespace
@@ -371,11 +386,12 @@ int sai_index_score_topk(const uint8_t* q_fp8, const float* w, const uint8_t* kc
                          int64_t num_blocks, const int32_t* block_table, int64_t bt_rows, int64_t bt_stride,
                          const int32_t* row_to_batch, const int32_t* seq_lens, int64_t rows, int32_t heads,
                          int32_t dim, int32_t block_size, int32_t max_seq_len, int32_t group_rows, int32_t k,
-                         int32_t* out_slots, int32_t* out_indices, float* out_scores, void* workspace,
-                         size_t workspace_bytes, sai_stream_t stream) {
+                         int32_t* out_slots, int32_t* out_indices, float* out_scores, int32_t list_block_size,
+                         int32_t* out_blocks, int32_t* out_counts, void* workspace, size_t workspace_bytes,
+                         sai_stream_t stream) {
   return fused_topk(q_fp8, w, kcache_fp8, kscale, false, num_blocks, block_table, bt_rows, bt_stride, row_to_batch,
                     seq_lens, rows, heads, dim, block_size, max_seq_len, group_rows, k, out_slots, out_indices,
-                    out_scores, workspace, workspace_bytes, stream);
+                    out_scores, list_block_size, out_blocks, out_counts, workspace, workspace_bytes, stream);
 }
 
 int sai_index_score_topk_bf16(const uint16_t* q_bf16, const float* w, const uint16_t* kcache_bf16,
@@ -383,10 +399,11 @@ int sai_index_score_topk_bf16(const uint16_t* q_bf16, const float* w, const uint
                               int64_t bt_stride, const int32_t* row_to_batch, const int32_t* seq_lens, int64_t rows,
                               int32_t heads, int32_t dim, int32_t block_size, int32_t max_seq_len, int32_t group_rows,
                               int32_t k, int32_t* out_slots, int32_t* out_indices, float* out_scores,
-                              void* workspace, size_t workspace_bytes, sai_stream_t stream) {
+                              int32_t list_block_size, int32_t* out_blocks, int32_t* out_counts, void* workspace,
+                              size_t workspace_bytes, sai_stream_t stream) {
   return fused_topk(q_bf16, w, kcache_bf16, kscale, true, num_blocks, block_table, bt_rows, bt_stride, row_to_batch,
                     seq_lens, rows, heads, dim, block_size, max_seq_len, group_rows, k, out_slots, out_indices,
-                    out_scores, workspace, workspace_bytes, stream);
+                    out_scores, list_block_size, out_blocks, out_counts, workspace, workspace_bytes, stream);
 }
 
 int sai_index_score(const uint8_t* q_fp8, const float* w, const uint8_t* kcache_fp8, const float* kscale,

@@ -33,6 +33,9 @@ struct TopkLaunch {
   int* part_cnt;       // [rows*chunks]
   int* work;           // unit counter, zero at launch (null: fixed unit order)
   int* status;
+  int block_size;      // out_blocks: per-row ascending distinct blocks of the slots
+  int* out_blocks;     // [rows, 512] or null
+  int* out_counts;     // [rows] or null
 };
 
 // Bytes at the start of a topk_transform workspace: the unit counter.
@@ -65,6 +68,9 @@ struct MergeLaunch {
   int* out_idx;
   float* out_scores;           // optional: scores of the selected (fused path)
   int* status;
+  int block_size;              // out_blocks: per-row ascending distinct blocks of the slots
+  int* out_blocks;             // [rows, 512] or null
+  int* out_counts;             // [rows] or null
 };
 cudaError_t launch_merge(const MergeLaunch& p, cudaStream_t stream);
 

@@ -63,6 +63,6 @@ extern "C" int sai_topk_transform_noalloc(const float* scores, int64_t rows, int
   // clears it on the stream before its launch; every work unit writes its
   // candidate count and entries before the merge kernel reads them.
   return sai_topk_transform(scores, rows, score_stride, row_starts, seq_lens, page_tables, pt_rows, pt_stride,
-                            row_to_batch, page_size, k, out_slots, out_indices, scratch,
+                            row_to_batch, page_size, k, out_slots, out_indices, 0, nullptr, nullptr, scratch,
                             scratch ? static_cast<size_t>(SAI_NOALLOC_SCRATCH_BYTES) : 0, stream);
 }

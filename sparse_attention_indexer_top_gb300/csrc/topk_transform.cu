@@ -40,6 +40,7 @@
 #include <algorithm>
 #include <cstdint>
 
+#include "sai_blocks.cuh"
 #include "sai_internal.h"
 #include "sai_ptx.cuh"
 #include "sai_select.cuh"
@@ -101,6 +102,7 @@ struct __align__(128) Smem {
       uint32_t hist[1024];
       uint16_t bucket[kTopK];
     } rank;                             // final ranking (likewise)
+    BlockScratch blocks;                // block lists of the output (likewise)
   } cand;
   uint32_t aux_key[kTopK];
   int32_t aux_idx[kTopK];
@@ -573,19 +575,29 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
       }
       if (p.chunks == 1) {
         const long long o = (long long)row * kTopK;
+        int32_t sl[kTopK / kThreads];  // this thread's slots, for the block lists
 #pragma unroll
         for (int e = 0; e < kTopK / kThreads; ++e) {
+          sl[e] = -1;
           if (ix[e] < 0) continue;
           if (p.out_idx) p.out_idx[o + rk[e]] = ix[e];
-          if (p.out_slots) {
+          if (p.out_slots || p.out_blocks) {
             const int ps = p.page_size;
             const long long page = p.page_tables[(long long)batch * p.pt_stride + (ps == 1 ? ix[e] : ix[e] / ps)];
-            p.out_slots[o + rk[e]] = static_cast<int>(ps == 1 ? page : page * ps + ix[e] % ps);
+            sl[e] = static_cast<int>(ps == 1 ? page : page * ps + ix[e] % ps);
+            if (p.out_slots) p.out_slots[o + rk[e]] = sl[e];
           }
         }
         for (int j = cnt + tid; j < kTopK; j += kThreads) {
           if (p.out_idx) p.out_idx[o + j] = -1;
           if (p.out_slots) p.out_slots[o + j] = -1;
+        }
+        if (p.out_blocks) {
+          // the distinct blocks of the row's slots, built here from the
+          // slots in registers (the ranking's scratch is free once read)
+          named_bar(kBar, kThreads);
+          row_blocks128(sl, kTopK, p.block_size, p.out_blocks + o, p.out_counts ? p.out_counts + row : nullptr,
+                        S.cand.blocks, tid, kBar, true);
         }
       } else {
         const long long o = (long long)unit * kTopK;
@@ -636,6 +648,8 @@ struct __align__(16) MergeSmem {
   uint32_t bcast[4];
   uint32_t umin[kMergeUnits];  // lowest key of each full partial list
   uint32_t kmin, kmax;         // range of the kept candidates
+  int32_t slot_s[kTopK];       // the row's slots, for its block list
+  BlockScratch blocks;
 };
 
 __global__ void __launch_bounds__(kTopK, 1) merge_kernel(const __grid_constant__ MergeLaunch p) {
@@ -647,6 +661,7 @@ __global__ void __launch_bounds__(kTopK, 1) merge_kernel(const __grid_constant__
   reinterpret_cast<uint4*>(S.hist)[2 * tid] = make_uint4(0, 0, 0, 0);
   reinterpret_cast<uint4*>(S.hist)[2 * tid + 1] = make_uint4(0, 0, 0, 0);
   if (tid < kMergeUnits) S.umin[tid] = 0xFFFFFFFFu;
+  S.slot_s[tid] = -1;
   if (tid == 0) {
     S.kmin = 0xFFFFFFFFu;
     S.kmax = 0u;
@@ -735,10 +750,12 @@ __global__ void __launch_bounds__(kTopK, 1) merge_kernel(const __grid_constant__
   auto emit = [&](uint32_t key, int32_t ix, int rk) {
     if (p.out_idx) p.out_idx[o + rk] = ix;
     if (p.out_scores) p.out_scores[o + rk] = key_to_float(key);
-    if (p.out_slots) {
+    if (p.out_slots || p.out_blocks) {
       const int ps = p.page_size;
       const long long page = p.page_tables[(long long)batch * p.pt_stride + (ps == 1 ? ix : ix / ps)];
-      p.out_slots[o + rk] = static_cast<int>(ps == 1 ? page : page * ps + ix % ps);
+      const int slot = static_cast<int>(ps == 1 ? page : page * ps + ix % ps);
+      if (p.out_slots) p.out_slots[o + rk] = slot;
+      S.slot_s[rk] = slot;
     }
   };
   uint32_t k2[2];
@@ -768,6 +785,16 @@ __global__ void __launch_bounds__(kTopK, 1) merge_kernel(const __grid_constant__
     if (p.out_slots) p.out_slots[o + tid] = -1;
     if (p.out_scores) p.out_scores[o + tid] = __int_as_float(0x7FC00000);
   }
+  if (p.out_blocks) {  // the distinct blocks of the row's slots, by the first 128 threads
+    __syncthreads();
+    if (tid < kBlockThreads) {
+      int32_t sl[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sl[e] = S.slot_s[4 * tid + e];
+      row_blocks128(sl, kTopK, p.block_size, p.out_blocks + o, p.out_counts ? p.out_counts + row : nullptr, S.blocks,
+                    tid, 3, true);
+    }
+  }
 }
 
 // ---------------------------------------------------------------- rank
@@ -789,6 +816,7 @@ struct __align__(16) RankRowSmem {
     unsigned long long sortbuf[kTopK];
   } s;
   SelectScratch sc;
+  BlockScratch blocks;
 };
 
 __global__ void __launch_bounds__(kRankRows * 128) rank_kernel(const __grid_constant__ MergeLaunch p) {
@@ -822,14 +850,17 @@ __global__ void __launch_bounds__(kRankRows * 128) rank_kernel(const __grid_cons
   const long long o = row * kTopK;
   const int batch = p.row_to_batch ? p.row_to_batch[row] : (int)row;
   const int ps = p.page_size;
+  int32_t sl[4];  // this thread's slots, for the block list
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
+    sl[e] = -1;
     if (i4[e] < 0) continue;
     if (p.out_idx) p.out_idx[o + rk4[e]] = i4[e];
     if (p.out_scores) p.out_scores[o + rk4[e]] = key_to_float(k4[e]);
-    if (p.out_slots) {
+    if (p.out_slots || p.out_blocks) {
       const long long page = p.page_tables[(long long)batch * p.pt_stride + (ps == 1 ? i4[e] : i4[e] / ps)];
-      p.out_slots[o + rk4[e]] = static_cast<int>(ps == 1 ? page : page * ps + i4[e] % ps);
+      sl[e] = static_cast<int>(ps == 1 ? page : page * ps + i4[e] % ps);
+      if (p.out_slots) p.out_slots[o + rk4[e]] = sl[e];
     }
   }
   for (int j = cnt + t; j < kTopK; j += 128) {
@@ -837,10 +868,14 @@ __global__ void __launch_bounds__(kRankRows * 128) rank_kernel(const __grid_cons
     if (p.out_slots) p.out_slots[o + j] = -1;
     if (p.out_scores) p.out_scores[o + j] = __int_as_float(0x7FC00000);
   }
+  if (p.out_blocks)
+    row_blocks128(sl, kTopK, p.block_size, p.out_blocks + o, p.out_counts ? p.out_counts + row : nullptr, S.blocks, t,
+                  bar, true);
 }
 
 bool g_attr_done[64];
 bool g_merge_attr_done[64];
+bool g_rank_attr_done[64];
 
 }  // namespace
 
@@ -887,12 +922,18 @@ cudaError_t launch_dependent(Kernel kernel, int grid, int block, size_t smem, cu
 cudaError_t launch_merge(const MergeLaunch& p, cudaStream_t stream) {
   if (p.rows <= 0) return cudaSuccess;
   if (p.units_per_row < 1 || p.units_per_row > kMergeUnits) return cudaErrorInvalidValue;
+  int dev = 0;
+  cudaGetDevice(&dev);
   if (p.units_per_row == 1) {
+    if (dev < 64 && !g_rank_attr_done[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)(kRankRows * sizeof(RankRowSmem)));
+      if (e != cudaSuccess) return e;
+      g_rank_attr_done[dev] = true;
+    }
     const int grid = (p.rows + kRankRows - 1) / kRankRows;
     return launch_dependent(rank_kernel, grid, kRankRows * 128, kRankRows * sizeof(RankRowSmem), stream, p);
   }
-  int dev = 0;
-  cudaGetDevice(&dev);
   if (dev < 64 && !g_merge_attr_done[dev]) {
     cudaError_t e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)sizeof(MergeSmem));
@@ -940,6 +981,9 @@ cudaError_t launch_topk_transform(const TopkLaunch& p, int num_sms, cudaStream_t
   m.out_idx = p.out_idx;
   m.out_scores = nullptr;
   m.status = p.status;
+  m.block_size = p.block_size;
+  m.out_blocks = p.out_blocks;
+  m.out_counts = p.out_counts;
   return launch_merge(m, stream);
 }
 

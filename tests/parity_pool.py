@@ -44,9 +44,10 @@ def _chunks(rows, n_chunks):
 # ------------------------------------------------------------------ top-k
 def _topk_task(args):
     import workloads as W
+    from oracle.blocks import sparse_blocks as oracle_blocks
     from oracle.topk import topk_transform
 
-    seed, rows, seq_lens, r2b, pt, page_size, k, gs, gi = args
+    seed, rows, seq_lens, r2b, pt, page_size, k, gs, gi, gb, gc, block_size = args
     bad = []
     for j, i in enumerate(rows):
         n = int(seq_lens[j])
@@ -56,14 +57,22 @@ def _topk_task(args):
             bad.append(f"row {int(i)}: indices differ at {np.flatnonzero(gi[j] != ri[0])[:5].tolist()}")
         elif not np.array_equal(gs[j], rs[0]):
             bad.append(f"row {int(i)}: slots differ at {np.flatnonzero(gs[j] != rs[0])[:5].tolist()}")
+        elif gb is not None:
+            rb, rc = oracle_blocks(rs, block_size)
+            if not (np.array_equal(gb[j], rb[0]) and int(gc[j]) == int(rc[0])):
+                bad.append(f"row {int(i)}: block list differs")
     return bad
 
 
-def check_packed_extend_rows(seed, seq_lens, row_to_batch, page_tables, page_size, k, slots, idx, rows=None):
+def check_packed_extend_rows(seed, seq_lens, row_to_batch, page_tables, page_size, k, slots, idx, rows=None,
+                             blocks=None, counts=None, block_size=128):
     """Every listed row (all by default) of a packed-extend output against the
-    oracle, element by element; returns the failing rows' messages."""
+    oracle, element by element (and the block lists, when given, against the
+    oracle's block lists of the oracle's slots); returns the failing rows'
+    messages."""
     rows = np.arange(seq_lens.size) if rows is None else np.asarray(rows)
-    tasks = [(seed, c, seq_lens[c], row_to_batch[c], page_tables, page_size, k, slots[c], idx[c])
+    tasks = [(seed, c, seq_lens[c], row_to_batch[c], page_tables, page_size, k, slots[c], idx[c],
+              None if blocks is None else blocks[c], None if counts is None else counts[c], block_size)
              for c in _chunks(rows, 8 * workers())]
     with _pool() as pool:
         return [m for part in pool.imap_unordered(_topk_task, tasks) for m in part]

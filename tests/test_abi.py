@@ -48,12 +48,14 @@ def test_status_strings(lib):
 
 def _call(lib, **kw):
     a = dict(scores=1 << 20, rows=4, stride=4096, row_starts=None, seq_lens=1 << 21, pt=1 << 22, pt_rows=4,
-             pt_stride=4096, r2b=None, ps=1, k=512, out_slots=1 << 23, out_idx=None, ws=None, ws_bytes=0)
+             pt_stride=4096, r2b=None, ps=1, k=512, out_slots=1 << 23, out_idx=None, bs=128, out_blocks=None,
+             out_counts=None, ws=None, ws_bytes=0)
     a.update(kw)
     v = lambda x: None if x is None else ctypes.c_void_p(x)
     return lib.sai_topk_transform(v(a["scores"]), a["rows"], a["stride"], v(a["row_starts"]), v(a["seq_lens"]),
                                   v(a["pt"]), a["pt_rows"], a["pt_stride"], v(a["r2b"]), a["ps"], a["k"],
-                                  v(a["out_slots"]), v(a["out_idx"]), v(a["ws"]), a["ws_bytes"], None)
+                                  v(a["out_slots"]), v(a["out_idx"]), a["bs"], v(a["out_blocks"]),
+                                  v(a["out_counts"]), v(a["ws"]), a["ws_bytes"], None)
 
 
 def test_host_validation(lib):
@@ -70,6 +72,11 @@ def test_host_validation(lib):
     assert _call(lib, stride=0) == -2
     assert _call(lib, scores=(1 << 20) + 2) == -7  # fp32 pointer not 4-byte aligned
     assert _call(lib, rows=0) == 0  # nothing to do
+    # block lists: a block size of at least 1, counts only with blocks, a page table
+    assert _call(lib, out_blocks=1 << 24, bs=0) == -2
+    assert _call(lib, out_counts=1 << 24) == -1
+    assert _call(lib, out_slots=None, out_idx=None, out_blocks=1 << 24, pt=None) == -1
+    assert _call(lib, out_blocks=(1 << 24) + 2) == -7
 
 
 def test_workspace_query_without_args(lib):
@@ -100,20 +107,23 @@ def test_fused_argument_errors(lib):
 
     for name in ("sai_index_score_topk", "sai_index_score_topk_bf16"):
         f = getattr(lib, name)
-        tail = (512, p, p, p, p, 1 << 20, None)
+        tail = (512, p, p, p, 128, None, None, p, 1 << 20, None)
         assert f(*args(heads=32), *tail) == -3
         assert f(*args(group=2), *tail) == -3
         assert f(*args(rows=-1), *tail) == -2
         assert f(*args(q=None), *tail) == -1
         assert f(*args(rows=0), *tail) == 0
+        assert f(*args(), 512, p, p, p, 0, p, None, p, 1 << 20, None) == -2  # block lists need a block size
+        assert f(*args(), 512, p, p, p, 128, None, p, p, 1 << 20, None) == -1  # counts without blocks
     for name in ("sai_index_score", "sai_index_score_bf16"):
         f = getattr(lib, name)
         assert f(*args(heads=32), p, 1024, None) == -3
         assert f(*args(q=None), p, 1024, None) == -1
     # a missing key scale is an error for the FP8 cache only: the bf16 calls
     # get past the null check and stop at the misaligned q
-    assert lib.sai_index_score_topk(*args(q=odd, kscale=None), 512, p, p, p, p, 1 << 20, None) == -1
-    assert lib.sai_index_score_topk_bf16(*args(q=odd, kscale=None), 512, p, p, p, p, 1 << 20, None) == -7
+    assert lib.sai_index_score_topk(*args(q=odd, kscale=None), 512, p, p, p, 128, None, None, p, 1 << 20, None) == -1
+    assert lib.sai_index_score_topk_bf16(*args(q=odd, kscale=None), 512, p, p, p, 128, None, None, p, 1 << 20,
+                                         None) == -7
     assert lib.sai_index_score(*args(q=odd, kscale=None), p, 1024, None) == -1
     assert lib.sai_index_score_bf16(*args(q=odd, kscale=None), p, 1024, None) == -7
 

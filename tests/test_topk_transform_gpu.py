@@ -9,6 +9,7 @@ import pytest
 import torch
 
 import workloads as W
+from oracle.blocks import sparse_blocks as oracle_blocks
 from oracle.topk import topk_transform as oracle_topk
 from parity_pool import check_packed_extend_rows
 
@@ -21,40 +22,51 @@ def _t(a):
     return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
 
 
-def _run(inp, force_single=False, scores_t=None):
+def _run(inp, force_single=False, scores_t=None, block_size=None):
+    """GPU (slots, indices), plus (blocks, counts) built by the same call when
+    block_size is given."""
     import sparse_attention_indexer_top_gb300 as sai
 
     ws = torch.empty(16, dtype=torch.uint8, device=DEV) if force_single else None
     s = _t(inp.scores) if scores_t is None else scores_t
-    slots, idx = sai.topk_transform(s, _t(inp.seq_lens), _t(inp.page_tables), page_size=inp.page_size,
-                                    row_starts=_t(inp.row_starts), row_to_batch=_t(inp.row_to_batch),
-                                    want_indices=True, workspace=ws)
+    out = sai.topk_transform(s, _t(inp.seq_lens), _t(inp.page_tables), page_size=inp.page_size,
+                             row_starts=_t(inp.row_starts), row_to_batch=_t(inp.row_to_batch), want_indices=True,
+                             want_blocks=block_size is not None, block_size=block_size or 128, workspace=ws)
     torch.cuda.synchronize()
     assert sai.device_status() == 0
-    return slots.cpu().numpy(), idx.cpu().numpy()
+    return tuple(t.cpu().numpy() for t in out)
 
 
-def _oracle(inp, rows=None):
-    return oracle_topk(inp.scores, inp.seq_lens, inp.page_tables, inp.page_size, 512, inp.row_starts,
-                       inp.row_to_batch, rows=rows)
+def _oracle(inp, rows=None, block_size=None):
+    slots, idx = oracle_topk(inp.scores, inp.seq_lens, inp.page_tables, inp.page_size, 512, inp.row_starts,
+                             inp.row_to_batch, rows=rows)
+    if block_size is None:
+        return slots, idx
+    return (slots, idx) + oracle_blocks(slots, block_size)
 
 
 def _assert_equal(got, ref, what=""):
-    gs, gi = got
-    rs, ri = ref
-    bad = np.flatnonzero((gi != ri).any(axis=1) | (gs != rs).any(axis=1))
+    assert len(got) == len(ref)
+    bad = np.zeros(got[0].shape[0], bool)
+    for g, r in zip(got, ref):
+        bad |= (g != r).reshape(g.shape[0], -1).any(axis=1)
+    bad = np.flatnonzero(bad)
     assert bad.size == 0, f"{what}: {bad.size} rows differ, first {bad[:5]}"
 
 
 def test_tiny_decode():
     inp = W.tiny_decode()
     _assert_equal(_run(inp), _oracle(inp), "tiny decode")
+    _assert_equal(_run(inp, block_size=128), _oracle(inp, block_size=128), "tiny decode, block lists")
 
 
 @pytest.mark.parametrize("single", [False, True])
 def test_decode_bf16_ties(single):
+    # the decode workload's page size is 128: the block lists are the
+    # distinct pages of the selected slots (split rows: built by the merge)
     inp = W.decode_topk()
-    _assert_equal(_run(inp, force_single=single), _oracle(inp), f"decode single={single}")
+    _assert_equal(_run(inp, force_single=single, block_size=128), _oracle(inp, block_size=128),
+                  f"decode single={single}")
 
 
 @pytest.mark.parametrize("kind", ["normal", "bf16", "int", "const", "signed_zero", "inf", "ascending", "descending"])
@@ -64,7 +76,7 @@ def test_value_kinds(kind, single):
     lens = [0, 1, 3, 7, 9, 100, 511, 512, 513, 2047, 2048, 2049, 3071, 3072, 3073, 6000, 6143, 6145, 9001, 20000,
             33333]
     inp = W.make_topk_inputs(31, lens, 33340, 128, (len(lens), 261), kind=kind, fill=np.inf)
-    _assert_equal(_run(inp, force_single=single), _oracle(inp), kind)
+    _assert_equal(_run(inp, force_single=single, block_size=64), _oracle(inp, block_size=64), kind)
 
 
 @pytest.mark.parametrize("stride_pad", [0, 1, 2, 3])
@@ -73,6 +85,17 @@ def test_packed_extend_ragged(stride_pad):
     inp = W.packed_extend(seed=12, reqs=3, new_tokens=97, kv_len=12345, fill=np.inf, stride_pad=stride_pad)
     _assert_equal(_run(inp), _oracle(inp), f"packed pad={stride_pad}")
     _assert_equal(_run(inp, force_single=True), _oracle(inp), f"packed single pad={stride_pad}")
+
+
+@pytest.mark.parametrize("block_size", [1, 7, 128, 1 << 20])
+def test_block_lists_block_sizes(block_size):
+    """Block lists built by the top-k call for page size 1 slots of a wide
+    pool: one slot per block (block_size 1, blocks spanning far more than the
+    16384 ids of the bitmap), odd sizes, and one block for everything."""
+    inp = W.packed_extend(seed=17, reqs=2, new_tokens=40, kv_len=70000, fill=np.inf)
+    _assert_equal(_run(inp, block_size=block_size), _oracle(inp, block_size=block_size), f"bs={block_size}")
+    _assert_equal(_run(inp, force_single=True, block_size=block_size), _oracle(inp, block_size=block_size),
+                  f"single bs={block_size}")
 
 
 @pytest.mark.parametrize("single", [False, True])
@@ -139,9 +162,10 @@ def test_bad_row_metadata_is_flagged_and_emptied():
 def test_packed_extend_full_size():
     """The packed-extend prefill workload at full size ([16384, 140000]
     scores, two requests on a 70000-token KV, +inf outside the windows), in
-    the launch configuration the benchmark times; every row against the
-    oracle, element by element (the oracle runs in a pool of processes over
-    the host cores, each regenerating its rows' windows from the seed)."""
+    the launch configuration the benchmark times, with the block lists of
+    128-token blocks built by the same call; every row against the oracle,
+    element by element (the oracle runs in a pool of processes over the host
+    cores, each regenerating its rows' windows from the seed)."""
     import sparse_attention_indexer_top_gb300 as sai
 
     row_starts, seq_lens, r2b, width = W.packed_extend_meta()
@@ -154,11 +178,13 @@ def test_packed_extend_full_size():
         W.fill_rows(hn, r0, 3, row_starts, seq_lens, fill=np.inf)
         scores[r0:r0 + chunk].copy_(host)
     pt = W.page_table_perm(3, (2, 70000))
-    slots, idx = sai.topk_transform(scores, _t(seq_lens), _t(pt), row_starts=_t(row_starts),
-                                    row_to_batch=_t(r2b), want_indices=True)
+    slots, idx, blocks, counts = sai.topk_transform(scores, _t(seq_lens), _t(pt), row_starts=_t(row_starts),
+                                                    row_to_batch=_t(r2b), want_indices=True, want_blocks=True,
+                                                    block_size=128)
     torch.cuda.synchronize()
     assert sai.device_status() == 0
-    bad = check_packed_extend_rows(3, seq_lens, r2b, pt, 1, 512, slots.cpu().numpy(), idx.cpu().numpy())
+    bad = check_packed_extend_rows(3, seq_lens, r2b, pt, 1, 512, slots.cpu().numpy(), idx.cpu().numpy(),
+                                   blocks=blocks.cpu().numpy(), counts=counts.cpu().numpy(), block_size=128)
     assert not bad, f"{len(bad)} rows differ: {bad[:5]}"
 
 

@@ -50,7 +50,7 @@ def _with_workspace(lib, inp, stream):
     slots = torch.full((rows, 512), -7, dtype=torch.int32, device=DEV)
     idx = torch.full((rows, 512), -7, dtype=torch.int32, device=DEV)
     st = lib.sai_topk_transform(_p(s), rows, stride, _p(rs), _p(sl), _p(pt), pt.shape[0], pt.shape[1], _p(rb),
-                                inp.page_size, 512, _p(slots), _p(idx), _p(ws), ws_bytes, stream)
+                                inp.page_size, 512, _p(slots), _p(idx), 0, None, None, _p(ws), ws_bytes, stream)
     assert st == 0
     return slots, idx
 
