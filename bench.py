@@ -243,12 +243,12 @@ def _pin(a):
     return t.pin_memory()
 
 
-def build_topk_part(dev, new_tokens: int):
+def build_topk_part(dev, new_tokens: int, name: str = "topk_packed_extend"):
     import torch
 
     import workloads as W
 
-    part = Part("topk_packed_extend")
+    part = Part(name)
     row_starts, seq_lens, r2b, width = W.packed_extend_meta(new_tokens=new_tokens)
     rows = int(seq_lens.size)
     host = torch.empty((rows, width), dtype=torch.float32, pin_memory=True)
@@ -265,9 +265,14 @@ def build_topk_part(dev, new_tokens: int):
     ws = sai.topk_transform_workspace(rows, width)
     part.out = {"slots": torch.empty((rows, K), dtype=torch.int32, device=dev),
                 "workspace": torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)}
+    if name == "topk_blocks":  # the same call also writes each row's 128-token block list
+        part.out["blocks"] = torch.empty((rows, K), dtype=torch.int32, device=dev)
+        part.out["counts"] = torch.empty((rows,), dtype=torch.int32, device=dev)
     part.rows = rows
     part.keys = float(seq_lens.astype(np.int64).sum())
     part.bytes = part.keys * 4 + pt.nbytes + rows * (3 * 4 + K * 4)
+    if name == "topk_blocks":
+        part.bytes += rows * (K * 4 + 4)
     part.launches = 1
     part.meta = dict(row_starts=row_starts, seq_lens=seq_lens, row_to_batch=r2b, page_tables=pt, width=width)
     return part
@@ -399,6 +404,8 @@ def build_parts(dev, args):
     parts = []
     if "topk_packed_extend" in args.paths:
         parts.append(build_topk_part(dev, args.new_tokens))
+    if "topk_blocks" in args.paths:
+        parts.append(build_topk_part(dev, args.new_tokens, "topk_blocks"))
     if "fused_decode" in args.paths:
         parts.append(build_fused_part(dev, "fused_decode", W.fused_decode(), 1))
     if "fused_prefill" in args.paths:
@@ -435,6 +442,10 @@ def launch_part(part, stream):
         sai.topk_transform(d["scores"], d["seq_lens"], d["page_tables"], row_starts=d["row_starts"],
                            row_to_batch=d["row_to_batch"], out_slots=o["slots"], workspace=o["workspace"],
                            stream=stream)
+    elif part.name == "topk_blocks":
+        sai.topk_transform(d["scores"], d["seq_lens"], d["page_tables"], row_starts=d["row_starts"],
+                           row_to_batch=d["row_to_batch"], out_slots=o["slots"], block_size=128,
+                           out_blocks=o["blocks"], out_counts=o["counts"], workspace=o["workspace"], stream=stream)
     else:
         sai.index_score_topk(d["q"], d["w"], d["kcache"], d["kscale"], d["block_table"], d["seq_lens"],
                              max_seq_len=part.meta["max_len"], row_to_batch=d.get("row_to_batch"),
@@ -493,11 +504,13 @@ def _oracle_rows(task):
     done, spent = 0, 0.0
     for i in rows:
         i = int(i)
-        if name == "topk_packed_extend":
+        if name in ("topk_packed_extend", "topk_blocks"):
             n = int(spec["seq_lens"][i])
             w = W.packed_extend_window(3, i, n)
             t0 = time.perf_counter()
-            oracle_topk(w[None, :], np.array([n]), spec["page_tables"][[int(spec["row_to_batch"][i])]], 1, K)
+            sl, _ = oracle_topk(w[None, :], np.array([n]), spec["page_tables"][[int(spec["row_to_batch"][i])]], 1, K)
+            if name == "topk_blocks":
+                oracle_blocks(sl, 128)
         elif name == "topk_decode":
             n = int(data["seq_lens"][i])
             t0 = time.perf_counter()
@@ -522,7 +535,7 @@ def _oracle_specs(parts_meta, folder):
     """Per part: (name, rows of the step, worker input spec, item order)."""
     specs = []
     for name, nrows, meta in parts_meta:
-        if name == "topk_packed_extend":
+        if name in ("topk_packed_extend", "topk_blocks"):
             spec = dict(kind="packed", seq_lens=meta["seq_lens"], row_to_batch=meta["row_to_batch"],
                         page_tables=meta["page_tables"])
             items = np.arange(nrows)
@@ -721,6 +734,12 @@ def run_gpu(args):
             else:
                 entry["fp8_frac"] = entry["tflops"] / fp8_peak
         paths[part.name] = entry
+    if "topk_blocks" in paths and "topk_packed_extend" in paths:
+        added = paths["topk_blocks"]["ms"] - paths["topk_packed_extend"]["ms"]
+        entry = {"added_ms_in_topk": added}
+        if "sparse_blocks" in paths:
+            entry["separate_pass_ms"] = paths["sparse_blocks"]["ms"]
+        paths["block_lists"] = entry
     # the dominant kernel's roofline
     top = int(np.argmax(part_ms))
     tp, tm = parts[top], part_ms[top]

@@ -83,14 +83,20 @@ def kth(s, k):
     return float(np.sort(s)[::-1][min(s.size, k) - 1]) if s.size else 0.0
 
 
-def check_fused_rows(inp, rows, ref_scores, slots, idx, scores, k=512):
+def check_fused_rows(inp, rows, ref_scores, slots, idx, scores, k=512, blocks=None, counts=None, block_size=128):
     """The fused top-k of the listed rows against the oracle's scores
     (``ref_scores[j]`` for ``rows[j]``; ``slots``/``idx``/``scores`` indexed by
     row). Selection rule: count min(n, k), distinct in-range indices, every
     pick's oracle score >= the oracle k-th score minus the tolerance; the
     GPU's scores within the tolerance of the oracle's, descending, equal GPU
     scores in ascending index order; slots = the transform of the GPU's own
-    indices. Returns the failing rows' messages."""
+    indices. Block lists (when given): where the GPU picked the oracle's
+    set, equal to the oracle's block lists of the oracle's slots; on every
+    row, the ascending distinct blocks of the GPU's own slots. Returns the
+    failing rows' messages."""
+    from oracle.blocks import sparse_blocks as oracle_blocks
+    from oracle.topk import page_transform, topk_row
+
     bad = []
     for j, i in enumerate(rows):
         i = int(i)
@@ -128,6 +134,20 @@ def check_fused_rows(inp, rows, ref_scores, slots, idx, scores, k=512):
         pages = inp.block_table[b][sel // 128].astype(np.int64)
         if not np.array_equal(slots[i][:kk], pages * 128 + sel % 128):
             bad.append(f"row {i}: slots")
+            continue
+        if blocks is not None:
+            own = np.unique(slots[i][:kk].astype(np.int64) // block_size)
+            gb, gc = np.asarray(blocks[i]), int(counts[i])
+            if gc != own.size or not np.array_equal(gb[:gc], own) or not (gb[gc:] == -1).all():
+                bad.append(f"row {i}: block list is not the distinct blocks of the row's slots")
+                continue
+            ora = topk_row(s_ora.astype(np.float32), k)
+            if np.array_equal(np.sort(ora), np.sort(sel)):
+                ora_slots = np.full((1, gb.size), -1, np.int32)
+                ora_slots[0, :ora.size] = page_transform(ora, inp.block_table[b], 128)
+                ob, oc = oracle_blocks(ora_slots, block_size)
+                if oc[0] != gc or not np.array_equal(ob[0], gb):
+                    bad.append(f"row {i}: block list differs from the oracle's")
     return bad
 
 
@@ -138,7 +158,7 @@ def _fused_task(args):
     import workloads as W
     from oracle.score import index_scores
 
-    folder, dtype, rows, slots, idx, scores = args
+    folder, dtype, rows, slots, idx, scores, blocks, counts, block_size = args
     arr = {}
     for f in _FIELDS:
         path = os.path.join(folder, f + ".npy")
@@ -152,10 +172,12 @@ def _fused_task(args):
     sl = {int(r): slots[j] for r, j in local.items()}
     ix = {int(r): idx[j] for r, j in local.items()}
     sc = {int(r): scores[j] for r, j in local.items()}
-    return check_fused_rows(inp, rows, ref, sl, ix, sc, inp.k)
+    bl = None if blocks is None else {int(r): blocks[j] for r, j in local.items()}
+    cn = None if counts is None else {int(r): counts[j] for r, j in local.items()}
+    return check_fused_rows(inp, rows, ref, sl, ix, sc, inp.k, bl, cn, block_size)
 
 
-def check_fused_all_rows(inp, slots, idx, scores, rows=None):
+def check_fused_all_rows(inp, slots, idx, scores, rows=None, blocks=None, counts=None, block_size=128):
     """check_fused_rows over every listed row (all by default), in the pool."""
     rows = np.arange(inp.rows) if rows is None else np.asarray(rows)
     with tempfile.TemporaryDirectory() as folder:
@@ -163,6 +185,7 @@ def check_fused_all_rows(inp, slots, idx, scores, rows=None):
             a = getattr(inp, f)
             if a is not None:
                 np.save(os.path.join(folder, f + ".npy"), np.ascontiguousarray(a))
-        tasks = [(folder, inp.dtype, c, slots[c], idx[c], scores[c]) for c in _chunks(rows, 8 * workers())]
+        tasks = [(folder, inp.dtype, c, slots[c], idx[c], scores[c], None if blocks is None else blocks[c],
+                  None if counts is None else counts[c], block_size) for c in _chunks(rows, 8 * workers())]
         with _pool() as pool:
             return [m for part in pool.imap_unordered(_fused_task, tasks) for m in part]

@@ -52,17 +52,19 @@ def _dense(inp, group_rows=1):
     return out.cpu().numpy()
 
 
-def _fused(inp, group_rows=1):
+def _fused(inp, group_rows=1, block_size=None):
+    """GPU (slots, indices, scores), plus (blocks, counts) built by the same
+    call when block_size is given."""
     import sparse_attention_indexer_top_gb300 as sai
 
     d = _dev_inputs(inp)
     max_len = int(inp.seq_lens.max()) if inp.rows else 0
-    slots, idx, scores = sai.index_score_topk(d["q"], d["w"], d["kcache"], d["kscale"], d["block_table"],
-                                              d["seq_lens"], max_seq_len=max_len, row_to_batch=d["row_to_batch"],
-                                              group_rows=group_rows)
+    out = sai.index_score_topk(d["q"], d["w"], d["kcache"], d["kscale"], d["block_table"], d["seq_lens"],
+                               max_seq_len=max_len, row_to_batch=d["row_to_batch"], group_rows=group_rows,
+                               want_blocks=block_size is not None, block_size=block_size or 128)
     torch.cuda.synchronize()
     assert sai.device_status() == 0
-    return slots.cpu().numpy(), idx.cpu().numpy(), scores.cpu().numpy()
+    return tuple(t.cpu().numpy() for t in out)
 
 
 def _check_dense(got, inp, exact=False, rows=None):
@@ -80,17 +82,19 @@ def _check_dense(got, inp, exact=False, rows=None):
             assert err.max() <= TOL, f"row {i}: max rel err {err.max():.3e} at {int(err.argmax())}"
 
 
-def _check_topk(got, inp, rows=None, k=512):
-    slots, idx, scores = got
+def _check_topk(got, inp, rows=None, k=512, block_size=128):
+    slots, idx, scores = got[:3]
+    blocks, counts = got[3:] if len(got) == 5 else (None, None)
     rows = list(range(inp.rows)) if rows is None else rows
-    bad = check_fused_rows(inp, rows, index_scores(inp, rows), slots, idx, scores, k)
+    bad = check_fused_rows(inp, rows, index_scores(inp, rows), slots, idx, scores, k, blocks, counts, block_size)
     assert not bad, f"{len(bad)} rows fail: {bad[:5]}"
 
 
-def _check_all_rows_in_pool(got, inp):
+def _check_all_rows_in_pool(got, inp, block_size=128):
     """Every row against the oracle, the rows spread over the host cores."""
-    slots, idx, scores = got
-    bad = check_fused_all_rows(inp, slots, idx, scores)
+    slots, idx, scores = got[:3]
+    blocks, counts = got[3:] if len(got) == 5 else (None, None)
+    bad = check_fused_all_rows(inp, slots, idx, scores, blocks=blocks, counts=counts, block_size=block_size)
     assert not bad, f"{len(bad)} rows fail: {bad[:5]}"
 
 
@@ -146,9 +150,11 @@ def test_topk_decode_many_chunks():
 
 def test_fused_decode_full_size():
     """The fused decode workload at full size (64 rows, 64 heads x 128,
-    seq_lens U[4096, 32768], 16384-block pool), every row checked."""
+    seq_lens U[4096, 32768], 16384-block pool), every row checked, with the
+    per-row lists of 128-token KV blocks built by the same call (the merge)."""
     inp = W.fused_decode()
     _check_topk(_fused(inp), inp)
+    _check_topk(_fused(inp, block_size=128), inp)
 
 
 def test_fused_prefill_full_size():
@@ -157,6 +163,20 @@ def test_fused_prefill_full_size():
     every row against the oracle."""
     inp = W.fused_prefill()
     _check_all_rows_in_pool(_fused(inp, group_rows=4), inp)
+
+
+@pytest.mark.parametrize("block_size", [128, 256, 1])
+def test_fused_block_lists(block_size):
+    """Block lists built by the fused call's last stage: the ranking path
+    (one KV chunk per row: grouped prefill rows) and the merge path (decode
+    rows over several chunks)."""
+    rows, kv = 64, 6000
+    lens = (kv - rows + 1 + np.arange(rows)).astype(np.int32)
+    blocks = -(-kv // 128)
+    inp = W.make_fused_inputs(44, rows, 64, 128, blocks, lens, (1, blocks), row_to_batch=np.zeros(rows, np.int32))
+    _check_topk(_fused(inp, group_rows=4, block_size=block_size), inp, block_size=block_size)
+    dec = W.fused_decode(seed=45, rows=16, min_len=3000, max_len=20000)
+    _check_topk(_fused(dec, block_size=block_size), dec, block_size=block_size)
 
 
 @pytest.mark.parametrize("kind", ["normal", "int"])

@@ -42,3 +42,18 @@ def test_fused_checker():
     bad_tops[7, 5] *= 1.01  # a score off by 1%
     msgs = check_fused_all_rows(inp, slots, bad_idx, bad_tops)
     assert sorted(m.split(":")[0] for m in msgs) == ["row 3", "row 7"]
+
+
+def test_fused_checker_block_lists():
+    from oracle.blocks import sparse_blocks
+    from parity_pool import check_fused_rows
+
+    inp = W.make_fused_inputs(61, 6, 64, 128, 24, np.array([1, 130, 300, 330, 200, 380], np.int32), (6, 4))
+    slots, idx, tops, scores = index_score_topk(inp)
+    for bs in (128, 1):
+        blocks, counts = sparse_blocks(slots, bs)
+        assert check_fused_rows(inp, list(range(6)), scores, slots, idx, tops, 512, blocks, counts, bs) == []
+    blocks, counts = sparse_blocks(slots, 128)
+    blocks[2, 0] += 1  # a wrong block
+    msgs = check_fused_rows(inp, list(range(6)), scores, slots, idx, tops, 512, blocks, counts, 128)
+    assert [m.split(":")[0] for m in msgs] == ["row 2"]
