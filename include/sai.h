@@ -68,6 +68,20 @@ const char* sai_last_error(void);
 int sai_device_status(int* out_bits, int clear, sai_stream_t stream);
 
 /*
+ * Test hook for the bounded waits (not part of the computation; the paper
+ * has no counterpart). Every pipeline wait inside the kernels gives up after
+ * about two seconds, sets status bit 2 and lets the launch finish, so a lost
+ * arrival can never hang the GPU. To exercise that exit, the next
+ * sai_index_score_topk / sai_index_score_topk_bf16 call made by this host
+ * thread streams no key tiles for its work unit `unit` (a unit is a group of
+ * query rows and a chunk of their KV blocks; unit 0 holds the first rows'
+ * first chunk): that unit's waits run out, the call completes with status
+ * bit 2 set, and the rows of that unit are undefined. -1 clears the hook;
+ * the call consumes it either way.
+ */
+void sai_test_stall_next_fused(int32_t unit);
+
+/*
  * Workspace bytes that sai_topk_transform wants for these sizes on the
  * current device: a 256-byte header (a work counter that lets CTAs take
  * rows as they finish, zeroed by the call on its stream), plus, when long

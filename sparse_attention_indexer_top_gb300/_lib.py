@@ -19,6 +19,7 @@ SIGNATURES = {
     "sai_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "sai_last_error": (ctypes.c_char_p, []),
     "sai_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int), ctypes.c_int, _vp]),
+    "sai_test_stall_next_fused": (None, [_c_i32]),
     "sai_topk_transform_workspace": (_c_size, [_c_i64, _c_i64, _c_i32]),
     "sai_topk_transform": (ctypes.c_int, [_vp, _c_i64, _c_i64, _vp, _vp, _vp, _c_i64, _c_i64, _vp, _c_i32, _c_i32,
                                           _vp, _vp, _c_i32, _vp, _vp, _vp, _c_size, _vp]),

@@ -449,7 +449,9 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
         bool again = true;
         while (again && run) {
           int page_next = __ldg(bt + tile_at(0, ntiles));
-          for (int i = 0; i < ntiles && run; ++i) {
+          // (test hook: a stalled unit streams no key tiles, so every wait
+          // for them runs out)
+          for (int i = 0; i < ntiles && run && u != p.stall_unit; ++i) {
             int page = page_next;
             if (i + 1 < ntiles) page_next = __ldg(bt + tile_at(i + 1, ntiles));
             if (page < 0 || page >= p.num_blocks) page = 0;  // the epilogue masks this block
@@ -557,7 +559,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
         continue;
       }
       const bool row_live = r < m.nrows;
-      const int nr = n[r];
+      const int nr = row_live ? n[r] : 0;
       const int32_t* bt = p.block_table + (long long)m.batch * p.bt_stride + m.blk0;
       // keys of this row in this unit
       const int n_unit = row_live ? max(0, min(nr - m.blk0 * kBlk, ntiles * kBlk)) : 0;
@@ -588,29 +590,41 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
         uint32_t tau = 0;   // keep keys whose order key >= tau
         float tf = tau_float(0);
         bool spec_used = false;
-        int page_next = __ldg(bt + tile_at(0, ntiles));
-        bool ok_next = page_next >= 0 && page_next < p.num_blocks;
-        float ks_next = (ok_next && active) ? key_scale(page_next) : 0.f;
-        for (int i = 0; i < ntiles; ++i, ++tt) {
-          const int blk = m.blk0 + tile_at(i, ntiles), buf = tt & 1;
+        // position i of the walk holds tile `cur` of the unit (rotated to
+        // start in the middle, see tile_at); `nxt` is position i + 1's
+        int nxt = tile_at(0, ntiles);
+        int page_next = __ldg(bt + nxt);
+        bool ok_next = static_cast<unsigned>(page_next) < static_cast<unsigned>(p.num_blocks);
+        float ks_next = ok_next ? key_scale(page_next) : 0.f;
+        if (!active) {
+          // drain: free each accumulator buffer of the pass (a done row of a
+          // group whose other rows stream the unit again)
+          for (int i = 0; i < ntiles; ++i, ++tt) {
+            const int buf = tt & 1;
+            ok = ok && __all_sync(0xFFFFFFFFu, mbar_wait(&S.tfull[buf], (tt >> 1) & 1u));
+            tc_fence_after();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0 && ok) mbar_arrive(&S.tempty[buf]);
+          }
+        }
+        for (int i = 0; active && i < ntiles; ++i, ++tt) {
+          const int cur = nxt, buf = tt & 1;
+          nxt = cur + 1 == ntiles ? 0 : cur + 1;
+          const int blk = m.blk0 + cur;
           const int t = blk * kBlk + kl;
           const bool page_ok = ok_next;
           const float ks = ks_next;
           const int page = page_next;
           if (i + 1 < ntiles) {
-            page_next = __ldg(bt + tile_at(i + 1, ntiles));
-            ok_next = page_next >= 0 && page_next < p.num_blocks;
-            ks_next = (ok_next && active) ? key_scale(page_next) : 0.f;
+            page_next = __ldg(bt + nxt);
+            ok_next = static_cast<unsigned>(page_next) < static_cast<unsigned>(p.num_blocks);
+            ks_next = ok_next ? key_scale(page_next) : 0.f;
           }
-          if (!page_ok && et == 0 && r == 0 && pass == 0) atomicOr(p.status, kDevBadPage);
+          if (!page_ok) {
+            if (et == 0 && r == 0 && pass == 0) atomicOr(p.status, kDevBadPage);
+          }
           ok = ok && __all_sync(0xFFFFFFFFu, mbar_wait(&S.tfull[buf], (tt >> 1) & 1u));
-          if (!active) {  // drain: free the accumulator buffer
-            if (ok) tc_fence_after();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0 && ok) mbar_arrive(&S.tempty[buf]);
-            continue;
-          }
           float score = 0.f;
           if (ok) {
             tc_fence_after();
@@ -620,7 +634,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
             // a max would go, is the busier one), then packed f32x2 FMAs; the
             // power-of-two scalings are exact, so every product is w_h relu(s_h).
             // acc[k] = this lane's partial for keys l/4, l/4+8, 16+l/4, 24+l/4
-            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            float2 acc[4];  // set by the first head pair's multiply
             // per-head mode: the scales of this lane's 4 keys, and its row's
             // [64, dense_stride] block of the output
             float ksq[4] = {0.f, 0.f, 0.f, 0.f};
@@ -664,6 +678,9 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
                     o0[t1] = page_ok ? x1.x * w2[j].x * sc : sc;
                     o1[t1] = page_ok ? x1.y * w2[j].y * sc : sc;
                   }
+                } else if (j == 0) {
+                  acc[2 * half] = __fmul2_rn(x0, w2[j]);
+                  acc[2 * half + 1] = __fmul2_rn(x1, w2[j]);
                 } else {
                   acc[2 * half] = __ffma2_rn(x0, w2[j], acc[2 * half]);
                   acc[2 * half + 1] = __ffma2_rn(x1, w2[j], acc[2 * half + 1]);
@@ -682,25 +699,29 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
             const float keep = hi ? k1 : k0;
             score = (keep + __shfl_xor_sync(0xFFFFFFFFu, hi ? k0 : k1, 2)) * ks;
           }
-          const bool live = ok && row_live && page_ok && t < nr;
+          const bool live = ok && page_ok && t < nr;  // (nr = 0 for a row past the group's end)
           if constexpr (MODE == kModeDense) {
             if (live) p.dense[(long long)(m.row0 + r) * p.dense_stride + t] = score;
           } else if constexpr (MODE == kModeTopk) {
             // running top-k filter: cut this warp's list if the tile's
             // survivors might not fit, then append them
-            if (wc > kSub - 32) {
-              tau = max(tau, warp_cut512(my_key, my_idx, wc, whist, lane));
-              tf = tau_float(tau);
-              wc = kTopK;
-            }
             const bool pass_ = live && score >= tf;
             const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass_);
-            if (pass_) {
-              const int pos = wc + __popc(bal & ((1u << lane) - 1u));
-              my_key[pos] = order_key(score);
-              my_idx[pos] = t;
+            if (bal) {
+              // cut this warp's list first if the survivors might not fit
+              // (they passed the old threshold: keeping them is still exact)
+              if (wc > kSub - 32) {
+                tau = max(tau, warp_cut512(my_key, my_idx, wc, whist, lane));
+                tf = tau_float(tau);
+                wc = kTopK;
+              }
+              if (pass_) {
+                const int pos = wc + __popc(bal & ((1u << lane) - 1u));
+                my_key[pos] = order_key(score);
+                my_idx[pos] = t;
+              }
+              wc += __popc(bal);
             }
-            wc += __popc(bal);
             if (spec && i == kSampleTiles - 1) {
               // the sample tiles are in: the row's start threshold
               const uint2 sw = spec_threshold(S.wcnt[r], S.sc[r], S.aux_key[r], my_key, my_idx, wc, n_unit, quad, et,

@@ -41,6 +41,7 @@ bool device_setup(int* dev_out, int** status, int* sms) {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 thread_local const char* t_last_error = "";
+thread_local int t_stall_unit = -1;  // test hook, consumed by the thread's next fused top-k call
 
 // Map a CUDA error to a status, remembering its text for sai_last_error.
 int cuda_status(cudaError_t e) {
@@ -54,6 +55,8 @@ int cuda_status(cudaError_t e) {
 extern "C" {
 
 const char* sai_last_error(void) { return t_last_error; }
+
+void sai_test_stall_next_fused(int32_t unit) { t_stall_unit = unit < 0 ? -1 : unit; }
 
 const char* sai_status_string(int status) {
   switch (status) {
@@ -190,6 +193,7 @@ sai::FusedLaunch fused_launch(const void* q, const float* w, const float* kscale
                               const int32_t* row_to_batch, const int32_t* seq_lens, int64_t rows,
                               int32_t max_seq_len, const sai::FusedPlan& plan, int* st) {
   sai::FusedLaunch p{};
+  p.stall_unit = -1;
   p.q = q;
   p.w = w;
   p.kscale = kscale;
@@ -237,6 +241,8 @@ int fused_topk(const void* q, const float* w, const void* kcache, const float* k
   p.part_key = reinterpret_cast<uint32_t*>(ws);
   p.part_idx = reinterpret_cast<int32_t*>(ws + units * SAI_TOPK * 4);
   p.part_cnt = reinterpret_cast<int*>(ws + units * SAI_TOPK * 8);
+  p.stall_unit = t_stall_unit;
+  t_stall_unit = -1;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = sai::launch_fused(p, plan.group, sai::FusedOut::kTopk, bf16, kcache, s);
   if (e != cudaSuccess) return cuda_status(e);

@@ -98,6 +98,7 @@ struct FusedLaunch {
   int sign_w;        // per-head mode: use sign(w_h) for w_h (same order per (row, head), comparable scales)
   long long dense_stride;
   int* status;
+  int stall_unit;    // test hook: this work unit streams no key tiles (-1: none)
 };
 struct FusedPlan {
   int group;         // query rows per CTA (1 or 4)

@@ -13,6 +13,8 @@ workloads are checked on every row, in a pool of processes over the host
 cores (tests/parity_pool.py).
 """
 
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -318,3 +320,30 @@ def test_chunked_prefix_calls_match_one_call(dtype):
         assert np.array_equal(s.cpu().numpy(), whole[0][lo:hi])
         assert np.array_equal(i.cpu().numpy(), whole[1][lo:hi])
         assert np.array_equal(sc.cpu().numpy().view(np.uint32), whole[2][lo:hi].view(np.uint32))
+
+
+def test_stalled_unit_wait_runs_out():
+    """The bounded waits, exercised without a GPU fault: the test hook makes
+    the next fused call stream no key tiles for its work unit 0 (row 0's
+    first KV chunk), so every wait for those tiles gives up after about two
+    seconds. The call must still finish, set status bit 2, leave the other
+    rows exact, and leave the context usable (the same call without the hook
+    is exact)."""
+    import sparse_attention_indexer_top_gb300 as sai
+    from sparse_attention_indexer_top_gb300 import _lib
+
+    inp = W.fused_decode(seed=46, rows=4, min_len=3000, max_len=6000)
+    d = _dev_inputs(inp)
+    max_len = int(inp.seq_lens.max())
+    _lib.load().sai_test_stall_next_fused(0)
+    t0 = time.time()
+    out = sai.index_score_topk(d["q"], d["w"], d["kcache"], d["kscale"], d["block_table"], d["seq_lens"],
+                               max_seq_len=max_len)
+    torch.cuda.synchronize()
+    elapsed = time.time() - t0
+    bits = sai.device_status(clear=True)
+    assert bits & 2, f"status bits {bits}: no wait gave up"
+    assert elapsed < 60
+    got = tuple(t.cpu().numpy() for t in out)
+    _check_topk(got, inp, rows=[1, 2, 3])
+    _check_topk(_fused(inp), inp)  # the hook is consumed; the next call is exact
