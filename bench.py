@@ -91,18 +91,18 @@ def measure_fp8_peak(dev, n: int = 8192, reps: int = 10):
         return None, f"fp8 GEMM unavailable ({type(exc).__name__}: {exc})"
 
 # DRAM bytes (read + write) per key, from one ncu capture of each kernel as
-# it stands (summaries under profiles/, by kernel and workload): top-k stream
-# on 2048 packed-extend rows, 584.77 MB + 2.96 MB for 142.3 M keys; fused
-# prefill on 4096 rows, 39.14 MB + 0.0003 MB for 125.8 M keys; fused decode
-# on 64 rows, 158.42 MB + 3.42 MB for 1.19 M keys; the bf16-cache variants of
-# the same two workloads, 76.90 MB + 1.03 MB and 312.09 MB + 0.43 MB. Traffic
+# it stands (the launch list of the default step, one pass, at full size;
+# summaries under profiles/, by kernel and workload): top-k stream on the
+# 16384 packed-extend rows, 4335.61 MB + 0.09 MB per launch for 1079.8 M
+# keys; fused prefill on 4096 rows, 39.43 MB + 0.05 MB for 125.8 M keys;
+# fused decode on 64 rows, 158.92 MB + 1.32 MB for 1.19 M keys. Traffic
 # grows with the keys streamed. Set an entry to None whenever its kernel
 # changes until it is re-captured.
 TRAFFIC_BYTES_PER_KEY = {
-    "topk_packed_extend": (584.774144e6 + 2.956544e6) / 142312448,
-    "fused_prefill": (39.135488e6 + 0.000256e6) / 125831168,
-    "fused_decode": (158.424064e6 + 3.421696e6) / 1190814,
-    # bf16 kernels changed after their capture (relu on the FMA pipe)
+    "topk_packed_extend": (21678060800 + 467456) / 5 / 1079779328,
+    "fused_prefill": (197137920 + 229376) / 5 / 125831168,
+    "fused_decode": (794580480 + 6599936) / 5 / 1190814,
+    # not re-captured since the fused kernel changed (four rows per CTA)
     "fused_prefill_bf16": None,
     "fused_decode_bf16": None,
 }
