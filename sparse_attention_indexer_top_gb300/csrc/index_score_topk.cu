@@ -647,20 +647,19 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
                                  : __int_as_float(0xFF800000);  // a key on a bad block scores -inf
               }
             }
+            // The 32 keys x 64 heads come in four 16-lane x 32-column loads
+            // (half = keys 0-15 / 16-31 of the quadrant, hq = heads 0-31 /
+            // 32-63); with one CTA per SM (groups of four rows) each is
+            // issued before the math of the one before it, so the TMEM
+            // latency hides behind the FMA work. Load (half, hq)
+            // gives lane l keys l/4 and l/4 + 8 of the half at heads
+            // 32 hq + 8j + 2(l%4) + {0, 1}, j < 4: weights w2[4 hq + j].
+            auto math = [&](const uint32_t (&a)[16], int half, int hq) {
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              uint32_t a[32];
-              tmem_ld16x256_x8(col + (static_cast<uint32_t>(16 * half) << 16), a);
-              tmem_ld_wait();
-              if (half == 1) {  // the accumulator buffer is free once both halves are in registers
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&S.tempty[buf]);
-              }
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float2 x0 = make_float2(relu_of<BF16>(a[4 * j]), relu_of<BF16>(a[4 * j + 1]));
-                const float2 x1 = make_float2(relu_of<BF16>(a[4 * j + 2]), relu_of<BF16>(a[4 * j + 3]));
+              for (int jj = 0; jj < 4; ++jj) {
+                const int j = 4 * hq + jj;
+                const float2 x0 = make_float2(relu_of<BF16>(a[4 * jj]), relu_of<BF16>(a[4 * jj + 1]));
+                const float2 x1 = make_float2(relu_of<BF16>(a[4 * jj + 2]), relu_of<BF16>(a[4 * jj + 3]));
                 if constexpr (MODE == kModePerHead) {
                   // heads h0, h0 + 1 of keys key0 and key0 + 8: w_h relu(s_h) x scale
                   const int h0 = 8 * j + 2 * (lane & 3);
@@ -684,6 +683,48 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
                 } else {
                   acc[2 * half] = __ffma2_rn(x0, w2[j], acc[2 * half]);
                   acc[2 * half + 1] = __ffma2_rn(x1, w2[j], acc[2 * half + 1]);
+                }
+              }
+            };
+            auto taddr = [&](int half, int hq) {
+              return col + (static_cast<uint32_t>(16 * half) << 16) + static_cast<uint32_t>(32 * hq);
+            };
+            if constexpr (R >= 4) {
+              uint32_t b0[16], b1[16];
+              tmem_ld16x256_x4(taddr(0, 0), b0);
+              tmem_ld_wait16(b0);
+              tmem_ld16x256_x4(taddr(0, 1), b1);
+              math(b0, 0, 0);
+              tmem_ld_wait16(b1);
+              tmem_ld16x256_x4(taddr(1, 0), b0);
+              math(b1, 0, 1);
+              tmem_ld_wait16(b0);
+              tmem_ld16x256_x4(taddr(1, 1), b1);
+              math(b0, 1, 0);
+              tmem_ld_wait16(b1);
+              // the accumulator buffer is free once all its loads are in registers
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&S.tempty[buf]);
+              math(b1, 1, 1);
+            } else {
+              // single rows (three CTAs per SM hide the latency): one
+              // 16-lane x 64-column load per half
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {
+                uint32_t a[32];
+                tmem_ld16x256_x8(col + (static_cast<uint32_t>(16 * half) << 16), a);
+                tmem_ld_wait();
+                if (half == 1) {  // the accumulator buffer is free once both halves are in registers
+                  tc_fence_before();
+                  __syncwarp();
+                  if (lane == 0) mbar_arrive(&S.tempty[buf]);
+                }
+#pragma unroll
+                for (int hq = 0; hq < 2; ++hq) {
+                  // registers 16 hq .. 16 hq + 15 are the head quarter hq
+                  const uint32_t(&aq)[16] = *reinterpret_cast<const uint32_t(*)[16]>(a + 16 * hq);
+                  math(aq, half, hq);
                 }
               }
             }
