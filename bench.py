@@ -326,7 +326,7 @@ def build_fused_part(dev, name: str, inp, group_rows: int):
 def build_topk_decode_part(dev):
     """The decode-layout top-k: 128 rows, seq_lens U[8192, 32768], bf16-rounded
     N(0,1) scores in a [128, 32768] buffer (ties certain), 128-token pages
-    (slot = block*128 + idx%128). Few long rows: split over CTAs + merge.
+    (slot = block*128 + idx%128). Rows of up to 32768 scores: one CTA each.
     Not part of the default step (it is launch-latency bound)."""
     import torch
 

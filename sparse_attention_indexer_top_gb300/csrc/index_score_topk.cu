@@ -909,6 +909,10 @@ cudaError_t launch_fused_t(const FusedLaunch& p, const void* kcache, cudaStream_
 
 }  // namespace
 
+#ifndef SAI_FUSED_UNITS_PER_SM
+#define SAI_FUSED_UNITS_PER_SM 4  // work units per SM the plan aims at
+#endif
+
 FusedPlan fused_plan(long long rows, int max_seq_len, int group_rows, int num_sms) {
   FusedPlan pl{1, 1, 1, 0};
   // Packed prefill rows come in groups of 4 sharing a request; the kernel
@@ -921,7 +925,7 @@ FusedPlan fused_plan(long long rows, int max_seq_len, int group_rows, int num_sm
   // about four units per SM (a little over one wave of three resident
   // single-row CTAs): measured against 2, 3, 5, 6 and 8 per SM on the
   // decode workload
-  const long long target = 4LL * num_sms;
+  const long long target = (long long)SAI_FUSED_UNITS_PER_SM * num_sms;
   long long chunks = groups > 0 ? (target + groups - 1) / groups : 1;
   chunks = std::max<long long>(1, std::min<long long>({chunks, 12LL, max_blocks}));
   const long long cb = (max_blocks + chunks - 1) / chunks;

@@ -52,12 +52,22 @@ constexpr int kThreads = 128;                    // 4 warps per CTA
 #ifndef SAI_TOPK_VEC
 #define SAI_TOPK_VEC 6
 #endif
+#ifndef SAI_TOPK_MIN_CHUNK
+// Shortest window piece of a split row: rows of up to twice this stay on one
+// CTA (measured on 128 decode rows of 8K-32K scores: 0.048 ms unsplit, 0.069
+// in pieces of 8192 and 0.096 in pieces of 4096, the merge of the pieces'
+// lists taking ~20 us).
+#define SAI_TOPK_MIN_CHUNK 16384
+#endif
 #ifndef SAI_TOPK_CTAS
 #define SAI_TOPK_CTAS 5
 #endif
 constexpr int kVec = SAI_TOPK_VEC;               // float4 loads per thread per stage
 constexpr int kStage = kVec * 4 * kThreads;      // floats per stage (12 KB)
-constexpr int kNStage = 2;                       // 24 KB in flight per CTA
+#ifndef SAI_TOPK_NSTAGE
+#define SAI_TOPK_NSTAGE 2
+#endif
+constexpr int kNStage = SAI_TOPK_NSTAGE;         // 24 KB in flight per CTA
 constexpr int kWarps = kThreads / 32;
 constexpr int kCap = 1536;                       // candidate capacity (all warps)
 constexpr int kSub = kCap / kWarps;              // one candidate sub-list per warp
@@ -883,7 +893,7 @@ TopkPlan topk_plan(long long rows, long long max_window, int num_sms) {
   TopkPlan pl{1, 0, kTopkWorkHeader};
   if (rows <= 0 || max_window <= 0) return TopkPlan{1, 0, 0};
   const long long slots = 2LL * num_sms;
-  constexpr long long kMinChunk = 4096;
+  constexpr long long kMinChunk = SAI_TOPK_MIN_CHUNK;
   if (rows < slots && max_window > 2 * kMinChunk) {
     long long chunks = (max_window + kMinChunk - 1) / kMinChunk;
     chunks = std::min<long long>(chunks, kMergeUnits);

@@ -60,6 +60,14 @@ def test_tiny_decode():
     _assert_equal(_run(inp, block_size=128), _oracle(inp, block_size=128), "tiny decode, block lists")
 
 
+def test_decode_long_rows_split_ties():
+    """Few rows longer than two split pieces (rows of 33K-60K bf16-rounded
+    scores, so ties are certain): split over CTAs and merged, with the block
+    lists built by the merge."""
+    inp = W.decode_topk(seed=24, rows=40, min_len=33000, max_len=60000)
+    _assert_equal(_run(inp, block_size=128), _oracle(inp, block_size=128), "long decode rows")
+
+
 @pytest.mark.parametrize("single", [False, True])
 def test_decode_bf16_ties(single):
     # the decode workload's page size is 128: the block lists are the

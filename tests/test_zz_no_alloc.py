@@ -87,11 +87,11 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     from sparse_attention_indexer_top_gb300 import _lib
 
     lib = _lib.load()
-    # fewer rows than two per SM, each 65536 scores long: the call splits
-    # every row into 12 chunks, and on a part with at least 86 SMs their
-    # partial lists (rows x 12 x 4100 bytes) outgrow the fixed array
+    # fewer rows than two per SM, each 12 x 16384 scores long: the call
+    # splits every row into 12 chunks, and on a part with at least 86 SMs
+    # their partial lists (rows x 12 x 4100 bytes) outgrow the fixed array
     sms = torch.cuda.get_device_properties(DEV).multi_processor_count
-    rows, stride = 2 * sms - 1, 65536
+    rows, stride = 2 * sms - 1, 12 * 16384
     need = lib.sai_topk_transform_workspace(rows, stride, 512)
     if need <= (8 << 20):
         pytest.skip(f"{sms} SMs: {rows} split rows fit the fixed array")
