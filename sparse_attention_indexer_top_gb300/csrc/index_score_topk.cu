@@ -375,6 +375,11 @@ __host__ __device__ constexpr int fused_threads() {
 // head-summed scores, or the dense per-head scores (each head's summand).
 constexpr int kModeTopk = 0, kModeDense = 1, kModePerHead = 2;
 
+// Work units are walked last to first: a packed prefill batch's later
+// rows see the most keys, so its longest units start in the first wave and
+// the shortest fill the last one.
+__device__ __forceinline__ int unit_at(int i, int units) { return units - 1 - i; }
+
 template <int R, int MODE, bool BF16>
 __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16>()))
     fused_score_topk_kernel(const __grid_constant__ FusedLaunch p, const __grid_constant__ CUtensorMap kmap,
@@ -420,10 +425,10 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
   const uint32_t tmem = S.tmem_base;
   if constexpr (MODE == kModeTopk) pdl_trigger();  // the merge may be scheduled now; it waits for this grid to finish
 
-  // Every role walks the same units (u = blockIdx.x, + gridDim.x, ...) and
-  // passes (a unit is streamed again when the epilogue's verdict says so)
-  // and derives the same tile counts, so the barrier phases below (counted
-  // over all tiles, passes and units of this CTA) stay in step.
+  // Every role walks the same units (blockIdx.x, + gridDim.x, ..., mapped
+  // by unit_at) and passes (a unit is streamed again when the epilogue's
+  // verdict says so) and derives the same tile counts, so the barrier phases
+  // below (counted over all tiles, passes and units of this CTA) stay in step.
   if (warp == kTmaWarp) {
     // ---------------- TMA producer: the unit's query tile, then its key
     // blocks through the ring; the block ids come straight from the table
@@ -433,7 +438,8 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
       const uint64_t keep = l2_policy_evict_last();  // q and K are re-read by other CTAs
       uint32_t it = 0, qn = 0, vn = 0;
       bool run = true;
-      for (int u = blockIdx.x; u < units && run; u += gridDim.x) {
+      for (int iu = blockIdx.x; iu < units && run; iu += gridDim.x) {
+        const int u = unit_at(iu, units);
         int n[R];
         const GroupMeta m = group_meta<R>(p, u / p.chunks, u % p.chunks, n, false);
         const int ntiles = m.blk1 - m.blk0;
@@ -478,7 +484,8 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
     if (lane == 0) {
       uint32_t it = 0, rs = 0, qn = 0, vn = 0;  // tiles (accumulator buffers), ring slots, query tiles, verdicts
       bool run = true;
-      for (int u = blockIdx.x; u < units && run; u += gridDim.x) {
+      for (int iu = blockIdx.x; iu < units && run; iu += gridDim.x) {
+        const int u = unit_at(iu, units);
         int n[R];
         const GroupMeta m = group_meta<R>(p, u / p.chunks, u % p.chunks, n, false);
         const int ntiles = m.blk1 - m.blk0;
@@ -548,7 +555,8 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
     bool ok = true;     // false after a pipeline wait gave up (then nothing more is waited for)
     uint32_t tt = 0;    // tiles so far (accumulator buffer and phase)
     uint32_t vn = 0;    // verdicts so far (passes over units)
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    for (int iu = blockIdx.x; iu < units; iu += gridDim.x) {
+      const int u = unit_at(iu, units);
       const int g = u / p.chunks, c = u - g * p.chunks;
       int n[R];
       const GroupMeta m = group_meta<R>(p, g, c, n, et == 0 && r == 0 && c == 0);

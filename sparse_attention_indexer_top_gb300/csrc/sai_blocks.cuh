@@ -36,7 +36,8 @@ struct __align__(16) BlockScratch {
     uint32_t bitmap[kBitmapWords];
   } u;
   uint32_t wsum[32];
-  int32_t last[4];  // each warp's last sorted block
+  unsigned long long wtot[4];  // each warp's packed word counts (bitmap path)
+  int32_t last[4];             // each warp's last sorted block
   int32_t wmin[4], wmax[4];
 };
 
@@ -82,26 +83,46 @@ __device__ __forceinline__ void row_blocks128(const int32_t (&slot)[4], int k, i
       if (v4[e]) atomicOr(&S.u.bitmap[(b[e] - bmin) >> 5], 1u << ((b[e] - bmin) & 31));
     }
     named_bar(bar, kBlockThreads);
-    // thread t owns words 4t .. 4t+3
+    // Thread t owns words t + 128e (e = 0..3), so a row spanning few words
+    // spreads its set bits over many threads. Its four word counts travel
+    // as 16-bit fields of one 64-bit value through a single scan: the first
+    // word of field e lands after every word of the fields before it, then
+    // after the same field's words of lower threads (ascending word order).
     uint32_t wv[4];
-    int nf = 0;
+    unsigned long long packed = 0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int w = 4 * t + e;
+      const int w = t + kBlockThreads * e;
       wv[e] = w < words ? S.u.bitmap[w] : 0u;
-      nf += __popc(wv[e]);
+      packed |= static_cast<unsigned long long>(__popc(wv[e])) << (16 * e);
     }
-    int count;
-    int out = block_exscan<kBlockThreads>(nf, &count, S.wsum, t, bar);
+    unsigned long long incl = packed;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const unsigned long long o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+      if (lane >= d) incl += o;
+    }
+    if (lane == 31) S.wtot[warp] = incl;
+    named_bar(bar, kBlockThreads);
+    unsigned long long before = incl - packed, total = 0;
+#pragma unroll
+    for (int w = 0; w < kBlockThreads / 32; ++w) {
+      const unsigned long long v = S.wtot[w];
+      before += w < warp ? v : 0ull;
+      total += v;
+    }
     named_bar(bar, kBlockThreads);  // the scratch is read before the group reuses it
     if (!live) return;
+    int count = 0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
+      int out = count + static_cast<int>((before >> (16 * e)) & 0xFFFFu);
+      count += static_cast<int>((total >> (16 * e)) & 0xFFFFu);
       uint32_t m = wv[e];
       while (m) {
         const int bit = __ffs(m) - 1;
         m &= m - 1u;
-        out_blocks[out++] = bmin + 32 * (4 * t + e) + bit;
+        out_blocks[out++] = bmin + 32 * (t + kBlockThreads * e) + bit;
       }
     }
     for (int j = count + t; j < k; j += kBlockThreads) out_blocks[j] = -1;
