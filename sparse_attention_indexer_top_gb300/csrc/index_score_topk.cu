@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S.tfull[i], 1);
-      mbar_init(&S.tempty[i], kEpiWarps);
+      mbar_init(&S.tempty[i], kEpiWarps * 32);
     }
     mbar_init(&S.qfull, 1);
     mbar_init(&S.qempty, 1);
@@ -540,6 +540,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
     uint32_t* const ckey = S.ckey[r];
     int32_t* const cidx = S.cidx[r];
     uint32_t* const my_key = ckey + quad * kSub;
+    const uint32_t lt_mask = (1u << lane) - 1u;
     int32_t* const my_idx = cidx + quad * kSub;
     // this warp's histogram for cutting its own list: its quarter of aux
     uint32_t* const whist = quad < 2 ? S.aux_key[r] + 256 * quad : reinterpret_cast<uint32_t*>(S.aux_idx[r]) + 256 * (quad - 2);
@@ -612,10 +613,10 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
             ok = ok && __all_sync(0xFFFFFFFFu, mbar_wait(&S.tfull[buf], (tt >> 1) & 1u));
             tc_fence_after();
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0 && ok) mbar_arrive(&S.tempty[buf]);
+            if (ok) mbar_arrive(&S.tempty[buf]);
           }
         }
+        bool bad_page = false;  // reported once, after the pass
         for (int i = 0; active && i < ntiles; ++i, ++tt) {
           const int cur = nxt, buf = tt & 1;
           nxt = cur + 1 == ntiles ? 0 : cur + 1;
@@ -624,15 +625,13 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
           const bool page_ok = ok_next;
           const float ks = ks_next;
           const int page = page_next;
-          if (i + 1 < ntiles) {
-            page_next = __ldg(bt + nxt);
-            ok_next = static_cast<unsigned>(page_next) < static_cast<unsigned>(p.num_blocks);
-            ks_next = ok_next ? key_scale(page_next) : 0.f;
-          }
-          if (!page_ok) {
-            if (et == 0 && r == 0 && pass == 0) atomicOr(p.status, kDevBadPage);
-          }
-          ok = ok && __all_sync(0xFFFFFFFFu, mbar_wait(&S.tfull[buf], (tt >> 1) & 1u));
+          // (after the last position nxt wraps to a tile already read: in range)
+          page_next = __ldg(bt + nxt);
+          ok_next = static_cast<unsigned>(page_next) < static_cast<unsigned>(p.num_blocks);
+          ks_next = ok_next ? key_scale(page_next) : 0.f;
+          bad_page |= !page_ok;
+          if (ok && !__all_sync(0xFFFFFFFFu, mbar_try_wait(&S.tfull[buf], (tt >> 1) & 1u)))
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait_slow(&S.tfull[buf], (tt >> 1) & 1u));
           float score = 0.f;
           if (ok) {
             tc_fence_after();
@@ -712,8 +711,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
               tmem_ld_wait16(b1);
               // the accumulator buffer is free once all its loads are in registers
               tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&S.tempty[buf]);
+              mbar_arrive(&S.tempty[buf]);
               math(b1, 1, 1);
             } else {
               // single rows (three CTAs per SM hide the latency): one
@@ -725,8 +723,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
                 tmem_ld_wait();
                 if (half == 1) {  // the accumulator buffer is free once both halves are in registers
                   tc_fence_before();
-                  __syncwarp();
-                  if (lane == 0) mbar_arrive(&S.tempty[buf]);
+                  mbar_arrive(&S.tempty[buf]);
                 }
 #pragma unroll
                 for (int hq = 0; hq < 2; ++hq) {
@@ -764,11 +761,9 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
                 tf = tau_float(tau);
                 wc = kTopK;
               }
-              if (pass_) {
-                const int pos = wc + __popc(bal & ((1u << lane) - 1u));
-                my_key[pos] = order_key(score);
-                my_idx[pos] = t;
-              }
+              const int pos = wc + __popc(bal & lt_mask);
+              st_shared_if(pass_, my_key + pos, order_key(score));
+              st_shared_if(pass_, reinterpret_cast<uint32_t*>(my_idx) + pos, static_cast<uint32_t>(t));
               wc += __popc(bal);
             }
             if (spec && i == kSampleTiles - 1) {
@@ -784,6 +779,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
             }
           }
         }
+        if (bad_page && et == 0 && r == 0 && pass == 0) atomicOr(p.status, kDevBadPage);
         bool row_failed = false;
         if constexpr (MODE == kModeTopk) {
           if (active) {

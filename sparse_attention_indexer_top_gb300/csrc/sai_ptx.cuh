@@ -85,6 +85,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// mbar_wait out of line: hot loops poll once with mbar_try_wait and call
+// this only when the phase is not complete yet, which keeps the sleeping
+// loop's branches out of their instruction stream.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity) { return mbar_wait(bar, parity); }
+
+// Store v at the shared address p when `pred` holds, as one predicated
+// store (no branch around it).
+__device__ __forceinline__ void st_shared_if(bool pred, uint32_t* p, uint32_t v) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t@q st.shared.b32 [%1], %2;\n\t}" ::"r"(static_cast<int>(pred)),
+      "r"(smem_u32(p)), "r"(v)
+      : "memory");
+}
+
 // Same, with an L2 evict-first hint for data read exactly once.
 __device__ __forceinline__ void bulk_g2s_stream(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
                                                 uint64_t policy) {
