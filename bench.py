@@ -93,16 +93,16 @@ def measure_fp8_peak(dev, n: int = 8192, reps: int = 10):
 # DRAM bytes (read + write) per key, from one ncu capture of each kernel as
 # it stands (the launch list of the default step, one pass, at full size;
 # summaries under profiles/, by kernel and workload): top-k stream on the
-# 16384 packed-extend rows, 4335.61 MB + 0.09 MB per launch for 1079.8 M
-# keys; fused prefill on 4096 rows, 39.43 MB + 0.05 MB for 125.8 M keys;
-# fused decode on 64 rows, 158.92 MB + 1.32 MB for 1.19 M keys. Traffic
+# 16384 packed-extend rows, 4335.76 MB + 0.09 MB per launch for 1079.8 M
+# keys; fused prefill on 4096 rows, 39.09 MB + 0.06 MB for 125.8 M keys;
+# fused decode on 64 rows, 159.08 MB + 1.44 MB for 1.19 M keys. Traffic
 # grows with the keys streamed. Set an entry to None whenever its kernel
 # changes until it is re-captured.
 TRAFFIC_BYTES_PER_KEY = {
-    "topk_packed_extend": (21678060800 + 467456) / 5 / 1079779328,
-    "fused_prefill": (197137920 + 229376) / 5 / 125831168,
-    "fused_decode": (794580480 + 6599936) / 5 / 1190814,
-    # not re-captured since the fused kernel changed (four rows per CTA)
+    "topk_packed_extend": (21678812928 + 444672) / 5 / 1079779328,
+    "fused_prefill": (195466496 + 278016) / 5 / 125831168,
+    "fused_decode": (795416064 + 7191296) / 5 / 1190814,
+    # not re-captured since the fused kernel changed (its tile loop)
     "fused_prefill_bf16": None,
     "fused_decode_bf16": None,
 }
@@ -740,6 +740,31 @@ def run_gpu(args):
         if "sparse_blocks" in paths:
             entry["separate_pass_ms"] = paths["sparse_blocks"]["ms"]
         paths["block_lists"] = entry
+    # Report-only parts (default: the decode-layout top-k, the latency-bound
+    # serving shape): timed after the step with their own events and an L2
+    # flush before each launch, not part of the step or its rate.
+    report = [n for n in args.report if n not in args.paths]
+    if report:
+        rparts = build_parts(dev, argparse.Namespace(**{**vars(args), "paths": report}))
+        for part in rparts:
+            with torch.cuda.stream(stream):
+                for _ in range(args.warmup):
+                    launch_part(part, stream)
+            torch.cuda.synchronize()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+            for e0, e1 in evs:
+                with torch.cuda.stream(stream):
+                    flush.fill_(1)
+                e0.record(stream)
+                launch_part(part, stream)
+                e1.record(stream)
+            torch.cuda.synchronize()
+            pm = float(np.median([e0.elapsed_time(e1) for e0, e1 in evs]))
+            paths[part.name] = {"ms": pm, "rows_per_s": part.rows / (pm * 1e-3), "keys_per_s": part.keys / (pm * 1e-3),
+                                "hbm_gbs": part.bytes / (pm * 1e-3) / 1e9,
+                                "hbm_frac": part.bytes / (pm * 1e-3) / 1e9 / hbm_peak, "in_step": False}
+        assert sai.device_status() == 0, "a kernel flagged its inputs"
     # the dominant kernel's roofline
     top = int(np.argmax(part_ms))
     tp, tm = parts[top], part_ms[top]
@@ -823,11 +848,14 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
     ap.add_argument("--paths", default=",".join(PATHS), help="comma-separated parts of the step")
+    ap.add_argument("--report", default="topk_decode",
+                    help="comma-separated parts timed after the step, outside it (reported in config.paths)")
     ap.add_argument("--new-tokens", type=int, default=8192,
                     help="query rows per request of the packed-extend part (8192 = full chunk)")
     ap.add_argument("--prefill-rows", type=int, default=4096, help="query rows of the fused prefill part")
     args = ap.parse_args()
     args.paths = [p for p in args.paths.split(",") if p]
+    args.report = [p for p in args.report.split(",") if p]
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -383,6 +383,10 @@ __device__ __forceinline__ uint32_t stage_mask(const float4 (&a)[kVec], int nvec
   return mask;
 }
 
+// kBlocks: this launch builds block lists in the single-unit row ends (the
+// instantiation without it carries none of that code, so the stream loop
+// keeps its registers when no block lists are asked for).
+template <bool kBlocks>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const __grid_constant__ TopkLaunch p) {
   extern __shared__ unsigned char smem_raw[];
   Smem& S = smem_ref(smem_raw);
@@ -591,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
           sl[e] = -1;
           if (ix[e] < 0) continue;
           if (p.out_idx) p.out_idx[o + rk[e]] = ix[e];
-          if (p.out_slots || p.out_blocks) {
+          if (p.out_slots || (kBlocks && p.out_blocks)) {
             const int ps = p.page_size;
             const long long page = p.page_tables[(long long)batch * p.pt_stride + (ps == 1 ? ix[e] : ix[e] / ps)];
             sl[e] = static_cast<int>(ps == 1 ? page : page * ps + ix[e] % ps);
@@ -602,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
           if (p.out_idx) p.out_idx[o + j] = -1;
           if (p.out_slots) p.out_slots[o + j] = -1;
         }
-        if (p.out_blocks) {
+        if (kBlocks && p.out_blocks) {
           // the distinct blocks of the row's slots, built here from the
           // slots in registers (the ranking's scratch is free once read)
           named_bar(kBar, kThreads);
@@ -883,7 +887,7 @@ __global__ void __launch_bounds__(kRankRows * 128) rank_kernel(const __grid_cons
                   bar, true);
 }
 
-bool g_attr_done[64];
+bool g_attr_done[2][64];
 bool g_merge_attr_done[64];
 bool g_rank_attr_done[64];
 
@@ -953,27 +957,36 @@ cudaError_t launch_merge(const MergeLaunch& p, cudaStream_t stream) {
   return launch_dependent(merge_kernel, p.rows, kTopK, sizeof(MergeSmem), stream, p);
 }
 
-cudaError_t launch_topk_transform(const TopkLaunch& p, int num_sms, cudaStream_t stream) {
-  if (p.rows <= 0) return cudaSuccess;
+template <bool kBlocks>
+static cudaError_t launch_stream(const TopkLaunch& p, int num_sms, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !g_attr_done[dev]) {
-    cudaError_t e =
-        cudaFuncSetAttribute(topk_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (dev < 64 && !g_attr_done[kBlocks][dev]) {
+    cudaError_t e = cudaFuncSetAttribute(topk_stream_kernel<kBlocks>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    g_attr_done[dev] = true;
+    g_attr_done[kBlocks][dev] = true;
   }
   static int ctas_per_sm[64];
   if (dev < 64 && ctas_per_sm[dev] == 0) {
     int nb = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, topk_stream_kernel, kThreads, kSmemBytes);
+    cudaError_t e =
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, topk_stream_kernel<kBlocks>, kThreads, kSmemBytes);
     if (e != cudaSuccess) return e;
     ctas_per_sm[dev] = nb > 0 ? nb : 1;
   }
   const long long units = (long long)p.rows * p.chunks;
   const int grid = (int)std::min<long long>(units, (long long)(dev < 64 ? ctas_per_sm[dev] : 1) * num_sms);
-  topk_stream_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  topk_stream_kernel<kBlocks><<<grid, kThreads, kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk_transform(const TopkLaunch& p, int num_sms, cudaStream_t stream) {
+  if (p.rows <= 0) return cudaSuccess;
+  // block lists come from the stream kernel only when it ends the rows
+  // itself (one unit per row); split rows get theirs from the merge
+  cudaError_t e = p.out_blocks && p.chunks == 1 ? launch_stream<true>(p, num_sms, stream)
+                                                : launch_stream<false>(p, num_sms, stream);
   if (e != cudaSuccess || p.chunks == 1) return e;
   MergeLaunch m{};
   m.rows = p.rows;
