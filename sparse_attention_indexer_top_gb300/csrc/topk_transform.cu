@@ -820,17 +820,21 @@ __global__ void __launch_bounds__(kTopK, 1) merge_kernel(const __grid_constant__
 constexpr int kRankRows = 4;
 
 struct __align__(16) RankRowSmem {
-  uint32_t aux_key[kTopK];
-  int32_t aux_idx[kTopK];
   union {
     struct {
-      uint32_t hist[1024];
-      uint16_t bucket[kTopK];
-    } r;
-    unsigned long long sortbuf[kTopK];
-  } s;
-  SelectScratch sc;
-  BlockScratch blocks;
+      uint32_t aux_key[kTopK];
+      int32_t aux_idx[kTopK];
+      union {
+        struct {
+          uint32_t hist[1024];
+          uint16_t bucket[kTopK];
+        } r;
+        unsigned long long sortbuf[kTopK];
+      } s;
+      SelectScratch sc;
+    } k;
+    BlockScratch blocks;  // the row's block list, once its ranks are in registers
+  } u;
 };
 
 __global__ void __launch_bounds__(kRankRows * 128) rank_kernel(const __grid_constant__ MergeLaunch p) {
@@ -843,16 +847,17 @@ __global__ void __launch_bounds__(kRankRows * 128) rank_kernel(const __grid_cons
   pdl_wait();  // the lists come from the grid launched just before
   const int cnt = live ? min(max(p.part_cnt[row], 0), kTopK) : 0;
   for (int j = t; j < cnt; j += 128) {
-    S.aux_key[j] = p.part_key[row * kTopK + j];
-    S.aux_idx[j] = p.part_idx[row * kTopK + j];
+    S.u.k.aux_key[j] = p.part_key[row * kTopK + j];
+    S.u.k.aux_idx[j] = p.part_idx[row * kTopK + j];
   }
   named_bar(bar, 128);
   uint32_t k4[4];
   int32_t i4[4];
   int rk4[4];
-  if (!bucket_rank512<128>(S.aux_key, S.aux_idx, cnt, S.s.r.hist, S.s.r.bucket, S.sc, k4, i4, rk4, t, bar)) {
+  if (!bucket_rank512<128>(S.u.k.aux_key, S.u.k.aux_idx, cnt, S.u.k.s.r.hist, S.u.k.s.r.bucket, S.u.k.sc, k4, i4,
+                           rk4, t, bar)) {
     unsigned long long v[4];
-    bitonic_sort512_128(S.aux_key, S.aux_idx, cnt, S.s.sortbuf, v, t, bar);
+    bitonic_sort512_128(S.u.k.aux_key, S.u.k.aux_idx, cnt, S.u.k.s.sortbuf, v, t, bar);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       k4[e] = static_cast<uint32_t>(v[e] >> 32);
@@ -882,9 +887,11 @@ __global__ void __launch_bounds__(kRankRows * 128) rank_kernel(const __grid_cons
     if (p.out_slots) p.out_slots[o + j] = -1;
     if (p.out_scores) p.out_scores[o + j] = __int_as_float(0x7FC00000);
   }
-  if (p.out_blocks)
-    row_blocks128(sl, kTopK, p.block_size, p.out_blocks + o, p.out_counts ? p.out_counts + row : nullptr, S.blocks, t,
-                  bar, true);
+  if (p.out_blocks) {
+    named_bar(bar, 128);  // the ranking's scratch is read; the block list reuses it
+    row_blocks128(sl, kTopK, p.block_size, p.out_blocks + o, p.out_counts ? p.out_counts + row : nullptr, S.u.blocks,
+                  t, bar, true);
+  }
 }
 
 bool g_attr_done[2][64];
