@@ -38,8 +38,9 @@
 // twice per unit. (1) The unit's tiles are streamed starting from its middle
 // tile (then wrapping around); after the first kSampleTiles tiles every
 // key of those tiles is a candidate, and the row sets a start threshold at
-// the m-th largest of those sampled scores, m chosen so that about
-// kSpecMargin x 512 keys of the whole unit are expected to pass. (2) At the
+// the m-th largest of those sampled scores, m about four standard
+// deviations above the number of samples expected among the unit's top 512
+// (so fewer than 512 keys reach it only rarely). (2) At the
 // unit end the row's candidates are cut to its top 512. The start threshold
 // is a guess: if fewer than 512 candidates reached it, keys above the true
 // 512th may have been dropped, so the unit is streamed again (TMA, MMA and
@@ -106,7 +107,6 @@ static_assert(kSub >= kTopK + 32 && kSub % 32 == 0 && kSub / 32 <= 32, "sub-list
 constexpr int kEpiRow = 128;       // epilogue threads per query row (4 warps, one TMEM lane quadrant each)
 constexpr int kSampleTiles = 8;    // tiles sampled, spread over the unit, before the start threshold
 constexpr int kSpecMinKeys = 2048; // a row's unit needs this many keys to start from a sampled threshold
-constexpr int kSpecMargin = 2;     // about kSpecMargin x 512 of the unit's keys are expected to pass it
 
 template <int R, bool BF16>
 struct __align__(1024) FusedSmem {
@@ -334,9 +334,15 @@ __device__ __noinline__ uint32_t warp_cut512(uint32_t* key, int32_t* idx, int n,
 
 // The row's start threshold after its sample tiles (all 128 threads of the
 // row, named barrier `bar`): the m-th largest of the row's sampled scores,
-// m = kSpecMargin x 512 x sampled / n_unit, as the lowest key of the radix
-// bin that holds it (at least m sampled keys reach it); each warp then keeps
-// only its list's entries at or above it. Returns {threshold (0: none set),
+// as the lowest key of the radix bin that holds it (at least m sampled keys
+// reach it); each warp then keeps only its list's entries at or above it.
+// Of the `sampled` keys, about e = 512 x sampled / n_unit are expected
+// among the unit's top 512 (a count with a standard deviation of at most
+// sqrt(e)); m = e + 4 sqrt(e) + 2, so the threshold lies above the unit's
+// 512th key (and the unit is replayed) only when that count runs four
+// standard deviations high. The unit then keeps about 512 m / e candidates:
+// ~680 for a decode unit sampling a third of its keys, ~1100 for a prefill
+// unit sampling a thirtieth. Returns {threshold (0: none set),
 // this warp's new list size}. `bins` (512 words) is the row's aux array.
 __device__ __forceinline__ uint2 spec_threshold(int* wcnt, SelectScratch& sc, uint32_t* bins, uint32_t* my_key,
                                              int32_t* my_idx, int wc, int n_unit, int quad, int et, int lane,
@@ -352,7 +358,8 @@ __device__ __forceinline__ uint2 spec_threshold(int* wcnt, SelectScratch& sc, ui
     sampled += counts[q];
   }
   uint32_t ts = 0;
-  const long long mm = ((long long)kSpecMargin * kTopK * sampled + n_unit - 1) / n_unit;
+  const float e = static_cast<float>(kTopK) * static_cast<float>(sampled) / static_cast<float>(n_unit);
+  const long long mm = static_cast<long long>(ceilf(e + 4.f * sqrtf(e) + 2.f));
   if (mm >= 1 && mm < sampled) {
     const int cq = counts[quad];
     const Threshold th = radix_threshold_fast<kEpiRow>((uint32_t)mm, sc, bins, et, bar, [&](auto fn) {

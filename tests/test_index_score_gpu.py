@@ -167,6 +167,43 @@ def test_fused_prefill_full_size():
     _check_all_rows_in_pool(_fused(inp, group_rows=4), inp)
 
 
+def test_start_threshold_replay():
+    """A unit whose sampled tiles hold far higher scores than the rest of it:
+    the start threshold set from the sample then lets fewer than 512 of the
+    unit's keys through, so the unit must be streamed again with no
+    threshold. Four rows of 32768 keys are split into chunks as the host
+    plan splits them (every unit of at least 16 tiles streams from its
+    middle tile, so its first 8 tiles are the sample); in one chunk of each
+    row the sampled tiles' keys get a 64x scale. The row's top 512 then lies
+    among those 1024 keys, while without the replay that chunk would report
+    only the few hundred that reached its threshold."""
+    rows, n = 4, 32768
+    per_row = n // 128
+    inp = W.make_fused_inputs(48, rows, 64, 128, rows * per_row, np.full(rows, n, np.int32), (rows, per_row))
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    chunks = max(1, min(-(-4 * sms // rows), 12, per_row))  # the plan: about four units per SM, at most 12
+    cb = -(-per_row // chunks)
+    boosted = 0
+    for r in range(rows):
+        c = 1 + r  # a different chunk in each row
+        start = c * cb
+        tiles = min(cb, per_row - start)
+        assert tiles >= 16 and tiles * 128 >= 2048, "the chunk must sample"
+        for i in range(8):
+            t = start + (i + tiles // 2) % tiles
+            inp.kscale[inp.block_table[r, t]] *= np.float32(64.0)
+            boosted += 1
+    assert boosted == 8 * rows
+    got = _fused(inp)
+    _check_topk(got, inp)
+    # every selected key comes from the boosted tiles
+    for r in range(rows):
+        c = 1 + r
+        tiles = min(cb, per_row - c * cb)
+        sampled = {c * cb + (i + tiles // 2) % tiles for i in range(8)}
+        assert set((got[1][r] // 128).tolist()) <= sampled, f"row {r}: a pick outside the boosted tiles"
+
+
 @pytest.mark.parametrize("block_size", [128, 256, 1])
 def test_fused_block_lists(block_size):
     """Block lists built by the fused call's last stage: the ranking path
