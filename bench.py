@@ -92,17 +92,17 @@ def measure_fp8_peak(dev, n: int = 8192, reps: int = 10):
 
 # DRAM bytes (read + write) per key, from one ncu capture of each kernel as
 # it stands (one pass, at full size; summaries under profiles/, by kernel
-# and workload): top-k stream on the 16384 packed-extend rows, 4335.76 MB +
-# 0.09 MB per launch for 1079.8 M keys; fused prefill on 4096 rows, 39.09 MB
-# + 0.06 MB for 125.8 M keys; fused decode on 64 rows, 159.08 MB + 1.44 MB
+# and workload): top-k stream on the 16384 packed-extend rows, 4336.33 MB +
+# 0.23 MB per launch for 1079.8 M keys; fused prefill on 4096 rows, 39.10 MB
+# + 0.06 MB for 125.8 M keys; fused decode on 64 rows, 159.08 MB + 1.45 MB
 # for 1.19 M keys; the bf16-cache kernels on the same shapes, 76.88 MB +
 # 2.23 MB (prefill) and 312.57 MB + 2.37 MB (decode). Traffic grows with the
 # keys streamed. Set an entry to None whenever its kernel changes until it
 # is re-captured.
 TRAFFIC_BYTES_PER_KEY = {
-    "topk_packed_extend": (21678812928 + 444672) / 5 / 1079779328,
-    "fused_prefill": (195466496 + 278016) / 5 / 125831168,
-    "fused_decode": (795416064 + 7191296) / 5 / 1190814,
+    "topk_packed_extend": (21681633536 + 1127424) / 5 / 1079779328,
+    "fused_prefill": (195485952 + 288768) / 5 / 125831168,
+    "fused_decode": (795407616 + 7244544) / 5 / 1190814,
     "fused_prefill_bf16": (384384256 + 11137792) / 5 / 125831168,
     "fused_decode_bf16": (1562842624 + 11865856) / 5 / 1190814,
 }

@@ -45,6 +45,22 @@ def test_random_slots_with_duplicates_and_padding(k, block_size):
     _check(slots, block_size)
 
 
+@pytest.mark.parametrize("span", [4095, 4097, 8193, 12289, 16384])
+def test_bitmap_spans_across_word_fields(span):
+    """Rows whose blocks span just across 128, 256 and 384 bitmap words (the
+    second to fourth word each thread owns) and the bitmap's full 16384 ids:
+    the packed per-thread word counts must keep the blocks in order."""
+    rng = np.random.default_rng(300 + span)
+    rows, k = 9, 512
+    lo = rng.integers(0, 1 << 20, size=(rows, 1))
+    slots = (lo + rng.integers(0, span, size=(rows, k))).astype(np.int32)
+    slots[:, 0] = lo[:, 0]                   # both ends of the span present
+    slots[:, 1] = lo[:, 0] + span - 1
+    slots[2, 300:] = -1                      # padding
+    slots[4] = np.sort(slots[4])[::-1]       # order of the input slots is irrelevant
+    _check(slots, 1)
+
+
 def test_blocks_of_a_topk_output():
     import sparse_attention_indexer_top_gb300 as sai
 

@@ -95,11 +95,14 @@ def test_packed_extend_ragged(stride_pad):
     _assert_equal(_run(inp, force_single=True), _oracle(inp), f"packed single pad={stride_pad}")
 
 
-@pytest.mark.parametrize("block_size", [1, 7, 128, 1 << 20])
+@pytest.mark.parametrize("block_size", [1, 7, 9, 16, 128, 1 << 20])
 def test_block_lists_block_sizes(block_size):
-    """Block lists built by the top-k call for page size 1 slots of a wide
-    pool: one slot per block (block_size 1, blocks spanning far more than the
-    16384 ids of the bitmap), odd sizes, and one block for everything."""
+    """Block lists built by the top-k call for page size 1 slots of a
+    140000-slot pool: one slot per block (block_size 1, blocks spanning far
+    more than the 16384 ids of the bitmap; 7 likewise), spans of ~15600 and
+    ~8750 blocks (9, 16: bitmap words beyond the first 128 and 256, i.e.
+    every thread's second to fourth word), ~1100 blocks (128), and one block
+    for everything."""
     inp = W.packed_extend(seed=17, reqs=2, new_tokens=40, kv_len=70000, fill=np.inf)
     _assert_equal(_run(inp, block_size=block_size), _oracle(inp, block_size=block_size), f"bs={block_size}")
     _assert_equal(_run(inp, force_single=True, block_size=block_size), _oracle(inp, block_size=block_size),
