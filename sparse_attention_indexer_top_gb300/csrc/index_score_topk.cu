@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(fused_threads<R>(), (fused_ctas_per_sm<R, BF16
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S.tfull[i], 1);
-      mbar_init(&S.tempty[i], kEpiWarps * 32);
+      mbar_init(&S.tempty[i], kEpiWarps * 32);  // every epilogue thread arrives (no lane-0 branch)
     }
     mbar_init(&S.qfull, 1);
     mbar_init(&S.qempty, 1);
