@@ -204,6 +204,34 @@ def test_start_threshold_replay():
         assert set((got[1][r] // 128).tolist()) <= sampled, f"row {r}: a pick outside the boosted tiles"
 
 
+def test_start_threshold_replay_grouped_rows():
+    """The replay in a four-row group where one row does not fail: the four
+    rows share a request's 32768 keys, one chunk's sampled tiles get a 64x
+    key scale (rows 0, 2 and 3 then let too few keys through and replay it),
+    while row 1 has q = 0 (every score 0, so every key reaches its
+    threshold): during the replay row 1 only frees the accumulator buffers,
+    and all four rows must still come out exact."""
+    rows, n = 4, 32768
+    per_row = n // 128
+    inp = W.make_fused_inputs(49, rows, 64, 128, per_row + 8, np.full(rows, n, np.int32), (1, per_row),
+                              row_to_batch=np.zeros(rows, np.int32))
+    inp.q[1] = 0  # e4m3 code 0 = +0
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    chunks = max(1, min(-(-4 * sms // 1), 12, per_row))  # one group of four rows
+    cb = -(-per_row // chunks)
+    c = 2
+    tiles = min(cb, per_row - c * cb)
+    assert tiles >= 16 and tiles * 128 >= 2048, "the chunk must sample"
+    sampled = [c * cb + (i + tiles // 2) % tiles for i in range(8)]
+    for t in sampled:
+        inp.kscale[inp.block_table[0, t]] *= np.float32(64.0)
+    got = _fused(inp, group_rows=4)
+    _check_topk(got, inp)
+    for r in (0, 2, 3):
+        assert set((got[1][r] // 128).tolist()) <= set(sampled), f"row {r}: a pick outside the boosted tiles"
+    assert np.array_equal(got[1][1], np.arange(512)), "row 1: equal scores go to the lowest indices"
+
+
 @pytest.mark.parametrize("block_size", [128, 256, 1])
 def test_fused_block_lists(block_size):
     """Block lists built by the fused call's last stage: the ranking path
