@@ -234,6 +234,13 @@ class Part:
         self.flops = 0.0    # algorithmic tensor flops per launch
         self.launches = 0
         self.meta = {}
+        self.uploads = None  # [(device view, pinned host tensor)]; None: every host tensor to its device copy
+
+    def upload_pairs(self):
+        """The host-to-device copies of this part's inputs for one step."""
+        if self.uploads is not None:
+            return self.uploads
+        return [(self.dev[k], t) for k, t in self.host.items()]
 
 
 def _pin(a):
@@ -251,15 +258,30 @@ def build_topk_part(dev, new_tokens: int, name: str = "topk_packed_extend"):
     part = Part(name)
     row_starts, seq_lens, r2b, width = W.packed_extend_meta(new_tokens=new_tokens)
     rows = int(seq_lens.size)
-    host = torch.empty((rows, width), dtype=torch.float32, pin_memory=True)
-    hn = host.numpy()
+    reqs = int(r2b.max()) + 1
+    per_req = width // reqs  # columns of the shared buffer one request's windows lie in
+    # Host side: each request's [rows of the request, its columns] block,
+    # pinned and contiguous; the rest of the shared buffer is never read.
+    blocks = [torch.empty((new_tokens, per_req), dtype=torch.float32, pin_memory=True) for _ in range(reqs)]
     chunk = 1024
+    tmp = np.empty((chunk, width), dtype=np.float32)
     for r0 in range(0, rows, chunk):
-        W.fill_rows(hn[r0:r0 + chunk], r0, 3, row_starts, seq_lens, fill=0.0)
+        n = min(chunk, rows - r0)
+        W.fill_rows(tmp[:n], r0, 3, row_starts, seq_lens, fill=0.0)
+        for q in range(reqs):  # rows r0 .. r0+n-1 of request q, if any
+            a, b = max(r0, q * new_tokens), min(r0 + n, (q + 1) * new_tokens)
+            if a < b:
+                blocks[q].numpy()[a - q * new_tokens:b - q * new_tokens] = tmp[a - r0:b - r0, q * per_req:(q + 1) * per_req]
     pt = W.page_table_perm(3, (2, 70000))
-    part.host = {"scores": host, "seq_lens": _pin(seq_lens), "row_starts": _pin(row_starts),
-                 "row_to_batch": _pin(r2b), "page_tables": _pin(pt)}
+    part.host = {"seq_lens": _pin(seq_lens), "row_starts": _pin(row_starts), "row_to_batch": _pin(r2b),
+                 "page_tables": _pin(pt)}
     part.dev = {k: v.to(dev) for k, v in part.host.items()}
+    scores = torch.zeros((rows, width), dtype=torch.float32, device=dev)
+    views = [scores[q * new_tokens:(q + 1) * new_tokens, q * per_req:(q + 1) * per_req] for q in range(reqs)]
+    for v, h in zip(views, blocks):
+        v.copy_(h)
+    part.dev["scores"] = scores
+    part.uploads = [(part.dev[k], t) for k, t in part.host.items()] + list(zip(views, blocks))
     import sparse_attention_indexer_top_gb300 as sai
 
     ws = sai.topk_transform_workspace(rows, width)
@@ -787,7 +809,7 @@ def run_gpu(args):
     if not args.no_e2e:
         outs_host = {(p.name, k): torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
                      for p in parts for k, v in p.out.items() if k != "workspace"}
-        h2d = sum(t.numel() * t.element_size() for p in parts for t in p.host.values())
+        h2d = sum(t.numel() * t.element_size() for p in parts for _, t in p.upload_pairs())
         d2h = sum(t.numel() * t.element_size() for t in outs_host.values())
         n_e2e = max(1, min(3, args.steps))
         torch.cuda.synchronize()
@@ -797,8 +819,8 @@ def run_gpu(args):
         with torch.cuda.stream(stream):
             for _ in range(n_e2e):
                 for p in parts:
-                    for k, t in p.host.items():
-                        p.dev[k].copy_(t, non_blocking=True)
+                    for dst, t in p.upload_pairs():
+                        dst.copy_(t, non_blocking=True)
                 step()
                 for p in parts:
                     for k, v in p.out.items():
