@@ -811,13 +811,17 @@ def run_gpu(args):
                      for p in parts for k, v in p.out.items() if k != "workspace"}
         h2d = sum(t.numel() * t.element_size() for p in parts for _, t in p.upload_pairs())
         d2h = sum(t.numel() * t.element_size() for t in outs_host.values())
-        n_e2e = max(1, min(3, args.steps))
+        # warm-up steps first (the first uploads also allocate the staging
+        # buffers of the strided copies), then the median of the timed ones
+        n_e2e = max(1, min(5, args.steps))
+        n_warm = max(2, min(args.warmup, 5))
+        evs = []
         torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        with torch.cuda.stream(stream):
-            for _ in range(n_e2e):
+        for i in range(n_warm + n_e2e):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            with torch.cuda.stream(stream):
                 for p in parts:
                     for dst, t in p.upload_pairs():
                         dst.copy_(t, non_blocking=True)
@@ -826,9 +830,11 @@ def run_gpu(args):
                     for k, v in p.out.items():
                         if k != "workspace":
                             outs_host[(p.name, k)].copy_(v, non_blocking=True)
-        e1.record(stream)
+            e1.record(stream)
+            if i >= n_warm:
+                evs.append((e0, e1))
         torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / n_e2e
+        e2e_ms = float(np.median([a.elapsed_time(b) for a, b in evs]))
         e2e = {"value": rows / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     cpu = None
