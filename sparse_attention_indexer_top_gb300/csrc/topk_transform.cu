@@ -68,6 +68,10 @@ constexpr int kStage = kVec * 4 * kThreads;      // floats per stage (12 KB)
 #define SAI_TOPK_NSTAGE 2
 #endif
 constexpr int kNStage = SAI_TOPK_NSTAGE;         // 24 KB in flight per CTA
+#ifndef SAI_TOPK_DEEP_STAGES
+#define SAI_TOPK_DEEP_STAGES 16
+#endif
+constexpr int kDeepStages = SAI_TOPK_DEEP_STAGES;  // ring of a call whose units all fit on the SMs at once
 constexpr int kWarps = kThreads / 32;
 constexpr int kCap = 1536;                       // candidate capacity (all warps)
 constexpr int kSub = kCap / kWarps;              // one candidate sub-list per warp
@@ -100,8 +104,19 @@ struct StageDesc {
   UnitInfo u;
 };
 
-struct __align__(128) Smem {
-  float stage[kNStage][kStage];
+// Thread 0's walk over its work units (the issue side of the ring).
+struct Cursor {
+  int unit;          // current unit (>= units: done)
+  int s, nst;        // stage index within the unit, stage count
+  int base;          // row-local index of the next stage's element 0
+  int body_left;     // TMA elements not issued yet
+  const float* src;  // global address of the next stage
+  UnitInfo u;
+};
+
+template <int NS>
+struct __align__(128) SmemT {
+  float stage[NS][kStage];
   union {
     struct {
       uint32_t key[kCap];
@@ -116,32 +131,27 @@ struct __align__(128) Smem {
   } cand;
   uint32_t aux_key[kTopK];
   int32_t aux_idx[kTopK];
-  StageDesc desc[kNStage];
-  uint64_t full[kNStage];
+  StageDesc desc[NS];
+  uint64_t full[NS];
   SelectScratch sc;
   uint32_t spec_keys[2];  // keys at ranks 256 and 512 of the last finished unit
   int wcnt[kWarps];       // sub-list sizes, published before a cut
   int wapp[kWarps];       // per-warp appends of the unit, published at its end
   int timeout;            // set by a thread whose stage wait gave up
-  struct Cursor {         // thread 0's walk over its work units (issue side)
-    int unit;             // current unit (>= units: done)
-    int s, nst;           // stage index within the unit, stage count
-    int base;             // row-local index of the next stage's element 0
-    int body_left;        // TMA elements not issued yet
-    const float* src;     // global address of the next stage
-    UnitInfo u;
-  } cur;
+  Cursor cur;
 };
 
-constexpr size_t kSmemBytes = sizeof(Smem) + 128;  // + alignment slack
-
-__device__ __forceinline__ Smem& smem_ref(unsigned char* raw) {
-  uintptr_t a = reinterpret_cast<uintptr_t>(raw);
-  a = (a + 127) & ~static_cast<uintptr_t>(127);
-  return *reinterpret_cast<Smem*>(a);
+template <int NS>
+constexpr size_t smem_bytes() {
+  return sizeof(SmemT<NS>) + 128;  // + alignment slack
 }
 
-using Cursor = Smem::Cursor;
+template <int NS>
+__device__ __forceinline__ SmemT<NS>& smem_ref(unsigned char* raw) {
+  uintptr_t a = reinterpret_cast<uintptr_t>(raw);
+  a = (a + 127) & ~static_cast<uintptr_t>(127);
+  return *reinterpret_cast<SmemT<NS>*>(a);
+}
 
 __device__ void cursor_load(const TopkLaunch& p, Cursor& c) {
   const int units = p.rows * p.chunks;
@@ -188,7 +198,8 @@ __device__ void cursor_load(const TopkLaunch& p, Cursor& c) {
 
 // Issue the cursor's next stage into `slot` (thread 0 only) and advance.
 // Returns false once the terminal descriptor has been issued.
-__device__ bool issue_stage(const TopkLaunch& p, Smem& S, int slot, uint64_t policy) {
+template <int NS>
+__device__ bool issue_stage(const TopkLaunch& p, SmemT<NS>& S, int slot, uint64_t policy) {
   Cursor& c = S.cur;
   StageDesc& d = S.desc[slot];
   if (c.unit >= p.rows * p.chunks) {
@@ -303,7 +314,8 @@ __device__ __forceinline__ void write_survivors_smem(uint32_t* key, int32_t* idx
 // exactly and redoes the unit otherwise); about 1024 + len/128 scores then
 // pass. 0 (no threshold) for windows under 4096. Out of line: it runs once
 // per CTA or so, and stays out of the stream loop's registers.
-__device__ __noinline__ uint32_t sample_tau(const float* win, int len, Smem& S, int tid) {
+template <int NS>
+__device__ __noinline__ uint32_t sample_tau(const float* win, int len, SmemT<NS>& S, int tid) {
   constexpr int kSamples = 1024, kPer = kSamples / kThreads;
   if (len < 4096) return 0u;
   const uint32_t expect = static_cast<uint32_t>(((long long)kSamples * kTopK + len - 1) / len);
@@ -325,7 +337,8 @@ __device__ __noinline__ uint32_t sample_tau(const float* win, int len, Smem& S, 
 // Gather every warp's sub-list into aux: the exact top 512 of their union
 // when it holds more (tau rises to the cut), else all of it. All threads
 // call this with their warp's wcnt; returns the number in aux.
-__device__ int gather_to_aux(Smem& S, int wcnt, uint32_t& tau, int tid) {
+template <int NS>
+__device__ int gather_to_aux(SmemT<NS>& S, int wcnt, uint32_t& tau, int tid) {
   const int lane = tid & 31, warp = tid >> 5;
   if (lane == 0) S.wcnt[warp] = wcnt;
   named_bar(kBar, kThreads);
@@ -354,7 +367,8 @@ __device__ int gather_to_aux(Smem& S, int wcnt, uint32_t& tau, int tid) {
 
 // Cut all sub-lists together (gather_to_aux) and deal the kept entries back,
 // 128 per warp. Returns the warp's new sub-list size.
-__device__ __forceinline__ int prune(Smem& S, int wcnt, uint32_t& tau, int tid) {
+template <int NS>
+__device__ __forceinline__ int prune(SmemT<NS>& S, int wcnt, uint32_t& tau, int tid) {
   const int lane = tid & 31, warp = tid >> 5;
   const int total = gather_to_aux(S, wcnt, tau, tid);
   constexpr int kShare = kTopK / kWarps;
@@ -386,10 +400,10 @@ __device__ __forceinline__ uint32_t stage_mask(const float4 (&a)[kVec], int nvec
 // kBlocks: this launch builds block lists in the single-unit row ends (the
 // instantiation without it carries none of that code, so the stream loop
 // keeps its registers when no block lists are asked for).
-template <bool kBlocks>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const __grid_constant__ TopkLaunch p) {
+template <bool kBlocks, int NS, int CPS>
+__global__ void __launch_bounds__(kThreads, CPS) topk_stream_kernel(const __grid_constant__ TopkLaunch p) {
   extern __shared__ unsigned char smem_raw[];
-  Smem& S = smem_ref(smem_raw);
+  SmemT<NS>& S = smem_ref<NS>(smem_raw);
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   pdl_trigger();  // the merge may be scheduled now; it waits for this grid to finish
@@ -398,14 +412,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
   uint64_t policy = 0;
   bool issuing = false;
   if (tid == 0) {
-    for (int i = 0; i < kNStage; ++i) mbar_init(&S.full[i], 1);
+    for (int i = 0; i < NS; ++i) mbar_init(&S.full[i], 1);
     S.timeout = 0;
     fence_mbar_init();
     policy = l2_policy_evict_first();
     S.cur.unit = blockIdx.x;
     cursor_load(p, S.cur);
     issuing = true;
-    for (int i = 0; i < kNStage && issuing; ++i) issuing = issue_stage(p, S, i, policy);
+    for (int i = 0; i < NS && issuing; ++i) issuing = issue_stage(p, S, i, policy);
   }
   __syncthreads();
   uint32_t it = 0;
@@ -441,8 +455,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
     return added;
   };
   while (true) {
-    const int slot = it % kNStage;
-    const uint32_t ph = (it / kNStage) & 1u;
+    const int slot = it % NS;
+    const uint32_t ph = (it / NS) & 1u;
     const bool ok = mbar_wait(&S.full[slot], ph);
     // after a timeout the descriptor is not trusted: process nothing, then
     // leave together at the barrier below
@@ -508,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) topk_stream_kernel(const
       if (tid == 0) {
         atomicOr(p.status, kDevWaitTimeout);
         // let the copies already issued land before the CTA exits (bounded)
-        for (int k = 1; k < kNStage; ++k) mbar_wait(&S.full[(it + k) % kNStage], ((it + k) / kNStage) & 1u);
+        for (int k = 1; k < NS; ++k) mbar_wait(&S.full[(it + k) % NS], ((it + k) / NS) & 1u);
       }
       break;
     }
@@ -894,7 +908,6 @@ __global__ void __launch_bounds__(kRankRows * 128) rank_kernel(const __grid_cons
   }
 }
 
-bool g_attr_done[2][64];
 bool g_merge_attr_done[64];
 bool g_rank_attr_done[64];
 
@@ -964,36 +977,48 @@ cudaError_t launch_merge(const MergeLaunch& p, cudaStream_t stream) {
   return launch_dependent(merge_kernel, p.rows, kTopK, sizeof(MergeSmem), stream, p);
 }
 
-template <bool kBlocks>
+template <bool kBlocks, int NS, int CPS>
 static cudaError_t launch_stream(const TopkLaunch& p, int num_sms, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !g_attr_done[kBlocks][dev]) {
-    cudaError_t e = cudaFuncSetAttribute(topk_stream_kernel<kBlocks>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
+  constexpr size_t kBytes = smem_bytes<NS>();
+  static bool attr_done[64];
+  if (dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(topk_stream_kernel<kBlocks, NS, CPS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBytes);
     if (e != cudaSuccess) return e;
-    g_attr_done[kBlocks][dev] = true;
+    attr_done[dev] = true;
   }
   static int ctas_per_sm[64];
   if (dev < 64 && ctas_per_sm[dev] == 0) {
     int nb = 0;
     cudaError_t e =
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, topk_stream_kernel<kBlocks>, kThreads, kSmemBytes);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, topk_stream_kernel<kBlocks, NS, CPS>, kThreads, kBytes);
     if (e != cudaSuccess) return e;
     ctas_per_sm[dev] = nb > 0 ? nb : 1;
   }
   const long long units = (long long)p.rows * p.chunks;
   const int grid = (int)std::min<long long>(units, (long long)(dev < 64 ? ctas_per_sm[dev] : 1) * num_sms);
-  topk_stream_kernel<kBlocks><<<grid, kThreads, kSmemBytes, stream>>>(p);
+  topk_stream_kernel<kBlocks, NS, CPS><<<grid, kThreads, kBytes, stream>>>(p);
   return cudaGetLastError();
+}
+
+// Stream kernel instance for a call: a call whose units all fit on the SMs
+// at once runs one CTA per SM with a deep ring (nothing else shares the SM,
+// so its stream is not limited by a two-stage pipeline); otherwise five CTAs
+// per SM with two stages each. Block lists come from the stream kernel only
+// when it ends the rows itself (one unit per row); split rows get theirs
+// from the merge.
+template <bool kBlocks>
+static cudaError_t launch_stream_for(const TopkLaunch& p, int num_sms, cudaStream_t stream) {
+  if ((long long)p.rows * p.chunks <= num_sms) return launch_stream<kBlocks, kDeepStages, 1>(p, num_sms, stream);
+  return launch_stream<kBlocks, kNStage, kCtasPerSm>(p, num_sms, stream);
 }
 
 cudaError_t launch_topk_transform(const TopkLaunch& p, int num_sms, cudaStream_t stream) {
   if (p.rows <= 0) return cudaSuccess;
-  // block lists come from the stream kernel only when it ends the rows
-  // itself (one unit per row); split rows get theirs from the merge
-  cudaError_t e = p.out_blocks && p.chunks == 1 ? launch_stream<true>(p, num_sms, stream)
-                                                : launch_stream<false>(p, num_sms, stream);
+  cudaError_t e = p.out_blocks && p.chunks == 1 ? launch_stream_for<true>(p, num_sms, stream)
+                                                : launch_stream_for<false>(p, num_sms, stream);
   if (e != cudaSuccess || p.chunks == 1) return e;
   MergeLaunch m{};
   m.rows = p.rows;
